@@ -1,0 +1,319 @@
+/*
+ * Oracle for sliding-window softmax attention with attention sinks, SWA(w,s).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
+ * this file: only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA library; both sides only see the same seeded bf16 inputs.
+ *
+ * What it computes (the plain definition, fp64 throughout):
+ *
+ *   Window formula -- "Sliding-window beats linear attention" (paper summary
+ *   page), section "Prerequisites / Sliding-window attention SWA(w, s)", the
+ *   displayed equation for x_t: each position t attends to the most recent w
+ *   tokens with scale 1/sqrt(d), and the softmax is normalised only over the
+ *   attended tokens.
+ *
+ *   Sinks -- same page, same section, the notation paragraph, and section
+ *   "Method steps", step two: in SWA(w,s) the window w keeps s of its places
+ *   for the first tokens of the sequence, so position t attends to the first s
+ *   tokens plus the most recent w-s tokens.  The blog page "Microsoft SWA paper
+ *   overturns linear attention", section "What they tested", gives the worked
+ *   case w=64, s=4: the first 4 tokens plus the latest 60.
+ *
+ *   Fixed cache -- news page "No post-training, just 4 more tokens: sliding
+ *   window attention overtakes linear attention", section "Research method":
+ *   once the cache holds the window it stops growing; the blog page above says
+ *   the method only changes the attention mask and the KV-cache eviction rule.
+ *
+ * Readings taken where the pages are silent (each is restated in the design
+ * notes):
+ *   - indices are 0-based: A(t) = {i : 0 <= i < min(s, t+1)}
+ *                                 U {i : max(0, t-(w-s)+1) <= i <= t},
+ *     a set union, so a token in both parts counts once; |A(t)| = min(t+1, w);
+ *   - w < 0 stands for w = infinity, i.e. full causal attention, A(t) = [0, t];
+ *   - grouped-query heads: query head h reads key/value head h / (Hq/Hkv);
+ *   - a cache slot for position p is p for p < s and s + (p-s) mod (w-s)
+ *     otherwise (for w = infinity, slot = p); appending writes positions in
+ *     increasing order, so a later position overwrites an earlier one in the
+ *     same slot;
+ *   - inputs are bf16 bit patterns, widened exactly to fp64.
+ *
+ * Softmax is the usual two-pass, max-subtracted form, which equals the
+ * equation above in exact arithmetic.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening of a bf16 bit pattern to double. */
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_get_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Membership of key position i in the attended set A(t) of query position t. */
+int oracle_in_window(int64_t t, int64_t i, int64_t w, int64_t s)
+{
+    if (i < 0 || i > t) return 0;            /* causal: keys up to t only      */
+    if (w < 0) return 1;                      /* w = infinity: full causal      */
+    if (i < s) return 1;                      /* one of the first s tokens      */
+    return i >= t - (w - s) + 1;              /* one of the latest w-s tokens   */
+}
+
+/*
+ * Softmax attention of one query row over an explicit list of key rows.
+ * q: d values; keys/vals: base pointers, row r of the list is at
+ * keys + idx[r]*row_stride.  Writes out[d] and returns the log-sum-exp of the
+ * scaled scores (natural log).
+ */
+static double attend_list(const uint16_t *q, const uint16_t *keys, const uint16_t *vals,
+                          const int64_t *idx, int64_t n, int64_t row_stride, int d,
+                          double *score, double *out)
+{
+    const double scale = 1.0 / sqrt((double)d);
+    double m = -INFINITY;
+    for (int64_t r = 0; r < n; ++r) {
+        const uint16_t *k = keys + idx[r] * row_stride;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += bf16_bits_to_double(q[c]) * bf16_bits_to_double(k[c]);
+        score[r] = dot * scale;
+        if (score[r] > m) m = score[r];
+    }
+    double den = 0.0;
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    for (int64_t r = 0; r < n; ++r) {
+        const uint16_t *v = vals + idx[r] * row_stride;
+        double p = exp(score[r] - m);
+        den += p;
+        for (int c = 0; c < d; ++c) out[c] += p * bf16_bits_to_double(v[c]);
+    }
+    for (int c = 0; c < d; ++c) out[c] /= den;
+    return m + log(den);
+}
+
+/* The attended positions of query position t, in increasing order. */
+static int64_t window_indices(int64_t t, int64_t w, int64_t s, int64_t *idx)
+{
+    int64_t n = 0;
+    if (w < 0) {
+        for (int64_t i = 0; i <= t; ++i) idx[n++] = i;
+        return n;
+    }
+    /* the first s tokens (those that exist by position t) */
+    int64_t sink_end = s < t + 1 ? s : t + 1;
+    for (int64_t i = 0; i < sink_end; ++i) idx[n++] = i;
+    /* the latest w-s tokens; start at s so that a sink is not counted twice */
+    int64_t lo = t - (w - s) + 1;
+    if (lo < s) lo = s;
+    for (int64_t i = lo; i <= t; ++i) idx[n++] = i;
+    return n;
+}
+
+/*
+ * One output row (b, t, h) of prefill.  q, k, v: bf16 bits, q [B,L,Hq,d],
+ * k and v [B,L,Hkv,d].  o_row: d doubles.  Returns the row's log-sum-exp.
+ * scratch_idx / scratch_score: room for L entries each.
+ */
+static double prefill_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t b, int64_t t, int64_t h, int64_t L, int64_t Hq,
+                          int64_t Hkv, int d, int64_t w, int64_t s,
+                          int64_t *scratch_idx, double *scratch_score, double *o_row)
+{
+    int64_t G = Hq / Hkv;
+    int64_t kvh = h / G;
+    int64_t n = window_indices(t, w, s, scratch_idx);
+    const uint16_t *qrow = q + ((b * L + t) * Hq + h) * d;
+    const uint16_t *kbase = k + (b * L * Hkv + kvh) * d;   /* position 0 of (b, kvh) */
+    const uint16_t *vbase = v + (b * L * Hkv + kvh) * d;
+    return attend_list(qrow, kbase, vbase, scratch_idx, n, Hkv * d, d, scratch_score, o_row);
+}
+
+/*
+ * Full prefill: o [B,L,Hq,d] (double), lse [B,Hq,L] (double, may be NULL).
+ * Work buffers: work_idx holds nthreads*L int64, work_score nthreads*L
+ * doubles; nthreads >= 1 is the number of OpenMP threads used.
+ */
+int oracle_swa_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       double *o, double *lse, int64_t B, int64_t L, int64_t Hq,
+                       int64_t Hkv, int64_t d, int64_t w, int64_t s,
+                       int64_t *work_idx, double *work_score, int nthreads)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    if (w >= 0 && w <= s) return -1;
+    int64_t rows = B * L * Hq;
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads)
+    for (int64_t r = 0; r < rows; ++r) {
+#ifdef _OPENMP
+        int tid = omp_get_thread_num();
+#else
+        int tid = 0;
+#endif
+        int64_t h = r % Hq;
+        int64_t t = (r / Hq) % L;
+        int64_t b = r / (Hq * L);
+        double ls = prefill_row(q, k, v, b, t, h, L, Hq, Hkv, (int)d, w, s,
+                                work_idx + (int64_t)tid * L, work_score + (int64_t)tid * L,
+                                o + r * d);
+        if (lse) lse[(b * Hq + h) * L + t] = ls;
+    }
+    return 0;
+}
+
+/*
+ * Selected prefill rows.  rows: n triples (b, t, h).  o: n*d doubles,
+ * lse: n doubles (may be NULL).  Work buffers as above.
+ */
+int oracle_swa_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const int64_t *rows, int64_t n, double *o, double *lse,
+                            int64_t B, int64_t L, int64_t Hq, int64_t Hkv, int64_t d,
+                            int64_t w, int64_t s, int64_t *work_idx, double *work_score,
+                            int nthreads)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    if (w >= 0 && w <= s) return -1;
+    for (int64_t r = 0; r < n; ++r) {
+        int64_t b = rows[3 * r], t = rows[3 * r + 1], h = rows[3 * r + 2];
+        if (b < 0 || b >= B || t < 0 || t >= L || h < 0 || h >= Hq) return -1;
+    }
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+    for (int64_t r = 0; r < n; ++r) {
+#ifdef _OPENMP
+        int tid = omp_get_thread_num();
+#else
+        int tid = 0;
+#endif
+        double ls = prefill_row(q, k, v, rows[3 * r], rows[3 * r + 1], rows[3 * r + 2], L, Hq,
+                                Hkv, (int)d, w, s, work_idx + (int64_t)tid * L,
+                                work_score + (int64_t)tid * L, o + r * d);
+        if (lse) lse[r] = ls;
+    }
+    return 0;
+}
+
+/*
+ * Decode over the full history: the query of sequence b sits at position
+ * pos[b] and attends to A(pos[b]) of k_hist/v_hist [B,P,Hkv,d] (P > pos[b]).
+ * q [B,Hq,d], o [B,Hq,d] doubles.  Work buffers: nthreads * P entries each.
+ */
+int oracle_swa_decode(const uint16_t *q, const uint16_t *k_hist, const uint16_t *v_hist,
+                      const int64_t *pos, double *o, int64_t B, int64_t P, int64_t Hq,
+                      int64_t Hkv, int64_t d, int64_t w, int64_t s, int64_t *work_idx,
+                      double *work_score, int nthreads)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    if (w >= 0 && w <= s) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        if (pos[b] < 0 || pos[b] >= P) return -1;
+    int64_t G = Hq / Hkv;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t r = 0; r < B * Hq; ++r) {
+#ifdef _OPENMP
+        int tid = omp_get_thread_num();
+#else
+        int tid = 0;
+#endif
+        int64_t b = r / Hq, h = r % Hq, kvh = h / G;
+        int64_t *idx = work_idx + (int64_t)tid * P;
+        int64_t n = window_indices(pos[b], w, s, idx);
+        const uint16_t *kbase = k_hist + (b * P * Hkv + kvh) * d;
+        const uint16_t *vbase = v_hist + (b * P * Hkv + kvh) * d;
+        attend_list(q + r * d, kbase, vbase, idx, n, Hkv * d, (int)d,
+                    work_score + (int64_t)tid * P, o + r * d);
+    }
+    return 0;
+}
+
+/* Cache slot of position p: sinks keep their own slot, the rest share a ring. */
+int64_t oracle_cache_slot(int64_t p, int64_t w, int64_t s)
+{
+    if (w < 0 || p < s) return p;
+    return s + (p - s) % (w - s);
+}
+
+/*
+ * Host simulation of appending positions pos0 .. pos0+n-1 to a cache.
+ * cache_k, cache_v: [B,Hkv,cap,d] bf16 bits; k_new, v_new: [B,n,Hkv,d].
+ * Positions are written one after the other, so where two positions share a
+ * slot the later one is what remains.  Returns -1 if a slot falls outside cap.
+ */
+int oracle_cache_append(uint16_t *cache_k, uint16_t *cache_v, const uint16_t *k_new,
+                        const uint16_t *v_new, int64_t B, int64_t Hkv, int64_t d, int64_t cap,
+                        int64_t w, int64_t s, int64_t n, int64_t pos0)
+{
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t slot = oracle_cache_slot(pos0 + j, w, s);
+            if (slot < 0 || slot >= cap) return -1;
+            for (int64_t h = 0; h < Hkv; ++h) {
+                const uint16_t *ks = k_new + ((b * n + j) * Hkv + h) * d;
+                const uint16_t *vs = v_new + ((b * n + j) * Hkv + h) * d;
+                uint16_t *kd = cache_k + ((b * Hkv + h) * cap + slot) * d;
+                uint16_t *vd = cache_v + ((b * Hkv + h) * cap + slot) * d;
+                memcpy(kd, ks, (size_t)d * sizeof(uint16_t));
+                memcpy(vd, vs, (size_t)d * sizeof(uint16_t));
+            }
+        }
+    return 0;
+}
+
+/*
+ * Decode over the cache contents: attention of q over the filled slots
+ * [0, min(pos+1, cap_eff)) of each (b, kv head), cap_eff = w (or cap for
+ * w = infinity).  Slot order is not position order; the softmax over a set
+ * does not depend on the order, so this equals oracle_swa_decode on the same
+ * history.  Work buffers: nthreads * cap entries each.
+ */
+int oracle_swa_decode_cache(const uint16_t *q, const uint16_t *cache_k, const uint16_t *cache_v,
+                            const int64_t *pos, double *o, int64_t B, int64_t Hq, int64_t Hkv,
+                            int64_t d, int64_t cap, int64_t w, int64_t s, int64_t *work_idx,
+                            double *work_score, int nthreads)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    if (w >= 0 && (w <= s || w > cap)) return -1;
+    int64_t G = Hq / Hkv;
+    int64_t cap_eff = w < 0 ? cap : w;
+    for (int64_t b = 0; b < B; ++b)
+        if (pos[b] < 0 || (w < 0 && pos[b] >= cap)) return -1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t r = 0; r < B * Hq; ++r) {
+#ifdef _OPENMP
+        int tid = omp_get_thread_num();
+#else
+        int tid = 0;
+#endif
+        int64_t b = r / Hq, h = r % Hq, kvh = h / G;
+        int64_t n = pos[b] + 1 < cap_eff ? pos[b] + 1 : cap_eff;
+        int64_t *idx = work_idx + (int64_t)tid * cap;
+        for (int64_t i = 0; i < n; ++i) idx[i] = i;
+        const uint16_t *kbase = cache_k + (b * Hkv + kvh) * cap * d;
+        const uint16_t *vbase = cache_v + (b * Hkv + kvh) * cap * d;
+        attend_list(q + r * d, kbase, vbase, idx, n, d, (int)d,
+                    work_score + (int64_t)tid * cap, o + r * d);
+    }
+    return 0;
+}

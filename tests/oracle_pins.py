@@ -1,0 +1,286 @@
+"""Checks that pin the oracle to things other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError on
+a mismatch.  ``test_oracle.py`` runs them against the oracle as built; the
+mutation test runs them against copies of the oracle with a plausible mistake
+planted in the C source and expects at least one pin to fail for each.
+
+What pins what:
+  * hand-written fixtures of attended sets and cache contents
+    (tests/golden/, each line citing the page statement it follows);
+  * brute force: dense L x L attention with a boolean mask built by slicing
+    "the first s" and "the latest w-s" positions, in numpy;
+  * a library routine: torch's scaled_dot_product_attention (fp64, causal),
+    which SWA(w,s) must equal when the window covers the whole prefix;
+  * closed forms: t = 0 gives v_0; q = 0 gives the plain mean of the attended
+    values; two keys in d = 1 give a two-term weighted mean;
+  * invariants: equal values give that value; permuting the history inside
+    the attended set changes nothing; decoding at position t equals prefill
+    row t; decoding over the ring cache equals decoding over the history.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle as oracle_mod
+from oracle import W_INF, bits_to_f64
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLDEN = os.path.join(HERE, "golden")
+
+
+def _bf16(x: np.ndarray) -> np.ndarray:
+    return oracle_mod.bf16_bits(torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16))
+
+
+def _rand_bits(rng: np.random.Generator, shape) -> np.ndarray:
+    return _bf16(rng.standard_normal(shape).astype(np.float32))
+
+
+def _parse_ranges(text: str) -> list[int]:
+    out: list[int] = []
+    for part in text.split(","):
+        lo, hi = part.strip().split("-")
+        out.extend(range(int(lo), int(hi) + 1))
+    return out
+
+
+def _read_fixture(name: str):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, ranges, cite = [x.strip() for x in line.split("|")]
+            a, b, c = head.split()
+            w = W_INF if a == "inf" else int(a)
+            rows.append((w, int(b), int(c), _parse_ranges(ranges), cite))
+    return rows
+
+
+def _first_and_latest(t: int, w: int, s: int) -> list[int]:
+    """The attended set built by slicing the prefix [0..t]: first s, latest w-s."""
+    prefix = list(range(t + 1))
+    if w == W_INF:
+        return prefix
+    first = prefix[:s]
+    latest = prefix[-(w - s):] if w - s <= len(prefix) else prefix
+    return sorted(set(first) | set(latest))
+
+
+def _dense_reference(q, k, v, w, s):
+    """Brute-force masked attention: full score matrix, -inf outside the set."""
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    B, L, Hq, d = qf.shape
+    Hkv = kf.shape[2]
+    G = Hq // Hkv
+    mask = np.zeros((L, L), dtype=bool)
+    for t in range(L):
+        mask[t, _first_and_latest(t, w, s)] = True
+    o = np.zeros_like(qf)
+    for b in range(B):
+        for h in range(Hq):
+            kk = kf[b, :, h // G, :]
+            vv = vf[b, :, h // G, :]
+            sc = (qf[b, :, h, :] @ kk.T) / math.sqrt(d)
+            sc = np.where(mask, sc, -np.inf)
+            sc = sc - sc.max(axis=1, keepdims=True)
+            p = np.exp(sc)
+            o[b, :, h, :] = (p @ vv) / p.sum(axis=1, keepdims=True)
+    return o
+
+
+def _sdpa_causal(q, k, v):
+    """torch scaled_dot_product_attention in fp64 with a causal mask (BSHD in/out)."""
+    qf, kf, vf = (torch.from_numpy(bits_to_f64(x)) for x in (q, k, v))
+    G = qf.shape[2] // kf.shape[2]
+    kf = kf.repeat_interleave(G, dim=2)
+    vf = vf.repeat_interleave(G, dim=2)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        qf.transpose(1, 2), kf.transpose(1, 2), vf.transpose(1, 2), is_causal=True)
+    return out.transpose(1, 2).numpy()
+
+
+# ---------------------------------------------------------------------------
+def pin_golden_sets(orc) -> None:
+    for w, s, t, expect, cite in _read_fixture("attended_sets.txt"):
+        got = orc.window(t, w, s)
+        assert got == expect, f"A({t}) for SWA({w},{s}) [{cite}]: {got[:8]}... != {expect[:8]}..."
+
+
+def pin_window_size(orc) -> None:
+    for w, s in [(8, 0), (8, 2), (8, 7), (5, 1), (64, 4)]:
+        for t in range(0, 3 * w):
+            n = len(orc.window(t, w, s))
+            assert n == min(t + 1, w), (w, s, t, n)
+
+
+def pin_brute_force(orc) -> None:
+    rng = np.random.default_rng(1)
+    cases = [(2, 37, 4, 2, 8, 8, 2), (1, 29, 2, 2, 16, 5, 0), (1, 40, 4, 1, 8, 12, 4),
+             (1, 23, 3, 1, 4, 64, 4), (1, 33, 2, 1, 8, W_INF, 0), (1, 21, 8, 2, 8, 6, 5)]
+    for B, L, Hq, Hkv, d, w, s in cases:
+        q = _rand_bits(rng, (B, L, Hq, d))
+        k = _rand_bits(rng, (B, L, Hkv, d))
+        v = _rand_bits(rng, (B, L, Hkv, d))
+        o, _ = orc.prefill(q, k, v, w, s, threads=2)
+        ref = _dense_reference(q, k, v, w, s)
+        err = np.abs(o - ref).max()
+        assert err < 1e-12, f"brute force {B, L, Hq, Hkv, d, w, s}: {err}"
+
+
+def pin_causal_library(orc) -> None:
+    rng = np.random.default_rng(2)
+    B, L, Hq, Hkv, d = 2, 48, 4, 2, 16
+    q = _rand_bits(rng, (B, L, Hq, d))
+    k = _rand_bits(rng, (B, L, Hkv, d))
+    v = _rand_bits(rng, (B, L, Hkv, d))
+    ref = _sdpa_causal(q, k, v)
+    for w, s in [(W_INF, 0), (L, 4), (L + 7, 0), (1000, 3)]:
+        o, _ = orc.prefill(q, k, v, w, s, threads=2)
+        assert np.abs(o - ref).max() < 1e-12, (w, s)
+    # rows whose prefix fits the window are plain causal attention
+    for w, s in [(16, 4), (9, 0), (12, 11)]:
+        o, _ = orc.prefill(q, k, v, w, s, threads=2)
+        assert np.abs(o[:, :w] - ref[:, :w]).max() < 1e-12, (w, s)
+        assert np.abs(o[:, w:] - ref[:, w:]).max() > 1e-6, (w, s)
+
+
+def pin_closed_forms(orc) -> None:
+    rng = np.random.default_rng(3)
+    B, L, Hq, Hkv, d = 1, 30, 4, 2, 8
+    q = _rand_bits(rng, (B, L, Hq, d))
+    k = _rand_bits(rng, (B, L, Hkv, d))
+    v = _rand_bits(rng, (B, L, Hkv, d))
+    vf = bits_to_f64(v)
+    o, _ = orc.prefill(q, k, v, 6, 2, threads=1)
+    for h in range(Hq):                      # t = 0 attends only to itself
+        assert np.array_equal(o[0, 0, h], vf[0, 0, h // 2])
+    zero = np.zeros_like(q)                  # q = 0: uniform weights over A(t)
+    o, _ = orc.prefill(zero, k, v, 6, 2, threads=1)
+    for t in range(L):
+        idx = _first_and_latest(t, 6, 2)
+        for h in range(Hq):
+            mean = vf[0, idx, h // 2].mean(axis=0)
+            assert np.abs(o[0, t, h] - mean).max() < 1e-12, (t, h)
+    # d = 1, two keys: a two-term weighted mean with weights exp(q k_i)
+    q1 = _bf16(np.array([0.75], np.float32)).reshape(1, 1, 1, 1).repeat(2, axis=1)
+    k1 = _bf16(np.array([1.5, -0.5], np.float32)).reshape(1, 2, 1, 1)
+    v1 = _bf16(np.array([2.0, 10.0], np.float32)).reshape(1, 2, 1, 1)
+    o, lse = orc.prefill(q1, k1, v1, W_INF, 0, threads=1)
+    a, b = 0.75 * 1.5, 0.75 * -0.5
+    expect = (math.exp(a) * 2.0 + math.exp(b) * 10.0) / (math.exp(a) + math.exp(b))
+    assert abs(o[0, 1, 0, 0] - expect) < 1e-14
+    assert abs(lse[0, 0, 1] - math.log(math.exp(a) + math.exp(b))) < 1e-14
+
+
+def pin_equal_values(orc) -> None:
+    rng = np.random.default_rng(4)
+    B, L, Hq, Hkv, d = 2, 40, 4, 1, 8
+    q = _rand_bits(rng, (B, L, Hq, d))
+    k = _rand_bits(rng, (B, L, Hkv, d))
+    row = _rand_bits(rng, (B, 1, Hkv, d))
+    v = np.ascontiguousarray(np.repeat(row, L, axis=1))
+    o, _ = orc.prefill(q, k, v, 10, 3, threads=2)
+    vf = bits_to_f64(row)
+    for h in range(Hq):
+        assert np.abs(o[:, :, h] - vf[:, :, 0]).max() < 1e-13
+
+
+def pin_decode_history(orc) -> None:
+    """Decode at position t equals prefill row t; permutations inside A(t) change nothing."""
+    rng = np.random.default_rng(5)
+    B, P, Hq, Hkv, d, w, s = 2, 50, 4, 2, 8, 12, 3
+    q = _rand_bits(rng, (B, P, Hq, d))
+    k = _rand_bits(rng, (B, P, Hkv, d))
+    v = _rand_bits(rng, (B, P, Hkv, d))
+    o_pre, _ = orc.prefill(q, k, v, w, s, threads=2)
+    for t in [0, 2, 11, 12, 30, P - 1]:
+        o_dec = orc.decode(np.ascontiguousarray(q[:, t]), k, v, [t] * B, w, s, threads=2)
+        assert np.abs(o_dec - o_pre[:, t]).max() < 1e-13, t
+    t = P - 1
+    idx = _first_and_latest(t, w, s)
+    perm = rng.permutation(idx)
+    kp, vp = k.copy(), v.copy()
+    kp[:, idx] = k[:, perm]
+    vp[:, idx] = v[:, perm]
+    qt = np.ascontiguousarray(q[:, t])
+    a = orc.decode(qt, k, v, [t] * B, w, s, threads=1)
+    b = orc.decode(qt, kp, vp, [t] * B, w, s, threads=1)
+    assert np.abs(a - b).max() < 1e-12
+    # changing a key outside A(t) leaves the result as it is; changing one
+    # inside A(t) (the oldest of the latest w-s) does not
+    outside = [i for i in range(t + 1) if i not in idx]
+    kq = k.copy()
+    kq[:, outside[-1]] = k[:, idx[-1]]
+    c = orc.decode(qt, kq, v, [t] * B, w, s, threads=1)
+    assert np.abs(a - c).max() == 0.0
+    kr = k.copy()
+    kr[:, idx[s]] = k[:, idx[-1]]
+    e = orc.decode(qt, kr, v, [t] * B, w, s, threads=1)
+    assert np.abs(a - e).max() > 1e-9
+
+
+def pin_golden_cache(orc) -> None:
+    """Cache contents after a prompt match the hand-written fixtures."""
+    for w, s, P, expect, cite in _read_fixture("cache_contents.txt"):
+        B, Hkv, d = 1, 1, 2
+        ck = np.zeros((B, Hkv, w, d), np.uint16)
+        cv = np.zeros((B, Hkv, w, d), np.uint16)
+        # payload: the position in the low 15 bits (+1 so that 0 means "empty")
+        pay = (np.arange(P, dtype=np.uint16) + 1).reshape(1, P, 1, 1).repeat(d, axis=3)
+        orc.cache_append(ck, cv, pay, pay, 0, w, s)
+        held = sorted(int(x) - 1 for x in ck[0, 0, :, 0] if x != 0)
+        assert held == expect, f"SWA({w},{s}) after {P} [{cite}]: {held[:6]}..."
+        assert np.array_equal(ck, cv)
+
+
+def pin_ring_mapping(orc) -> None:
+    """Exhaustive over p < 4w: slots stay in [0, w) and the cache holds A(p)."""
+    for w, s in [(8, 0), (8, 3), (9, 4), (64, 4), (5, 4), (16, 1)]:
+        cap = w
+        ck = np.zeros((1, 1, cap, 1), np.uint16)
+        cv = np.zeros((1, 1, cap, 1), np.uint16)
+        for p in range(4 * w):
+            slot = orc.cache_slot(p, w, s)
+            assert 0 <= slot < cap, (w, s, p, slot)
+            pay = np.array([[[[p + 1]]]], np.uint16)
+            orc.cache_append(ck, cv, pay, pay, p, w, s)
+            held = sorted(int(x) - 1 for x in ck[0, 0, :, 0] if x != 0)
+            assert held == _first_and_latest(p, w, s), (w, s, p)
+        # bulk append of the same stream gives the same bits
+        bk = np.zeros_like(ck)
+        bv = np.zeros_like(cv)
+        pay = (np.arange(4 * w, dtype=np.uint16) + 1).reshape(1, 4 * w, 1, 1)
+        orc.cache_append(bk, bv, pay, pay, 0, w, s)
+        assert np.array_equal(bk, ck), (w, s)
+
+
+def pin_decode_cache(orc) -> None:
+    """Decode over the ring cache equals decode over the full history."""
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, d = 2, 4, 2, 8
+    for w, s, P in [(16, 4, 60), (16, 4, 10), (7, 0, 30), (W_INF, 0, 25)]:
+        cap = P if w == W_INF else w
+        k = _rand_bits(rng, (B, P, Hkv, d))
+        v = _rand_bits(rng, (B, P, Hkv, d))
+        q = _rand_bits(rng, (B, Hq, d))
+        ck = np.zeros((B, Hkv, cap, d), np.uint16)
+        cv = np.zeros((B, Hkv, cap, d), np.uint16)
+        orc.cache_append(ck, cv, k[:, : P // 2], v[:, : P // 2], 0, w, s)
+        for j in range(P // 2, P):
+            orc.cache_append(ck, cv, np.ascontiguousarray(k[:, j:j + 1]),
+                             np.ascontiguousarray(v[:, j:j + 1]), j, w, s)
+        a = orc.decode(q, k, v, [P - 1] * B, w, s, threads=2)
+        b = orc.decode_cache(q, ck, cv, [P - 1] * B, w, s, threads=2)
+        assert np.abs(a - b).max() < 1e-12, (w, s, P)
+
+
+ALL_PINS = [pin_golden_sets, pin_window_size, pin_brute_force, pin_causal_library,
+            pin_closed_forms, pin_equal_values, pin_decode_history, pin_golden_cache,
+            pin_ring_mapping, pin_decode_cache]

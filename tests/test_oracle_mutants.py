@@ -1,0 +1,52 @@
+"""Plant plausible mistakes in a copy of the oracle; the pins must catch each one.
+
+Every mutant is a textual edit of oracle/swa_oracle.c compiled to a temporary
+library.  The real oracle is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = {
+    # off-by-one in the start of the latest w-s tokens
+    "window_one_too_wide": ("int64_t lo = t - (w - s) + 1;", "int64_t lo = t - (w - s);"),
+    # sinks counted twice when they also fall inside the recent window
+    "sink_double_count": ("if (lo < s) lo = s;", ""),
+    # the 1/sqrt(d) scale dropped
+    "no_scale": ("score[r] = dot * scale;", "score[r] = dot;"),
+    # the wrong key/value head for a query head
+    "gqa_modulo": ("int64_t kvh = h / G;", "int64_t kvh = h % Hkv;"),
+    # keys and values transposed
+    "k_v_swapped": ("return attend_list(qrow, kbase, vbase,", "return attend_list(qrow, vbase, kbase,"),
+    # ring slot computed from p instead of p - s
+    "ring_offset": ("return s + (p - s) % (w - s);", "return s + p % (w - s);"),
+    # membership test with a strict bound
+    "in_window_strict": ("return i >= t - (w - s) + 1;", "return i > t - (w - s) + 1;"),
+    # the sinks dropped from the attended set
+    "no_sinks": ("int64_t sink_end = s < t + 1 ? s : t + 1;", "int64_t sink_end = 0;"),
+    # the softmax weight of the query's own position lost (causal end exclusive)
+    "exclusive_end": ("for (int64_t i = lo; i <= t; ++i) idx[n++] = i;",
+                      "for (int64_t i = lo; i < t; ++i) idx[n++] = i;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path = os.path.join(tmp_path, "mutant.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_source(path, os.path.join(tmp_path, "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError, ZeroDivisionError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the mutant {name}"
