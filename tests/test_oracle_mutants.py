@@ -1,14 +1,20 @@
 """Plant plausible mistakes in a copy of the oracle; the pins must catch each one.
 
 Every mutant is a textual edit of oracle/swa_oracle.c compiled to a temporary
-library.  The real oracle is never modified.
+library and checked in a child process (a planted mistake may write past a
+buffer; the child keeps that away from the test process).  The real oracle is
+never modified.
 """
 import os
+import subprocess
+import sys
 
 import pytest
 
 import oracle
-import oracle_pins
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
 
 MUTANTS = {
     # off-by-one in the start of the latest w-s tokens
@@ -27,10 +33,24 @@ MUTANTS = {
     "in_window_strict": ("return i >= t - (w - s) + 1;", "return i > t - (w - s) + 1;"),
     # the sinks dropped from the attended set
     "no_sinks": ("int64_t sink_end = s < t + 1 ? s : t + 1;", "int64_t sink_end = 0;"),
-    # the softmax weight of the query's own position lost (causal end exclusive)
+    # the query's own position left out (causal end exclusive)
     "exclusive_end": ("for (int64_t i = lo; i <= t; ++i) idx[n++] = i;",
                       "for (int64_t i = lo; i < t; ++i) idx[n++] = i;"),
 }
+
+CHILD = r"""
+import sys
+sys.path[:0] = [{root!r}, {tests!r}]
+import oracle, oracle_pins
+orc = oracle.Oracle({lib!r})
+caught = []
+for pin in oracle_pins.ALL_PINS:
+    try:
+        pin(orc)
+    except Exception:
+        caught.append(pin.__name__)
+print("CAUGHT", ",".join(caught), flush=True)
+"""
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -42,11 +62,10 @@ def test_mutant_is_caught(name, tmp_path):
     with open(path, "w") as f:
         f.write(src.replace(old, new))
     lib = oracle.compile_source(path, os.path.join(tmp_path, "libmutant.so"))
-    orc = oracle.Oracle(lib)
-    caught = []
-    for pin in oracle_pins.ALL_PINS:
-        try:
-            pin(orc)
-        except (AssertionError, ValueError, ZeroDivisionError):
-            caught.append(pin.__name__)
+    code = CHILD.format(root=ROOT, tests=HERE, lib=lib)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    lines = [l for l in r.stdout.splitlines() if l.startswith("CAUGHT")]
+    if r.returncode != 0 and not lines:
+        return  # the planted mistake crashed the oracle outright: caught
+    caught = [c for c in lines[-1][len("CAUGHT"):].strip().split(",") if c]
     assert caught, f"no pin catches the mutant {name}"
