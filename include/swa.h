@@ -1,0 +1,190 @@
+/*
+ * swa.h -- C ABI of the GB300 (sm_103a) library for sliding-window softmax
+ * attention with attention sinks, SWA(w,s).
+ *
+ * The operation.  Query position t attends to the attended set
+ *
+ *     A(t) = { i : 0 <= i < min(s, t+1) }  U  { i : max(0, t-(w-s)+1) <= i <= t }
+ *
+ * (0-based positions: the first s tokens plus the latest w-s tokens, each
+ * counted once, so |A(t)| = min(t+1, w)), and
+ *
+ *     o_t = sum_{i in A(t)} exp(c q_t.k_i) v_i / sum_{i in A(t)} exp(c q_t.k_i),
+ *     c = 1/sqrt(d).
+ *
+ * Source: "Sliding-window beats linear attention" (paper summary page),
+ * section "Prerequisites / Sliding-window attention SWA(w, s)" -- the window
+ * equation for x_t and the SWA(w,s) notation; section "Method steps", step two
+ * (w includes the s sinks; s = 4).  w = SWA_W_INF gives full causal attention,
+ * the "FA" baseline of the same page's "Research motivation".  Grouped-query
+ * heads: query head h reads key/value head h / (Hq/Hkv).
+ *
+ * Conventions for every call:
+ *   - tensors are bf16, dense (contiguous) in the stated layout, in device
+ *     memory of the current device, 16-byte aligned; the caller owns them and
+ *     keeps them alive until the stream work completes;
+ *   - calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *     the library never allocates device memory and never synchronises, except
+ *     swa_get_device_error, which synchronises `stream`;
+ *   - errors are return codes; nothing aborts the process.  Argument errors
+ *     are detected on the host before anything is enqueued.  Kernels that hit
+ *     an internal wait limit record an error code on the device, read with
+ *     swa_get_device_error;
+ *   - Q and K arrive already position-encoded: the method changes only the
+ *     mask and the cache eviction rule ("Microsoft SWA paper overturns linear
+ *     attention", blog page, section "What they tested").
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *swa_stream_t;
+
+typedef enum {
+    SWA_OK = 0,
+    SWA_ERR_INVALID_ARG = -1,  /* shape, window or pointer argument out of range      */
+    SWA_ERR_UNSUPPORTED = -2,  /* valid but not built: head size, group size, device   */
+    SWA_ERR_ALIGNMENT = -3,    /* a pointer is not 16-byte aligned                     */
+    SWA_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required           */
+    SWA_ERR_CUDA = -5,         /* a CUDA runtime/driver call or a launch failed        */
+    SWA_ERR_TIMEOUT = -6,      /* a kernel gave up waiting (device error word)         */
+    SWA_ERR_BOUNDS = -7        /* a kernel skipped an out-of-range access (device word)*/
+} swa_status;
+
+/* Infinite window: full causal attention (A(t) = [0, t]); s is then ignored. */
+#define SWA_W_INF (-1)
+
+/* Largest number of sink tokens s this build supports. */
+#define SWA_MAX_SINKS 64
+
+/*
+ * swa_prefill -- attention of every position of a prompt to its attended set.
+ *
+ *   q   [B, L, Hq,  d] bf16   queries (position-encoded)
+ *   k   [B, L, Hkv, d] bf16   keys (position-encoded)
+ *   v   [B, L, Hkv, d] bf16   values
+ *   o   [B, L, Hq,  d] bf16   output, written; o_t as defined above, fp32
+ *                             accumulation, rounded to bf16 (nearest even)
+ *   lse [B, Hq, L]     fp32   optional (NULL to skip): natural-log
+ *                             log-sum-exp of c q_t.k_i over A(t)
+ *
+ * Requires B >= 0, L >= 0 (B*L == 0 is a no-op returning SWA_OK), Hkv >= 1,
+ * Hq a multiple of Hkv with G = Hq/Hkv a power of two <= 128, d in {64, 128};
+ * w == SWA_W_INF or 0 <= s < w with s <= SWA_MAX_SINKS.  o and lse must not
+ * overlap the inputs.  The band of keys a query tile needs is the sink block
+ * plus the latest w-s keys before the tile ("Sliding-window beats linear
+ * attention", section "Core method": zero new operators, only the mask
+ * changes).
+ */
+swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int L, int Hq, int Hkv, int d, int w, int s,
+                       swa_stream_t stream);
+
+/*
+ * The fixed-size cache of one layer.  k and v are bf16 [B, Hkv, cap, d] in
+ * device memory owned by the caller.  Position p lives in slot
+ *     slot(p) = p                      if w == SWA_W_INF or p < s,
+ *     slot(p) = s + (p - s) mod (w-s)  otherwise,
+ * so cap == w for a finite window (s sink slots + a (w-s)-slot ring: the
+ * cache stops growing once it holds the window -- news page "No
+ * post-training, just 4 more tokens: sliding window attention overtakes linear
+ * attention", section "Research method"), and cap is the longest sequence
+ * for w == SWA_W_INF.  While fewer than w positions have been written, they
+ * occupy slots [0, pos+1).
+ */
+typedef struct {
+    void *k;
+    void *v;
+    int32_t B, Hkv, d, cap, w, s;
+} swa_cache;
+
+/*
+ * swa_cache_append -- write the keys/values of positions pos0 .. pos0+n-1.
+ *
+ *   k_new, v_new [B, n, Hkv, d] bf16 (device)
+ *
+ * Each position is copied bit for bit to slot(p).  When n > w - s several
+ * positions share a ring slot; only the latest one is written, so the result
+ * equals appending the positions one at a time (the eviction rule of the blog
+ * page above).  Requires pos0 >= 0, n >= 0 (0 is a no-op), and for
+ * w == SWA_W_INF pos0 + n <= cap.  The cache fields must be consistent
+ * (cap == w for finite w, 0 <= s < w, d in {64, 128}).
+ */
+swa_status swa_cache_append(const swa_cache *cache, const void *k_new, const void *v_new,
+                            int n, int64_t pos0, swa_stream_t stream);
+
+/*
+ * swa_decode_workspace_bytes -- device workspace swa_decode needs for this
+ * shape (0 if none).  Depends only on the arguments and the device's SM count;
+ * call it with the same device current as swa_decode.
+ */
+size_t swa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, int w);
+
+/*
+ * swa_decode -- one new token per sequence attends to the cache.
+ *
+ *   q   [B, Hq, d] bf16   the query of position pos[b] for each sequence b
+ *   pos [B] int32 (device) position of that query; the cache must already
+ *                          hold positions 0..pos[b] (append before decode, so
+ *                          the token attends to itself: the window equation's
+ *                          sum ends at i = t)
+ *   o   [B, Hq, d] bf16   output, written
+ *   workspace              device memory of at least
+ *                          swa_decode_workspace_bytes(...) bytes (may be NULL
+ *                          when that is 0); contents need no initialisation
+ *
+ * Supported group sizes G = Hq/Hkv: 1, 2, 4 for d = 128; 1, 2, 4, 8 for
+ * d = 64 (others return SWA_ERR_UNSUPPORTED).
+ * w and s must equal the cache's.  Reads the filled slots
+ * [0, min(pos[b]+1, w)) (or [0, pos[b]+1) for SWA_W_INF); the softmax over a
+ * set does not depend on slot order.  pos is read on the device and is not
+ * advanced, so a captured CUDA graph can be replayed with new positions.
+ * A pos[b] outside [0, cap) (infinite window) is recorded as SWA_ERR_BOUNDS in
+ * the device error word and that sequence's output is left untouched.
+ */
+swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos, int Hq,
+                      int w, int s, void *o, void *workspace, size_t workspace_bytes,
+                      swa_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *swa_status_string(swa_status status);
+
+/*
+ * swa_get_device_error -- synchronise `stream`, then read and clear the device
+ * error word of the current device.  Returns SWA_OK if no kernel recorded an
+ * error since the last call, else the recorded code (SWA_ERR_TIMEOUT,
+ * SWA_ERR_BOUNDS); SWA_ERR_CUDA if the synchronisation itself failed.
+ */
+swa_status swa_get_device_error(swa_stream_t stream);
+
+/*
+ * Host-only argument checks: the validation the calls above run before
+ * enqueuing anything, without touching the GPU.  Same return codes.
+ */
+swa_status swa_check_prefill(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, int B, int L, int Hq, int Hkv, int d, int w,
+                             int s);
+swa_status swa_check_append(const swa_cache *cache, const void *k_new, const void *v_new, int n,
+                            int64_t pos0);
+swa_status swa_check_decode(const void *q, const swa_cache *cache, const int32_t *pos, int Hq,
+                            int w, int s, const void *o, const void *workspace,
+                            size_t workspace_bytes, size_t required_bytes);
+
+/* Slot of position p in a cache of window w with s sinks (host helper; -1 if invalid). */
+int64_t swa_cache_slot(int64_t p, int w, int s);
+
+/* Library version, e.g. "0.1.0". */
+const char *swa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

@@ -1,0 +1,225 @@
+// swa_api.cu -- the C ABI (include/swa.h): argument validation, planning,
+// launches on the caller's stream, status strings and the device error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "swa_internal.h"
+
+namespace swa {
+
+cuTensorMapEncodeTiled_fn tensor_map_encoder() {
+    static cuTensorMapEncodeTiled_fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<cuTensorMapEncodeTiled_fn>(ptr);
+    });
+    return fn;
+}
+
+int device_sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+}  // namespace swa
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Byte ranges [a, a+na) and [b, b+nb) overlap?
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
+swa_status check_window(int w, int s) {
+    if (w == SWA_W_INF) return SWA_OK;
+    if (w < 1 || s < 0 || s >= w) return SWA_ERR_INVALID_ARG;
+    if (s > SWA_MAX_SINKS) return SWA_ERR_UNSUPPORTED;
+    return SWA_OK;
+}
+
+swa_status check_cache(const swa_cache *c) {
+    if (c == nullptr) return SWA_ERR_INVALID_ARG;
+    if (c->B < 0 || c->Hkv < 1 || c->cap < 1) return SWA_ERR_INVALID_ARG;
+    if (c->d != 64 && c->d != 128) return c->d < 1 ? SWA_ERR_INVALID_ARG : SWA_ERR_UNSUPPORTED;
+    const swa_status ws = check_window(c->w, c->s);
+    if (ws != SWA_OK) return ws;
+    if (c->w != SWA_W_INF && c->cap != c->w) return SWA_ERR_INVALID_ARG;
+    if (c->B > 0) {
+        if (c->k == nullptr || c->v == nullptr) return SWA_ERR_INVALID_ARG;
+        if (!aligned16(c->k) || !aligned16(c->v)) return SWA_ERR_ALIGNMENT;
+        const size_t bytes = static_cast<size_t>(c->B) * c->Hkv * c->cap * c->d * 2;
+        if (overlap(c->k, bytes, c->v, bytes)) return SWA_ERR_INVALID_ARG;
+    }
+    return SWA_OK;
+}
+
+bool decode_group_supported(int d, int G) {
+    if (d == 128) return G == 1 || G == 2 || G == 4;
+    return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+cudaStream_t as_cuda(swa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char *swa_version(void) { return "0.1.0"; }
+
+const char *swa_status_string(swa_status st) {
+    switch (st) {
+        case SWA_OK: return "SWA_OK";
+        case SWA_ERR_INVALID_ARG: return "SWA_ERR_INVALID_ARG";
+        case SWA_ERR_UNSUPPORTED: return "SWA_ERR_UNSUPPORTED";
+        case SWA_ERR_ALIGNMENT: return "SWA_ERR_ALIGNMENT";
+        case SWA_ERR_WORKSPACE: return "SWA_ERR_WORKSPACE";
+        case SWA_ERR_CUDA: return "SWA_ERR_CUDA";
+        case SWA_ERR_TIMEOUT: return "SWA_ERR_TIMEOUT";
+        case SWA_ERR_BOUNDS: return "SWA_ERR_BOUNDS";
+    }
+    return "SWA_ERR_UNKNOWN";
+}
+
+int64_t swa_cache_slot(int64_t p, int w, int s) {
+    if (p < 0 || check_window(w, s) != SWA_OK) return -1;
+    if (w == SWA_W_INF || p < s) return p;
+    return s + (p - s) % (w - s);
+}
+
+swa_status swa_check_prefill(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, int B, int L, int Hq, int Hkv, int d, int w,
+                             int s) {
+    if (B < 0 || L < 0 || Hkv < 1 || Hq < 1 || d < 1) return SWA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return SWA_ERR_INVALID_ARG;
+    const swa_status ws = check_window(w, s);
+    if (ws != SWA_OK) return ws;
+    if (d != 64 && d != 128) return SWA_ERR_UNSUPPORTED;
+    const int G = Hq / Hkv;
+    if (!pow2(G) || G > 128) return SWA_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0) return SWA_OK;
+    if (!q || !k || !v || !o) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SWA_ERR_ALIGNMENT;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_ALIGNMENT;
+    // tensor-map limit: strides below 2^40 bytes
+    if (static_cast<uint64_t>(L) * Hq * d * 2 >= (1ull << 40)) return SWA_ERR_UNSUPPORTED;
+    const uint64_t qbytes = static_cast<uint64_t>(B) * L * Hq * d * 2;
+    const uint64_t kbytes = static_cast<uint64_t>(B) * L * Hkv * d * 2;
+    if (overlap(o, qbytes, q, qbytes) || overlap(o, qbytes, k, kbytes) ||
+        overlap(o, qbytes, v, kbytes))
+        return SWA_ERR_INVALID_ARG;
+    if (lse) {
+        const uint64_t lbytes = static_cast<uint64_t>(B) * Hq * L * 4;
+        if (overlap(lse, lbytes, o, qbytes) || overlap(lse, lbytes, q, qbytes) ||
+            overlap(lse, lbytes, k, kbytes) || overlap(lse, lbytes, v, kbytes))
+            return SWA_ERR_INVALID_ARG;
+    }
+    return SWA_OK;
+}
+
+swa_status swa_check_append(const swa_cache *cache, const void *k_new, const void *v_new, int n,
+                            int64_t pos0) {
+    const swa_status cs = check_cache(cache);
+    if (cs != SWA_OK) return cs;
+    if (n < 0 || pos0 < 0) return SWA_ERR_INVALID_ARG;
+    if (cache->w == SWA_W_INF && pos0 + n > cache->cap) return SWA_ERR_INVALID_ARG;
+    if (n == 0 || cache->B == 0) return SWA_OK;
+    if (!k_new || !v_new) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return SWA_ERR_ALIGNMENT;
+    const size_t nb = static_cast<size_t>(cache->B) * n * cache->Hkv * cache->d * 2;
+    const size_t cb = static_cast<size_t>(cache->B) * cache->Hkv * cache->cap * cache->d * 2;
+    if (overlap(k_new, nb, cache->k, cb) || overlap(k_new, nb, cache->v, cb) ||
+        overlap(v_new, nb, cache->k, cb) || overlap(v_new, nb, cache->v, cb))
+        return SWA_ERR_INVALID_ARG;
+    return SWA_OK;
+}
+
+swa_status swa_check_decode(const void *q, const swa_cache *cache, const int32_t *pos, int Hq,
+                            int w, int s, const void *o, const void *workspace,
+                            size_t workspace_bytes, size_t required_bytes) {
+    const swa_status cs = check_cache(cache);
+    if (cs != SWA_OK) return cs;
+    if (Hq < 1 || Hq % cache->Hkv != 0) return SWA_ERR_INVALID_ARG;
+    if (w != cache->w) return SWA_ERR_INVALID_ARG;
+    if (w != SWA_W_INF && s != cache->s) return SWA_ERR_INVALID_ARG;
+    if (!decode_group_supported(cache->d, Hq / cache->Hkv)) return SWA_ERR_UNSUPPORTED;
+    if (cache->B == 0) return SWA_OK;
+    if (!q || !o || !pos) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o)) return SWA_ERR_ALIGNMENT;
+    if (reinterpret_cast<uintptr_t>(pos) & 3u) return SWA_ERR_ALIGNMENT;
+    if (required_bytes > 0) {
+        if (!workspace || workspace_bytes < required_bytes) return SWA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SWA_ERR_ALIGNMENT;
+    }
+    const size_t qb = static_cast<size_t>(cache->B) * Hq * cache->d * 2;
+    const size_t cb = static_cast<size_t>(cache->B) * cache->Hkv * cache->cap * cache->d * 2;
+    if (overlap(o, qb, q, qb) || overlap(o, qb, cache->k, cb) || overlap(o, qb, cache->v, cb))
+        return SWA_ERR_INVALID_ARG;
+    if (required_bytes > 0 && (overlap(workspace, required_bytes, o, qb) ||
+                               overlap(workspace, required_bytes, cache->k, cb) ||
+                               overlap(workspace, required_bytes, cache->v, cb)))
+        return SWA_ERR_INVALID_ARG;
+    return SWA_OK;
+}
+
+swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int L, int Hq, int Hkv, int d, int w, int s, swa_stream_t stream) {
+    const swa_status st = swa_check_prefill(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s);
+    if (st != SWA_OK || B == 0 || L == 0) return st;
+    return swa::prefill_launch(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, as_cuda(stream));
+}
+
+swa_status swa_cache_append(const swa_cache *cache, const void *k_new, const void *v_new, int n,
+                            int64_t pos0, swa_stream_t stream) {
+    const swa_status st = swa_check_append(cache, k_new, v_new, n, pos0);
+    if (st != SWA_OK) return st;
+    return swa::append_launch(*cache, k_new, v_new, n, pos0, as_cuda(stream));
+}
+
+size_t swa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, int w) {
+    if (B <= 0 || Hq < 1 || Hkv < 1 || cap < 1 || (d != 64 && d != 128)) return 0;
+    return swa::decode_plan(B, Hq, Hkv, d, cap, w, swa::device_sm_count()).workspace;
+}
+
+swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos, int Hq, int w,
+                      int s, void *o, void *workspace, size_t workspace_bytes,
+                      swa_stream_t stream) {
+    if (cache == nullptr) return SWA_ERR_INVALID_ARG;
+    const int sms = swa::device_sm_count();
+    if (sms <= 0) return SWA_ERR_CUDA;
+    const swa::DecodePlan plan =
+        swa::decode_plan(cache->B, Hq, cache->Hkv, cache->d, cache->cap, cache->w, sms);
+    const swa_status st =
+        swa_check_decode(q, cache, pos, Hq, w, s, o, workspace, workspace_bytes, plan.workspace);
+    if (st != SWA_OK || cache->B == 0) return st;
+    return swa::decode_launch(q, *cache, pos, Hq, o, workspace, plan, as_cuda(stream));
+}
+
+swa_status swa_get_device_error(swa_stream_t stream) {
+    const int a = swa::prefill_read_clear_error(as_cuda(stream));
+    const int b = swa::decode_read_clear_error(as_cuda(stream));
+    if (a == SWA_ERR_CUDA || b == SWA_ERR_CUDA) return SWA_ERR_CUDA;
+    if (a != 0) return static_cast<swa_status>(a);
+    return static_cast<swa_status>(b);
+}
+
+}  // extern "C"

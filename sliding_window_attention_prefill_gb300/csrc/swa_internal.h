@@ -1,0 +1,48 @@
+// swa_internal.h -- declarations shared by the library's translation units
+// (host side only; kernels stay private to their .cu file).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "swa.h"
+
+typedef CUresult (*cuTensorMapEncodeTiled_fn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                              void *, const cuuint64_t *, const cuuint64_t *,
+                                              const cuuint32_t *, const cuuint32_t *,
+                                              CUtensorMapInterleave, CUtensorMapSwizzle,
+                                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+namespace swa {
+
+// Driver entry point for tensor-map encoding (resolved once through the
+// runtime, so the library needs no link-time dependency on libcuda).
+cuTensorMapEncodeTiled_fn tensor_map_encoder();
+
+// Number of SMs of the current device (cached per device); <= 0 on error.
+int device_sm_count();
+
+// Decode work plan: how many key splits each (sequence, kv head) gets.
+struct DecodePlan {
+    int splits;          // >= 1
+    size_t workspace;    // bytes of fp32 partials (0 when splits == 1)
+};
+DecodePlan decode_plan(int B, int Hq, int Hkv, int d, int cap, int w, int sm_count);
+
+// Launchers (arguments already validated).
+swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream);
+swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_new, int n,
+                         int64_t pos0, cudaStream_t stream);
+swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,
+                         void *workspace, const DecodePlan &plan, cudaStream_t stream);
+
+// Read and clear each module's device error word (synchronises `stream`).
+// Returns 0 or a negative swa_status value.
+int prefill_read_clear_error(cudaStream_t stream);
+int decode_read_clear_error(cudaStream_t stream);
+
+}  // namespace swa

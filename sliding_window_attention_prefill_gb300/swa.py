@@ -1,0 +1,240 @@
+"""Python binding of libswa: argument marshalling over the C ABI in include/swa.h.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensor properties, passes raw device pointers and sizes, and uses
+the current torch stream.  If the library has not been built, every call
+raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+W_INF = -1
+
+_c_int = ctypes.c_int
+_c_i32 = ctypes.c_int32
+_c_i64 = ctypes.c_int64
+_c_size = ctypes.c_size_t
+_c_p = ctypes.c_void_p
+
+
+class SwaCacheStruct(ctypes.Structure):
+    """Mirror of ``swa_cache``."""
+    _fields_ = [("k", _c_p), ("v", _c_p), ("B", _c_i32), ("Hkv", _c_i32), ("d", _c_i32),
+                ("cap", _c_i32), ("w", _c_i32), ("s", _c_i32)]
+
+
+STATUS = {0: "SWA_OK", -1: "SWA_ERR_INVALID_ARG", -2: "SWA_ERR_UNSUPPORTED",
+          -3: "SWA_ERR_ALIGNMENT", -4: "SWA_ERR_WORKSPACE", -5: "SWA_ERR_CUDA",
+          -6: "SWA_ERR_TIMEOUT", -7: "SWA_ERR_BOUNDS"}
+
+
+def status_string(status: int) -> str:
+    return STATUS.get(int(status), f"SWA_ERR_UNKNOWN({status})")
+
+
+class SwaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _declare(L) -> None:
+    P = ctypes.POINTER
+    L.swa_prefill.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7 + [_c_p]
+    L.swa_prefill.restype = _c_int
+    L.swa_cache_append.argtypes = [P(SwaCacheStruct), _c_p, _c_p, _c_int, _c_i64, _c_p]
+    L.swa_cache_append.restype = _c_int
+    L.swa_decode_workspace_bytes.argtypes = [_c_int] * 6
+    L.swa_decode_workspace_bytes.restype = _c_size
+    L.swa_decode.argtypes = [_c_p, P(SwaCacheStruct), _c_p, _c_int, _c_int, _c_int, _c_p, _c_p,
+                             _c_size, _c_p]
+    L.swa_decode.restype = _c_int
+    L.swa_status_string.argtypes = [_c_int]
+    L.swa_status_string.restype = ctypes.c_char_p
+    L.swa_get_device_error.argtypes = [_c_p]
+    L.swa_get_device_error.restype = _c_int
+    L.swa_check_prefill.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
+    L.swa_check_prefill.restype = _c_int
+    L.swa_check_append.argtypes = [P(SwaCacheStruct), _c_p, _c_p, _c_int, _c_i64]
+    L.swa_check_append.restype = _c_int
+    L.swa_check_decode.argtypes = [_c_p, P(SwaCacheStruct), _c_p, _c_int, _c_int, _c_int, _c_p,
+                                   _c_p, _c_size, _c_size]
+    L.swa_check_decode.restype = _c_int
+    L.swa_cache_slot.argtypes = [_c_i64, _c_int, _c_int]
+    L.swa_cache_slot.restype = _c_i64
+    L.swa_version.argtypes = []
+    L.swa_version.restype = ctypes.c_char_p
+
+
+def lib():
+    """The loaded library (loaded once; raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"the CUDA library is not built ({path} missing): run "
+                "`python -m sliding_window_attention_prefill_gb300.build`")
+        L = ctypes.CDLL(path)
+        _declare(L)
+        _lib = L
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/swa.h declares."""
+    text = open(os.path.join(_build.INCLUDE, "swa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swa_[a-z_0-9]+)\s*\(", text)))
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise SwaError(status, what)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ----------------------------------------------------------------------------- prefill
+def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: int,
+            out: torch.Tensor | None = None, return_lse: bool = False):
+    """SWA(w,s) attention of every prompt position.
+
+    q [B, L, Hq, d], k/v [B, L, Hkv, d] bf16 CUDA tensors; returns o [B, L, Hq, d]
+    (and lse [B, Hq, L] fp32 if ``return_lse``).  ``w = W_INF`` is full causal.
+    """
+    _need(q, "q"), _need(k, "k"), _need(v, "v")
+    B, L, Hq, d = q.shape
+    if k.shape[:2] != (B, L) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    Hkv = k.shape[2]
+    o = torch.empty_like(q) if out is None else out
+    _need(o, "out")
+    if o.shape != q.shape:
+        raise ValueError("out must have the shape of q")
+    lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device) if return_lse else None
+    st = lib().swa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, L, Hq, Hkv, d,
+                           int(w), int(s), _stream(q.device))
+    _check(st, "swa_prefill")
+    return (o, lse) if return_lse else o
+
+
+# ----------------------------------------------------------------------------- cache
+class Cache:
+    """One layer's fixed SWA(w,s) cache: k, v bf16 [B, Hkv, cap, d] (torch-owned).
+
+    cap = w for a finite window (s sink slots + a (w-s)-slot ring), or
+    ``max_len`` for ``w = W_INF``.
+    """
+
+    def __init__(self, B: int, Hkv: int, d: int, w: int, s: int, max_len: int | None = None,
+                 device="cuda"):
+        if w == W_INF:
+            if not max_len:
+                raise ValueError("an infinite window needs max_len")
+            cap = int(max_len)
+        else:
+            cap = int(w)
+        self.B, self.Hkv, self.d, self.w, self.s, self.cap = B, Hkv, d, int(w), int(s), cap
+        self.k = torch.zeros(B, Hkv, cap, d, dtype=torch.bfloat16, device=device)
+        self.v = torch.zeros(B, Hkv, cap, d, dtype=torch.bfloat16, device=device)
+
+    @classmethod
+    def from_tensors(cls, k: torch.Tensor, v: torch.Tensor, w: int, s: int) -> "Cache":
+        _need(k, "cache k"), _need(v, "cache v")
+        obj = cls.__new__(cls)
+        obj.B, obj.Hkv, obj.cap, obj.d = k.shape
+        obj.w, obj.s, obj.k, obj.v = int(w), int(s), k, v
+        return obj
+
+    def struct(self) -> SwaCacheStruct:
+        return SwaCacheStruct(self.k.data_ptr(), self.v.data_ptr(), self.B, self.Hkv, self.d,
+                              self.cap, self.w, self.s)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int) -> None:
+        """Write positions pos0 .. pos0+n-1 from k_new/v_new [B, n, Hkv, d]."""
+        _need(k_new, "k_new"), _need(v_new, "v_new")
+        if (k_new.shape != v_new.shape or k_new.shape[0] != self.B
+                or tuple(k_new.shape[2:]) != (self.Hkv, self.d)):
+            raise ValueError(f"k_new/v_new must be [B, n, Hkv, d], got {tuple(k_new.shape)}")
+        c = self.struct()
+        st = lib().swa_cache_append(ctypes.byref(c), _ptr(k_new), _ptr(v_new), k_new.shape[1],
+                                    int(pos0), _stream(self.k.device))
+        _check(st, "swa_cache_append")
+
+
+# ----------------------------------------------------------------------------- decode
+_workspaces: dict = {}
+
+
+def decode_workspace_bytes(B: int, Hq: int, Hkv: int, d: int, cap: int, w: int) -> int:
+    return int(lib().swa_decode_workspace_bytes(B, Hq, Hkv, d, cap, w))
+
+
+def workspace_for(cache: "Cache", Hq: int) -> torch.Tensor | None:
+    """A (reused) device workspace large enough for decoding with this cache."""
+    n = decode_workspace_bytes(cache.B, Hq, cache.Hkv, cache.d, cache.cap, cache.w)
+    if n == 0:
+        return None
+    key = (cache.k.device, n)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.empty(n, dtype=torch.uint8, device=cache.k.device)
+        _workspaces[key] = ws
+    return ws
+
+
+def decode(q: torch.Tensor, cache: Cache, pos: torch.Tensor, out: torch.Tensor | None = None,
+           workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """One token per sequence: q [B, Hq, d] at positions pos [B] (int32, device)."""
+    _need(q, "q")
+    _need(pos, "pos", torch.int32)
+    B, Hq, d = q.shape
+    if B != cache.B or d != cache.d or pos.numel() != B:
+        raise ValueError("q / pos do not match the cache")
+    o = torch.empty_like(q) if out is None else out
+    _need(o, "out")
+    ws = workspace if workspace is not None else workspace_for(cache, Hq)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    c = cache.struct()
+    st = lib().swa_decode(_ptr(q), ctypes.byref(c), _ptr(pos), Hq, cache.w, cache.s, _ptr(o),
+                          _ptr(ws), nbytes, _stream(q.device))
+    _check(st, "swa_decode")
+    return o
+
+
+def device_error(device=None) -> int:
+    """Synchronise the current stream and read/clear the library's device error word."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return int(lib().swa_get_device_error(_stream(dev)))

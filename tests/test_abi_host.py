@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/swa.h declares, and rejects bad arguments before touching
+the device."""
+import ctypes
+
+import pytest
+
+import oracle
+from sliding_window_attention_prefill_gb300 import build as swa_build
+from sliding_window_attention_prefill_gb300 import swa
+
+OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE = 0, -1, -2, -3, -4
+INF = swa.W_INF
+
+
+@pytest.fixture(scope="module")
+def L():
+    swa_build.build()
+    return swa.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = swa.declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/swa.h but not exported"
+
+
+def test_version_and_status_strings(L):
+    assert L.swa_version().decode().count(".") == 2
+    for code, name in swa.STATUS.items():
+        assert L.swa_status_string(code).decode() == name
+    assert L.swa_status_string(-99).decode() == "SWA_ERR_UNKNOWN"
+
+
+FAKE = 0x10000  # an aligned, never dereferenced address
+
+
+def _p(off=0):
+    return ctypes.c_void_p(FAKE * (1 + off))
+
+
+def test_check_prefill(L):
+    q, k, v, o = _p(0), _p(1000), _p(2000), _p(3000)
+    c = L.swa_check_prefill
+    assert c(q, k, v, o, None, 1, 256, 4, 1, 64, 64, 4) == OK
+    assert c(q, k, v, o, None, 2, 4096, 32, 8, 128, INF, 0) == OK
+    assert c(None, None, None, None, None, 0, 10, 4, 1, 64, 64, 4) == OK      # empty batch
+    assert c(q, k, v, o, None, 1, 0, 4, 1, 64, 64, 4) == OK                   # empty prompt
+    assert c(q, k, v, o, None, 1, 256, 4, 1, 64, 4, 4) == INVALID             # w <= s
+    assert c(q, k, v, o, None, 1, 256, 4, 1, 64, 8, -1) == INVALID
+    assert c(q, k, v, o, None, 1, 256, 4, 1, 64, 0, 0) == INVALID
+    assert c(q, k, v, o, None, 1, 256, 4, 1, 64, -2, 0) == INVALID
+    assert c(q, k, v, o, None, 1, 256, 6, 4, 64, 64, 4) == INVALID            # Hq % Hkv
+    assert c(q, k, v, o, None, 1, 256, 6, 2, 64, 64, 4) == UNSUPPORTED        # G = 3
+    assert c(q, k, v, o, None, 1, 256, 4, 1, 96, 64, 4) == UNSUPPORTED        # d
+    assert c(q, k, v, o, None, 1, 256, 4, 1, 64, 128, 65) == UNSUPPORTED      # s > max sinks
+    assert c(None, k, v, o, None, 1, 256, 4, 1, 64, 64, 4) == INVALID
+    assert c(ctypes.c_void_p(FAKE + 8), k, v, o, None, 1, 256, 4, 1, 64, 64, 4) == ALIGN
+    assert c(q, k, v, q, None, 1, 256, 4, 1, 64, 64, 4) == INVALID           # o aliases q
+    assert c(q, k, v, o, ctypes.c_void_p(FAKE * 5000 + 2), 1, 256, 4, 1, 64, 64, 4) == ALIGN
+
+
+def _cache(B=2, Hkv=2, d=128, cap=64, w=64, s=4, k=None, v=None):
+    return swa.SwaCacheStruct(k if k is not None else FAKE * 10, v if v is not None else FAKE * 900,
+                              B, Hkv, d, cap, w, s)
+
+
+def test_check_append(L):
+    c = L.swa_check_append
+    kn, vn = _p(5000), _p(6000)
+    assert c(ctypes.byref(_cache()), kn, vn, 1, 4096) == OK
+    assert c(ctypes.byref(_cache()), kn, vn, 4096, 0) == OK                  # bulk prompt
+    assert c(ctypes.byref(_cache()), kn, vn, 0, 0) == OK
+    assert c(ctypes.byref(_cache()), kn, vn, -1, 0) == INVALID
+    assert c(ctypes.byref(_cache()), kn, vn, 1, -1) == INVALID
+    assert c(ctypes.byref(_cache(cap=65)), kn, vn, 1, 0) == INVALID          # cap != w
+    assert c(ctypes.byref(_cache(w=INF, s=0, cap=100)), kn, vn, 100, 0) == OK
+    assert c(ctypes.byref(_cache(w=INF, s=0, cap=100)), kn, vn, 1, 100) == INVALID  # past cap
+    assert c(ctypes.byref(_cache(d=80)), kn, vn, 1, 0) == UNSUPPORTED
+    assert c(ctypes.byref(_cache(k=FAKE * 10 + 4)), kn, vn, 1, 0) == ALIGN
+    assert c(None, kn, vn, 1, 0) == INVALID
+    assert c(ctypes.byref(_cache()), kn, ctypes.c_void_p(FAKE * 10), 1, 0) == INVALID  # aliases cache
+
+
+def test_check_decode(L):
+    c = L.swa_check_decode
+    q, pos, o, ws = _p(7000), _p(7100), _p(7200), _p(7300)
+    cache = _cache(B=2, Hkv=2, d=128, cap=64, w=64, s=4)
+    assert c(q, ctypes.byref(cache), pos, 8, 64, 4, o, None, 0, 0) == OK
+    assert c(q, ctypes.byref(cache), pos, 8, 64, 4, o, ws, 1024, 1024) == OK
+    assert c(q, ctypes.byref(cache), pos, 8, 64, 4, o, ws, 512, 1024) == WORKSPACE
+    assert c(q, ctypes.byref(cache), pos, 8, 64, 4, o, None, 0, 1024) == WORKSPACE
+    assert c(q, ctypes.byref(cache), pos, 8, 128, 4, o, None, 0, 0) == INVALID   # w differs
+    assert c(q, ctypes.byref(cache), pos, 8, 64, 3, o, None, 0, 0) == INVALID    # s differs
+    assert c(q, ctypes.byref(cache), pos, 7, 64, 4, o, None, 0, 0) == INVALID    # Hq % Hkv
+    assert c(q, ctypes.byref(cache), pos, 16, 64, 4, o, None, 0, 0) == UNSUPPORTED  # G = 8, d = 128
+    assert c(q, ctypes.byref(cache), ctypes.c_void_p(FAKE * 7100 + 2), 8, 64, 4, o, None, 0, 0) == ALIGN
+    assert c(q, ctypes.byref(cache), None, 8, 64, 4, o, None, 0, 0) == INVALID
+
+
+def test_slot_map_matches_oracle(L):
+    orc = oracle.get()
+    for w, s in [(64, 4), (512, 4), (9, 0), (5, 4), (INF, 0), (128, 64)]:
+        for p in range(0, 3 * (w if w > 0 else 50)):
+            assert L.swa_cache_slot(p, w, s) == orc.cache_slot(p, w, s), (w, s, p)
+    assert L.swa_cache_slot(-1, 64, 4) == -1
+    assert L.swa_cache_slot(3, 4, 4) == -1
