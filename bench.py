@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark of the SWA(w,s) hot path on GB300.
+
+One step = the whole path over one batch of synthetic input:
+  prefill of a 4096-token prompt (sliding-window attention with sinks, SWA(64,4),
+  Llama-3.1-8B attention shape: 32 query heads, 8 key/value heads, d = 128,
+  first 4 key rows x8), bulk append of the prompt's keys/values into a fixed
+  SWA(64,4) cache, then one decode token (append + decode).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl swa|reference]
+Under torchrun each rank runs its own batch on its own GPU (no data exchange;
+weak scaling) and rank 0 prints one JSON line.
+
+`value` is tokens/s of the whole step (prompt tokens + decoded tokens), device
+time from CUDA events on the launching stream, inputs resident in HBM, L2
+flushed (256 MiB write) before every timed step.  `e2e` is the same metric
+through the C ABI with pinned host buffers, copies inside the timed region.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORK = dict(B=1, L=4096, Hq=32, Hkv=8, d=128, w=64, s=4, sink_rows=4)
+METRIC = "SWA(w,4) decode tok/s + KV-read GB/s vs HBM peak; prefill TFLOP/s vs tensor peak"
+WORKLOAD_NAME = ("prefill SWA(64,4) B=1 L=4096 Hq=32 Hkv=8 d=128 (first 4 key rows x8) "
+                 "+ bulk cache append + 1 decode token")
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- arithmetic
+def window_sum(L: int, w: int) -> int:
+    """sum over t < L of |A(t)| = min(t+1, w) (w < 0: t+1)."""
+    if w < 0 or w >= L:
+        return L * (L + 1) // 2
+    return w * (w + 1) // 2 + (L - w) * w
+
+
+def prefill_flops(B, L, Hq, d, w) -> float:
+    return 4.0 * d * Hq * B * window_sum(L, w)
+
+
+def prefill_bytes(B, L, Hq, Hkv, d) -> float:
+    return 2.0 * (2 * B * L * Hq * d + 2 * B * L * Hkv * d)
+
+
+def decode_bytes(B, Hq, Hkv, d, n_valid) -> float:
+    return B * (2 * Hq * d * 2 + 4 * Hkv * d * 2 + 2 * Hkv * d * 2 * n_valid)
+
+
+def peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def prefill_traffic():
+    """dram bytes per prefill launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "prefill_traffic.json")
+    src = os.path.join(ROOT, "sliding_window_attention_prefill_gb300", "csrc", "swa_prefill.cu")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("kernel_sha256") == h and rec.get("workload") == WORKLOAD_NAME:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.4)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def result(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except Exception:
+                continue
+        inside = [r for r in rows if self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        used = inside if inside else rows
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in used:
+            for n, v in zip(names, r[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median([r[1] for r in used]) if used else None,
+                "sm_max_mhz": max(r[2] for r in used) if used else None,
+                "reasons": sorted(reasons), "samples": len(used),
+                "window": "timed region" if inside else "around the timed region"}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_step_rate(sample_positions: int, seed: int = 0):
+    """Time the oracle on the step restricted to `sample_positions` prompt
+    positions (all heads) + the decode token.  Returns (seconds, tokens)."""
+    import numpy as np
+
+    import oracle
+    from sliding_window_attention_prefill_gb300 import inputs
+    W = WORK
+    q, k, v = inputs.prefill_inputs(W["B"], W["L"], W["Hq"], W["Hkv"], W["d"], seed=seed,
+                                    sink_rows=W["sink_rows"])
+    orc = oracle.get()
+    qb, kb, vb = oracle.bf16_bits(q), oracle.bf16_bits(k), oracle.bf16_bits(v)
+    L = W["L"]
+    ts = np.linspace(0, L - 1, sample_positions).astype(np.int64)
+    rows = np.array([[b, t, h] for b in range(W["B"]) for t in ts for h in range(W["Hq"])], np.int64)
+    g = inputs.generator(seed + 1)
+    k1 = oracle.bf16_bits(inputs.normal_bf16((W["B"], 1, W["Hkv"], W["d"]), g))
+    v1 = oracle.bf16_bits(inputs.normal_bf16((W["B"], 1, W["Hkv"], W["d"]), g))
+    q1 = oracle.bf16_bits(inputs.normal_bf16((W["B"], W["Hq"], W["d"]), g))
+    hist_k = np.concatenate([kb, k1], axis=1)
+    hist_v = np.concatenate([vb, v1], axis=1)
+    ck = np.zeros((W["B"], W["Hkv"], W["w"], W["d"]), np.uint16)
+    cv = np.zeros_like(ck)
+
+    def run():
+        orc.prefill_rows(qb, kb, vb, rows, W["w"], W["s"])
+        orc.cache_append(ck, cv, kb, vb, 0, W["w"], W["s"])
+        orc.cache_append(ck, cv, k1, v1, L, W["w"], W["s"])
+        orc.decode_cache(q1, ck, cv, [L] * W["B"], W["w"], W["s"])
+
+    return run, W["B"] * (sample_positions + 1), orc, hist_k, hist_v
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    orc = oracle.get()
+    cores = orc.threads(None)
+    # size the sample so the whole run stays within ~2 minutes
+    calib_run, calib_tok, *_ = oracle_step_rate(64)
+    t = time.perf_counter()
+    calib_run()
+    per_pos = (time.perf_counter() - t) / 64
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    S = int(max(16, min(WORK["L"], budget / max(per_pos, 1e-9))))
+    run, tokens, *_ = oracle_step_rate(S)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t)
+    mean = sum(times) / len(times)
+    value = tokens / mean
+    sample = (f"{S} of {WORK['L']} prompt positions (all {WORK['Hq']} heads, evenly spaced) + "
+              f"the cache append + 1 decode token per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "oracle": "fp64 C, OpenMP over rows"},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_swa(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    import sliding_window_attention_prefill_gb300 as swa
+    from sliding_window_attention_prefill_gb300 import build, inputs
+
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    W = WORK
+    B, L, Hq, Hkv, d, w, s = W["B"], W["L"], W["Hq"], W["Hkv"], W["d"], W["w"], W["s"]
+    seed = 1000 * rank
+    q_h, k_h, v_h = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=seed, sink_rows=W["sink_rows"])
+    g = inputs.generator(seed + 1)
+    k1_h = inputs.normal_bf16((B, 1, Hkv, d), g)
+    v1_h = inputs.normal_bf16((B, 1, Hkv, d), g)
+    q1_h = inputs.normal_bf16((B, Hq, d), g)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    k1, v1, q1 = k1_h.to(dev), v1_h.to(dev), q1_h.to(dev)
+    o = torch.empty_like(q)
+    od = torch.empty_like(q1)
+    cache = swa.Cache(B, Hkv, d, w, s, device=dev)
+    pos = torch.full((B,), L, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def prefill_part():
+        swa.prefill(q, k, v, w, s, out=o)
+
+    def cache_decode_part():
+        cache.append(k, v, 0)
+        cache.append(k1, v1, L)
+        swa.decode(q1, cache, pos, out=od)
+
+    launches_per_step = 1 + 2 + 1 + (1 if swa.decode_workspace_bytes(B, Hq, Hkv, d, cache.cap, w) else 0)
+    stream = torch.cuda.current_stream(dev)
+    # warm up once outside capture (sets kernel attributes), then capture
+    prefill_part()
+    cache_decode_part()
+    torch.cuda.synchronize()
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(stream)
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(g1, stream=cs):
+            prefill_part()
+        with torch.cuda.graph(g2, stream=cs):
+            cache_decode_part()
+    stream.wait_stream(cs)
+    torch.cuda.synchronize()
+
+    # flush time, to stretch the timed region so clock samples land in it
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_a.record()
+    for _ in range(5):
+        flush.fill_(1)
+    ev_b.record()
+    torch.cuda.synchronize()
+    t_flush = ev_a.elapsed_time(ev_b) / 5e3
+    flush_reps = max(1, math.ceil((0.6 / max(args.steps, 1)) / max(t_flush, 1e-6)))
+    flush_reps = min(flush_reps, 64)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        g1.replay()
+        g2.replay()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    for i in range(args.steps):
+        for _ in range(flush_reps):
+            flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        g1.replay()
+        ev[i][1].record()
+        g2.replay()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    if sampler:
+        sampler.mark_end()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    mean_step = sum(step_ms) / len(step_ms)
+    mean_pre = sum(pre_ms) / len(pre_ms)
+    mean_dec = sum(dec_ms) / len(dec_ms)
+
+    # ---- end to end: pinned host buffers, copies inside the timed region
+    host = {n: t.pin_memory() for n, t in
+            dict(q=q_h, k=k_h, v=v_h, k1=k1_h, v1=v1_h, q1=q1_h).items()}
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    od_host = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * 2 + od_host.numel() * 2
+
+    def e2e_step():
+        q.copy_(host["q"], non_blocking=True)
+        k.copy_(host["k"], non_blocking=True)
+        v.copy_(host["v"], non_blocking=True)
+        k1.copy_(host["k1"], non_blocking=True)
+        v1.copy_(host["v1"], non_blocking=True)
+        q1.copy_(host["q1"], non_blocking=True)
+        swa.prefill(q, k, v, w, s, out=o)
+        cache.append(k, v, 0)
+        cache.append(k1, v1, L)
+        swa.decode(q1, cache, pos, out=od)
+        o_host.copy_(o, non_blocking=True)
+        od_host.copy_(od, non_blocking=True)
+
+    for _ in range(max(3, min(args.warmup, 10))):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 200))
+    e2e_ms = []
+    for i in range(n_e2e):
+        flush.fill_(i & 0xFF)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        e2e_step()
+        b_.record()
+        b_.synchronize()
+        e2e_ms.append(a.elapsed_time(b_))
+    mean_e2e = sum(e2e_ms) / len(e2e_ms)
+
+    # ---- max over ranks
+    if world > 1:
+        t = torch.tensor([mean_step, mean_pre, mean_dec, mean_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_step, mean_pre, mean_dec, mean_e2e = t.tolist()
+
+    if rank != 0:
+        return
+    tokens = B * (L + 1) * world
+    value = tokens / (mean_step * 1e-3)
+    pk = peaks()
+    pbytes = prefill_bytes(B, L, Hq, Hkv, d)
+    pflops = prefill_flops(B, L, Hq, d, w)
+    n_valid = min(L + 1, w)
+    dbytes = decode_bytes(B, Hq, Hkv, d, n_valid)
+    achieved_gbs = pbytes / (mean_pre * 1e-3) / 1e9
+    tflops = pflops / (mean_pre * 1e-3) / 1e12
+    clocks = sampler.result() if sampler else None
+    cpu = None
+    if world == 1:
+        cpu = cpu_baseline()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "global_batch": B * world, "seq_len": L,
+                   "window": w, "sinks": s, "l2": f"flushed before each step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "timing": "CUDA events around CUDA-graph replays of the step"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"],
+                     "traffic": prefill_traffic(), "kernel": "swa_prefill_kernel",
+                     "algorithmic_bytes_per_launch": pbytes,
+                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
+        "prefill": {"ms": mean_pre, "tflops": tflops, "frac_tensor_peak": tflops / pk["bf16_tflops"],
+                    "gbs": achieved_gbs, "algorithmic_gflop": pflops / 1e9},
+        "decode": {"ms_append_and_decode": mean_dec, "tok_s": B * world / (mean_dec * 1e-3),
+                   "kv_bytes": dbytes, "note": "one token after the prompt; B=1 is latency-bound"},
+        "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e},
+        "clocks": clocks,
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline() -> dict:
+    """The oracle on a bounded sample of the same step (about 10-20 s of CPU work)."""
+    import oracle
+    oracle.build()
+    S = 512
+    run, tokens, orc, *_ = oracle_step_rate(S)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run()
+        n += 1
+        if time.perf_counter() - t0 > 10.0 or n >= 50:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": tokens / dt, "unit": "tok/s", "cores": orc.threads(None), "kind": "oracle",
+            "sample": f"{S} of {WORK['L']} prompt positions (all heads) + cache append + 1 decode "
+                      f"token per step, {n} steps"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["swa", "reference"], default="swa")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_swa(args, rank, world, local_rank)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
