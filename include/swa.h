@@ -153,6 +153,38 @@ swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos,
                       int w, int s, void *o, void *workspace, size_t workspace_bytes,
                       swa_stream_t stream);
 
+/* Size of the device scratch built into the library for swa_decode_noalloc. */
+#define SWA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * swa_decode_noalloc -- swa_decode for callers that cannot allocate device
+ * memory.  The paper has no counterpart; this is a convenience of the library.
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocator -- for
+ * instance a plugin whose host framework owns all device memory and hands it
+ * only the input and output buffers, or a latency-critical serving loop that
+ * must not risk the device-wide synchronisation or failure an allocation can
+ * bring.  Such callers cannot provide the workspace swa_decode asks for.
+ *
+ * Same arguments and result as swa_decode, minus the workspace: the split
+ * partials go to a device array of SWA_NOALLOC_SCRATCH_BYTES that the library
+ * defines at file scope, so every GPU that loads the library holds those 4 MiB
+ * until the process exits.  Nothing is allocated and no allocating routine is
+ * called.  The first call on each device looks up the array's device address
+ * (once, with that device current); make that first call before any stream
+ * capture.  If the decode plan for the shape needs more scratch than
+ * SWA_NOALLOC_SCRATCH_BYTES, returns SWA_ERR_WORKSPACE before launching
+ * anything (on a 152-SM GB300 every supported shape fits).
+ *
+ * All calls share the one array and it keeps whatever the last call wrote;
+ * nothing in it needs to start at zero (each call writes every partial it
+ * reads).  Calls whose work overlaps on the GPU -- on different streams, or
+ * on different host threads without ordering -- race on the array: keep them
+ * ordered, e.g. on one stream.
+ */
+swa_status swa_decode_noalloc(const void *q, const swa_cache *cache, const int32_t *pos, int Hq,
+                              int w, int s, void *o, swa_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *swa_status_string(swa_status status);
 

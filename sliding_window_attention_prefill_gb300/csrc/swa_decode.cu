@@ -27,6 +27,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "swa_internal.h"
 #include "swa_ptx.cuh"
@@ -496,4 +497,51 @@ int decode_read_clear_error(cudaStream_t stream) {
     return v;
 }
 
+// ---------------------------------------------------------------------------
+// decode without a caller-provided workspace (swa_decode_noalloc)
+// ---------------------------------------------------------------------------
+// Split partials for callers that cannot allocate: a fixed device array owned
+// by the library.  Host code must not use the symbol itself as an address;
+// noalloc_scratch() looks the device address up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SWA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device (looked up once
+// per device, with that device current); nullptr if the lookup fails.
+void *noalloc_scratch() {
+    static void *addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
 }  // namespace swa
+
+extern "C" swa_status swa_decode_noalloc(const void *q, const swa_cache *cache, const int32_t *pos,
+                                         int Hq, int w, int s, void *o, swa_stream_t stream) {
+    if (cache == nullptr) return SWA_ERR_INVALID_ARG;
+    const int sms = swa::device_sm_count();
+    if (sms <= 0) return SWA_ERR_CUDA;
+    const swa::DecodePlan plan =
+        swa::decode_plan(cache->B, Hq, cache->Hkv, cache->d, cache->cap, cache->w, sms);
+    if (plan.workspace > SWA_NOALLOC_SCRATCH_BYTES) return SWA_ERR_WORKSPACE;
+    void *ws = nullptr;
+    if (plan.workspace > 0) {
+        ws = swa::noalloc_scratch();
+        if (ws == nullptr) return SWA_ERR_CUDA;
+    }
+    const swa_status st = swa_check_decode(q, cache, pos, Hq, w, s, o, ws,
+                                           SWA_NOALLOC_SCRATCH_BYTES, plan.workspace);
+    if (st != SWA_OK || cache->B == 0) return st;
+    return swa::decode_launch(q, *cache, pos, Hq, o, ws, plan, reinterpret_cast<cudaStream_t>(stream));
+}
