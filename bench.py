@@ -86,6 +86,25 @@ def prefill_traffic():
     return None
 
 
+# ----------------------------------------------------------------------------- ranks
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own batch (weak scaling: independent sequences)."""
+    return 1000 * rank
+
+
+def tokens_per_step(world: int) -> int:
+    """Tokens all ranks process in one step: every rank's prompt + decoded token."""
+    return WORK["B"] * (WORK["L"] + 1) * world
+
+
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (the slowest rank sets the pace)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -225,7 +244,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     W = WORK
     B, L, Hq, Hkv, d, w, s = W["B"], W["L"], W["Hq"], W["Hkv"], W["d"], W["w"], W["s"]
-    seed = 1000 * rank
+    seed = rank_seed(rank)
     q_h, k_h, v_h = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=seed, sink_rows=W["sink_rows"])
     g = inputs.generator(seed + 1)
     k1_h = inputs.normal_bf16((B, 1, Hkv, d), g)
@@ -347,13 +366,12 @@ def run_swa(args, rank: int, world: int, local_rank: int):
 
     # ---- max over ranks
     if world > 1:
-        t = torch.tensor([mean_step, mean_pre, mean_dec, mean_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_step, mean_pre, mean_dec, mean_e2e = t.tolist()
+        mean_step, mean_pre, mean_dec, mean_e2e = max_over_ranks(
+            [mean_step, mean_pre, mean_dec, mean_e2e], dev)
 
     if rank != 0:
         return
-    tokens = B * (L + 1) * world
+    tokens = tokens_per_step(world)
     value = tokens / (mean_step * 1e-3)
     pk = peaks()
     pbytes = prefill_bytes(B, L, Hq, Hkv, d)

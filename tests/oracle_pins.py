@@ -281,6 +281,21 @@ def pin_decode_cache(orc) -> None:
         assert np.abs(a - b).max() < 1e-12, (w, s, P)
 
 
+def pin_rows_match_full(orc) -> None:
+    """The selected-rows entry gives the same rows as the full prefill (so the
+    sampled parity checks at full size inherit the full prefill's pins)."""
+    rng = np.random.default_rng(7)
+    B, L, Hq, Hkv, d, w, s = 2, 45, 8, 2, 16, 10, 3
+    q = _rand_bits(rng, (B, L, Hq, d))
+    k = _rand_bits(rng, (B, L, Hkv, d))
+    v = _rand_bits(rng, (B, L, Hkv, d))
+    o, lse = orc.prefill(q, k, v, w, s, threads=2)
+    rows = np.array([[b, t, h] for b in range(B) for t in (0, 2, 9, 10, 44) for h in (0, 5, 7)])
+    ro, rl = orc.prefill_rows(q, k, v, rows, w, s, threads=2)
+    assert np.array_equal(ro, o[rows[:, 0], rows[:, 1], rows[:, 2]])
+    assert np.array_equal(rl, lse[rows[:, 0], rows[:, 2], rows[:, 1]])
+
+
 ALL_PINS = [pin_golden_sets, pin_window_size, pin_brute_force, pin_causal_library,
             pin_closed_forms, pin_equal_values, pin_decode_history, pin_golden_cache,
-            pin_ring_mapping, pin_decode_cache]
+            pin_ring_mapping, pin_decode_cache, pin_rows_match_full]
