@@ -429,13 +429,120 @@ def cpu_baseline() -> dict:
                       f"token per step, {n} steps"}
 
 
+# ----------------------------------------------------------------------------- suites
+def _time_graph(fn, steps: int, flush, warm: int = 3) -> float:
+    """Mean ms of `fn` replayed as a CUDA graph, L2 flushed before each replay."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(warm):
+        flush.fill_(1)
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        g.replay()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
+    """Prefill kernel alone on the prefill configs: B=1 L=4096 SWA(64,4) and
+    B=2 L=32768 SWA(w,4) for w in {128, 256, 512} (Hq=32, Hkv=8, d=128).
+    only_w / B_ / L_ restrict or resize the list (smaller cases for ncu)."""
+    import torch
+
+    import sliding_window_attention_prefill_gb300 as swa
+    from sliding_window_attention_prefill_gb300 import build, inputs
+    build.build()
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    cases = [(1, 4096, 64, 4), (2, 32768, 128, 0), (2, 32768, 256, 0), (2, 32768, 512, 0)]
+    if only_w is not None:
+        cases = [c for c in cases if c[2] == only_w]
+    cases = [(B_ or c[0], L_ or c[1], c[2], c[3]) for c in cases]
+    for B, L, w, sink_rows in cases:
+        Hq, Hkv, d, s = 32, 8, 128, 4
+        q, k, v = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=0, sink_rows=sink_rows)
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        o = torch.empty_like(q)
+        ms = _time_graph(lambda: swa.prefill(q, k, v, w, s, out=o), steps, flush)
+        fl, by = prefill_flops(B, L, Hq, d, w), prefill_bytes(B, L, Hq, Hkv, d)
+        tf = fl / (ms * 1e-3) / 1e12
+        attainable = min(pk["bf16_tflops"], fl / by * pk["hbm_gbs"] / 1e3)
+        print(json.dumps({"suite": "prefill", "B": B, "L": L, "w": w, "s": s, "ms": ms,
+                          "tflops": tf, "frac_tensor_peak": tf / pk["bf16_tflops"],
+                          "frac_attainable": tf / attainable, "attainable_tflops": attainable,
+                          "gbs": by / (ms * 1e-3) / 1e9, "flop_per_byte": fl / by}), flush=True)
+        del q, k, v, o
+        torch.cuda.empty_cache()
+
+
+def suite_decode(steps: int):
+    """Decode step (append one token + decode) at B=64, Hq=32, Hkv=8, d=128,
+    SWA(w,4) for w in {64, 512}, after a 4096-token prompt, L2 flushed."""
+    import torch
+
+    import sliding_window_attention_prefill_gb300 as swa
+    from sliding_window_attention_prefill_gb300 import build, inputs
+    build.build()
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    B, Hq, Hkv, d, s, prompt = 64, 32, 8, 128, 4, 4096
+    for w in (64, 512):
+        kp, vp, ks, vs, qs = inputs.decode_stream(B, Hq, Hkv, d, prompt, 1, seed=0)
+        c = swa.Cache(B, Hkv, d, w, s)
+        c.append(kp.cuda(), vp.cuda(), 0)
+        k1, v1, q1 = ks[0].cuda(), vs[0].cuda(), qs[0].cuda()
+        pos = torch.full((B,), prompt, dtype=torch.int32, device="cuda")
+        od = torch.empty_like(q1)
+        ws = swa.workspace_for(c, Hq)
+
+        def step():
+            c.append(k1, v1, prompt)
+            swa.decode(q1, c, pos, out=od, workspace=ws)
+
+        ms = _time_graph(step, steps, flush)
+        ms_dec = _time_graph(lambda: swa.decode(q1, c, pos, out=od, workspace=ws), steps, flush)
+        n_valid = min(prompt + 1, w)
+        by = decode_bytes(B, Hq, Hkv, d, n_valid)
+        kv = 2 * B * Hkv * d * 2 * n_valid
+        print(json.dumps({"suite": "decode", "B": B, "w": w, "s": s, "pos": prompt,
+                          "ms_step": ms, "tok_s": B / (ms * 1e-3), "ms_decode": ms_dec,
+                          "kv_read_gbs": kv / (ms_dec * 1e-3) / 1e9,
+                          "frac_hbm": by / (ms_dec * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "bytes_decode": by}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["swa", "reference"], default="swa")
+    ap.add_argument("--suite", choices=["prefill", "decode"], default=None,
+                    help="auxiliary per-config lines instead of the headline step")
+    ap.add_argument("--w", type=int, default=None, help="prefill suite: only this window")
+    ap.add_argument("--B", type=int, default=None, help="prefill suite: batch override")
+    ap.add_argument("--L", type=int, default=None, help="prefill suite: length override")
     args = ap.parse_args()
+    if args.suite == "prefill":
+        suite_prefill(max(args.steps // 10, 10), args.w, args.B, args.L)
+        return
+    if args.suite == "decode":
+        suite_decode(max(args.steps // 4, 20))
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -185,6 +185,13 @@ swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos,
 swa_status swa_decode_noalloc(const void *q, const swa_cache *cache, const int32_t *pos, int Hq,
                               int w, int s, void *o, swa_stream_t stream);
 
+/*
+ * swa_last_cuda_error -- name and description of the CUDA error behind the
+ * most recent SWA_ERR_CUDA returned to the calling thread ("" if none).
+ * Diagnostic only; static or thread-local storage owned by the library.
+ */
+const char *swa_last_cuda_error(void);
+
 /* Human-readable name of a status code (static storage). */
 const char *swa_status_string(swa_status status);
 

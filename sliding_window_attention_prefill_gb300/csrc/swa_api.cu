@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -24,6 +25,18 @@ cuTensorMapEncodeTiled_fn tensor_map_encoder() {
     });
     return fn;
 }
+
+namespace {
+thread_local char g_last_cuda[256] = "";
+}
+
+swa_status cuda_fail(cudaError_t e, const char *where) {
+    std::snprintf(g_last_cuda, sizeof(g_last_cuda), "%s: %s (%s)", where, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return SWA_ERR_CUDA;
+}
+
+const char *last_cuda_error() { return g_last_cuda; }
 
 int device_sm_count() {
     static int cached[64] = {};
@@ -85,6 +98,8 @@ cudaStream_t as_cuda(swa_stream_t s) { return reinterpret_cast<cudaStream_t>(s);
 extern "C" {
 
 const char *swa_version(void) { return "0.1.0"; }
+
+const char *swa_last_cuda_error(void) { return swa::last_cuda_error(); }
 
 const char *swa_status_string(swa_status st) {
     switch (st) {
@@ -205,7 +220,7 @@ swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos,
                       swa_stream_t stream) {
     if (cache == nullptr) return SWA_ERR_INVALID_ARG;
     const int sms = swa::device_sm_count();
-    if (sms <= 0) return SWA_ERR_CUDA;
+    if (sms <= 0) return swa::cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const swa::DecodePlan plan =
         swa::decode_plan(cache->B, Hq, cache->Hkv, cache->d, cache->cap, cache->w, sms);
     const swa_status st =

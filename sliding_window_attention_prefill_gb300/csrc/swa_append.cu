@@ -8,10 +8,11 @@
 // post-training, just 4 more tokens", section "Research method").
 //
 // A bulk append of n > w-s positions maps several of them to one ring slot;
-// only the latest of them (p + (w-s) >= pos0 + n) is written, so the result is
-// the same as appending one position at a time and no two threads write the
-// same slot.  Pure copy: 16-byte vectors, one per thread-iteration,
-// coalesced on both sides.
+// only the survivors are written -- the sinks among the new positions and
+// the latest w-s of them -- so the result is the same as appending one
+// position at a time, no two threads write the same slot, and a long prompt
+// costs O(w) rather than O(n).  Pure copy: 16-byte vectors, one per
+// thread-iteration, coalesced on both sides.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -27,31 +28,28 @@ struct AppendParams {
     uint4 *cv;
     int64_t pos0;
     int B, n, Hkv, vpr, cap, w, s;  // vpr: 16-byte vectors per row (d / 8)
+    int a, b0;  // surviving new positions: j in [0, a) and j in [b0, n)
 };
 
 __global__ void __launch_bounds__(256) swa_append_kernel(const AppendParams p) {
-    const int64_t total = static_cast<int64_t>(p.B) * p.n * p.Hkv * p.vpr;
-    const int64_t last = p.pos0 + p.n;  // one past the last position written
+    const int m = p.a + (p.n - p.b0);  // surviving positions per sequence
+    const int64_t total = static_cast<int64_t>(p.B) * m * p.Hkv * p.vpr;
     for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = idx / p.vpr;           // (b * n + j) * Hkv + h
+        const int64_t r = idx / p.vpr;           // (b * m + jj) * Hkv + h
         const int vec = static_cast<int>(idx - r * p.vpr);
         const int h = static_cast<int>(r % p.Hkv);
         const int64_t bj = r / p.Hkv;
-        const int j = static_cast<int>(bj % p.n);
-        const int b = static_cast<int>(bj / p.n);
+        const int jj = static_cast<int>(bj % m);
+        const int b = static_cast<int>(bj / m);
+        const int j = jj < p.a ? jj : p.b0 + (jj - p.a);
         const int64_t pos = p.pos0 + j;
-        int64_t slot;
-        if (p.w < 0 || pos < p.s) {
-            slot = pos;
-        } else {
-            const int64_t ring = p.w - p.s;
-            if (pos + ring < last) continue;  // overwritten later in this same append
-            slot = p.s + (pos - p.s) % ring;
-        }
+        const int64_t slot =
+            (p.w < 0 || pos < p.s) ? pos : p.s + (pos - p.s) % static_cast<int64_t>(p.w - p.s);
+        const int64_t src = ((static_cast<int64_t>(b) * p.n + j) * p.Hkv + h) * p.vpr + vec;
         const int64_t dst = ((static_cast<int64_t>(b) * p.Hkv + h) * p.cap + slot) * p.vpr + vec;
-        p.ck[dst] = p.k_new[idx];
-        p.cv[dst] = p.v_new[idx];
+        p.ck[dst] = p.k_new[src];
+        p.cv[dst] = p.v_new[src];
     }
 }
 
@@ -71,13 +69,26 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
     p.cap = c.cap;
     p.w = c.w < 0 ? -1 : c.w;
     p.s = c.w < 0 ? 0 : c.s;
-    const int64_t total = static_cast<int64_t>(p.B) * n * p.Hkv * p.vpr;
+    if (p.w < 0) {
+        p.a = n;  // every position keeps its own slot
+        p.b0 = n;
+    } else {
+        // sinks among the new positions, then the latest w-s of them
+        const int64_t a = p.s - pos0;
+        p.a = static_cast<int>(a < 0 ? 0 : (a > n ? n : a));
+        const int64_t b0 = static_cast<int64_t>(n) - (p.w - p.s);
+        p.b0 = static_cast<int>(b0 < p.a ? p.a : b0);
+    }
+    const int m = p.a + (n - p.b0);
+    const int64_t total = static_cast<int64_t>(p.B) * m * p.Hkv * p.vpr;
+    if (total == 0) return SWA_OK;
     const int sms = device_sm_count();
     int64_t blocks = (total + 255) / 256;
     const int64_t max_blocks = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;
     if (blocks > max_blocks) blocks = max_blocks;
     swa_append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-    return cudaPeekAtLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    const cudaError_t e = cudaPeekAtLastError();
+    return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_append_kernel");
 }
 
 }  // namespace swa

@@ -425,21 +425,24 @@ template <int D, int G>
 swa_status launch_decode(const DecodeParams &p, cudaStream_t stream) {
     using SL = DecSmem<D, G>;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
-        if (cudaFuncSetAttribute(swa_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SL::kBytes) != cudaSuccess)
-            return SWA_ERR_CUDA;
+        e = cudaFuncSetAttribute(swa_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SL::kBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode)");
         configured[dev] = true;
     }
     dim3 grid(p.splits, p.Hkv, p.B);
     swa_decode_kernel<D, G><<<grid, kDecThreads, SL::kBytes, stream>>>(p);
-    if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_kernel");
     if (p.splits > 1) {
         const int rows = p.B * p.Hq;
         swa_decode_merge_kernel<D><<<(rows + 3) / 4, 128, 0, stream>>>(p);
-        if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
+        e = cudaPeekAtLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_merge_kernel");
     }
     return SWA_OK;
 }

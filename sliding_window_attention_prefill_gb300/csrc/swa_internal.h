@@ -40,6 +40,11 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
 swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,
                          void *workspace, const DecodePlan &plan, cudaStream_t stream);
 
+// Record the CUDA error behind an SWA_ERR_CUDA (per host thread) and return
+// SWA_ERR_CUDA; `where` names the failing call.
+swa_status cuda_fail(cudaError_t e, const char *where);
+const char *last_cuda_error();
+
 // Read and clear each module's device error word (synchronises `stream`).
 // Returns 0 or a negative swa_status value.
 int prefill_read_clear_error(cudaStream_t stream);

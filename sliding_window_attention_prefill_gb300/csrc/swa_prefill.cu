@@ -10,22 +10,28 @@
 // tile).  Its 128 MMA rows pack the G = Hq/Hkv query heads that share kvh for
 // P = 128/G consecutive positions: row r is position t0 + r/G, head
 // kvh*G + r%G, which is exactly a box of the [B, L, Hq, d] query tensor, so
-// one TMA box loads it and one TMA box stores the output.  The unit needs the
-// sink keys [0, s) and the band [lo, t1] with lo = max(s, t0-(w-s)+1): the
-// key columns are laid out as [s_pad sink rows | band ...] in 128-column key
-// tiles, the sink block (s rounded up to 8 rows) sharing the first tile.
+// one TMA box loads it.  The unit needs the sink keys [0, s) and the band
+// [lo, t1] with lo = max(s, t0-(w-s)+1): the key columns are laid out as
+// [s_pad sink rows | band ...] in 128-column key tiles, the sink block (s
+// rounded up to 8 rows) sharing the first tile.
 //
-// Roles (192 threads, one persistent CTA per SM):
-//   warp 0      TMA producer: Q (double-buffered), K/V key tiles (NS stages)
-//   warp 1      tcgen05 issuer; owns the 512-column TMEM allocation
-//               S0 | S1 (double-buffered scores) | O (output accumulator)
-//   warps 2..5  softmax + epilogue, one thread per MMA row (TMEM lane)
-// Per key tile g the MMA warp issues S_g = Q K_g^T, then O += P_{g-1} V_{g-1},
-// so the scores of the next tile are computed while the softmax of the
-// current one runs.  P is written to shared memory in the 128-byte-swizzled
-// K-major layout the MMA reads.  The running max is only raised when it grows
-// by more than 2^8 (exact: numerator and denominator share the same stale
-// max), so the O rescale through TMEM is rare.
+// Roles (320 threads, one persistent CTA per SM):
+//   warp 0       TMA producer: Q (one buffer per softmax warpgroup), K tiles
+//                (NSK-slot ring), V tiles (NSV-slot ring)
+//   warp 1       tcgen05 issuer; owns the 512-column TMEM allocation
+//                S_A | S_B | O_A | O_B
+//   warps 2..5   softmax warpgroup A, warps 6..9 softmax warpgroup B: each
+//                takes every other work unit of the CTA, one thread per MMA
+//                row (TMEM lane)
+// The two warpgroups ping-pong on the tensor cores: while A runs the softmax
+// of its tile, the MMA warp computes B's O += P V and next S = Q K^T, and
+// vice versa.  A warpgroup writes P (bf16) over the first 64 columns of its
+// own S and the P V product reads it from tensor memory (tcgen05.mma with the
+// A operand in TMEM); the next S of that warpgroup is issued after that P V
+// by the same thread, and tcgen05 MMAs of one thread execute in issue order.
+// The running max is only raised when it grows by more than 2^8 (exact:
+// numerator and denominator share the same stale max), so the O rescale
+// through TMEM is rare.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -41,7 +47,7 @@ namespace swa {
 __device__ int g_prefill_error;
 
 struct PrefillMaps {
-    CUtensorMap q, o;                 // box {64, G, P, 1} over [B, L, Hq, d]
+    CUtensorMap q;                    // box {64, G, P, 1} over [B, L, Hq, d]
     CUtensorMap k_band, v_band;       // box {64, 1, 128, 1} over [B, L, Hkv, d]
     CUtensorMap k_sink, v_sink;       // box {64, 1, s_pad, 1}
     CUtensorMap k_band0, v_band0;     // box {64, 1, 128 - s_pad, 1}
@@ -54,6 +60,7 @@ struct PrefillParams {
     int n_qtiles, n_units;
     float scale_log2;         // log2(e) / sqrt(d)
     float scale;              // 1 / sqrt(d)
+    uint16_t *o;              // [B, L, Hq, d] bf16
     float *lse;               // optional [B, Hq, L]
 };
 
@@ -86,33 +93,57 @@ __device__ __forceinline__ int tile_width(const Unit &x, int j) {
     return (n + 15) & ~15;
 }
 
-template <int D, int NS>
+// The sequence of key tiles one softmax warpgroup works through: the CTA's
+// units u = blockIdx.x + (2k + wg) * gridDim.x, k = 0, 1, ..., each split
+// into its key tiles.
+struct TileStream {
+    int k, u, j;
+    bool valid;
+    Unit x;
+    __device__ __forceinline__ void init(int wg, const PrefillParams &p) {
+        k = 0;
+        j = 0;
+        u = blockIdx.x + wg * gridDim.x;
+        valid = u < p.n_units;
+        if (valid) x = unit_geom(u, p);
+    }
+    __device__ __forceinline__ void next(const PrefillParams &p) {
+        if (++j >= x.n_tiles) {
+            j = 0;
+            ++k;
+            u += 2 * gridDim.x;
+            valid = u < p.n_units;
+            if (valid) x = unit_geom(u, p);
+        }
+    }
+};
+
+template <int D, int NSK, int NSV>
 struct PrefillSmem {
     static constexpr int kRegion = 128 * 128;           // one 64-column slab of 128 rows
-    static constexpr int kQBytes = 128 * D * 2;         // Q / K / V tile bytes
-    static constexpr int kQ = 0;                        // 2 Q buffers
-    static constexpr int kK = kQ + 2 * kQBytes;         // NS K stages
-    static constexpr int kV = kK + NS * kQBytes;        // NS V stages
-    static constexpr int kP = kV + NS * kQBytes;        // P (2 slabs), also O staging
-    static constexpr int kBar = kP + 2 * kRegion;       // mbarriers
+    static constexpr int kTile = 128 * D * 2;           // Q / K / V tile bytes
+    static constexpr int kQ = 0;                        // Q buffer per warpgroup
+    static constexpr int kK = kQ + 2 * kTile;           // K ring
+    static constexpr int kV = kK + NSK * kTile;         // V ring
+    static constexpr int kBar = kV + NSV * kTile;       // mbarriers
     // barrier slots (8 bytes each)
-    static constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kVFull = 4 + NS,
-                         kKVEmpty = 4 + 2 * NS, kSFull = 4 + 3 * NS, kSEmpty = 6 + 3 * NS,
-                         kPFull = 8 + 3 * NS, kPVDone = 9 + 3 * NS, kNumBars = 10 + 3 * NS;
+    static constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = 4 + NSK,
+                         kVFull = 4 + 2 * NSK, kVEmpty = 4 + 2 * NSK + NSV,
+                         kSFull = 4 + 2 * NSK + 2 * NSV, kPFull = kSFull + 2, kODone = kPFull + 2,
+                         kNumBars = kODone + 2;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;        // room to align the base to 1024
 };
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;
 
-template <int D, int NS>
+template <int D, int NSK, int NSV>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
-    using SL = PrefillSmem<D, NS>;
+    using SL = PrefillSmem<D, NSK, NSV>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -126,9 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SL::kNumBars; ++i) {
-            uint32_t cnt = 1;
-            if (i == SL::kSEmpty || i == SL::kSEmpty + 1 || i == SL::kPFull) cnt = 4;
-            mbar_init(bar(i), cnt);
+            const bool four = (i == SL::kPFull || i == SL::kPFull + 1);
+            mbar_init(bar(i), four ? 4u : 1u);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -148,160 +178,196 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&maps.q);
             tma_prefetch_desc(&maps.k_band);
             tma_prefetch_desc(&maps.v_band);
-            constexpr uint32_t kTileBytes = SL::kQBytes;
-            uint32_t g = 0, uc = 0;
+            constexpr uint32_t kBytes = SL::kTile;
+            TileStream st[2];
+            st[0].init(0, p);
+            st[1].init(1, p);
+            uint32_t gi = 0;  // global tile index, in the order the MMA warp issues S
+            uint32_t nq[2] = {0, 0};
             bool ok = true;
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
-                const Unit x = unit_geom(u, p);
-                const uint32_t qb = uc & 1;
-                ok = mbar_wait(bar(SL::kQEmpty + qb), ((uc >> 1) & 1) ^ 1, &g_prefill_error,
-                               abort_flag);
-                if (!ok) break;
-                const uint32_t qdst = base + SL::kQ + qb * SL::kQBytes;
-                mbar_arrive_expect_tx(bar(SL::kQFull + qb), kTileBytes);
+            while (ok && (st[0].valid || st[1].valid)) {
+                for (int wg = 0; wg < 2 && ok; ++wg) {
+                    if (!st[wg].valid) continue;
+                    const Unit &x = st[wg].x;
+                    const int j = st[wg].j;
+                    if (j == 0) {  // Q of a new unit of this warpgroup
+                        ok = mbar_wait(bar(SL::kQEmpty + wg), (nq[wg] & 1) ^ 1, &g_prefill_error,
+                                       abort_flag);
+                        if (!ok) break;
+                        const uint32_t qdst = base + SL::kQ + wg * SL::kTile;
+                        mbar_arrive_expect_tx(bar(SL::kQFull + wg), kBytes);
 #pragma unroll
-                for (int db = 0; db < D / 64; ++db)
-                    tma_load_4d(qdst + db * SL::kRegion, &maps.q, bar(SL::kQFull + qb), db * 64,
-                                x.kvh * p.G, x.t0, x.b);
-                for (int j = 0; j < x.n_tiles; ++j, ++g) {
-                    const uint32_t st = g % NS;
-                    ok = mbar_wait(bar(SL::kKVEmpty + st), ((g / NS) & 1) ^ 1, &g_prefill_error,
+                        for (int db = 0; db < D / 64; ++db)
+                            tma_load_4d(qdst + db * SL::kRegion, &maps.q, bar(SL::kQFull + wg),
+                                        db * 64, x.kvh * p.G, x.t0, x.b);
+                        ++nq[wg];
+                    }
+                    const uint32_t ks = gi % NSK, vs = gi % NSV;
+                    ok = mbar_wait(bar(SL::kKEmpty + ks), ((gi / NSK) & 1) ^ 1, &g_prefill_error,
                                    abort_flag);
                     if (!ok) break;
-                    const uint32_t kdst = base + SL::kK + st * SL::kQBytes;
-                    const uint32_t vdst = base + SL::kV + st * SL::kQBytes;
+                    const uint32_t kdst = base + SL::kK + ks * SL::kTile;
                     const int key0 = x.lo + 128 * j - p.s_pad;  // key of column 0 (band)
-                    mbar_arrive_expect_tx(bar(SL::kKFull + st), kTileBytes);
-                    mbar_arrive_expect_tx(bar(SL::kVFull + st), kTileBytes);
+                    const bool sink_tile = (j == 0 && p.s_pad > 0);
+                    const uint32_t off = p.s_pad * 128;
+                    mbar_arrive_expect_tx(bar(SL::kKFull + ks), kBytes);
 #pragma unroll
                     for (int db = 0; db < D / 64; ++db) {
-                        const uint32_t ko = kdst + db * SL::kRegion, vo = vdst + db * SL::kRegion;
-                        if (j == 0 && p.s_pad > 0) {
-                            const uint32_t off = p.s_pad * 128;
-                            tma_load_4d(ko, &maps.k_sink, bar(SL::kKFull + st), db * 64, x.kvh, 0, x.b);
-                            tma_load_4d(ko + off, &maps.k_band0, bar(SL::kKFull + st), db * 64,
-                                        x.kvh, x.lo, x.b);
-                            tma_load_4d(vo, &maps.v_sink, bar(SL::kVFull + st), db * 64, x.kvh, 0, x.b);
-                            tma_load_4d(vo + off, &maps.v_band0, bar(SL::kVFull + st), db * 64,
+                        const uint32_t dst = kdst + db * SL::kRegion;
+                        if (sink_tile) {
+                            tma_load_4d(dst, &maps.k_sink, bar(SL::kKFull + ks), db * 64, x.kvh, 0, x.b);
+                            tma_load_4d(dst + off, &maps.k_band0, bar(SL::kKFull + ks), db * 64,
                                         x.kvh, x.lo, x.b);
                         } else {
-                            tma_load_4d(ko, &maps.k_band, bar(SL::kKFull + st), db * 64, x.kvh,
-                                        key0, x.b);
-                            tma_load_4d(vo, &maps.v_band, bar(SL::kVFull + st), db * 64, x.kvh,
+                            tma_load_4d(dst, &maps.k_band, bar(SL::kKFull + ks), db * 64, x.kvh,
                                         key0, x.b);
                         }
                     }
+                    ok = mbar_wait(bar(SL::kVEmpty + vs), ((gi / NSV) & 1) ^ 1, &g_prefill_error,
+                                   abort_flag);
+                    if (!ok) break;
+                    const uint32_t vdst = base + SL::kV + vs * SL::kTile;
+                    mbar_arrive_expect_tx(bar(SL::kVFull + vs), kBytes);
+#pragma unroll
+                    for (int db = 0; db < D / 64; ++db) {
+                        const uint32_t dst = vdst + db * SL::kRegion;
+                        if (sink_tile) {
+                            tma_load_4d(dst, &maps.v_sink, bar(SL::kVFull + vs), db * 64, x.kvh, 0, x.b);
+                            tma_load_4d(dst + off, &maps.v_band0, bar(SL::kVFull + vs), db * 64,
+                                        x.kvh, x.lo, x.b);
+                        } else {
+                            tma_load_4d(dst, &maps.v_band, bar(SL::kVFull + vs), db * 64, x.kvh,
+                                        key0, x.b);
+                        }
+                    }
+                    ++gi;
+                    st[wg].next(p);
                 }
             }
-            // Drain: every copy this thread started has landed before exit.
-            // (Bounded waits that ignore the abort flag; in the normal path the
-            // consumers already saw these phases complete.)
+            // Drain: every copy this thread started has landed before exit
+            // (bounded waits that ignore the abort flag; in the normal path the
+            // consumers already saw these phases complete).
             int no_abort = 0;
-            for (uint32_t i = 0; i < NS && i < g; ++i) {
-                const uint32_t gl = g - 1 - i;  // the last fill of stage gl % NS
-                const uint32_t st = gl % NS, par = (gl / NS) & 1;
-                mbar_wait(bar(SL::kKFull + st), par, &g_prefill_error, &no_abort);
-                mbar_wait(bar(SL::kVFull + st), par, &g_prefill_error, &no_abort);
+            for (uint32_t i = 0; i < NSK && i < gi; ++i) {
+                const uint32_t g = gi - 1 - i;
+                mbar_wait(bar(SL::kKFull + g % NSK), (g / NSK) & 1, &g_prefill_error, &no_abort);
             }
-            for (uint32_t i = 0; i < 2 && i < uc; ++i) {
-                const uint32_t ul = uc - 1 - i;
-                mbar_wait(bar(SL::kQFull + (ul & 1)), (ul >> 1) & 1, &g_prefill_error, &no_abort);
+            for (uint32_t i = 0; i < NSV && i < gi; ++i) {
+                const uint32_t g = gi - 1 - i;
+                mbar_wait(bar(SL::kVFull + g % NSV), (g / NSV) & 1, &g_prefill_error, &no_abort);
             }
+            for (int wg = 0; wg < 2; ++wg)
+                if (nq[wg] > 0)
+                    mbar_wait(bar(SL::kQFull + wg), (nq[wg] - 1) & 1, &g_prefill_error, &no_abort);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 0, false);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
-            uint32_t g = 0, uc = 0;
-            bool ok = true;
-            bool have_prev = false;
-            uint32_t prev_g = 0;
-            int prev_n = 0;
-            bool prev_first = false;
-            uint32_t last_commit_g = 0;
-            bool any_commit = false;
+            TileStream st[2];
+            st[0].init(0, p);
+            st[1].init(1, p);
+            uint32_t gi = 0;
+            uint32_t nq[2] = {0, 0}, npv[2] = {0, 0};
+            bool pend[2] = {false, false}, pend_first[2] = {false, false};
+            uint32_t pend_gi[2] = {0, 0};
+            int pend_n[2] = {0, 0};
+            bool ok = true, any_pv = false;
 
-            auto issue_pv = [&](uint32_t pg, int pn, bool first) -> bool {
-                const uint32_t st = pg % NS;
-                if (!mbar_wait(bar(SL::kPFull), pg & 1, &g_prefill_error, abort_flag)) return false;
-                if (!mbar_wait(bar(SL::kVFull + st), (pg / NS) & 1, &g_prefill_error, abort_flag))
+            // S = Q K^T for the next tile of warpgroup wg (into S_wg).
+            auto issue_s = [&](int wg) -> bool {
+                const Unit &x = st[wg].x;
+                const int j = st[wg].j;
+                if (j == 0) {
+                    if (!mbar_wait(bar(SL::kQFull + wg), nq[wg] & 1, &g_prefill_error, abort_flag))
+                        return false;
+                }
+                const uint32_t ks = gi % NSK;
+                if (!mbar_wait(bar(SL::kKFull + ks), (gi / NSK) & 1, &g_prefill_error, abort_flag))
                     return false;
                 tc_fence_after_sync();
-                const uint32_t pbase = base + SL::kP;
-                const uint32_t vbase = base + SL::kV + st * SL::kQBytes;
-                for (int ks = 0; ks < pn / 16; ++ks) {
-                    // A = P (K-major, keys contiguous), B = V (MN-major: d contiguous,
-                    // 64-column slabs LBO apart, 8-key groups SBO apart)
-                    const uint64_t a = smem_desc_sw128(
-                        pbase + (ks >> 2) * SL::kRegion + (ks & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(vbase + ks * 16 * 128, SL::kRegion, 1024);
-                    mma_bf16_ss(tmem + kTmemO, a, b, kIdescPV, (!first || ks > 0) ? 1u : 0u);
+                const int n = tile_width(x, j);
+                const uint32_t idesc = kIdescS | (static_cast<uint32_t>(n >> 3) << 17);
+                const uint32_t qbase = base + SL::kQ + wg * SL::kTile;
+                const uint32_t kbase = base + SL::kK + ks * SL::kTile;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * SL::kRegion + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + wg * 128, smem_desc_sw128(qbase + off, 16, 1024),
+                                smem_desc_sw128(kbase + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(SL::kPVDone));
-                mma_commit(bar(SL::kKVEmpty + st));
-                last_commit_g = pg;
-                any_commit = true;
+                mma_commit(bar(SL::kSFull + wg));
+                mma_commit(bar(SL::kKEmpty + ks));
+                const bool last = (j == x.n_tiles - 1);
+                if (last) {
+                    mma_commit(bar(SL::kQEmpty + wg));
+                    ++nq[wg];
+                }
+                pend[wg] = true;
+                pend_gi[wg] = gi;
+                pend_n[wg] = n;
+                pend_first[wg] = (j == 0);
+                ++gi;
+                st[wg].next(p);
+                return true;
+            };
+            // O += P V for warpgroup wg's pending tile (P from TMEM over S_wg).
+            auto issue_pv = [&](int wg) -> bool {
+                const uint32_t g = pend_gi[wg];
+                const uint32_t vs = g % NSV;
+                if (!mbar_wait(bar(SL::kPFull + wg), npv[wg] & 1, &g_prefill_error, abort_flag))
+                    return false;
+                if (!mbar_wait(bar(SL::kVFull + vs), (g / NSV) & 1, &g_prefill_error, abort_flag))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t vbase = base + SL::kV + vs * SL::kTile;
+                const uint32_t o_tmem = tmem + 256 + wg * 128;
+                for (int kk = 0; kk < pend_n[wg] / 16; ++kk) {
+                    const uint64_t b = smem_desc_sw128(vbase + kk * 16 * 128, SL::kRegion, 1024);
+                    mma_bf16_ts(o_tmem, tmem + wg * 128 + kk * 8, b, kIdescPV,
+                                (!pend_first[wg] || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(SL::kODone + wg));
+                mma_commit(bar(SL::kVEmpty + vs));
+                ++npv[wg];
+                pend[wg] = false;
+                any_pv = true;
                 return true;
             };
 
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
-                const Unit x = unit_geom(u, p);
-                const uint32_t qb = uc & 1;
-                ok = mbar_wait(bar(SL::kQFull + qb), (uc >> 1) & 1, &g_prefill_error, abort_flag);
-                if (!ok) break;
-                tc_fence_after_sync();
-                const uint32_t qbase = base + SL::kQ + qb * SL::kQBytes;
-                for (int j = 0; j < x.n_tiles; ++j, ++g) {
-                    const uint32_t st = g % NS;
-                    const uint32_t sb = g & 1;
-                    ok = mbar_wait(bar(SL::kKFull + st), (g / NS) & 1, &g_prefill_error, abort_flag) &&
-                         mbar_wait(bar(SL::kSEmpty + sb), ((g >> 1) & 1) ^ 1, &g_prefill_error,
-                                   abort_flag);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    const int n = tile_width(x, j);
-                    const uint32_t idesc = kIdescS | (static_cast<uint32_t>(n >> 3) << 17);
-                    const uint32_t kbase = base + SL::kK + st * SL::kQBytes;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * SL::kRegion + (ks & 3) * 32;
-                        const uint64_t a = smem_desc_sw128(qbase + off, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(kbase + off, 16, 1024);
-                        mma_bf16_ss(tmem + sb * 128, a, b, idesc, ks > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(SL::kSFull + sb));
-                    if (j == x.n_tiles - 1) mma_commit(bar(SL::kQEmpty + qb));
-                    if (have_prev) {
-                        ok = issue_pv(prev_g, prev_n, prev_first);
-                        if (!ok) break;
-                    }
-                    have_prev = true;
-                    prev_g = g;
-                    prev_n = n;
-                    prev_first = (j == 0);
+            for (int wg = 0; wg < 2 && ok; ++wg)
+                if (st[wg].valid) ok = issue_s(wg);
+            while (ok && (pend[0] || pend[1])) {
+                for (int wg = 0; wg < 2 && ok; ++wg) {
+                    if (!pend[wg]) continue;
+                    ok = issue_pv(wg);
+                    if (ok && st[wg].valid) ok = issue_s(wg);
                 }
             }
-            if (ok && have_prev) issue_pv(prev_g, prev_n, prev_first);
             // Drain: all issued MMAs complete before TMEM is released.
-            if (any_commit) {
+            if (any_pv) {
                 int no_abort = 0;
-                mbar_wait(bar(SL::kPVDone), last_commit_g & 1, &g_prefill_error, &no_abort);
+                for (int wg = 0; wg < 2; ++wg)
+                    if (npv[wg] > 0)
+                        mbar_wait(bar(SL::kODone + wg), (npv[wg] - 1) & 1, &g_prefill_error,
+                                  &no_abort);
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
+        const int wg = (warp - 2) >> 2;           // warpgroup 0 (warps 2..5) or 1 (6..9)
         const int quarter = warp & 3;             // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;      // MMA row == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_addr + wg * 128;
+        const uint32_t o_tmem = tmem + lane_addr + 256 + wg * 128;
         const int prow = row / p.G;               // position offset within the tile
         const int hrow = row - prow * p.G;        // head offset within the group
-        const bool leader = (threadIdx.x == 64);  // first softmax thread issues stores
-        const uint32_t pbase = base + SL::kP;
-        uint32_t g = 0;
+        uint32_t nt = 0;                          // tiles this warpgroup has finished
 
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+        for (int u = blockIdx.x + wg * gridDim.x; u < p.n_units; u += 2 * gridDim.x) {
             const Unit x = unit_geom(u, p);
             const int t = x.t0 + prow;
             const bool row_valid = (t <= x.t1);
@@ -309,42 +375,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_run = -INFINITY;
             float l_run = 0.f;
 
-            for (int j = 0; j < x.n_tiles; ++j, ++g) {
-                const uint32_t sb = g & 1;
-                mbar_wait(bar(SL::kSFull + sb), (g >> 1) & 1, &g_prefill_error, abort_flag);
+            for (int j = 0; j < x.n_tiles; ++j, ++nt) {
+                mbar_wait(bar(SL::kSFull + wg), nt & 1, &g_prefill_error, abort_flag);
                 tc_fence_after_sync();
-                float sv[128];
-                {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        tmem_ld32(tmem + lane_addr + sb * 128 + c4 * 32, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) sv[c4 * 32 + i] = __uint_as_float(r[i]);
-                    }
-                }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(SL::kSEmpty + sb));
-
                 // mask: band columns [c_lo, c_hi], sink columns [0, sink_hi)
                 const int key0 = x.lo + 128 * j - p.s_pad;
                 int c_lo = max(j == 0 ? p.s_pad : 0, lo_t - key0);
-                int c_hi = t - key0;
+                int c_hi = min(t - key0, 127);
                 int sink_hi = (j == 0) ? min(p.s, t + 1) : 0;
                 if (!row_valid) {
-                    c_lo = 1;
-                    c_hi = 0;
+                    c_lo = 128;
+                    c_hi = -1;
                     sink_hi = 0;
                 }
-                float mx = -INFINITY;
+                // per 32-column chunk: all rows of the warp fully inside the
+                // band (no mask needed) or fully outside (no load, no exp)
+                bool chunk_full[4], chunk_empty[4];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const bool ok = (c >= c_lo && c <= c_hi) || (c < sink_hi);
-                    sv[c] = ok ? sv[c] : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
+                for (int q = 0; q < 4; ++q) {
+                    const bool full = (c_lo <= 32 * q) && (c_hi >= 32 * q + 31);
+                    const bool none =
+                        (c_hi < 32 * q || c_lo > 32 * q + 31 || c_lo > c_hi) && sink_hi <= 32 * q;
+                    chunk_full[q] = __all_sync(0xffffffffu, full);
+                    chunk_empty[q] = __all_sync(0xffffffffu, none);
                 }
+                auto masked = [&](float v, int c) {
+                    const bool ok = (c >= c_lo && c <= c_hi) || (c < sink_hi);
+                    return ok ? v : -INFINITY;
+                };
+                // pass 1: masked row max (S read from TMEM one chunk at a time)
+                float mxa[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (chunk_empty[q]) continue;
+                    uint32_t r[32];
+                    tmem_ld32(s_tmem + 32 * q, r);
+                    tmem_wait_ld();
+                    if (chunk_full[q]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            mxa[i & 7] = fmaxf(mxa[i & 7], __uint_as_float(r[i]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            mxa[i & 7] = fmaxf(mxa[i & 7], masked(__uint_as_float(r[i]), 32 * q + i));
+                    }
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                       fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
                 const float m_new = fmaxf(m_run, mx);
                 float alpha = 1.f;
                 if (m_new > m_run &&
@@ -353,97 +433,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_run = m_new;
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run * p.scale_log2;
-                uint32_t pk[64];
-                float lsum = 0.f;
+                // pass 2: P = exp2(S*scale - m) in bf16, written over the first
+                // 64 columns of S (chunk q's P lands on columns this pass has
+                // already read)
+                float lsa[8];
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float p0 = ex2_approx(fmaf(sv[2 * i], p.scale_log2, neg_m));
-                    const float p1 = ex2_approx(fmaf(sv[2 * i + 1], p.scale_log2, neg_m));
-                    pk[i] = pack_bf16x2(p0, p1);
-                    lsum += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
+                for (int i = 0; i < 8; ++i) lsa[i] = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16];
+                    if (chunk_empty[q]) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                    } else {
+                        uint32_t r[32];
+                        tmem_ld32(s_tmem + 32 * q, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+                            if (!chunk_full[q]) {
+                                s0 = masked(s0, 32 * q + 2 * i);
+                                s1 = masked(s1, 32 * q + 2 * i + 1);
+                            }
+                            const float p0 = ex2_approx(fmaf(s0, p.scale_log2, neg_m));
+                            const float p1 = ex2_approx(fmaf(s1, p.scale_log2, neg_m));
+                            pk[i] = pack_bf16x2(p0, p1);
+                            lsa[i & 7] += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
+                        }
+                    }
+                    tmem_st16(s_tmem + 16 * q, pk);
                 }
+                const float lsum = ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3])) +
+                                   ((lsa[4] + lsa[5]) + (lsa[6] + lsa[7]));
                 l_run = l_run * alpha + lsum;
-
-                // P may be overwritten once the previous P*V has completed.
-                if (g > 0)
-                    mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
-                tc_fence_after_sync();
-#pragma unroll
-                for (int cc = 0; cc < 16; ++cc) {
-                    const uint32_t addr = pbase + (cc >> 3) * SL::kRegion + row * 128 +
-                                          ((((cc & 7) ^ (row & 7))) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                 "r"(pk[4 * cc]), "r"(pk[4 * cc + 1]), "r"(pk[4 * cc + 2]),
-                                 "r"(pk[4 * cc + 3])
-                                 : "memory");
-                }
-                fence_proxy_async_smem();
                 // Rescale O when this warp raised any running max (not on the
-                // first tile: its P*V overwrites O).
+                // first tile: its P V overwrites O).  The previous P V of this
+                // warpgroup completed before this tile's S (same issuing thread).
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                    uint32_t r[32];
 #pragma unroll
                     for (int c4 = 0; c4 < D / 32; ++c4) {
-                        const uint32_t ta = tmem + lane_addr + kTmemO + c4 * 32;
-                        tmem_ld32(ta, r);
+                        uint32_t r[32];
+                        tmem_ld32(o_tmem + c4 * 32, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(ta, r);
+                        tmem_st32(o_tmem + c4 * 32, r);
                     }
-                    tmem_wait_st();
                 }
+                tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(SL::kPFull));
+                if (lane == 0) mbar_arrive(bar(SL::kPFull + wg));
             }
 
             // ---------------------------------------------------- epilogue
-            const uint32_t glast = g - 1;
-            mbar_wait(bar(SL::kPVDone), glast & 1, &g_prefill_error, abort_flag);
+            mbar_wait(bar(SL::kODone + wg), (nt - 1) & 1, &g_prefill_error, abort_flag);
             tc_fence_after_sync();
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            const bool store = row_valid && !*abort_flag;
+            uint16_t *orow =
+                p.o + ((static_cast<int64_t>(x.b) * p.L + t) * p.Hq + x.kvh * p.G + hrow) * D;
 #pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_addr + kTmemO + c4 * 32, r);
+                tmem_ld32(o_tmem + c4 * 32, r);
                 tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {  // four 16-byte chunks of 8 columns
-                    const int cc = c4 * 4 + q;
-                    const uint32_t v0 = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv_l,
-                                                    __uint_as_float(r[8 * q + 1]) * inv_l);
-                    const uint32_t v1 = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv_l,
-                                                    __uint_as_float(r[8 * q + 3]) * inv_l);
-                    const uint32_t v2 = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv_l,
-                                                    __uint_as_float(r[8 * q + 5]) * inv_l);
-                    const uint32_t v3 = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv_l,
-                                                    __uint_as_float(r[8 * q + 7]) * inv_l);
-                    const uint32_t addr = pbase + (cc >> 3) * SL::kRegion + row * 128 +
-                                          ((((cc & 7) ^ (row & 7))) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v0),
-                                 "r"(v1), "r"(v2), "r"(v3)
-                                 : "memory");
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
+                                        __uint_as_float(r[2 * i + 1]) * inv_l);
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c4 * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
-            fence_proxy_async_smem();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (leader && !*abort_flag) {
-#pragma unroll
-                for (int db = 0; db < D / 64; ++db)
-                    tma_store_4d(&maps.o, pbase + db * SL::kRegion, db * 64, x.kvh * p.G, x.t0, x.b);
-                tma_store_commit();
-                tma_store_wait_read_all();
-            }
-            if (p.lse != nullptr && row_valid && !*abort_flag) {
+            if (p.lse != nullptr && store) {
                 const int h = x.kvh * p.G + hrow;
                 p.lse[(static_cast<int64_t>(x.b) * p.Hq + h) * p.L + t] =
                     m_run * p.scale + logf(l_run);
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            tc_fence_before_sync();
         }
-        if (leader) tma_store_wait_all();
     }
 
     tc_fence_before_sync();
@@ -474,24 +549,27 @@ bool encode_map(CUtensorMap *m, const void *ptr, int d, int heads, int L, int B,
     return r == CUDA_SUCCESS;
 }
 
-template <int D, int NS>
+template <int D, int NSK, int NSV>
 swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaStream_t stream) {
-    using SL = PrefillSmem<D, NS>;
+    using SL = PrefillSmem<D, NSK, NSV>;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
-        if (cudaFuncSetAttribute(swa_prefill_kernel<D, NS>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SL::kAlloc) != cudaSuccess)
-            return SWA_ERR_CUDA;
+        e = cudaFuncSetAttribute(swa_prefill_kernel<D, NSK, NSV>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
         configured[dev] = true;
     }
     const int sms = device_sm_count();
-    if (sms <= 0) return SWA_ERR_CUDA;
-    const int grid = p.n_units < sms ? p.n_units : sms;
-    swa_prefill_kernel<D, NS><<<grid, kThreads, SL::kAlloc, stream>>>(maps, p);
-    return cudaPeekAtLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
+    // two warpgroups per CTA: half as many CTAs as units keeps both busy
+    const int want = (p.n_units + 1) / 2;
+    const int grid = want < sms ? want : sms;
+    swa_prefill_kernel<D, NSK, NSV><<<grid, kThreads, SL::kAlloc, stream>>>(maps, p);
+    e = cudaPeekAtLastError();
+    return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_prefill_kernel");
 }
 
 }  // namespace
@@ -512,12 +590,12 @@ swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, 
     p.n_units = B * Hkv * p.n_qtiles;
     p.scale = 1.0f / std::sqrt(static_cast<float>(d));
     p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
 
     PrefillMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     bool ok = encode_map(&maps.q, q, d, Hq, L, B, p.G, p.P) &&
-              encode_map(&maps.o, o, d, Hq, L, B, p.G, p.P) &&
               encode_map(&maps.k_band, k, d, Hkv, L, B, 1, 128) &&
               encode_map(&maps.v_band, v, d, Hkv, L, B, 1, 128);
     if (ok && p.s_pad > 0)
@@ -525,9 +603,9 @@ swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, 
              encode_map(&maps.v_sink, v, d, Hkv, L, B, 1, p.s_pad) &&
              encode_map(&maps.k_band0, k, d, Hkv, L, B, 1, 128 - p.s_pad) &&
              encode_map(&maps.v_band0, v, d, Hkv, L, B, 1, 128 - p.s_pad);
-    if (!ok) return SWA_ERR_CUDA;
-    if (d == 128) return launch_prefill<128, 2>(maps, p, stream);
-    return launch_prefill<64, 4>(maps, p, stream);
+    if (!ok) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    if (d == 128) return launch_prefill<128, 2, 3>(maps, p, stream);
+    return launch_prefill<64, 4, 6>(maps, p, stream);
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {

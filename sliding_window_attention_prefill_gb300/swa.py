@@ -78,6 +78,8 @@ def _declare(L) -> None:
     L.swa_cache_slot.restype = _c_i64
     L.swa_version.argtypes = []
     L.swa_version.restype = ctypes.c_char_p
+    L.swa_last_cuda_error.argtypes = []
+    L.swa_last_cuda_error.restype = ctypes.c_char_p
 
 
 def lib():
@@ -104,6 +106,8 @@ def declared_functions() -> list[str]:
 
 def _check(status: int, what: str) -> None:
     if status != 0:
+        if status == -5:
+            what = f"{what} [{lib().swa_last_cuda_error().decode(errors='replace')}]"
         raise SwaError(status, what)
 
 
