@@ -388,43 +388,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     c_hi = -1;
                     sink_hi = 0;
                 }
-                // per 32-column chunk: all rows of the warp fully inside the
-                // band (no mask needed) or fully outside (no load, no exp)
-                bool chunk_full[4], chunk_empty[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const bool full = (c_lo <= 32 * q) && (c_hi >= 32 * q + 31);
-                    const bool none =
-                        (c_hi < 32 * q || c_lo > 32 * q + 31 || c_lo > c_hi) && sink_hi <= 32 * q;
-                    chunk_full[q] = __all_sync(0xffffffffu, full);
-                    chunk_empty[q] = __all_sync(0xffffffffu, none);
-                }
-                auto masked = [&](float v, int c) {
-                    const bool ok = (c >= c_lo && c <= c_hi) || (c < sink_hi);
-                    return ok ? v : -INFINITY;
+                // Column c of this tile is attended by the row when c is in the
+                // band [c_lo, c_hi] or among the sinks [0, sink_hi).  Per
+                // 32-column chunk the warp checks whether every row has the
+                // whole chunk in its band ("full": no mask) or none of it
+                // ("empty": no load, P = 0).
+                const bool band_ok = c_lo <= c_hi;
+                const unsigned span = band_ok ? static_cast<unsigned>(c_hi - c_lo) : 0u;
+                const int band_from = band_ok ? c_lo : 1 << 20;
+                auto flags = [&](int q, bool &full, bool &empty) {
+                    const bool f = band_ok && c_lo <= 32 * q && c_hi >= 32 * q + 31;
+                    const bool e = (!band_ok || c_hi < 32 * q || c_lo > 32 * q + 31) &&
+                                   sink_hi <= 32 * q;
+                    full = __all_sync(0xffffffffu, f);
+                    empty = __all_sync(0xffffffffu, e);
                 };
-                // pass 1: masked row max (S read from TMEM one chunk at a time)
-                float mxa[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (chunk_empty[q]) continue;
-                    uint32_t r[32];
-                    tmem_ld32(s_tmem + 32 * q, r);
+                // pass 1: masked row max, S read from TMEM two chunks per wait
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                for (int q = 0; q < 4; q += 2) {
+                    bool f0, e0, f1, e1;
+                    flags(q, f0, e0);
+                    flags(q + 1, f1, e1);
+                    if (e0 && e1) continue;
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(s_tmem + 32 * q, r0);
+                    tmem_ld32(s_tmem + 32 * q + 32, r1);
                     tmem_wait_ld();
-                    if (chunk_full[q]) {
+                    const int x0 = 32 * q - band_from, sh = sink_hi - 32 * q;
+                    if (f0 && f1) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            mxa[i & 7] = fmaxf(mxa[i & 7], __uint_as_float(r[i]));
+                        for (int i = 0; i < 32; ++i) {
+                            m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r0[i]));
+                            m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r1[i]));
+                        }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            mxa[i & 7] = fmaxf(mxa[i & 7], masked(__uint_as_float(r[i]), 32 * q + i));
+                        for (int i = 0; i < 32; ++i) {
+                            const bool ok0 = static_cast<unsigned>(x0 + i) <= span || i < sh;
+                            const bool ok1 = static_cast<unsigned>(x0 + 32 + i) <= span || i + 32 < sh;
+                            m4[i & 3] = fmaxf(m4[i & 3], ok0 ? __uint_as_float(r0[i]) : -INFINITY);
+                            m4[i & 3] = fmaxf(m4[i & 3], ok1 ? __uint_as_float(r1[i]) : -INFINITY);
+                        }
                     }
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                                       fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 const float m_new = fmaxf(m_run, mx);
                 float alpha = 1.f;
                 if (m_new > m_run &&
@@ -434,38 +442,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run * p.scale_log2;
                 // pass 2: P = exp2(S*scale - m) in bf16, written over the first
-                // 64 columns of S (chunk q's P lands on columns this pass has
-                // already read)
-                float lsa[8];
+                // 64 columns of S (the P of chunks q, q+1 lands on columns
+                // 16q .. 16q+31, which this pass has already read)
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int q = 0; q < 4; q += 2) {
+                    bool f0, e0, f1, e1;
+                    flags(q, f0, e0);
+                    flags(q + 1, f1, e1);
+                    uint32_t pk[32];
+                    if (e0 && e1) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) lsa[i] = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t pk[16];
-                    if (chunk_empty[q]) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                        for (int i = 0; i < 32; ++i) pk[i] = 0u;
                     } else {
-                        uint32_t r[32];
-                        tmem_ld32(s_tmem + 32 * q, r);
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(s_tmem + 32 * q, r0);
+                        tmem_ld32(s_tmem + 32 * q + 32, r1);
                         tmem_wait_ld();
+                        if (!(f0 && f1)) {
+                            const int x0 = 32 * q - band_from, sh = sink_hi - 32 * q;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                if (!(static_cast<unsigned>(x0 + i) <= span || i < sh))
+                                    r0[i] = __float_as_uint(-INFINITY);
+                                if (!(static_cast<unsigned>(x0 + 32 + i) <= span || i + 32 < sh))
+                                    r1[i] = __float_as_uint(-INFINITY);
+                            }
+                        }
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
-                            if (!chunk_full[q]) {
-                                s0 = masked(s0, 32 * q + 2 * i);
-                                s1 = masked(s1, 32 * q + 2 * i + 1);
-                            }
-                            const float p0 = ex2_approx(fmaf(s0, p.scale_log2, neg_m));
-                            const float p1 = ex2_approx(fmaf(s1, p.scale_log2, neg_m));
-                            pk[i] = pack_bf16x2(p0, p1);
-                            lsa[i & 7] += bf16lo_to_f32(pk[i]) + bf16hi_to_f32(pk[i]);
+                            const float a0 = ex2_approx(fmaf(__uint_as_float(r0[2 * i]), p.scale_log2, neg_m));
+                            const float a1 = ex2_approx(fmaf(__uint_as_float(r0[2 * i + 1]), p.scale_log2, neg_m));
+                            const float b0 = ex2_approx(fmaf(__uint_as_float(r1[2 * i]), p.scale_log2, neg_m));
+                            const float b1 = ex2_approx(fmaf(__uint_as_float(r1[2 * i + 1]), p.scale_log2, neg_m));
+                            pk[i] = pack_bf16x2(a0, a1);
+                            pk[16 + i] = pack_bf16x2(b0, b1);
+                            l4[i & 3] += (a0 + a1) + (b0 + b1);
                         }
                     }
-                    tmem_st16(s_tmem + 16 * q, pk);
+                    uint32_t lo16[16], hi16[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        lo16[i] = pk[i];
+                        hi16[i] = pk[16 + i];
+                    }
+                    tmem_st16(s_tmem + 16 * q, lo16);
+                    tmem_st16(s_tmem + 16 * q + 16, hi16);
                 }
-                const float lsum = ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3])) +
-                                   ((lsa[4] + lsa[5]) + (lsa[6] + lsa[7]));
+                const float lsum = (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 l_run = l_run * alpha + lsum;
                 // Rescale O when this warp raised any running max (not on the
                 // first tile: its P V overwrites O).  The previous P V of this
