@@ -460,6 +460,7 @@ def _time_graph(fn, steps: int, flush, warm: int = 3) -> float:
 def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
     """Prefill kernel alone on the prefill configs: B=1 L=4096 SWA(64,4) and
     B=2 L=32768 SWA(w,4) for w in {128, 256, 512} (Hq=32, Hkv=8, d=128).
+    Also full causal attention (w = infinity) at B=1, L=16384.
     only_w / B_ / L_ restrict or resize the list (smaller cases for ncu)."""
     import torch
 
@@ -468,7 +469,8 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
     build.build()
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    cases = [(1, 4096, 64, 4), (2, 32768, 128, 0), (2, 32768, 256, 0), (2, 32768, 512, 0)]
+    cases = [(1, 4096, 64, 4), (2, 32768, 128, 0), (2, 32768, 256, 0), (2, 32768, 512, 0),
+             (1, 16384, -1, 0)]
     if only_w is not None:
         cases = [c for c in cases if c[2] == only_w]
     cases = [(B_ or c[0], L_ or c[1], c[2], c[3]) for c in cases]
@@ -481,7 +483,8 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
         fl, by = prefill_flops(B, L, Hq, d, w), prefill_bytes(B, L, Hq, Hkv, d)
         tf = fl / (ms * 1e-3) / 1e12
         attainable = min(pk["bf16_tflops"], fl / by * pk["hbm_gbs"] / 1e3)
-        print(json.dumps({"suite": "prefill", "B": B, "L": L, "w": w, "s": s, "ms": ms,
+        print(json.dumps({"suite": "prefill", "B": B, "L": L, "w": w if w > 0 else "inf",
+                          "s": s if w > 0 else 0, "ms": ms,
                           "tflops": tf, "frac_tensor_peak": tf / pk["bf16_tflops"],
                           "frac_attainable": tf / attainable, "attainable_tflops": attainable,
                           "gbs": by / (ms * 1e-3) / 1e9, "flop_per_byte": fl / by}), flush=True)
@@ -489,7 +492,7 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
         torch.cuda.empty_cache()
 
 
-def suite_decode(steps: int):
+def suite_decode(steps: int, only_w=None):
     """Decode step (append one token + decode) at B=64, Hq=32, Hkv=8, d=128,
     SWA(w,4) for w in {64, 512}, after a 4096-token prompt, L2 flushed."""
     import torch
@@ -500,7 +503,7 @@ def suite_decode(steps: int):
     pk = peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     B, Hq, Hkv, d, s, prompt = 64, 32, 8, 128, 4, 4096
-    for w in (64, 512):
+    for w in [x for x in (64, 512) if only_w is None or x == only_w]:
         kp, vp, ks, vs, qs = inputs.decode_stream(B, Hq, Hkv, d, prompt, 1, seed=0)
         c = swa.Cache(B, Hkv, d, w, s)
         c.append(kp.cuda(), vp.cuda(), 0)
@@ -541,7 +544,7 @@ def main():
         suite_prefill(max(args.steps // 10, 10), args.w, args.B, args.L)
         return
     if args.suite == "decode":
-        suite_decode(max(args.steps // 4, 20))
+        suite_decode(max(args.steps // 4, 20), args.w)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

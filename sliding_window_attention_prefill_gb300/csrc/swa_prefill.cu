@@ -11,27 +11,27 @@
 // P = 128/G consecutive positions: row r is position t0 + r/G, head
 // kvh*G + r%G, which is exactly a box of the [B, L, Hq, d] query tensor, so
 // one TMA box loads it.  The unit needs the sink keys [0, s) and the band
-// [lo, t1] with lo = max(s, t0-(w-s)+1): the key columns are laid out as
-// [s_pad sink rows | band ...] in 128-column key tiles, the sink block (s
-// rounded up to 8 rows) sharing the first tile.
+// [lo, t1] with lo = max(s, t0-(w-s)+1): its key columns are laid out as
+// [s_pad sink rows | band ...] and cut into key tiles of up to 256 columns,
+// the sink block (s rounded up to 8 rows) sharing the first tile.
 //
-// Roles (320 threads, one persistent CTA per SM):
-//   warp 0       TMA producer: Q (one buffer per softmax warpgroup), K tiles
-//                (NSK-slot ring), V tiles (NSV-slot ring)
+// Roles (384 threads = three warpgroups, one persistent CTA per SM):
+//   warp 0       TMA producer for Q (double-buffered) and K tiles
 //   warp 1       tcgen05 issuer; owns the 512-column TMEM allocation
-//                S_A | S_B | O_A | O_B
-//   warps 2..5   softmax warpgroup A, warps 6..9 softmax warpgroup B: each
-//                takes every other work unit of the CTA, one thread per MMA
-//                row (TMEM lane)
-// The two warpgroups ping-pong on the tensor cores: while A runs the softmax
-// of its tile, the MMA warp computes B's O += P V and next S = Q K^T, and
-// vice versa.  A warpgroup writes P (bf16) over the first 64 columns of its
-// own S and the P V product reads it from tensor memory (tcgen05.mma with the
-// A operand in TMEM); the next S of that warpgroup is issued after that P V
-// by the same thread, and tcgen05 MMAs of one thread execute in issue order.
-// The running max is only raised when it grows by more than 2^8 (exact:
-// numerator and denominator share the same stale max), so the O rescale
-// through TMEM is rare.
+//                S (256 columns) | P (128 columns, bf16 pairs) | O (d columns)
+//   warp 2       TMA producer for V tiles
+//   warp 3       idle
+//   warps 4..11  softmax + epilogue: two threads per MMA row (TMEM lane), each
+//                taking every other 32-column chunk of the key tile
+// Key tiles of 256 columns let S = Q K^T run as N = 256 MMAs (twice the work
+// per instruction of N = 128 at a similar issue cost on this part), and P
+// lives in its own TMEM columns, so the MMA warp issues S_{g+1} as soon as
+// the softmax has read S_g -- while the softmax of tile g is still running --
+// and O += P_g V_g afterwards.  The first warpgroup hands registers to the
+// two softmax warpgroups (setmaxnreg) so a thread keeps its 128 scores in
+// registers.  The running max is only raised when it grows by more than 2^8
+// (exact: numerator and denominator share the same stale max), so the O
+// rescale through TMEM is rare.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -46,11 +46,13 @@ namespace swa {
 
 __device__ int g_prefill_error;
 
+constexpr int kKT = 256;  // key tile width (columns)
+
 struct PrefillMaps {
     CUtensorMap q;                    // box {64, G, P, 1} over [B, L, Hq, d]
-    CUtensorMap k_band, v_band;       // box {64, 1, 128, 1} over [B, L, Hkv, d]
+    CUtensorMap k_band, v_band;       // box {64, 1, 256, 1} over [B, L, Hkv, d]
     CUtensorMap k_sink, v_sink;       // box {64, 1, s_pad, 1}
-    CUtensorMap k_band0, v_band0;     // box {64, 1, 128 - s_pad, 1}
+    CUtensorMap k_band0, v_band0;     // box {64, 1, 256 - s_pad, 1}
 };
 
 struct PrefillParams {
@@ -83,62 +85,41 @@ __device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p) {
     x.lo = p.w < 0 ? 0 : max(p.s, x.t0 - (p.w - p.s) + 1);
     const int nb = max(0, x.t1 - x.lo + 1);
     x.n_cols = p.s_pad + nb;
-    x.n_tiles = (x.n_cols + 127) / 128;
+    x.n_tiles = (x.n_cols + kKT - 1) / kKT;
     return x;
 }
 
 // Key columns of tile j, rounded up to the MMA's N granularity of 16.
 __device__ __forceinline__ int tile_width(const Unit &x, int j) {
-    const int n = min(128, x.n_cols - 128 * j);
+    const int n = min(kKT, x.n_cols - kKT * j);
     return (n + 15) & ~15;
 }
 
-// The sequence of key tiles one softmax warpgroup works through: the CTA's
-// units u = blockIdx.x + (2k + wg) * gridDim.x, k = 0, 1, ..., each split
-// into its key tiles.
-struct TileStream {
-    int k, u, j;
-    bool valid;
-    Unit x;
-    __device__ __forceinline__ void init(int wg, const PrefillParams &p) {
-        k = 0;
-        j = 0;
-        u = blockIdx.x + wg * gridDim.x;
-        valid = u < p.n_units;
-        if (valid) x = unit_geom(u, p);
-    }
-    __device__ __forceinline__ void next(const PrefillParams &p) {
-        if (++j >= x.n_tiles) {
-            j = 0;
-            ++k;
-            u += 2 * gridDim.x;
-            valid = u < p.n_units;
-            if (valid) x = unit_geom(u, p);
-        }
-    }
-};
-
 template <int D, int NSK, int NSV>
 struct PrefillSmem {
-    static constexpr int kRegion = 128 * 128;           // one 64-column slab of 128 rows
-    static constexpr int kTile = 128 * D * 2;           // Q / K / V tile bytes
-    static constexpr int kQ = 0;                        // Q buffer per warpgroup
-    static constexpr int kK = kQ + 2 * kTile;           // K ring
-    static constexpr int kV = kK + NSK * kTile;         // V ring
-    static constexpr int kBar = kV + NSV * kTile;       // mbarriers
-    // barrier slots (8 bytes each)
+    static constexpr int kQRegion = 128 * 128;          // 64 columns x 128 query rows
+    static constexpr int kKRegion = kKT * 128;          // 64 columns x 256 key rows
+    static constexpr int kQTile = 128 * D * 2;
+    static constexpr int kKTile = kKT * D * 2;
+    static constexpr int kQ = 0;                        // 2 Q buffers
+    static constexpr int kK = kQ + 2 * kQTile;          // K ring
+    static constexpr int kV = kK + NSK * kKTile;        // V ring
+    static constexpr int kRed = kV + NSV * kKTile;      // row max [2 parity][2 half][128]
+    static constexpr int kRedL = kRed + 2 * 2 * 128 * 4;  // row sum [2 half][128]
+    static constexpr int kBar = kRedL + 2 * 128 * 4;
     static constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = 4 + NSK,
                          kVFull = 4 + 2 * NSK, kVEmpty = 4 + 2 * NSK + NSV,
-                         kSFull = 4 + 2 * NSK + 2 * NSV, kPFull = kSFull + 2, kODone = kPFull + 2,
-                         kNumBars = kODone + 2;
+                         kSFull = 4 + 2 * NSK + 2 * NSV, kSEmpty = kSFull + 1,
+                         kPFull = kSFull + 2, kPVDone = kSFull + 3, kNumBars = kSFull + 4;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
     static constexpr int kAlloc = kBytes + 1024;        // room to align the base to 1024
 };
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0, kTmemP = 256, kTmemO = 384;
 
 template <int D, int NSK, int NSV>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -157,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SL::kNumBars; ++i) {
-            const bool four = (i == SL::kPFull || i == SL::kPFull + 1);
-            mbar_init(bar(i), four ? 4u : 1u);
+            const bool eight = (i == SL::kSEmpty || i == SL::kPFull);
+            mbar_init(bar(i), eight ? 8u : 1u);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -172,267 +153,233 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&maps.q);
-            tma_prefetch_desc(&maps.k_band);
-            tma_prefetch_desc(&maps.v_band);
-            constexpr uint32_t kBytes = SL::kTile;
-            TileStream st[2];
-            st[0].init(0, p);
-            st[1].init(1, p);
-            uint32_t gi = 0;  // global tile index, in the order the MMA warp issues S
-            uint32_t nq[2] = {0, 0};
+    // Register split: 3 x 128 threads launched at 168 registers each
+    // (64512); the first warpgroup drops to 80 and the softmax warpgroups
+    // rise to 208: 80*128 + 2*208*128 = 63488 <= 64512.
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+        if ((warp == 0 || warp == 2) && lane == 0) {
+            // -------------------------------------------------------- producers
+            const bool kq = (warp == 0);
+            if (kq) {
+                tma_prefetch_desc(&maps.q);
+                tma_prefetch_desc(&maps.k_band);
+            } else {
+                tma_prefetch_desc(&maps.v_band);
+            }
+            const CUtensorMap *m_sink = kq ? &maps.k_sink : &maps.v_sink;
+            const CUtensorMap *m_band0 = kq ? &maps.k_band0 : &maps.v_band0;
+            const CUtensorMap *m_band = kq ? &maps.k_band : &maps.v_band;
+            const uint32_t ns = kq ? NSK : NSV;
+            const int full0 = kq ? SL::kKFull : SL::kVFull;
+            const int empty0 = kq ? SL::kKEmpty : SL::kVEmpty;
+            const uint32_t ring = base + (kq ? SL::kK : SL::kV);
+            uint32_t g = 0, uc = 0;
             bool ok = true;
-            while (ok && (st[0].valid || st[1].valid)) {
-                for (int wg = 0; wg < 2 && ok; ++wg) {
-                    if (!st[wg].valid) continue;
-                    const Unit &x = st[wg].x;
-                    const int j = st[wg].j;
-                    if (j == 0) {  // Q of a new unit of this warpgroup
-                        ok = mbar_wait(bar(SL::kQEmpty + wg), (nq[wg] & 1) ^ 1, &g_prefill_error,
-                                       abort_flag);
-                        if (!ok) break;
-                        const uint32_t qdst = base + SL::kQ + wg * SL::kTile;
-                        mbar_arrive_expect_tx(bar(SL::kQFull + wg), kBytes);
-#pragma unroll
-                        for (int db = 0; db < D / 64; ++db)
-                            tma_load_4d(qdst + db * SL::kRegion, &maps.q, bar(SL::kQFull + wg),
-                                        db * 64, x.kvh * p.G, x.t0, x.b);
-                        ++nq[wg];
-                    }
-                    const uint32_t ks = gi % NSK, vs = gi % NSV;
-                    ok = mbar_wait(bar(SL::kKEmpty + ks), ((gi / NSK) & 1) ^ 1, &g_prefill_error,
+            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
+                const Unit x = unit_geom(u, p);
+                if (kq) {
+                    const uint32_t qb = uc & 1;
+                    ok = mbar_wait(bar(SL::kQEmpty + qb), ((uc >> 1) & 1) ^ 1, &g_prefill_error,
                                    abort_flag);
                     if (!ok) break;
-                    const uint32_t kdst = base + SL::kK + ks * SL::kTile;
-                    const int key0 = x.lo + 128 * j - p.s_pad;  // key of column 0 (band)
-                    const bool sink_tile = (j == 0 && p.s_pad > 0);
-                    const uint32_t off = p.s_pad * 128;
-                    mbar_arrive_expect_tx(bar(SL::kKFull + ks), kBytes);
+                    mbar_arrive_expect_tx(bar(SL::kQFull + qb), SL::kQTile);
 #pragma unroll
-                    for (int db = 0; db < D / 64; ++db) {
-                        const uint32_t dst = kdst + db * SL::kRegion;
-                        if (sink_tile) {
-                            tma_load_4d(dst, &maps.k_sink, bar(SL::kKFull + ks), db * 64, x.kvh, 0, x.b);
-                            tma_load_4d(dst + off, &maps.k_band0, bar(SL::kKFull + ks), db * 64,
-                                        x.kvh, x.lo, x.b);
-                        } else {
-                            tma_load_4d(dst, &maps.k_band, bar(SL::kKFull + ks), db * 64, x.kvh,
-                                        key0, x.b);
-                        }
-                    }
-                    ok = mbar_wait(bar(SL::kVEmpty + vs), ((gi / NSV) & 1) ^ 1, &g_prefill_error,
+                    for (int db = 0; db < D / 64; ++db)
+                        tma_load_4d(base + SL::kQ + qb * SL::kQTile + db * SL::kQRegion, &maps.q,
+                                    bar(SL::kQFull + qb), db * 64, x.kvh * p.G, x.t0, x.b);
+                }
+                for (int j = 0; j < x.n_tiles; ++j, ++g) {
+                    const uint32_t slot = g % ns;
+                    ok = mbar_wait(bar(empty0 + slot), ((g / ns) & 1) ^ 1, &g_prefill_error,
                                    abort_flag);
                     if (!ok) break;
-                    const uint32_t vdst = base + SL::kV + vs * SL::kTile;
-                    mbar_arrive_expect_tx(bar(SL::kVFull + vs), kBytes);
+                    const uint32_t dst0 = ring + slot * SL::kKTile;
+                    const int key0 = x.lo + kKT * j - p.s_pad;  // key of column 0 (band)
+                    const uint32_t fb = bar(full0 + slot);
+                    mbar_arrive_expect_tx(fb, SL::kKTile);
 #pragma unroll
                     for (int db = 0; db < D / 64; ++db) {
-                        const uint32_t dst = vdst + db * SL::kRegion;
-                        if (sink_tile) {
-                            tma_load_4d(dst, &maps.v_sink, bar(SL::kVFull + vs), db * 64, x.kvh, 0, x.b);
-                            tma_load_4d(dst + off, &maps.v_band0, bar(SL::kVFull + vs), db * 64,
-                                        x.kvh, x.lo, x.b);
+                        const uint32_t dst = dst0 + db * SL::kKRegion;
+                        if (j == 0 && p.s_pad > 0) {
+                            tma_load_4d(dst, m_sink, fb, db * 64, x.kvh, 0, x.b);
+                            tma_load_4d(dst + p.s_pad * 128, m_band0, fb, db * 64, x.kvh, x.lo, x.b);
                         } else {
-                            tma_load_4d(dst, &maps.v_band, bar(SL::kVFull + vs), db * 64, x.kvh,
-                                        key0, x.b);
+                            tma_load_4d(dst, m_band, fb, db * 64, x.kvh, key0, x.b);
                         }
                     }
-                    ++gi;
-                    st[wg].next(p);
                 }
             }
             // Drain: every copy this thread started has landed before exit
             // (bounded waits that ignore the abort flag; in the normal path the
             // consumers already saw these phases complete).
             int no_abort = 0;
-            for (uint32_t i = 0; i < NSK && i < gi; ++i) {
-                const uint32_t g = gi - 1 - i;
-                mbar_wait(bar(SL::kKFull + g % NSK), (g / NSK) & 1, &g_prefill_error, &no_abort);
+            for (uint32_t i = 0; i < ns && i < g; ++i) {
+                const uint32_t gl = g - 1 - i;
+                mbar_wait(bar(full0 + gl % ns), (gl / ns) & 1, &g_prefill_error, &no_abort);
             }
-            for (uint32_t i = 0; i < NSV && i < gi; ++i) {
-                const uint32_t g = gi - 1 - i;
-                mbar_wait(bar(SL::kVFull + g % NSV), (g / NSV) & 1, &g_prefill_error, &no_abort);
-            }
-            for (int wg = 0; wg < 2; ++wg)
-                if (nq[wg] > 0)
-                    mbar_wait(bar(SL::kQFull + wg), (nq[wg] - 1) & 1, &g_prefill_error, &no_abort);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+            if (kq)
+                for (uint32_t i = 0; i < 2 && i < uc; ++i) {
+                    const uint32_t ul = uc - 1 - i;
+                    mbar_wait(bar(SL::kQFull + (ul & 1)), (ul >> 1) & 1, &g_prefill_error,
+                              &no_abort);
+                }
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
             constexpr uint32_t kIdescS = idesc_bf16_f32(128, 0, false);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
-            TileStream st[2];
-            st[0].init(0, p);
-            st[1].init(1, p);
-            uint32_t gi = 0;
-            uint32_t nq[2] = {0, 0}, npv[2] = {0, 0};
-            bool pend[2] = {false, false}, pend_first[2] = {false, false};
-            uint32_t pend_gi[2] = {0, 0};
-            int pend_n[2] = {0, 0};
-            bool ok = true, any_pv = false;
+            uint32_t g = 0, uc = 0;
+            bool ok = true, have_prev = false, any_pv = false;
+            uint32_t prev_g = 0, last_pv_g = 0;
+            int prev_n = 0;
+            bool prev_first = false;
 
-            // S = Q K^T for the next tile of warpgroup wg (into S_wg).
-            auto issue_s = [&](int wg) -> bool {
-                const Unit &x = st[wg].x;
-                const int j = st[wg].j;
-                if (j == 0) {
-                    if (!mbar_wait(bar(SL::kQFull + wg), nq[wg] & 1, &g_prefill_error, abort_flag))
-                        return false;
-                }
-                const uint32_t ks = gi % NSK;
-                if (!mbar_wait(bar(SL::kKFull + ks), (gi / NSK) & 1, &g_prefill_error, abort_flag))
+            auto issue_pv = [&](uint32_t pg, int pn, bool first) -> bool {
+                const uint32_t vs = pg % NSV;
+                if (!mbar_wait(bar(SL::kPFull), pg & 1, &g_prefill_error, abort_flag)) return false;
+                if (!mbar_wait(bar(SL::kVFull + vs), (pg / NSV) & 1, &g_prefill_error, abort_flag))
                     return false;
                 tc_fence_after_sync();
-                const int n = tile_width(x, j);
-                const uint32_t idesc = kIdescS | (static_cast<uint32_t>(n >> 3) << 17);
-                const uint32_t qbase = base + SL::kQ + wg * SL::kTile;
-                const uint32_t kbase = base + SL::kK + ks * SL::kTile;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * SL::kRegion + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + wg * 128, smem_desc_sw128(qbase + off, 16, 1024),
-                                smem_desc_sw128(kbase + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+                const uint32_t vbase = base + SL::kV + vs * SL::kKTile;
+                for (int kk = 0; kk < pn / 16; ++kk) {
+                    // A = P (TMEM, two bf16 per column), B = V (MN-major:
+                    // 64-column slabs LBO apart, 8-key groups SBO apart)
+                    const uint64_t b = smem_desc_sw128(vbase + kk * 16 * 128, SL::kKRegion, 1024);
+                    mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + kk * 8, b, kIdescPV,
+                                (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(SL::kSFull + wg));
-                mma_commit(bar(SL::kKEmpty + ks));
-                const bool last = (j == x.n_tiles - 1);
-                if (last) {
-                    mma_commit(bar(SL::kQEmpty + wg));
-                    ++nq[wg];
-                }
-                pend[wg] = true;
-                pend_gi[wg] = gi;
-                pend_n[wg] = n;
-                pend_first[wg] = (j == 0);
-                ++gi;
-                st[wg].next(p);
-                return true;
-            };
-            // O += P V for warpgroup wg's pending tile (P from TMEM over S_wg).
-            auto issue_pv = [&](int wg) -> bool {
-                const uint32_t g = pend_gi[wg];
-                const uint32_t vs = g % NSV;
-                if (!mbar_wait(bar(SL::kPFull + wg), npv[wg] & 1, &g_prefill_error, abort_flag))
-                    return false;
-                if (!mbar_wait(bar(SL::kVFull + vs), (g / NSV) & 1, &g_prefill_error, abort_flag))
-                    return false;
-                tc_fence_after_sync();
-                const uint32_t vbase = base + SL::kV + vs * SL::kTile;
-                const uint32_t o_tmem = tmem + 256 + wg * 128;
-                for (int kk = 0; kk < pend_n[wg] / 16; ++kk) {
-                    const uint64_t b = smem_desc_sw128(vbase + kk * 16 * 128, SL::kRegion, 1024);
-                    mma_bf16_ts(o_tmem, tmem + wg * 128 + kk * 8, b, kIdescPV,
-                                (!pend_first[wg] || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(SL::kODone + wg));
+                mma_commit(bar(SL::kPVDone));
                 mma_commit(bar(SL::kVEmpty + vs));
-                ++npv[wg];
-                pend[wg] = false;
                 any_pv = true;
+                last_pv_g = pg;
                 return true;
             };
 
-            for (int wg = 0; wg < 2 && ok; ++wg)
-                if (st[wg].valid) ok = issue_s(wg);
-            while (ok && (pend[0] || pend[1])) {
-                for (int wg = 0; wg < 2 && ok; ++wg) {
-                    if (!pend[wg]) continue;
-                    ok = issue_pv(wg);
-                    if (ok && st[wg].valid) ok = issue_s(wg);
+            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
+                const Unit x = unit_geom(u, p);
+                const uint32_t qb = uc & 1;
+                ok = mbar_wait(bar(SL::kQFull + qb), (uc >> 1) & 1, &g_prefill_error, abort_flag);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t qbase = base + SL::kQ + qb * SL::kQTile;
+                for (int j = 0; j < x.n_tiles; ++j, ++g) {
+                    const uint32_t ks = g % NSK;
+                    ok = mbar_wait(bar(SL::kKFull + ks), (g / NSK) & 1, &g_prefill_error,
+                                   abort_flag) &&
+                         mbar_wait(bar(SL::kSEmpty), (g & 1) ^ 1, &g_prefill_error, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const int n = tile_width(x, j);
+                    const uint32_t idesc = kIdescS | (static_cast<uint32_t>(n >> 3) << 17);
+                    const uint32_t kbase = base + SL::kK + ks * SL::kKTile;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t a = smem_desc_sw128(
+                            qbase + (kk >> 2) * SL::kQRegion + (kk & 3) * 32, 16, 1024);
+                        const uint64_t b = smem_desc_sw128(
+                            kbase + (kk >> 2) * SL::kKRegion + (kk & 3) * 32, 16, 1024);
+                        mma_bf16_ss(tmem + kTmemS, a, b, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(SL::kSFull));
+                    mma_commit(bar(SL::kKEmpty + ks));
+                    if (j == x.n_tiles - 1) mma_commit(bar(SL::kQEmpty + qb));
+                    if (have_prev) {
+                        ok = issue_pv(prev_g, prev_n, prev_first);
+                        if (!ok) break;
+                    }
+                    have_prev = true;
+                    prev_g = g;
+                    prev_n = n;
+                    prev_first = (j == 0);
                 }
             }
+            if (ok && have_prev) issue_pv(prev_g, prev_n, prev_first);
             // Drain: all issued MMAs complete before TMEM is released.
             if (any_pv) {
                 int no_abort = 0;
-                for (int wg = 0; wg < 2; ++wg)
-                    if (npv[wg] > 0)
-                        mbar_wait(bar(SL::kODone + wg), (npv[wg] - 1) & 1, &g_prefill_error,
-                                  &no_abort);
+                mbar_wait(bar(SL::kPVDone), last_pv_g & 1, &g_prefill_error, &no_abort);
             }
         }
-        __syncwarp();
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
         // ------------------------------------------------------------ softmax + epilogue
-        const int wg = (warp - 2) >> 2;           // warpgroup 0 (warps 2..5) or 1 (6..9)
+        const int half = (warp - 4) >> 2;         // this thread's chunks: half, half+2, ...
         const int quarter = warp & 3;             // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;      // MMA row == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t s_tmem = tmem + lane_addr + wg * 128;
-        const uint32_t o_tmem = tmem + lane_addr + 256 + wg * 128;
+        const uint32_t t_lane = tmem + lane_addr;
         const int prow = row / p.G;               // position offset within the tile
         const int hrow = row - prow * p.G;        // head offset within the group
-        uint32_t nt = 0;                          // tiles this warpgroup has finished
+        float *red = reinterpret_cast<float *>(gbase + SL::kRed);    // [2][2][128]
+        float *redl = reinterpret_cast<float *>(gbase + SL::kRedL);  // [2][128]
+        uint32_t g = 0;
 
-        for (int u = blockIdx.x + wg * gridDim.x; u < p.n_units; u += 2 * gridDim.x) {
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             const Unit x = unit_geom(u, p);
             const int t = x.t0 + prow;
             const bool row_valid = (t <= x.t1);
             const int lo_t = p.w < 0 ? 0 : max(p.s, t - (p.w - p.s) + 1);
             float m_run = -INFINITY;
-            float l_run = 0.f;
+            float l_half = 0.f;
 
-            for (int j = 0; j < x.n_tiles; ++j, ++nt) {
-                mbar_wait(bar(SL::kSFull + wg), nt & 1, &g_prefill_error, abort_flag);
+            for (int j = 0; j < x.n_tiles; ++j, ++g) {
+                mbar_wait(bar(SL::kSFull), g & 1, &g_prefill_error, abort_flag);
                 tc_fence_after_sync();
-                // mask: band columns [c_lo, c_hi], sink columns [0, sink_hi)
-                const int key0 = x.lo + 128 * j - p.s_pad;
+                // this thread's chunks: columns 32*(half + 2i) .. +31, i = 0..3
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tmem_ld32(t_lane + kTmemS + 32 * (half + 2 * i), sr[i]);
+                // column c of this tile is attended when c is in the band
+                // [c_lo, c_hi] or among the sinks [0, sink_hi)
+                const int key0 = x.lo + kKT * j - p.s_pad;
                 int c_lo = max(j == 0 ? p.s_pad : 0, lo_t - key0);
-                int c_hi = min(t - key0, 127);
+                int c_hi = min(t - key0, kKT - 1);
                 int sink_hi = (j == 0) ? min(p.s, t + 1) : 0;
                 if (!row_valid) {
-                    c_lo = 128;
+                    c_lo = kKT;
                     c_hi = -1;
                     sink_hi = 0;
                 }
-                // Column c of this tile is attended by the row when c is in the
-                // band [c_lo, c_hi] or among the sinks [0, sink_hi).  Per
-                // 32-column chunk the warp checks whether every row has the
-                // whole chunk in its band ("full": no mask) or none of it
-                // ("empty": no load, P = 0).
                 const bool band_ok = c_lo <= c_hi;
                 const unsigned span = band_ok ? static_cast<unsigned>(c_hi - c_lo) : 0u;
                 const int band_from = band_ok ? c_lo : 1 << 20;
-                auto flags = [&](int q, bool &full, bool &empty) {
-                    const bool f = band_ok && c_lo <= 32 * q && c_hi >= 32 * q + 31;
-                    const bool e = (!band_ok || c_hi < 32 * q || c_lo > 32 * q + 31) &&
-                                   sink_hi <= 32 * q;
-                    full = __all_sync(0xffffffffu, f);
-                    empty = __all_sync(0xffffffffu, e);
-                };
-                // pass 1: masked row max, S read from TMEM two chunks per wait
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-                for (int q = 0; q < 4; q += 2) {
-                    bool f0, e0, f1, e1;
-                    flags(q, f0, e0);
-                    flags(q + 1, f1, e1);
-                    if (e0 && e1) continue;
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(s_tmem + 32 * q, r0);
-                    tmem_ld32(s_tmem + 32 * q + 32, r1);
-                    tmem_wait_ld();
-                    const int x0 = 32 * q - band_from, sh = sink_hi - 32 * q;
-                    if (f0 && f1) {
+                bool full[4], empty[4];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r0[i]));
-                            m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r1[i]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const bool ok0 = static_cast<unsigned>(x0 + i) <= span || i < sh;
-                            const bool ok1 = static_cast<unsigned>(x0 + 32 + i) <= span || i + 32 < sh;
-                            m4[i & 3] = fmaxf(m4[i & 3], ok0 ? __uint_as_float(r0[i]) : -INFINITY);
-                            m4[i & 3] = fmaxf(m4[i & 3], ok1 ? __uint_as_float(r1[i]) : -INFINITY);
-                        }
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const int c0 = 32 * (half + 2 * i);
+                    const bool f = band_ok && c_lo <= c0 && c_hi >= c0 + 31;
+                    const bool e = (!band_ok || c_hi < c0 || c_lo > c0 + 31) && sink_hi <= c0;
+                    full[i] = __all_sync(0xffffffffu, f);
+                    empty[i] = __all_sync(0xffffffffu, e);
                 }
-                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                tmem_wait_ld();
+                // S has been read: the MMA warp may compute the next S now.
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(SL::kSEmpty));
+
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (empty[i]) continue;
+                    if (!full[i]) {
+                        const int x0 = 32 * (half + 2 * i) - band_from;
+                        const int sh = sink_hi - 32 * (half + 2 * i);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (!(static_cast<unsigned>(x0 + e) <= span || e < sh))
+                                sr[i][e] = __float_as_uint(-INFINITY);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[i][e]));
+                }
+                // row max over both halves (shared memory, one barrier per tile;
+                // the buffer alternates with the tile parity)
+                float *rm = red + (g & 1) * 256;
+                rm[half * 128 + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                const float mx = fmaxf(rm[row], rm[128 + row]);
                 const float m_new = fmaxf(m_run, mx);
                 float alpha = 1.f;
                 if (m_new > m_run &&
@@ -441,107 +388,96 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_run = m_new;
                 }
                 const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run * p.scale_log2;
-                // pass 2: P = exp2(S*scale - m) in bf16, written over the first
-                // 64 columns of S (the P of chunks q, q+1 lands on columns
-                // 16q .. 16q+31, which this pass has already read)
-                float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                for (int q = 0; q < 4; q += 2) {
-                    bool f0, e0, f1, e1;
-                    flags(q, f0, e0);
-                    flags(q + 1, f1, e1);
-                    uint32_t pk[32];
-                    if (e0 && e1) {
+                const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
+                const uint64_t nm2 = f32x2(neg_m, neg_m);
+                uint64_t l2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+                uint32_t pk[4][16];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) pk[i] = 0u;
-                    } else {
-                        uint32_t r0[32], r1[32];
-                        tmem_ld32(s_tmem + 32 * q, r0);
-                        tmem_ld32(s_tmem + 32 * q + 32, r1);
-                        tmem_wait_ld();
-                        if (!(f0 && f1)) {
-                            const int x0 = 32 * q - band_from, sh = sink_hi - 32 * q;
+                for (int i = 0; i < 4; ++i) {
+                    if (empty[i]) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                if (!(static_cast<unsigned>(x0 + i) <= span || i < sh))
-                                    r0[i] = __float_as_uint(-INFINITY);
-                                if (!(static_cast<unsigned>(x0 + 32 + i) <= span || i + 32 < sh))
-                                    r1[i] = __float_as_uint(-INFINITY);
-                            }
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float a0 = ex2_approx(fmaf(__uint_as_float(r0[2 * i]), p.scale_log2, neg_m));
-                            const float a1 = ex2_approx(fmaf(__uint_as_float(r0[2 * i + 1]), p.scale_log2, neg_m));
-                            const float b0 = ex2_approx(fmaf(__uint_as_float(r1[2 * i]), p.scale_log2, neg_m));
-                            const float b1 = ex2_approx(fmaf(__uint_as_float(r1[2 * i + 1]), p.scale_log2, neg_m));
-                            pk[i] = pack_bf16x2(a0, a1);
-                            pk[16 + i] = pack_bf16x2(b0, b1);
-                            l4[i & 3] += (a0 + a1) + (b0 + b1);
-                        }
+                        for (int e = 0; e < 16; ++e) pk[i][e] = 0u;
+                        continue;
                     }
-                    uint32_t lo16[16], hi16[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        lo16[i] = pk[i];
-                        hi16[i] = pk[16 + i];
+                    for (int e = 0; e < 16; ++e) {
+                        float a0, a1;
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[i][2 * e]),
+                                                    __uint_as_float(sr[i][2 * e + 1])),
+                                              sc2, nm2),
+                                    a0, a1);
+                        a0 = ex2_approx(a0);
+                        a1 = ex2_approx(a1);
+                        pk[i][e] = pack_bf16x2(a0, a1);
+                        l2[e & 1] = add_f32x2(l2[e & 1], f32x2(a0, a1));
                     }
-                    tmem_st16(s_tmem + 16 * q, lo16);
-                    tmem_st16(s_tmem + 16 * q + 16, hi16);
                 }
-                const float lsum = (l4[0] + l4[1]) + (l4[2] + l4[3]);
-                l_run = l_run * alpha + lsum;
+                float lx, ly, lz, lw;
+                f32x2_split(l2[0], lx, ly);
+                f32x2_split(l2[1], lz, lw);
+                l_half = l_half * alpha + ((lx + ly) + (lz + lw));
+                // P and O may be touched once the previous P V has completed.
+                if (g > 0) mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
+                tc_fence_after_sync();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tmem_st16(t_lane + kTmemP + 16 * (half + 2 * i), pk[i]);
                 // Rescale O when this warp raised any running max (not on the
-                // first tile: its P V overwrites O).  The previous P V of this
-                // warpgroup completed before this tile's S (same issuing thread).
+                // first tile: its P V overwrites O).  Each half owns d/2 columns.
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int c4 = 0; c4 < D / 32; ++c4) {
+                    for (int c = 0; c < D / 64; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(o_tmem + c4 * 32, r);
+                        const uint32_t ta = t_lane + kTmemO + half * (D / 2) + 32 * c;
+                        tmem_ld32(ta, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_tmem + c4 * 32, r);
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(ta, r);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(SL::kPFull + wg));
+                if (lane == 0) mbar_arrive(bar(SL::kPFull));
             }
 
             // ---------------------------------------------------- epilogue
-            mbar_wait(bar(SL::kODone + wg), (nt - 1) & 1, &g_prefill_error, abort_flag);
+            redl[half * 128 + row] = l_half;
+            mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
             tc_fence_after_sync();
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            const float l_run = redl[row] + redl[128 + row];
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
             const bool store = row_valid && !*abort_flag;
-            uint16_t *orow =
-                p.o + ((static_cast<int64_t>(x.b) * p.L + t) * p.Hq + x.kvh * p.G + hrow) * D;
+            uint16_t *orow = p.o +
+                             ((static_cast<int64_t>(x.b) * p.L + t) * p.Hq + x.kvh * p.G + hrow) * D +
+                             half * (D / 2);
 #pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
-                tmem_ld32(o_tmem + c4 * 32, r);
+                tmem_ld32(t_lane + kTmemO + half * (D / 2) + 32 * c, r);
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
-                                        __uint_as_float(r[2 * i + 1]) * inv_l);
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
+                                        __uint_as_float(r[2 * e + 1]) * inv_l);
                 if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c4 * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
                         dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
-            if (p.lse != nullptr && store) {
+            if (p.lse != nullptr && store && half == 0) {
                 const int h = x.kvh * p.G + hrow;
                 p.lse[(static_cast<int64_t>(x.b) * p.Hq + h) * p.L + t] =
                     m_run * p.scale + logf(l_run);
             }
-            tc_fence_before_sync();
+            // the row-sum buffer is rewritten by the next unit's epilogue only
+            // after every thread has passed this barrier
+            asm volatile("bar.sync 1, 256;" ::: "memory");
         }
     }
 
@@ -588,9 +524,7 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
     }
     const int sms = device_sm_count();
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
-    // two warpgroups per CTA: half as many CTAs as units keeps both busy
-    const int want = (p.n_units + 1) / 2;
-    const int grid = want < sms ? want : sms;
+    const int grid = p.n_units < sms ? p.n_units : sms;
     swa_prefill_kernel<D, NSK, NSV><<<grid, kThreads, SL::kAlloc, stream>>>(maps, p);
     e = cudaPeekAtLastError();
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_prefill_kernel");
@@ -620,16 +554,16 @@ swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, 
     PrefillMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     bool ok = encode_map(&maps.q, q, d, Hq, L, B, p.G, p.P) &&
-              encode_map(&maps.k_band, k, d, Hkv, L, B, 1, 128) &&
-              encode_map(&maps.v_band, v, d, Hkv, L, B, 1, 128);
+              encode_map(&maps.k_band, k, d, Hkv, L, B, 1, kKT) &&
+              encode_map(&maps.v_band, v, d, Hkv, L, B, 1, kKT);
     if (ok && p.s_pad > 0)
         ok = encode_map(&maps.k_sink, k, d, Hkv, L, B, 1, p.s_pad) &&
              encode_map(&maps.v_sink, v, d, Hkv, L, B, 1, p.s_pad) &&
-             encode_map(&maps.k_band0, k, d, Hkv, L, B, 1, 128 - p.s_pad) &&
-             encode_map(&maps.v_band0, v, d, Hkv, L, B, 1, 128 - p.s_pad);
+             encode_map(&maps.k_band0, k, d, Hkv, L, B, 1, kKT - p.s_pad) &&
+             encode_map(&maps.v_band0, v, d, Hkv, L, B, 1, kKT - p.s_pad);
     if (!ok) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    if (d == 128) return launch_prefill<128, 2, 3>(maps, p, stream);
-    return launch_prefill<64, 4, 6>(maps, p, stream);
+    if (d == 128) return launch_prefill<128, 1, 1>(maps, p, stream);
+    return launch_prefill<64, 2, 2>(maps, p, stream);
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {
