@@ -140,8 +140,8 @@ size_t swa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, int w)
  *                          swa_decode_workspace_bytes(...) bytes (may be NULL
  *                          when that is 0); contents need no initialisation
  *
- * Supported group sizes G = Hq/Hkv: 1, 2, 4 for d = 128; 1, 2, 4, 8 for
- * d = 64 (others return SWA_ERR_UNSUPPORTED).
+ * Supported group sizes G = Hq/Hkv: 1, 2, 4, 8 (others return
+ * SWA_ERR_UNSUPPORTED), and B*Hkv*cap below 2^31.
  * w and s must equal the cache's.  Reads the filled slots
  * [0, min(pos[b]+1, w)) (or [0, pos[b]+1) for SWA_W_INF); the softmax over a
  * set does not depend on slot order.  pos is read on the device and is not

@@ -87,7 +87,7 @@ swa_status check_cache(const swa_cache *c) {
 }
 
 bool decode_group_supported(int d, int G) {
-    if (d == 128) return G == 1 || G == 2 || G == 4;
+    (void)d;
     return G == 1 || G == 2 || G == 4 || G == 8;
 }
 
@@ -177,6 +177,9 @@ swa_status swa_check_decode(const void *q, const swa_cache *cache, const int32_t
     if (w != cache->w) return SWA_ERR_INVALID_ARG;
     if (w != SWA_W_INF && s != cache->s) return SWA_ERR_INVALID_ARG;
     if (!decode_group_supported(cache->d, Hq / cache->Hkv)) return SWA_ERR_UNSUPPORTED;
+    // the cache is addressed as B*Hkv*cap rows with 32-bit row coordinates
+    if (static_cast<int64_t>(cache->B) * cache->Hkv * cache->cap >= (int64_t(1) << 31))
+        return SWA_ERR_UNSUPPORTED;
     if (cache->B == 0) return SWA_OK;
     if (!q || !o || !pos) return SWA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(o)) return SWA_ERR_ALIGNMENT;

@@ -9,24 +9,29 @@
 // growing at w tokens: news page "No post-training, just 4 more tokens",
 // section "Research method".
 //
-// The path is bound by HBM bandwidth (each K/V byte is used by the G query
-// heads of its group and nothing else), so it runs on the CUDA cores:
-//   grid (split, kv head, sequence); each CTA streams its share of the slots
-//   in 32-slot chunks.  One producer warp moves chunks of K and V into shared
-//   memory with 1-D bulk copies (TMA engine, 4 stages, mbarrier completion);
-//   four consumer warps take 8 slots of each chunk.  Scores: 8 lanes per slot
-//   row, 16-byte shared loads, fp32 dot products for all G heads, then a
-//   reduce-scatter over the 8 lanes (each lane ends with whole dot products).
-//   Each warp keeps an online softmax (running max, sum, fp32 accumulators);
-//   warps are merged through shared memory at the end.  With several splits
-//   per (sequence, kv head) the CTAs write fp32 partials (max, sum, weighted
-//   values) and a second kernel merges them: m = max m_j,
-//   l = sum l_j 2^(m_j - m), o = sum acc_j 2^(m_j - m) / l.
+// The path is bound by HBM bandwidth: each K/V byte is used by the G query
+// heads of its group and nothing else.  Grid (split, kv head, sequence); each
+// CTA streams its share of the slots in 64-slot chunks.  A producer warp moves
+// the K and V rows of a chunk into shared memory with 2-D TMA copies
+// (128-byte swizzle, 2-stage ring, mbarrier completion).  Four consumer warps
+// take 16 slots each and use the warp-level tensor-core MMA
+// (mma.sync m16n8k16, bf16 in, fp32 accumulate) for both products with the
+// G <= 8 heads as the N = 8 dimension:
+//   S^T [16 slots x 8 heads] = K [16 x d] . Q^T [d x 8]   (K via ldmatrix)
+//   O^T [d x 8 heads]       += V^T [d x 16] . P^T [16 x 8] (V via ldmatrix.trans)
+// with an online softmax per head in between (running max raised only when it
+// grows by more than 2^8, which keeps the rescale rare and is exact).  Warps
+// are merged through shared memory at the end.  With several splits per
+// (sequence, kv head) the CTAs write fp32 partials (max, sum, weighted values)
+// and a second kernel merges them: m = max m_j, l = sum l_j 2^(m_j - m),
+// o = sum acc_j 2^(m_j - m) / l.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "swa_internal.h"
@@ -36,15 +41,17 @@ namespace swa {
 
 __device__ int g_decode_error;
 
-constexpr int kDecCH = 32;              // slots per chunk
-constexpr int kDecStages = 4;           // chunk ring depth
-constexpr int kDecWarps = 4;            // consumer warps
+constexpr int kDecCH = 64;              // slots per chunk
+constexpr int kDecStages = 2;           // chunk ring depth
+constexpr int kDecWarps = 4;            // consumer warps, 16 slots each
 constexpr int kDecThreads = 32 * (kDecWarps + 1);
+
+struct DecodeMaps {
+    CUtensorMap k, v;  // 2-D: {d, B*Hkv*cap rows}, box {64, 64}, 128-byte swizzle
+};
 
 struct DecodeParams {
     const uint16_t *q;   // [B, Hq, D] bf16
-    const uint16_t *ck;  // [B, Hkv, cap, D]
-    const uint16_t *cv;
     const int32_t *pos;  // [B]
     uint16_t *o;         // [B, Hq, D]
     float *ws_acc;       // [B*Hq, splits, D]
@@ -55,17 +62,19 @@ struct DecodeParams {
 
 template <int D, int G>
 struct DecSmem {
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kChunkBytes = kDecCH * kRowBytes;
+    static constexpr int kRegion = kDecCH * 128;            // 64 rows x 64 columns (bf16)
+    static constexpr int kChunkBytes = (D / 64) * kRegion;  // one of K or V
     static constexpr int kK = 0;
     static constexpr int kV = kK + kDecStages * kChunkBytes;
-    static constexpr int kScore = kV + kDecStages * kChunkBytes;      // [warp][8*G] f32
-    static constexpr int kProb = kScore + kDecWarps * 8 * G * 4;       // [warp][8*G] f32
-    static constexpr int kAcc = kProb + kDecWarps * 8 * G * 4;         // [warp][G][D] f32
-    static constexpr int kML = kAcc + kDecWarps * G * D * 4;           // [warp][G][2] f32
-    static constexpr int kBar = kML + kDecWarps * G * 2 * 4;           // full[st], empty[st]
+    static constexpr int kP = kV + kDecStages * kChunkBytes;  // [warp][16 slots][8 heads] bf16
+    static constexpr int kBar = kP + kDecWarps * 16 * 8 * 2;  // full[st], empty[st]
     static constexpr int kAbort = kBar + 2 * kDecStages * 8;
     static constexpr int kBytes = kAbort + 16;
+    static constexpr int kAlloc = kBytes + 1024;              // align the base to 1024
+    // merge buffers reuse the K stages once every chunk has been consumed
+    static constexpr int kAcc = kK;                           // [warp][G][D] f32
+    static constexpr int kML = kAcc + kDecWarps * G * D * 4;  // [warp][G][2] f32
+    static_assert(kML + kDecWarps * G * 2 * 4 <= kV, "merge buffers overflow the K stages");
 };
 
 // Slot range of one split: [begin, end); `used` = number of non-empty splits.
@@ -78,33 +87,52 @@ __device__ __forceinline__ void split_range(int n_valid, int splits, int split, 
     end = min(begin + per * kDecCH, n_valid);
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
-    f[0] = bf16lo_to_f32(u.x);
-    f[1] = bf16hi_to_f32(u.x);
-    f[2] = bf16lo_to_f32(u.y);
-    f[3] = bf16hi_to_f32(u.y);
-    f[4] = bf16lo_to_f32(u.z);
-    f[5] = bf16hi_to_f32(u.z);
-    f[6] = bf16lo_to_f32(u.w);
-    f[7] = bf16hi_to_f32(u.w);
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                            int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
-    return v;
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Address of 16-byte chunk `cc` (of the row's d/8) of chunk row `row` in a
+// stage laid out by the 128-byte-swizzled TMA box.
+__device__ __forceinline__ uint32_t swz(uint32_t stage, int row, int cc) {
+    return stage + (cc >> 3) * (kDecCH * 128) + row * 128 + ((((cc & 7) ^ (row & 7))) << 4);
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kDecThreads) swa_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads)
+    swa_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     using SL = DecSmem<D, G>;
-    constexpr int SEG = D / 64;        // 16-byte pieces per lane per row
-    constexpr int EPL = SEG * 8;       // elements per lane per row
-    constexpr int NV = 2 * G;          // dot products per lane before the reduction
-    extern __shared__ __align__(128) uint8_t sm[];
-    const uint32_t sbase = smem_u32(sm);
+    constexpr int KS = D / 16;  // k-steps of S, d-tiles of O
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *sm = smem_raw + (sbase - raw);
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SL::kAbort);
@@ -133,24 +161,27 @@ __global__ void __launch_bounds__(kDecThreads) swa_decode_kernel(const DecodePar
     }
     __syncthreads();
 
-    const int64_t row_base = (static_cast<int64_t>(b) * p.Hkv + kvh) * p.cap;  // slot 0
+    const int row_base = (b * p.Hkv + kvh) * p.cap;  // row of slot 0 in the 2-D maps
 
     if (warp == kDecWarps) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(&maps.v);
             int issued = 0;
             for (int c = 0; c < n_chunks; ++c) {
                 const int st = c % kDecStages;
                 if (!mbar_wait(empty(st), ((c / kDecStages) & 1) ^ 1, &g_decode_error, abort_flag))
                     break;
-                const int row0 = begin + c * kDecCH;
-                const int rows = min(kDecCH, end - row0);
-                const uint32_t bytes = static_cast<uint32_t>(rows) * SL::kRowBytes;
-                mbar_arrive_expect_tx(full(st), 2 * bytes);
-                bulk_load_1d(sbase + SL::kK + st * SL::kChunkBytes, p.ck + (row_base + row0) * D,
-                             bytes, full(st));
-                bulk_load_1d(sbase + SL::kV + st * SL::kChunkBytes, p.cv + (row_base + row0) * D,
-                             bytes, full(st));
+                const int row = row_base + begin + c * kDecCH;
+                mbar_arrive_expect_tx(full(st), 2 * SL::kChunkBytes);
+#pragma unroll
+                for (int r = 0; r < D / 64; ++r) {
+                    tma_load_2d(sbase + SL::kK + st * SL::kChunkBytes + r * SL::kRegion, &maps.k,
+                                full(st), r * 64, row);
+                    tma_load_2d(sbase + SL::kV + st * SL::kChunkBytes + r * SL::kRegion, &maps.v,
+                                full(st), r * 64, row);
+                }
                 issued = c + 1;
             }
             int no_abort = 0;  // drain the copies this thread started
@@ -163,176 +194,149 @@ __global__ void __launch_bounds__(kDecThreads) swa_decode_kernel(const DecodePar
     }
 
     // -------------------------------------------------------------------- consumers
-    const int rg = lane >> 3;  // row group: slot row within a 4-row step
-    const int gi = lane & 7;   // lane within the row group
-    float qf[G][EPL];          // q * log2(e)/sqrt(d), this lane's elements
+    const int gq = lane >> 2;  // mma group id: slot row g (and g+8), head g of B
+    const int tq = lane & 3;   // thread in group: heads 2t, 2t+1; k pairs 2t
+    // Q^T fragments (B operand of S^T): rows of heads gq < G, zero otherwise
+    uint32_t qb[KS][2];
+    {
+        const bool real = gq < G;
+        const uint16_t *qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * G + (real ? gq : 0)) * D;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        const uint16_t *qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * G + h) * D;
-#pragma unroll
-        for (int sg = 0; sg < SEG; ++sg) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(qrow + sg * 64 + gi * 8);
-            float f[8];
-            unpack8(u, f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qf[h][sg * 8 + e] = f[e] * p.scale_log2;
+        for (int ks = 0; ks < KS; ++ks) {
+            const uint32_t v0 = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tq);
+            const uint32_t v1 = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tq);
+            qb[ks][0] = real ? v0 : 0u;
+            qb[ks][1] = real ? v1 : 0u;
         }
     }
-    float acc[G][EPL];
+    float acc[KS][4];  // O^T: d = 16*mt + gq (+8), heads 2tq, 2tq+1
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
-    // per-head running max / sum, held by the lanes whose (lane % G) is the head
-    float m_h = -INFINITY, l_h = 0.f;
-    float *score = reinterpret_cast<float *>(sm + SL::kScore) + warp * 8 * G;
-    float *prob = reinterpret_cast<float *>(sm + SL::kProb) + warp * 8 * G;
-    constexpr int KC = (8 * G + 31) / 32;  // score entries per lane in the softmax step
+        for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY;  // running max, heads 2tq and 2tq+1
+    float l0 = 0.f, l1 = 0.f;              // this thread's share of the sums
+    uint16_t *psm = reinterpret_cast<uint16_t *>(sm + SL::kP) + warp * 16 * 8;
+    const int slot0 = warp * 16;           // this warp's slots within a chunk
 
     for (int c = 0; c < n_chunks; ++c) {
         const int st = c % kDecStages;
         mbar_wait(full(st), (c / kDecStages) & 1, &g_decode_error, abort_flag);
-        const int row0 = begin + c * kDecCH;
-        const int rows = min(kDecCH, end - row0);
-        const int wrow0 = warp * 8;
-        if (wrow0 < rows) {
+        const int rows = min(kDecCH, end - (begin + c * kDecCH));
+        const int mine = rows - slot0;  // valid slots among this warp's 16
+        if (mine > 0) {
             const uint32_t kst = sbase + SL::kK + st * SL::kChunkBytes;
             const uint32_t vst = sbase + SL::kV + st * SL::kChunkBytes;
-            // ---- scores: lane (rg, gi) covers 8 elements per segment of rows
-            //      wrow0 + sub*4 + rg, sub = 0, 1
-            float dots[NV];
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-                const int r = wrow0 + sub * 4 + rg;
-                float kf[EPL];
-#pragma unroll
-                for (int sg = 0; sg < SEG; ++sg) {
-                    float f[8];
-                    unpack8(lds128(kst + r * SL::kRowBytes + sg * 128 + gi * 16), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) kf[sg * 8 + e] = f[e];
+            if (mine < 16) {
+                // rows past the range hold whatever the cache has there: zero
+                // the V rows so that 0-weights never meet a non-finite value
+                uint8_t *vb = sm + SL::kV + st * SL::kChunkBytes;
+                for (int i = lane; i < (16 - mine) * (D / 8); i += 32) {
+                    const int r = slot0 + mine + i / (D / 8), cc = i % (D / 8);
+                    *reinterpret_cast<uint4 *>(vb + (cc >> 3) * SL::kRegion + r * 128 + ((cc & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
+                __syncwarp();
+            }
+            // ---- S^T = K Q^T
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float a = 0.f;
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(swz(kst, slot0 + (lane & 15), 2 * ks + (lane >> 4)), a);
+                mma_16816(s, a, qb[ks][0], qb[ks][1]);
+            }
+            // ---- online softmax per head over this warp's 16 slots
+            const bool va = gq < mine, vb_ = gq + 8 < mine;
+            const float s0 = va ? s[0] * p.scale_log2 : -INFINITY;   // slot g,   head 2t
+            const float s1 = va ? s[1] * p.scale_log2 : -INFINITY;   // slot g,   head 2t+1
+            const float s2 = vb_ ? s[2] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t
+            const float s3 = vb_ ? s[3] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t+1
+            float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) a = fmaf(qf[h][e], kf[e], a);
-                    dots[sub * G + h] = a;
+            for (int msk = 4; msk < 32; msk <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, msk));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, msk));
+            }
+            float a0 = 1.f, a1 = 1.f;
+            if (x0 > m0 && (m0 == -INFINITY || x0 - m0 > 8.f)) {
+                a0 = ex2_approx(m0 - x0);
+                m0 = x0;
+            }
+            if (x1 > m1 && (m1 == -INFINITY || x1 - m1 > 8.f)) {
+                a1 = ex2_approx(m1 - x1);
+                m1 = x1;
+            }
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+                l0 *= a0;
+                l1 *= a1;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    acc[mt][0] *= a0;
+                    acc[mt][2] *= a0;
+                    acc[mt][1] *= a1;
+                    acc[mt][3] *= a1;
                 }
             }
-            // ---- reduce over the 8 lanes of the row group (scatter while it
-            //      halves the values, plain butterfly after that)
-            int n = NV, idx0 = 0;
-#pragma unroll
-            for (int step = 4; step >= 1; step >>= 1) {
-                if (n >= 2) {
-                    const int half = n / 2;
-                    const bool hi = (gi & step) != 0;
-#pragma unroll
-                    for (int i = 0; i < NV / 2; ++i) {
-                        if (i < half) {
-                            const float send = hi ? dots[i] : dots[half + i];
-                            const float keep = hi ? dots[half + i] : dots[i];
-                            dots[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
-                        }
-                    }
-                    if (hi) idx0 += half;
-                    n = half;
-                } else {
-                    dots[0] += __shfl_xor_sync(0xffffffffu, dots[0], step);
-                }
-            }
-            // lane holds combos idx0 .. idx0+n-1, combo = sub*G + h
-#pragma unroll
-            for (int i = 0; i < (NV >= 8 ? NV / 8 : 1); ++i) {
-                const int ci = idx0 + i;
-                const int sub = ci / G, h = ci - sub * G;
-                const int rw = sub * 4 + rg;  // row within this warp's 8
-                score[rw * G + h] = (wrow0 + rw < rows) ? dots[i] : -INFINITY;
-            }
+            const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+            const float p0 = ex2_approx(s0 - u0), p1 = ex2_approx(s1 - u1);
+            const float p2 = ex2_approx(s2 - u0), p3 = ex2_approx(s3 - u1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            // ---- P^T through shared memory into the B-operand layout
+            *reinterpret_cast<uint32_t *>(psm + gq * 8 + 2 * tq) = pack_bf16x2(p0, p1);
+            *reinterpret_cast<uint32_t *>(psm + (gq + 8) * 8 + 2 * tq) = pack_bf16x2(p2, p3);
             __syncwarp();
-            // ---- online softmax per head (lane's head = lane % G)
-            float sv[KC];
-            float mx = -INFINITY;
+            const uint32_t pb0 = static_cast<uint32_t>(psm[(2 * tq) * 8 + gq]) |
+                                 (static_cast<uint32_t>(psm[(2 * tq + 1) * 8 + gq]) << 16);
+            const uint32_t pb1 = static_cast<uint32_t>(psm[(2 * tq + 8) * 8 + gq]) |
+                                 (static_cast<uint32_t>(psm[(2 * tq + 9) * 8 + gq]) << 16);
+            // ---- O^T += V^T P^T
+            const int vrow = slot0 + ((lane >> 4) << 3) + (lane & 7);
 #pragma unroll
-            for (int k = 0; k < KC; ++k) {
-                const int cj = lane + 32 * k;
-                sv[k] = cj < 8 * G ? score[cj] : -INFINITY;
-                mx = fmaxf(mx, sv[k]);
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a[4];
+                ldsm_x4_t(swz(vst, vrow, 2 * mt + ((lane >> 3) & 1)), a);
+                mma_16816(acc[mt], a, pb0, pb1);
             }
-#pragma unroll
-            for (int msk = G; msk < 32; msk <<= 1)
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
-            const float m_new = fmaxf(m_h, mx);
-            const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m_h - m_new);
-            float psum = 0.f;
-#pragma unroll
-            for (int k = 0; k < KC; ++k) {
-                const int cj = lane + 32 * k;
-                const float pv = (sv[k] == -INFINITY) ? 0.f : ex2_approx(sv[k] - m_new);
-                psum += pv;
-                if (cj < 8 * G) prob[cj] = pv;
-            }
-#pragma unroll
-            for (int msk = G; msk < 32; msk <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, msk);
-            l_h = l_h * alpha + psum;
-            m_h = m_new;
-            __syncwarp();
-            // ---- values: rescale, then accumulate this lane's rows
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float ah = __shfl_sync(0xffffffffu, alpha, h);
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[h][e] *= ah;
-            }
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-                const int rw = sub * 4 + rg;
-                if (wrow0 + rw < rows) {
-                    float vf[EPL];
-#pragma unroll
-                    for (int sg = 0; sg < SEG; ++sg) {
-                        float f[8];
-                        unpack8(lds128(vst + (wrow0 + rw) * SL::kRowBytes + sg * 128 + gi * 16), f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) vf[sg * 8 + e] = f[e];
-                    }
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float ph = prob[rw * G + h];
-#pragma unroll
-                        for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(ph, vf[e], acc[h][e]);
-                    }
-                }
-            }
+            if (mine < 16) fence_proxy_async_smem();  // zeroed rows before the next TMA fill
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(st));
     }
 
     // -------------------------------------------------------------------- merge
-    // over the four row groups of the warp (lanes with equal gi)
+    // sums over the 8 row groups of the warp (lanes with equal tq)
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 8);
-            acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], 16);
-        }
+    for (int msk = 4; msk < 32; msk <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");  // stages free
     float *wacc = reinterpret_cast<float *>(sm + SL::kAcc);
     float *wml = reinterpret_cast<float *>(sm + SL::kML);
-    if (rg == 0) {
+    const int h0 = 2 * tq, h1 = 2 * tq + 1;
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int sg = 0; sg < SEG; ++sg)
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    wacc[(warp * G + h) * D + sg * 64 + gi * 8 + e] = acc[h][sg * 8 + e];
+    for (int mt = 0; mt < KS; ++mt) {
+        const int d0 = 16 * mt + gq;
+        if (h0 < G) {
+            wacc[(warp * G + h0) * D + d0] = acc[mt][0];
+            wacc[(warp * G + h0) * D + d0 + 8] = acc[mt][2];
+        }
+        if (h1 < G) {
+            wacc[(warp * G + h1) * D + d0] = acc[mt][1];
+            wacc[(warp * G + h1) * D + d0 + 8] = acc[mt][3];
+        }
     }
-    if (lane < G) {
-        wml[(warp * G + lane) * 2 + 0] = m_h;
-        wml[(warp * G + lane) * 2 + 1] = l_h;
+    if (gq == 0) {
+        if (h0 < G) {
+            wml[(warp * G + h0) * 2 + 0] = m0;
+            wml[(warp * G + h0) * 2 + 1] = l0;
+        }
+        if (h1 < G) {
+            wml[(warp * G + h1) * 2 + 0] = m1;
+            wml[(warp * G + h1) * 2 + 1] = l1;
+        }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
     // over the warps; thread t handles outputs t, t+128, ...
@@ -405,7 +409,7 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int d, int cap, int w, int sm_cou
     DecodePlan plan{1, 0};
     const int cap_eff = w < 0 ? cap : w;
     const int chunks = (cap_eff + kDecCH - 1) / kDecCH;
-    const int max_splits = (chunks + 3) / 4;  // at least 4 chunks (128 slots) per split
+    const int max_splits = (chunks + 3) / 4;  // at least 4 chunks (256 slots) per split
     const long long pairs = static_cast<long long>(B) * Hkv;
     const long long target = 6LL * (sm_count > 0 ? sm_count : 148);  // ~2 waves of 3 CTAs/SM
     if (pairs > 0 && pairs < target) {
@@ -421,8 +425,20 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int d, int cap, int w, int sm_cou
 
 namespace {
 
+bool encode_cache_map(CUtensorMap *m, const void *ptr, int d, uint64_t rows) {
+    const cuTensorMapEncodeTiled_fn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kDecCH};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int G>
-swa_status launch_decode(const DecodeParams &p, cudaStream_t stream) {
+swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStream_t stream) {
     using SL = DecSmem<D, G>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -430,12 +446,12 @@ swa_status launch_decode(const DecodeParams &p, cudaStream_t stream) {
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
         e = cudaFuncSetAttribute(swa_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SL::kBytes);
+                                 SL::kAlloc);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode)");
         configured[dev] = true;
     }
     dim3 grid(p.splits, p.Hkv, p.B);
-    swa_decode_kernel<D, G><<<grid, kDecThreads, SL::kBytes, stream>>>(p);
+    swa_decode_kernel<D, G><<<grid, kDecThreads, SL::kAlloc, stream>>>(maps, p);
     e = cudaPeekAtLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_kernel");
     if (p.splits > 1) {
@@ -454,8 +470,6 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
     if (c.B == 0) return SWA_OK;
     DecodeParams p{};
     p.q = static_cast<const uint16_t *>(q);
-    p.ck = static_cast<const uint16_t *>(c.k);
-    p.cv = static_cast<const uint16_t *>(c.v);
     p.pos = pos;
     p.o = static_cast<uint16_t *>(o);
     p.B = c.B;
@@ -469,20 +483,26 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
         p.ws_ml = p.ws_acc + static_cast<size_t>(c.B) * Hq * plan.splits * c.d;
     }
     p.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(c.d));
+    DecodeMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const uint64_t rows = static_cast<uint64_t>(c.B) * c.Hkv * c.cap;
+    if (!encode_cache_map(&maps.k, c.k, c.d, rows) || !encode_cache_map(&maps.v, c.v, c.d, rows))
+        return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(cache)");
     const int G = Hq / c.Hkv;
     if (c.d == 128) {
         switch (G) {
-            case 1: return launch_decode<128, 1>(p, stream);
-            case 2: return launch_decode<128, 2>(p, stream);
-            case 4: return launch_decode<128, 4>(p, stream);
+            case 1: return launch_decode<128, 1>(maps, p, stream);
+            case 2: return launch_decode<128, 2>(maps, p, stream);
+            case 4: return launch_decode<128, 4>(maps, p, stream);
+            case 8: return launch_decode<128, 8>(maps, p, stream);
             default: return SWA_ERR_UNSUPPORTED;
         }
     }
     switch (G) {
-        case 1: return launch_decode<64, 1>(p, stream);
-        case 2: return launch_decode<64, 2>(p, stream);
-        case 4: return launch_decode<64, 4>(p, stream);
-        case 8: return launch_decode<64, 8>(p, stream);
+        case 1: return launch_decode<64, 1>(maps, p, stream);
+        case 2: return launch_decode<64, 2>(maps, p, stream);
+        case 4: return launch_decode<64, 4>(maps, p, stream);
+        case 8: return launch_decode<64, 8>(maps, p, stream);
         default: return SWA_ERR_UNSUPPORTED;
     }
 }

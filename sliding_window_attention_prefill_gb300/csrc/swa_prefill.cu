@@ -105,8 +105,8 @@ struct PrefillSmem {
     static constexpr int kK = kQ + 2 * kQTile;          // K ring
     static constexpr int kV = kK + NSK * kKTile;        // V ring
     static constexpr int kRed = kV + NSV * kKTile;      // row max [2 parity][2 half][128]
-    static constexpr int kRedL = kRed + 2 * 2 * 128 * 4;  // row sum [2 half][128]
-    static constexpr int kBar = kRedL + 2 * 128 * 4;
+    static constexpr int kRedL = kRed + 2 * 2 * 128 * 4;  // row sum [2 parity][2 half][128]
+    static constexpr int kBar = kRedL + 2 * 2 * 128 * 4;
     static constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = 4 + NSK,
                          kVFull = 4 + 2 * NSK, kVEmpty = 4 + 2 * NSK + NSV,
                          kSFull = 4 + 2 * NSK + 2 * NSV, kSEmpty = kSFull + 1,
@@ -311,10 +311,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int prow = row / p.G;               // position offset within the tile
         const int hrow = row - prow * p.G;        // head offset within the group
         float *red = reinterpret_cast<float *>(gbase + SL::kRed);    // [2][2][128]
-        float *redl = reinterpret_cast<float *>(gbase + SL::kRedL);  // [2][128]
-        uint32_t g = 0;
+        float *redl = reinterpret_cast<float *>(gbase + SL::kRedL);  // [2][2][128]
+        uint32_t g = 0, uc = 0;
 
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+        // The epilogue of a unit (O / l -> bf16 -> global, LSE) is deferred
+        // into the first tile of the next unit: that tile's scores and
+        // weights are computed while the previous unit's last P V runs, and
+        // O is read out just before the new P is written.
+        bool pend = false, pend_valid = false;
+        int pend_b = 0, pend_kvh = 0, pend_t = 0;
+        float pend_m = 0.f, pend_l = 0.f;
+        auto epilogue = [&](float l_tot) {
+            const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const bool store = pend_valid && !*abort_flag;
+            uint16_t *orow =
+                p.o + ((static_cast<int64_t>(pend_b) * p.L + pend_t) * p.Hq + pend_kvh * p.G + hrow) * D +
+                half * (D / 2);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_lane + kTmemO + half * (D / 2) + 32 * c, r);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
+                                        __uint_as_float(r[2 * e + 1]) * inv_l);
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (p.lse != nullptr && store && half == 0) {
+                const int h = pend_kvh * p.G + hrow;
+                p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + pend_t] =
+                    pend_m * p.scale + logf(l_tot);
+            }
+        };
+
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++uc) {
             const Unit x = unit_geom(u, p);
             const int t = x.t0 + prow;
             const bool row_valid = (t <= x.t1);
@@ -374,12 +411,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e)
                         m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[i][e]));
                 }
-                // row max over both halves (shared memory, one barrier per tile;
-                // the buffer alternates with the tile parity)
+                // Row max over both halves through shared memory, one barrier
+                // per tile (buffers alternate with the tile parity); the first
+                // tile of a unit also exchanges the previous unit's row sums.
                 float *rm = red + (g & 1) * 256;
+                float *rl = redl + ((uc - 1) & 1) * 256;
                 rm[half * 128 + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                const bool do_epi = (j == 0 && pend);
+                if (do_epi) rl[half * 128 + row] = pend_l;
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 const float mx = fmaxf(rm[row], rm[128 + row]);
+                const float l_prev = do_epi ? rl[row] + rl[128 + row] : 0.f;
                 const float m_new = fmaxf(m_run, mx);
                 float alpha = 1.f;
                 if (m_new > m_run &&
@@ -416,9 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 f32x2_split(l2[0], lx, ly);
                 f32x2_split(l2[1], lz, lw);
                 l_half = l_half * alpha + ((lx + ly) + (lz + lw));
-                // P and O may be touched once the previous P V has completed.
+                // P and O may be touched once the previous P V (of this unit,
+                // or the last one of the previous unit) has completed.
                 if (g > 0) mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
                 tc_fence_after_sync();
+                if (do_epi) {
+                    epilogue(l_prev);
+                    pend = false;
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) tmem_st16(t_lane + kTmemP + 16 * (half + 2 * i), pk[i]);
                 // Rescale O when this warp raised any running max (not on the
@@ -441,43 +488,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(SL::kPFull));
             }
-
-            // ---------------------------------------------------- epilogue
-            redl[half * 128 + row] = l_half;
+            pend = true;
+            pend_valid = row_valid;
+            pend_b = x.b;
+            pend_kvh = x.kvh;
+            pend_t = t;
+            pend_m = m_run;
+            pend_l = l_half;
+        }
+        if (pend) {  // the last unit's epilogue
+            float *rl = redl + ((uc - 1) & 1) * 256;
+            rl[half * 128 + row] = pend_l;
             mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
             tc_fence_after_sync();
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            const float l_run = redl[row] + redl[128 + row];
-            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-            const bool store = row_valid && !*abort_flag;
-            uint16_t *orow = p.o +
-                             ((static_cast<int64_t>(x.b) * p.L + t) * p.Hq + x.kvh * p.G + hrow) * D +
-                             half * (D / 2);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t r[32];
-                tmem_ld32(t_lane + kTmemO + half * (D / 2) + 32 * c, r);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
-                                        __uint_as_float(r[2 * e + 1]) * inv_l);
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                }
-            }
-            if (p.lse != nullptr && store && half == 0) {
-                const int h = x.kvh * p.G + hrow;
-                p.lse[(static_cast<int64_t>(x.b) * p.Hq + h) * p.L + t] =
-                    m_run * p.scale + logf(l_run);
-            }
-            // the row-sum buffer is rewritten by the next unit's epilogue only
-            // after every thread has passed this barrier
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            epilogue(rl[row] + rl[128 + row]);
         }
     }
 

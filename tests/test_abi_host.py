@@ -94,7 +94,9 @@ def test_check_decode(L):
     assert c(q, ctypes.byref(cache), pos, 8, 128, 4, o, None, 0, 0) == INVALID   # w differs
     assert c(q, ctypes.byref(cache), pos, 8, 64, 3, o, None, 0, 0) == INVALID    # s differs
     assert c(q, ctypes.byref(cache), pos, 7, 64, 4, o, None, 0, 0) == INVALID    # Hq % Hkv
-    assert c(q, ctypes.byref(cache), pos, 16, 64, 4, o, None, 0, 0) == UNSUPPORTED  # G = 8, d = 128
+    assert c(q, ctypes.byref(cache), pos, 32, 64, 4, o, None, 0, 0) == UNSUPPORTED  # G = 16
+    big = _cache(B=1 << 12, Hkv=8, d=128, cap=1 << 16, w=INF, s=0, k=1 << 44, v=1 << 46)
+    assert c(q, ctypes.byref(big), pos, 32, INF, 0, o, None, 0, 0) == UNSUPPORTED  # 2^31 rows
     assert c(q, ctypes.byref(cache), ctypes.c_void_p(FAKE * 7100 + 2), 8, 64, 4, o, None, 0, 0) == ALIGN
     assert c(q, ctypes.byref(cache), None, 8, 64, 4, o, None, 0, 0) == INVALID
 

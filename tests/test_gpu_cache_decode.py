@@ -77,6 +77,8 @@ def test_decode_llama_batch64(w):
     (2, 8, 8, 128, 64, 4, 10),     # G=1, cache still filling
     (3, 8, 4, 128, 33, 1, 200),    # G=2, odd window
     (2, 16, 2, 64, 100, 4, 300),   # G=8 (d=64)
+    (2, 16, 2, 128, 96, 4, 150),   # G=8 (d=128)
+    (3, 8, 8, 64, 70, 2, 140),     # G=1, d=64, ragged tail chunks
     (1, 4, 1, 64, 5, 4, 40),       # ring of one slot
     (2, 8, 2, 128, 128, 0, 50),    # no sinks, filling
 ])
