@@ -10,21 +10,23 @@
 // section "Research method".
 //
 // The path is bound by HBM bandwidth: each K/V byte is used by the G query
-// heads of its group and nothing else.  Grid (split, kv head, sequence); each
-// CTA streams its share of the slots in 64-slot chunks.  A producer warp moves
-// the K and V rows of a chunk into shared memory with 2-D TMA copies
-// (128-byte swizzle, 2-stage ring, mbarrier completion).  Four consumer warps
-// take 16 slots each and use the warp-level tensor-core MMA
+// heads of its group and nothing else.  The work is a list of items
+// (sequence, kv head, split of the filled slots); a persistent grid of CTAs
+// walks it with a stride of gridDim.x.  In each CTA a producer warp streams
+// the K and V rows of its items in 64-slot chunks, back to back across item
+// boundaries, into shared memory with 2-D TMA copies (128-byte swizzle,
+// mbarrier ring); q of the item rides along with its first chunk.  Four
+// consumer warps take 16 slots each and use the warp-level tensor-core MMA
 // (mma.sync m16n8k16, bf16 in, fp32 accumulate) for both products with the
 // G <= 8 heads as the N = 8 dimension:
 //   S^T [16 slots x 8 heads] = K [16 x d] . Q^T [d x 8]   (K via ldmatrix)
 //   O^T [d x 8 heads]       += V^T [d x 16] . P^T [16 x 8] (V via ldmatrix.trans)
 // with an online softmax per head in between (running max raised only when it
-// grows by more than 2^8, which keeps the rescale rare and is exact).  Warps
-// are merged through shared memory at the end.  With several splits per
-// (sequence, kv head) the CTAs write fp32 partials (max, sum, weighted values)
-// and a second kernel merges them: m = max m_j, l = sum l_j 2^(m_j - m),
-// o = sum acc_j 2^(m_j - m) / l.
+// grows by more than 2^8, which keeps the rescale rare and is exact).  At the
+// end of an item the warps are merged through shared memory.  With several
+// splits per (sequence, kv head) the items write fp32 partials (max, sum,
+// weighted values) and a second kernel merges them: m = max m_j,
+// l = sum l_j 2^(m_j - m), o = sum acc_j 2^(m_j - m) / l.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,8 +43,17 @@ namespace swa {
 
 __device__ int g_decode_error;
 
+#ifndef SWA_DEC_STAGES
+#define SWA_DEC_STAGES 2
+#endif
+#ifndef SWA_DEC_ITEMS_PER_SM
+#define SWA_DEC_ITEMS_PER_SM 4
+#endif
+#ifndef SWA_DEC_CTAS_PER_SM
+#define SWA_DEC_CTAS_PER_SM 2
+#endif
 constexpr int kDecCH = 64;              // slots per chunk
-constexpr int kDecStages = 2;           // chunk ring depth
+constexpr int kDecStages = SWA_DEC_STAGES;  // chunk ring depth
 constexpr int kDecWarps = 4;            // consumer warps, 16 slots each
 constexpr int kDecThreads = 32 * (kDecWarps + 1);
 
@@ -64,17 +75,15 @@ template <int D, int G>
 struct DecSmem {
     static constexpr int kRegion = kDecCH * 128;            // 64 rows x 64 columns (bf16)
     static constexpr int kChunkBytes = (D / 64) * kRegion;  // one of K or V
-    static constexpr int kK = 0;
-    static constexpr int kV = kK + kDecStages * kChunkBytes;
-    static constexpr int kP = kV + kDecStages * kChunkBytes;  // [warp][16 slots][8 heads] bf16
-    static constexpr int kBar = kP + kDecWarps * 16 * 8 * 2;  // full[st], empty[st]
+    static constexpr int kQBytes = G * D * 2;               // q of the G heads of the item
+    static constexpr int kStage = 2 * kChunkBytes + ((kQBytes + 1023) & ~1023);  // K | V | q
+    static constexpr int kP = kDecStages * kStage;          // [warp][16 slots][8 heads] bf16
+    static constexpr int kAcc = kP + kDecWarps * 16 * 8 * 2;  // [warp][G][D] f32
+    static constexpr int kML = kAcc + kDecWarps * G * D * 4;  // [warp][G][2] f32
+    static constexpr int kBar = kML + kDecWarps * G * 2 * 4;  // full[st], empty[st]
     static constexpr int kAbort = kBar + 2 * kDecStages * 8;
     static constexpr int kBytes = kAbort + 16;
     static constexpr int kAlloc = kBytes + 1024;              // align the base to 1024
-    // merge buffers reuse the K stages once every chunk has been consumed
-    static constexpr int kAcc = kK;                           // [warp][G][D] f32
-    static constexpr int kML = kAcc + kDecWarps * G * D * 4;  // [warp][G][2] f32
-    static_assert(kML + kDecWarps * G * 2 * 4 <= kV, "merge buffers overflow the K stages");
 };
 
 // Slot range of one split: [begin, end); `used` = number of non-empty splits.
@@ -124,6 +133,35 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int row, int cc) {
     return stage + (cc >> 3) * (kDecCH * 128) + row * 128 + ((((cc & 7) ^ (row & 7))) << 4);
 }
 
+// One work item: the slots [begin, end) of (sequence b, kv head kvh) that
+// split `split` covers; n_chunks == 0 when there is nothing to do (empty
+// split, or a position outside the cache, which is recorded as an error).
+struct DecItem {
+    int b, kvh, split, begin, end, n_chunks;
+    bool bad;
+};
+
+__device__ __forceinline__ DecItem dec_item(int it, const DecodeParams &p) {
+    DecItem x;
+    const int pair = it / p.splits;
+    x.split = it - pair * p.splits;
+    x.b = pair / p.Hkv;
+    x.kvh = pair - x.b * p.Hkv;
+    const int pos = p.pos[x.b];
+    x.bad = pos < 0 || (p.w < 0 && pos >= p.cap);
+    x.begin = x.end = x.n_chunks = 0;
+    if (!x.bad) {
+        const int cap_eff = p.w < 0 ? p.cap : p.w;
+        int used;
+        split_range(min(pos + 1, cap_eff), p.splits, x.split, x.begin, x.end, used);
+        if (x.end > x.begin) x.n_chunks = (x.end - x.begin + kDecCH - 1) / kDecCH;
+    }
+    return x;
+}
+
+// Persistent: each CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...;
+// the producer streams their chunks back to back, so the latency of the
+// first loads is paid once per CTA rather than once per item.
 template <int D, int G>
 __global__ void __launch_bounds__(kDecThreads)
     swa_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
@@ -133,23 +171,11 @@ __global__ void __launch_bounds__(kDecThreads)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t *sm = smem_raw + (sbase - raw);
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SL::kAbort);
     auto full = [&](int st) { return sbase + SL::kBar + 8u * st; };
     auto empty = [&](int st) { return sbase + SL::kBar + 8u * (kDecStages + st); };
-
-    const int pos = p.pos[b];
-    if (pos < 0 || (p.w < 0 && pos >= p.cap)) {
-        if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicCAS(&g_decode_error, 0, kErrBounds);
-        return;
-    }
-    const int cap_eff = p.w < 0 ? p.cap : p.w;
-    const int n_valid = min(pos + 1, cap_eff);
-    int begin, end, used;
-    split_range(n_valid, p.splits, split, begin, end, used);
-    if (begin >= end) return;  // uniform over the block
-    const int n_chunks = (end - begin + kDecCH - 1) / kDecCH;
+    const int n_items = p.B * p.Hkv * p.splits;
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kDecStages; ++st) {
@@ -161,32 +187,38 @@ __global__ void __launch_bounds__(kDecThreads)
     }
     __syncthreads();
 
-    const int row_base = (b * p.Hkv + kvh) * p.cap;  // row of slot 0 in the 2-D maps
-
     if (warp == kDecWarps) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             tma_prefetch_desc(&maps.k);
             tma_prefetch_desc(&maps.v);
-            int issued = 0;
-            for (int c = 0; c < n_chunks; ++c) {
-                const int st = c % kDecStages;
-                if (!mbar_wait(empty(st), ((c / kDecStages) & 1) ^ 1, &g_decode_error, abort_flag))
-                    break;
-                const int row = row_base + begin + c * kDecCH;
-                mbar_arrive_expect_tx(full(st), 2 * SL::kChunkBytes);
+            int cg = 0;  // chunks issued by this CTA
+            bool ok = true;
+            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+                const DecItem x = dec_item(it, p);
+                if (x.bad && x.kvh == 0 && x.split == 0) atomicCAS(&g_decode_error, 0, kErrBounds);
+                const int row_base = (x.b * p.Hkv + x.kvh) * p.cap;  // row of slot 0
+                const uint16_t *qsrc = p.q + (static_cast<int64_t>(x.b) * p.Hq + x.kvh * G) * D;
+                for (int c = 0; c < x.n_chunks; ++c, ++cg) {
+                    const int st = cg % kDecStages;
+                    ok = mbar_wait(empty(st), ((cg / kDecStages) & 1) ^ 1, &g_decode_error, abort_flag);
+                    if (!ok) break;
+                    const uint32_t stage = sbase + st * SL::kStage;
+                    const int row = row_base + x.begin + c * kDecCH;
+                    // q rides along with the first chunk of each item
+                    mbar_arrive_expect_tx(full(st), 2 * SL::kChunkBytes + (c == 0 ? SL::kQBytes : 0));
 #pragma unroll
-                for (int r = 0; r < D / 64; ++r) {
-                    tma_load_2d(sbase + SL::kK + st * SL::kChunkBytes + r * SL::kRegion, &maps.k,
-                                full(st), r * 64, row);
-                    tma_load_2d(sbase + SL::kV + st * SL::kChunkBytes + r * SL::kRegion, &maps.v,
-                                full(st), r * 64, row);
+                    for (int r = 0; r < D / 64; ++r) {
+                        tma_load_2d(stage + r * SL::kRegion, &maps.k, full(st), r * 64, row);
+                        tma_load_2d(stage + SL::kChunkBytes + r * SL::kRegion, &maps.v, full(st),
+                                    r * 64, row);
+                    }
+                    if (c == 0) bulk_load_1d(stage + 2 * SL::kChunkBytes, qsrc, SL::kQBytes, full(st));
                 }
-                issued = c + 1;
             }
             int no_abort = 0;  // drain the copies this thread started
-            for (int i = 0; i < kDecStages && i < issued; ++i) {
-                const int c = issued - 1 - i;
+            for (int i = 0; i < kDecStages && i < cg; ++i) {
+                const int c = cg - 1 - i;
                 mbar_wait(full(c % kDecStages), (c / kDecStages) & 1, &g_decode_error, &no_abort);
             }
         }
@@ -196,172 +228,177 @@ __global__ void __launch_bounds__(kDecThreads)
     // -------------------------------------------------------------------- consumers
     const int gq = lane >> 2;  // mma group id: slot row g (and g+8), head g of B
     const int tq = lane & 3;   // thread in group: heads 2t, 2t+1; k pairs 2t
-    // Q^T fragments (B operand of S^T): rows of heads gq < G, zero otherwise
-    uint32_t qb[KS][2];
-    {
-        const bool real = gq < G;
-        const uint16_t *qrow = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * G + (real ? gq : 0)) * D;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const uint32_t v0 = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tq);
-            const uint32_t v1 = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tq);
-            qb[ks][0] = real ? v0 : 0u;
-            qb[ks][1] = real ? v1 : 0u;
-        }
-    }
-    float acc[KS][4];  // O^T: d = 16*mt + gq (+8), heads 2tq, 2tq+1
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY;  // running max, heads 2tq and 2tq+1
-    float l0 = 0.f, l1 = 0.f;              // this thread's share of the sums
     uint16_t *psm = reinterpret_cast<uint16_t *>(sm + SL::kP) + warp * 16 * 8;
-    const int slot0 = warp * 16;           // this warp's slots within a chunk
-
-    for (int c = 0; c < n_chunks; ++c) {
-        const int st = c % kDecStages;
-        mbar_wait(full(st), (c / kDecStages) & 1, &g_decode_error, abort_flag);
-        const int rows = min(kDecCH, end - (begin + c * kDecCH));
-        const int mine = rows - slot0;  // valid slots among this warp's 16
-        if (mine > 0) {
-            const uint32_t kst = sbase + SL::kK + st * SL::kChunkBytes;
-            const uint32_t vst = sbase + SL::kV + st * SL::kChunkBytes;
-            if (mine < 16) {
-                // rows past the range hold whatever the cache has there: zero
-                // the V rows so that 0-weights never meet a non-finite value
-                uint8_t *vb = sm + SL::kV + st * SL::kChunkBytes;
-                for (int i = lane; i < (16 - mine) * (D / 8); i += 32) {
-                    const int r = slot0 + mine + i / (D / 8), cc = i % (D / 8);
-                    *reinterpret_cast<uint4 *>(vb + (cc >> 3) * SL::kRegion + r * 128 + ((cc & 7) << 4)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                __syncwarp();
-            }
-            // ---- S^T = K Q^T
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a[4];
-                ldsm_x4(swz(kst, slot0 + (lane & 15), 2 * ks + (lane >> 4)), a);
-                mma_16816(s, a, qb[ks][0], qb[ks][1]);
-            }
-            // ---- online softmax per head over this warp's 16 slots
-            const bool va = gq < mine, vb_ = gq + 8 < mine;
-            const float s0 = va ? s[0] * p.scale_log2 : -INFINITY;   // slot g,   head 2t
-            const float s1 = va ? s[1] * p.scale_log2 : -INFINITY;   // slot g,   head 2t+1
-            const float s2 = vb_ ? s[2] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t
-            const float s3 = vb_ ? s[3] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t+1
-            float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
-#pragma unroll
-            for (int msk = 4; msk < 32; msk <<= 1) {
-                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, msk));
-                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, msk));
-            }
-            float a0 = 1.f, a1 = 1.f;
-            if (x0 > m0 && (m0 == -INFINITY || x0 - m0 > 8.f)) {
-                a0 = ex2_approx(m0 - x0);
-                m0 = x0;
-            }
-            if (x1 > m1 && (m1 == -INFINITY || x1 - m1 > 8.f)) {
-                a1 = ex2_approx(m1 - x1);
-                m1 = x1;
-            }
-            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
-                l0 *= a0;
-                l1 *= a1;
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    acc[mt][0] *= a0;
-                    acc[mt][2] *= a0;
-                    acc[mt][1] *= a1;
-                    acc[mt][3] *= a1;
-                }
-            }
-            const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
-            const float p0 = ex2_approx(s0 - u0), p1 = ex2_approx(s1 - u1);
-            const float p2 = ex2_approx(s2 - u0), p3 = ex2_approx(s3 - u1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // ---- P^T through shared memory into the B-operand layout
-            *reinterpret_cast<uint32_t *>(psm + gq * 8 + 2 * tq) = pack_bf16x2(p0, p1);
-            *reinterpret_cast<uint32_t *>(psm + (gq + 8) * 8 + 2 * tq) = pack_bf16x2(p2, p3);
-            __syncwarp();
-            const uint32_t pb0 = static_cast<uint32_t>(psm[(2 * tq) * 8 + gq]) |
-                                 (static_cast<uint32_t>(psm[(2 * tq + 1) * 8 + gq]) << 16);
-            const uint32_t pb1 = static_cast<uint32_t>(psm[(2 * tq + 8) * 8 + gq]) |
-                                 (static_cast<uint32_t>(psm[(2 * tq + 9) * 8 + gq]) << 16);
-            // ---- O^T += V^T P^T
-            const int vrow = slot0 + ((lane >> 4) << 3) + (lane & 7);
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                uint32_t a[4];
-                ldsm_x4_t(swz(vst, vrow, 2 * mt + ((lane >> 3) & 1)), a);
-                mma_16816(acc[mt], a, pb0, pb1);
-            }
-            if (mine < 16) fence_proxy_async_smem();  // zeroed rows before the next TMA fill
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty(st));
-    }
-
-    // -------------------------------------------------------------------- merge
-    // sums over the 8 row groups of the warp (lanes with equal tq)
-#pragma unroll
-    for (int msk = 4; msk < 32; msk <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");  // stages free
     float *wacc = reinterpret_cast<float *>(sm + SL::kAcc);
     float *wml = reinterpret_cast<float *>(sm + SL::kML);
-    const int h0 = 2 * tq, h1 = 2 * tq + 1;
+    const int slot0 = warp * 16;  // this warp's slots within a chunk
+    int cg = 0;                   // chunks consumed by this CTA
+
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const DecItem x = dec_item(it, p);
+        if (x.n_chunks == 0) continue;
+        float acc[KS][4];  // O^T: d = 16*mt + gq (+8), heads 2tq, 2tq+1
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-        const int d0 = 16 * mt + gq;
-        if (h0 < G) {
-            wacc[(warp * G + h0) * D + d0] = acc[mt][0];
-            wacc[(warp * G + h0) * D + d0 + 8] = acc[mt][2];
-        }
-        if (h1 < G) {
-            wacc[(warp * G + h1) * D + d0] = acc[mt][1];
-            wacc[(warp * G + h1) * D + d0 + 8] = acc[mt][3];
-        }
-    }
-    if (gq == 0) {
-        if (h0 < G) {
-            wml[(warp * G + h0) * 2 + 0] = m0;
-            wml[(warp * G + h0) * 2 + 1] = l0;
-        }
-        if (h1 < G) {
-            wml[(warp * G + h1) * 2 + 0] = m1;
-            wml[(warp * G + h1) * 2 + 1] = l1;
-        }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
-    // over the warps; thread t handles outputs t, t+128, ...
-    for (int idx = threadIdx.x; idx < G * D; idx += kDecWarps * 32) {
-        const int h = idx / D, e = idx - h * D;
-        float m = -INFINITY;
+        for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, wml[(w * G + h) * 2]);
-        float l = 0.f, a = 0.f;
+            for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY;  // running max, heads 2tq and 2tq+1
+        float l0 = 0.f, l1 = 0.f;              // this thread's share of the sums
+        uint32_t qb[KS][2];                    // Q^T fragments; heads gq >= G are zero columns
+
+        for (int c = 0; c < x.n_chunks; ++c, ++cg) {
+            const int st = cg % kDecStages;
+            mbar_wait(full(st), (cg / kDecStages) & 1, &g_decode_error, abort_flag);
+            const int rows = min(kDecCH, x.end - (x.begin + c * kDecCH));
+            const int mine = rows - slot0;  // valid slots among this warp's 16
+            if (c == 0) {
+                const uint16_t *qrow = reinterpret_cast<const uint16_t *>(
+                                           sm + st * SL::kStage + 2 * SL::kChunkBytes) +
+                                       (gq < G ? gq : 0) * D;
 #pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) {
-            const float wm = wml[(w * G + h) * 2];
-            const float f = (wm == -INFINITY) ? 0.f : ex2_approx(wm - m);
-            l = fmaf(wml[(w * G + h) * 2 + 1], f, l);
-            a = fmaf(wacc[(w * G + h) * D + e], f, a);
+                for (int ks = 0; ks < KS; ++ks) {
+                    qb[ks][0] = gq < G ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tq) : 0u;
+                    qb[ks][1] = gq < G ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tq) : 0u;
+                }
+            }
+            if (mine > 0) {
+                const uint32_t kst = sbase + st * SL::kStage;
+                const uint32_t vst = kst + SL::kChunkBytes;
+                if (mine < 16) {
+                    // rows past the range hold whatever the cache has there: zero
+                    // the V rows so that 0-weights never meet a non-finite value
+                    uint8_t *vb = sm + st * SL::kStage + SL::kChunkBytes;
+                    for (int i = lane; i < (16 - mine) * (D / 8); i += 32) {
+                        const int r = slot0 + mine + i / (D / 8), cc = i % (D / 8);
+                        *reinterpret_cast<uint4 *>(vb + (cc >> 3) * SL::kRegion + r * 128 +
+                                                   ((cc & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+                }
+                // ---- S^T = K Q^T
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a[4];
+                    ldsm_x4(swz(kst, slot0 + (lane & 15), 2 * ks + (lane >> 4)), a);
+                    mma_16816(s, a, qb[ks][0], qb[ks][1]);
+                }
+                // ---- online softmax per head over this warp's 16 slots
+                const bool va = gq < mine, vb_ = gq + 8 < mine;
+                const float s0 = va ? s[0] * p.scale_log2 : -INFINITY;   // slot g,   head 2t
+                const float s1 = va ? s[1] * p.scale_log2 : -INFINITY;   // slot g,   head 2t+1
+                const float s2 = vb_ ? s[2] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t
+                const float s3 = vb_ ? s[3] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t+1
+                float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int msk = 4; msk < 32; msk <<= 1) {
+                    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, msk));
+                    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, msk));
+                }
+                float a0 = 1.f, a1 = 1.f;
+                if (x0 > m0 && (m0 == -INFINITY || x0 - m0 > 8.f)) {
+                    a0 = ex2_approx(m0 - x0);
+                    m0 = x0;
+                }
+                if (x1 > m1 && (m1 == -INFINITY || x1 - m1 > 8.f)) {
+                    a1 = ex2_approx(m1 - x1);
+                    m1 = x1;
+                }
+                if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+                    l0 *= a0;
+                    l1 *= a1;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        acc[mt][0] *= a0;
+                        acc[mt][2] *= a0;
+                        acc[mt][1] *= a1;
+                        acc[mt][3] *= a1;
+                    }
+                }
+                const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+                const float p0 = ex2_approx(s0 - u0), p1 = ex2_approx(s1 - u1);
+                const float p2 = ex2_approx(s2 - u0), p3 = ex2_approx(s3 - u1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                // ---- P^T through shared memory into the B-operand layout
+                *reinterpret_cast<uint32_t *>(psm + gq * 8 + 2 * tq) = pack_bf16x2(p0, p1);
+                *reinterpret_cast<uint32_t *>(psm + (gq + 8) * 8 + 2 * tq) = pack_bf16x2(p2, p3);
+                __syncwarp();
+                const uint32_t pb0 = static_cast<uint32_t>(psm[(2 * tq) * 8 + gq]) |
+                                     (static_cast<uint32_t>(psm[(2 * tq + 1) * 8 + gq]) << 16);
+                const uint32_t pb1 = static_cast<uint32_t>(psm[(2 * tq + 8) * 8 + gq]) |
+                                     (static_cast<uint32_t>(psm[(2 * tq + 9) * 8 + gq]) << 16);
+                // ---- O^T += V^T P^T
+                const int vrow = slot0 + ((lane >> 4) << 3) + (lane & 7);
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t a[4];
+                    ldsm_x4_t(swz(vst, vrow, 2 * mt + ((lane >> 3) & 1)), a);
+                    mma_16816(acc[mt], a, pb0, pb1);
+                }
+                if (mine < 16) fence_proxy_async_smem();  // zeroed rows before the next TMA fill
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(st));
         }
-        const int64_t orow = static_cast<int64_t>(b) * p.Hq + kvh * G + h;
-        if (p.splits == 1) {
-            const float ov = l > 0.f ? a / l : 0.f;
-            p.o[orow * D + e] = __bfloat16_as_ushort(__float2bfloat16_rn(ov));
-        } else {
-            p.ws_acc[(orow * p.splits + split) * D + e] = a;
-            if (e == 0) {
-                p.ws_ml[(orow * p.splits + split) * 2 + 0] = m;
-                p.ws_ml[(orow * p.splits + split) * 2 + 1] = l;
+
+        // ---------------------------------------------------------------- merge
+        // sums over the 8 row groups of the warp (lanes with equal tq)
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
+        }
+        // every consumer has finished reading the previous item's buffers
+        asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+        const int h0 = 2 * tq, h1 = 2 * tq + 1;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int d0 = 16 * mt + gq;
+            if (h0 < G) {
+                wacc[(warp * G + h0) * D + d0] = acc[mt][0];
+                wacc[(warp * G + h0) * D + d0 + 8] = acc[mt][2];
+            }
+            if (h1 < G) {
+                wacc[(warp * G + h1) * D + d0] = acc[mt][1];
+                wacc[(warp * G + h1) * D + d0 + 8] = acc[mt][3];
+            }
+        }
+        if (gq == 0) {
+            if (h0 < G) {
+                wml[(warp * G + h0) * 2 + 0] = m0;
+                wml[(warp * G + h0) * 2 + 1] = l0;
+            }
+            if (h1 < G) {
+                wml[(warp * G + h1) * 2 + 0] = m1;
+                wml[(warp * G + h1) * 2 + 1] = l1;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+        // over the warps; thread t handles outputs t, t+128, ...
+        for (int idx = threadIdx.x; idx < G * D; idx += kDecWarps * 32) {
+            const int h = idx / D, e = idx - h * D;
+            float m = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, wml[(w * G + h) * 2]);
+            float l = 0.f, a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) {
+                const float wm = wml[(w * G + h) * 2];
+                const float f = (wm == -INFINITY) ? 0.f : ex2_approx(wm - m);
+                l = fmaf(wml[(w * G + h) * 2 + 1], f, l);
+                a = fmaf(wacc[(w * G + h) * D + e], f, a);
+            }
+            const int64_t orow = static_cast<int64_t>(x.b) * p.Hq + x.kvh * G + h;
+            if (p.splits == 1) {
+                const float ov = l > 0.f ? a / l : 0.f;
+                p.o[orow * D + e] = __bfloat16_as_ushort(__float2bfloat16_rn(ov));
+            } else {
+                p.ws_acc[(orow * p.splits + x.split) * D + e] = a;
+                if (e == 0) {
+                    p.ws_ml[(orow * p.splits + x.split) * 2 + 0] = m;
+                    p.ws_ml[(orow * p.splits + x.split) * 2 + 1] = l;
+                }
             }
         }
     }
@@ -406,15 +443,17 @@ __global__ void __launch_bounds__(128) swa_decode_merge_kernel(const DecodeParam
 // host side
 // ---------------------------------------------------------------------------
 DecodePlan decode_plan(int B, int Hq, int Hkv, int d, int cap, int w, int sm_count) {
+    // Split a (sequence, kv head) only to give the persistent CTAs enough
+    // items to balance: about SWA_DEC_ITEMS_PER_SM items per SM in total, at
+    // least one chunk per split.
     DecodePlan plan{1, 0};
     const int cap_eff = w < 0 ? cap : w;
-    const int chunks = (cap_eff + kDecCH - 1) / kDecCH;
-    const int max_splits = (chunks + 3) / 4;  // at least 4 chunks (256 slots) per split
+    const long long chunks = (cap_eff + kDecCH - 1) / kDecCH;
     const long long pairs = static_cast<long long>(B) * Hkv;
-    const long long target = 6LL * (sm_count > 0 ? sm_count : 148);  // ~2 waves of 3 CTAs/SM
+    const long long target = static_cast<long long>(SWA_DEC_ITEMS_PER_SM) * (sm_count > 0 ? sm_count : 148);
     if (pairs > 0 && pairs < target) {
-        long long s = (target + pairs - 1) / pairs;
-        if (s > max_splits) s = max_splits;
+        long long s = target / pairs;
+        if (s > chunks) s = chunks;
         if (s < 1) s = 1;
         plan.splits = static_cast<int>(s);
     }
@@ -450,7 +489,11 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStre
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode)");
         configured[dev] = true;
     }
-    dim3 grid(p.splits, p.Hkv, p.B);
+    const int sms = device_sm_count();
+    if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
+    const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
+    const long long cap_ctas = static_cast<long long>(SWA_DEC_CTAS_PER_SM) * sms;
+    const int grid = static_cast<int>(items < cap_ctas ? items : cap_ctas);
     swa_decode_kernel<D, G><<<grid, kDecThreads, SL::kAlloc, stream>>>(maps, p);
     e = cudaPeekAtLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_kernel");
