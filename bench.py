@@ -13,7 +13,7 @@ weak scaling) and rank 0 prints one JSON line.
 
 `value` is tokens/s of the whole step (prompt tokens + decoded tokens), device
 time from CUDA events on the launching stream, inputs resident in HBM, L2
-flushed (256 MiB write) before every timed step.  `e2e` is the same metric
+flushed (256 MiB written, another 256 MiB read) before every timed step.  `e2e` is the same metric
 through the C ABI with pinned host buffers, copies inside the timed region.
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
 workload on the host cores.
@@ -38,6 +38,24 @@ METRIC = "SWA(w,4) decode tok/s + KV-read GB/s vs HBM peak; prefill TFLOP/s vs t
 WORKLOAD_NAME = ("prefill SWA(64,4) B=1 L=4096 Hq=32 Hkv=8 d=128 (first 4 key rows x8) "
                  "+ bulk cache append + 1 decode token")
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = (f"flushed before each step: {L2_FLUSH_BYTES >> 20} MiB written, then another "
+           f"{L2_FLUSH_BYTES >> 20} MiB read, so the timed kernels start on a cold L2 that holds "
+           f"no dirty lines of the flush")
+
+
+class L2Flush:
+    """Evicts the timed kernels' data from L2 (129 MB on GB300): write one
+    buffer larger than L2, then read a second one, which also writes the
+    first buffer's dirty lines back before the timed region starts."""
+
+    def __init__(self, device="cuda"):
+        import torch
+        self.wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.rbuf = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def __call__(self, i: int = 1) -> None:
+        self.wbuf.fill_(i & 0xFF)
+        self.rbuf.sum()
 
 
 # ----------------------------------------------------------------------------- arithmetic
@@ -256,7 +274,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     od = torch.empty_like(q1)
     cache = swa.Cache(B, Hkv, d, w, s, device=dev)
     pos = torch.full((B,), L, dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def prefill_part():
         swa.prefill(q, k, v, w, s, out=o)
@@ -287,7 +305,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev_a.record()
     for _ in range(5):
-        flush.fill_(1)
+        flush(1)
     ev_b.record()
     torch.cuda.synchronize()
     t_flush = ev_a.elapsed_time(ev_b) / 5e3
@@ -295,7 +313,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     flush_reps = min(flush_reps, 64)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         g1.replay()
         g2.replay()
     torch.cuda.synchronize()
@@ -309,7 +327,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         sampler.mark_start()
     for i in range(args.steps):
         for _ in range(flush_reps):
-            flush.fill_(i & 0xFF)
+            flush(i)
         ev[i][0].record()
         g1.replay()
         ev[i][1].record()
@@ -355,7 +373,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     n_e2e = max(3, min(args.steps, 200))
     e2e_ms = []
     for i in range(n_e2e):
-        flush.fill_(i & 0xFF)
+        flush(i)
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         e2e_step()
@@ -389,7 +407,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME, "global_batch": B * world, "seq_len": L,
-                   "window": w, "sinks": s, "l2": f"flushed before each step ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "window": w, "sinks": s, "l2": L2_NOTE,
                    "timing": "CUDA events around CUDA-graph replays of the step"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
@@ -443,13 +461,13 @@ def _time_graph(fn, steps: int, flush, warm: int = 3) -> float:
             fn()
     torch.cuda.current_stream().wait_stream(s)
     for _ in range(warm):
-        flush.fill_(1)
+        flush(1)
         g.replay()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     for i in range(steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         evs[i][0].record()
         g.replay()
         evs[i][1].record()
@@ -468,7 +486,7 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
     from sliding_window_attention_prefill_gb300 import build, inputs
     build.build()
     pk = peaks()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     cases = [(1, 4096, 64, 4), (2, 32768, 128, 0), (2, 32768, 256, 0), (2, 32768, 512, 0),
              (1, 16384, -1, 0)]
     if only_w is not None:
@@ -492,40 +510,160 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
         torch.cuda.empty_cache()
 
 
-def suite_decode(steps: int, only_w=None):
-    """Decode step (append one token + decode) at B=64, Hq=32, Hkv=8, d=128,
-    SWA(w,4) for w in {64, 512}, after a 4096-token prompt, L2 flushed."""
+def suite_decode(steps: int, only_w=None, n_steps: int = 1024):
+    """Decode configuration: B=64, Hq=32, Hkv=8, d=128, SWA(w,4) for w in
+    {64, 512}; the cache is filled from a 4096-token N(0,1) prompt, then
+    `n_steps` decode steps each append one N(0,1) token and decode it.  Every
+    step is its own captured CUDA graph (its position is a launch argument);
+    L2 is flushed before each step.  Also times the decode kernel alone."""
     import torch
 
     import sliding_window_attention_prefill_gb300 as swa
     from sliding_window_attention_prefill_gb300 import build, inputs
     build.build()
     pk = peaks()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     B, Hq, Hkv, d, s, prompt = 64, 32, 8, 128, 4, 4096
     for w in [x for x in (64, 512) if only_w is None or x == only_w]:
-        kp, vp, ks, vs, qs = inputs.decode_stream(B, Hq, Hkv, d, prompt, 1, seed=0)
+        kp, vp, ks, vs, qs = inputs.decode_stream(B, Hq, Hkv, d, prompt, n_steps, seed=0)
         c = swa.Cache(B, Hkv, d, w, s)
         c.append(kp.cuda(), vp.cuda(), 0)
-        k1, v1, q1 = ks[0].cuda(), vs[0].cuda(), qs[0].cuda()
-        pos = torch.full((B,), prompt, dtype=torch.int32, device="cuda")
-        od = torch.empty_like(q1)
+        del kp, vp
+        ks, vs, qs = ks.cuda(), vs.cuda(), qs.cuda()
+        pos = (prompt + torch.arange(n_steps, dtype=torch.int32, device="cuda"))[:, None]
+        pos = pos.expand(n_steps, B).contiguous()
+        od = torch.empty_like(qs[0])
         ws = swa.workspace_for(c, Hq)
 
-        def step():
-            c.append(k1, v1, prompt)
-            swa.decode(q1, c, pos, out=od, workspace=ws)
+        def step(i):
+            c.append(ks[i], vs[i], prompt + i)
+            swa.decode(qs[i], c, pos[i], out=od, workspace=ws)
 
-        ms = _time_graph(step, steps, flush)
-        ms_dec = _time_graph(lambda: swa.decode(q1, c, pos, out=od, workspace=ws), steps, flush)
-        n_valid = min(prompt + 1, w)
+        step(0)  # kernel attributes are set outside capture
+        torch.cuda.synchronize()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        graphs = []
+        with torch.cuda.stream(cs):
+            for i in range(n_steps):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cs):
+                    step(i)
+                graphs.append(g)
+        torch.cuda.current_stream().wait_stream(cs)
+        torch.cuda.synchronize()
+        # step 0 ran once above; its graph re-appends the same token (idempotent)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_steps)]
+        for i, g in enumerate(graphs):
+            flush(i)
+            evs[i][0].record()
+            g.replay()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / n_steps
+        last = n_steps - 1
+        ms_dec = _time_graph(lambda: swa.decode(qs[last], c, pos[last], out=od, workspace=ws),
+                             steps, flush)
+        n_valid = min(prompt + n_steps, w)
         by = decode_bytes(B, Hq, Hkv, d, n_valid)
         kv = 2 * B * Hkv * d * 2 * n_valid
-        print(json.dumps({"suite": "decode", "B": B, "w": w, "s": s, "pos": prompt,
+        print(json.dumps({"suite": "decode", "B": B, "w": w, "s": s, "prompt": prompt,
+                          "decode_steps": n_steps, "ms_step": ms, "tok_s": B / (ms * 1e-3),
+                          "ms_decode": ms_dec, "kv_read_gbs": kv / (ms_dec * 1e-3) / 1e9,
+                          "frac_hbm": by / (ms_dec * 1e-3) / 1e9 / pk["hbm_gbs"],
+                          "bytes_decode": by, "l2": L2_NOTE}), flush=True)
+        del graphs, c, ks, vs, qs
+        torch.cuda.empty_cache()
+
+
+CONTEXT_POSITIONS = [1 << e for e in range(7, 19)]  # 128 .. 262144
+CONTEXT_WINDOWS = [64, 128, 256, 512, -1]
+CONTEXT_LAYERS = 4
+CONTEXT_MAX_CACHE_BYTES = 160 << 30  # all layers' caches of one point
+
+
+def context_cache_bytes(B, Hkv, d, cap, layers=CONTEXT_LAYERS) -> int:
+    """Bytes of K and V cache of `layers` layers with `cap` slots each."""
+    return layers * 2 * B * Hkv * cap * d * 2
+
+
+def context_points(batches=(1, 256)):
+    """(B, w, pos) of the context sweep whose caches fit the memory budget;
+    an infinite window needs pos+1 slots, a finite one w."""
+    pts, skipped = [], []
+    for B in batches:
+        for w in CONTEXT_WINDOWS:
+            for P in CONTEXT_POSITIONS:
+                cap = P + 1 if w < 0 else w
+                if context_cache_bytes(B, 8, 128, cap) > CONTEXT_MAX_CACHE_BYTES:
+                    skipped.append((B, w, P))
+                else:
+                    pts.append((B, w, P))
+    return pts, skipped
+
+
+def suite_context(steps: int, batches=(1, 256)):
+    """Decode context sweep through a stack of 4 attention layers (Hq=32,
+    Hkv=8, d=128, bf16, N(0,1)).  For each window w in {64,128,256,512} with
+    s=4, and w = infinity (full causal), batch 1 and 256, and position P from
+    128 to 262144: every layer holds a cache in the state reached after P
+    tokens (every slot a decode at P reads holds an N(0,1) value), and one
+    step appends token P and decodes it in each of the 4 layers.  Prints
+    tok/s, the decode kernel's KV read rate and the cache bytes held.
+    Points whose caches exceed 160 GiB are skipped (an infinite window at
+    batch 256 beyond 32768 positions) and listed."""
+    import torch
+
+    import sliding_window_attention_prefill_gb300 as swa
+    from sliding_window_attention_prefill_gb300 import build
+    build.build()
+    pk = peaks()
+    flush = L2Flush()
+    Hq, Hkv, d, s = 32, 8, 128, 4
+    gen = torch.Generator(device="cuda")
+    pts, skipped = context_points(batches)
+    for B, w, P in pts:
+        gen.manual_seed(B * 1000003 + P * 7 + (w + 1))
+        layers = []
+        for _ in range(CONTEXT_LAYERS):
+            c = swa.Cache(B, Hkv, d, w, s if w > 0 else 0, max_len=(P + 1 if w < 0 else None))
+            c.k.normal_(generator=gen)
+            c.v.normal_(generator=gen)
+            kn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(torch.bfloat16)
+            vn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(torch.bfloat16)
+            q = torch.randn(B, Hq, d, generator=gen, device="cuda").to(torch.bfloat16)
+            layers.append((c, kn, vn, q, torch.empty_like(q), swa.workspace_for(c, Hq)))
+        pos = torch.full((B,), P, dtype=torch.int32, device="cuda")
+
+        def step():
+            for c, kn, vn, q, o, ws in layers:
+                c.append(kn, vn, P)
+                swa.decode(q, c, pos, out=o, workspace=ws)
+
+        def decode_only():
+            for c, kn, vn, q, o, ws in layers:
+                swa.decode(q, c, pos, out=o, workspace=ws)
+
+        ms = _time_graph(step, steps, flush)
+        ms_dec = _time_graph(decode_only, steps, flush)
+        n_valid = P + 1 if w < 0 else min(P + 1, w)
+        kv = CONTEXT_LAYERS * 2 * B * Hkv * d * 2 * n_valid
+        by = CONTEXT_LAYERS * decode_bytes(B, Hq, Hkv, d, n_valid)
+        cap = layers[0][0].cap
+        print(json.dumps({"suite": "context", "B": B, "w": w if w > 0 else "inf",
+                          "s": s if w > 0 else 0, "pos": P, "layers": CONTEXT_LAYERS,
                           "ms_step": ms, "tok_s": B / (ms * 1e-3), "ms_decode": ms_dec,
                           "kv_read_gbs": kv / (ms_dec * 1e-3) / 1e9,
                           "frac_hbm": by / (ms_dec * 1e-3) / 1e9 / pk["hbm_gbs"],
-                          "bytes_decode": by}), flush=True)
+                          "cache_bytes_held": context_cache_bytes(B, Hkv, d, cap),
+                          "cache_bytes_read": kv}), flush=True)
+        del layers, step, decode_only
+        torch.cuda.empty_cache()
+    if skipped:
+        print(json.dumps({"suite": "context", "skipped": [
+            {"B": B, "w": "inf" if w < 0 else w, "pos": P} for B, w, P in skipped],
+            "reason": "caches above 160 GiB"}), flush=True)
 
 
 def main():
@@ -534,17 +672,23 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["swa", "reference"], default="swa")
-    ap.add_argument("--suite", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--suite", choices=["prefill", "decode", "context"], default=None,
                     help="auxiliary per-config lines instead of the headline step")
     ap.add_argument("--w", type=int, default=None, help="prefill suite: only this window")
     ap.add_argument("--B", type=int, default=None, help="prefill suite: batch override")
     ap.add_argument("--L", type=int, default=None, help="prefill suite: length override")
+    ap.add_argument("--decode-steps", type=int, default=1024, help="decode suite: steps")
+    ap.add_argument("--batches", type=str, default="1,256", help="context suite: batch sizes")
     args = ap.parse_args()
     if args.suite == "prefill":
         suite_prefill(max(args.steps // 10, 10), args.w, args.B, args.L)
         return
     if args.suite == "decode":
-        suite_decode(max(args.steps // 4, 20), args.w)
+        suite_decode(max(args.steps // 4, 20), args.w, args.decode_steps)
+        return
+    if args.suite == "context":
+        suite_context(max(min(args.steps // 40, 20), 5),
+                      tuple(int(b) for b in args.batches.split(",")))
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -6,14 +6,9 @@
 // (paper summary page), section "Prerequisites / Sliding-window attention
 // SWA(w, s)"; w = infinity is the full causal "FA" case of the same page.
 //
-// Work decomposition.  A work unit is (sequence b, key/value head kvh, query
-// tile).  Its 128 MMA rows pack the G = Hq/Hkv query heads that share kvh for
-// P = 128/G consecutive positions: row r is position t0 + r/G, head
-// kvh*G + r%G, which is exactly a box of the [B, L, Hq, d] query tensor, so
-// one TMA box loads it.  The unit needs the sink keys [0, s) and the band
-// [lo, t1] with lo = max(s, t0-(w-s)+1): its key columns are laid out as
-// [s_pad sink rows | band ...] and cut into key tiles of up to 256 columns,
-// the sink block (s rounded up to 8 rows) sharing the first tile.
+// Work decomposition (units of 128 query rows = G heads x 128/G positions;
+// key columns [sink block | band]): swa_prefill_common.cuh.  This kernel cuts
+// a unit's columns into key tiles of up to 256 and runs one unit at a time.
 //
 // Roles (384 threads = three warpgroups, one persistent CTA per SM):
 //   warp 0       TMA producer for Q (double-buffered) and K tiles
@@ -40,67 +35,32 @@
 #include <cstring>
 
 #include "swa_internal.h"
+#include "swa_prefill_common.cuh"
 #include "swa_ptx.cuh"
+
+#ifndef SWA_PREFILL_NARROW_MAX_COLS
+#define SWA_PREFILL_NARROW_MAX_COLS 128
+#endif
+#ifndef SWA_PREFILL_NARROW_NSK
+#define SWA_PREFILL_NARROW_NSK 2
+#endif
+#ifndef SWA_PREFILL_NARROW_NSV
+#define SWA_PREFILL_NARROW_NSV 2
+#endif
 
 namespace swa {
 
 __device__ int g_prefill_error;
 
-constexpr int kKT = 256;  // key tile width (columns)
-
-struct PrefillMaps {
-    CUtensorMap q;                    // box {64, G, P, 1} over [B, L, Hq, d]
-    CUtensorMap k_band, v_band;       // box {64, 1, 256, 1} over [B, L, Hkv, d]
-    CUtensorMap k_sink, v_sink;       // box {64, 1, s_pad, 1}
-    CUtensorMap k_band0, v_band0;     // box {64, 1, 256 - s_pad, 1}
-};
-
-struct PrefillParams {
-    int B, L, Hq, Hkv, G, P;  // P: positions per query tile (128 / G)
-    int w, s;                 // w < 0: infinite window (s is then 0)
-    int s_pad;                // sink rows loaded: s rounded up to 8 (0 if s == 0)
-    int n_qtiles, n_units;
-    float scale_log2;         // log2(e) / sqrt(d)
-    float scale;              // 1 / sqrt(d)
-    uint16_t *o;              // [B, L, Hq, d] bf16
-    float *lse;               // optional [B, Hq, L]
-};
-
-struct Unit {
-    int b, kvh, t0, t1, lo, n_cols, n_tiles;
-};
-
-// Geometry of work unit u.  Units run heaviest query tiles first (only
-// matters for the infinite window, where cost grows with the position).
-__device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p) {
-    const int bh = p.B * p.Hkv;
-    const int qt_rev = u / bh;
-    const int r = u - qt_rev * bh;
-    Unit x;
-    x.b = r / p.Hkv;
-    x.kvh = r - x.b * p.Hkv;
-    const int qt = p.n_qtiles - 1 - qt_rev;
-    x.t0 = qt * p.P;
-    x.t1 = min(x.t0 + p.P, p.L) - 1;
-    x.lo = p.w < 0 ? 0 : max(p.s, x.t0 - (p.w - p.s) + 1);
-    const int nb = max(0, x.t1 - x.lo + 1);
-    x.n_cols = p.s_pad + nb;
-    x.n_tiles = (x.n_cols + kKT - 1) / kKT;
-    return x;
-}
-
-// Key columns of tile j, rounded up to the MMA's N granularity of 16.
-__device__ __forceinline__ int tile_width(const Unit &x, int j) {
-    const int n = min(kKT, x.n_cols - kKT * j);
-    return (n + 15) & ~15;
-}
-
-template <int D, int NSK, int NSV>
+// Key tile width KT: 256 columns (one K or V tile of 64 KB at d = 128, so one
+// stage of each), or 128 columns for narrow bands (two stages of each in the
+// same shared memory, so the next unit's K and V load during this one).
+template <int D, int KT, int NSK, int NSV>
 struct PrefillSmem {
     static constexpr int kQRegion = 128 * 128;          // 64 columns x 128 query rows
-    static constexpr int kKRegion = kKT * 128;          // 64 columns x 256 key rows
+    static constexpr int kKRegion = KT * 128;           // 64 columns x KT key rows
     static constexpr int kQTile = 128 * D * 2;
-    static constexpr int kKTile = kKT * D * 2;
+    static constexpr int kKTile = KT * D * 2;
     static constexpr int kQ = 0;                        // 2 Q buffers
     static constexpr int kK = kQ + 2 * kQTile;          // K ring
     static constexpr int kV = kK + NSK * kKTile;        // V ring
@@ -110,7 +70,7 @@ struct PrefillSmem {
     static constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = 4 + NSK,
                          kVFull = 4 + 2 * NSK, kVEmpty = 4 + 2 * NSK + NSV,
                          kSFull = 4 + 2 * NSK + 2 * NSV, kSEmpty = kSFull + 1,
-                         kPFull = kSFull + 2, kPVDone = kSFull + 3, kNumBars = kSFull + 4;
+                         kPFull = kSFull + 2, kPVDone = kSFull + 3, kNumBars = kSFull + 5;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
@@ -119,12 +79,22 @@ struct PrefillSmem {
 
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0, kTmemP = 256, kTmemO = 384;
+constexpr uint32_t kTmemS = 0;
 
-template <int D, int NSK, int NSV>
+template <int D, int KT, int NSK, int NSV>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
-    using SL = PrefillSmem<D, NSK, NSV>;
+    using SL = PrefillSmem<D, KT, NSK, NSV>;
+    constexpr int NC = KT / 64;  // 32-column chunks of a tile per softmax thread
+    // TMEM columns.  256-column tiles: S [0,256) | P [256,384) | O [384,384+d).
+    // 128-column tiles leave room to double-buffer P (by tile) and O (by
+    // unit): S [0,128) | P0, P1 [128,256) | O0, O1 [256,256+2d); then the
+    // softmax of a tile need not wait for the previous P V to write its P,
+    // and a unit's epilogue runs while the next unit's P V goes on.
+    constexpr bool DB = (KT == 128);
+    constexpr uint32_t kTP = DB ? 128u : 256u;
+    constexpr uint32_t kTO = DB ? 256u : 384u;
+    static_assert(kTO + (DB ? 2 : 1) * D <= kTmemCols, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -177,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t g = 0, uc = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
-                const Unit x = unit_geom(u, p);
+                const Unit x = unit_geom<KT>(u, p);
                 if (kq) {
                     const uint32_t qb = uc & 1;
                     ok = mbar_wait(bar(SL::kQEmpty + qb), ((uc >> 1) & 1) ^ 1, &g_prefill_error,
@@ -195,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    abort_flag);
                     if (!ok) break;
                     const uint32_t dst0 = ring + slot * SL::kKTile;
-                    const int key0 = x.lo + kKT * j - p.s_pad;  // key of column 0 (band)
+                    const int key0 = x.lo + KT * j - p.s_pad;  // key of column 0 (band)
                     const uint32_t fb = bar(full0 + slot);
                     mbar_arrive_expect_tx(fb, SL::kKTile);
 #pragma unroll
@@ -230,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
             uint32_t g = 0, uc = 0;
             bool ok = true, have_prev = false, any_pv = false;
-            uint32_t prev_g = 0, last_pv_g = 0;
+            uint32_t prev_g = 0, last_pv_g = 0, prev_ob = 0;
             int prev_n = 0;
             bool prev_first = false;
 
-            auto issue_pv = [&](uint32_t pg, int pn, bool first) -> bool {
+            auto issue_pv = [&](uint32_t pg, int pn, bool first, uint32_t ob) -> bool {
                 const uint32_t vs = pg % NSV;
                 if (!mbar_wait(bar(SL::kPFull), pg & 1, &g_prefill_error, abort_flag)) return false;
                 if (!mbar_wait(bar(SL::kVFull + vs), (pg / NSV) & 1, &g_prefill_error, abort_flag))
@@ -245,10 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // A = P (TMEM, two bf16 per column), B = V (MN-major:
                     // 64-column slabs LBO apart, 8-key groups SBO apart)
                     const uint64_t b = smem_desc_sw128(vbase + kk * 16 * 128, SL::kKRegion, 1024);
-                    mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + kk * 8, b, kIdescPV,
+                    mma_bf16_ts(tmem + kTO + (DB ? ob * D : 0u),
+                                tmem + kTP + (DB ? (pg & 1) * 64 : 0u) + kk * 8, b, kIdescPV,
                                 (!first || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(SL::kPVDone));
+                mma_commit(bar(SL::kPVDone + (DB ? (pg & 1) : 0)));
                 mma_commit(bar(SL::kVEmpty + vs));
                 any_pv = true;
                 last_pv_g = pg;
@@ -256,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
 
             for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
-                const Unit x = unit_geom(u, p);
+                const Unit x = unit_geom<KT>(u, p);
                 const uint32_t qb = uc & 1;
                 ok = mbar_wait(bar(SL::kQFull + qb), (uc >> 1) & 1, &g_prefill_error, abort_flag);
                 if (!ok) break;
@@ -269,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          mbar_wait(bar(SL::kSEmpty), (g & 1) ^ 1, &g_prefill_error, abort_flag);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    const int n = tile_width(x, j);
+                    const int n = tile_width<KT>(x, j);
                     const uint32_t idesc = kIdescS | (static_cast<uint32_t>(n >> 3) << 17);
                     const uint32_t kbase = base + SL::kK + ks * SL::kKTile;
 #pragma unroll
@@ -284,20 +255,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(bar(SL::kKEmpty + ks));
                     if (j == x.n_tiles - 1) mma_commit(bar(SL::kQEmpty + qb));
                     if (have_prev) {
-                        ok = issue_pv(prev_g, prev_n, prev_first);
+                        ok = issue_pv(prev_g, prev_n, prev_first, prev_ob);
                         if (!ok) break;
                     }
                     have_prev = true;
                     prev_g = g;
                     prev_n = n;
                     prev_first = (j == 0);
+                    prev_ob = uc & 1;
                 }
             }
-            if (ok && have_prev) issue_pv(prev_g, prev_n, prev_first);
+            if (ok && have_prev) issue_pv(prev_g, prev_n, prev_first, prev_ob);
             // Drain: all issued MMAs complete before TMEM is released.
             if (any_pv) {
                 int no_abort = 0;
-                mbar_wait(bar(SL::kPVDone), last_pv_g & 1, &g_prefill_error, &no_abort);
+                if (DB)
+                    mbar_wait(bar(SL::kPVDone + (last_pv_g & 1)), (last_pv_g >> 1) & 1,
+                              &g_prefill_error, &no_abort);
+                else
+                    mbar_wait(bar(SL::kPVDone), last_pv_g & 1, &g_prefill_error, &no_abort);
             }
         }
     } else {
@@ -321,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool pend = false, pend_valid = false;
         int pend_b = 0, pend_kvh = 0, pend_t = 0;
         float pend_m = 0.f, pend_l = 0.f;
-        auto epilogue = [&](float l_tot) {
+        auto epilogue = [&](float l_tot, uint32_t ob) {
             const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const bool store = pend_valid && !*abort_flag;
             uint16_t *orow =
@@ -330,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
-                tmem_ld32(t_lane + kTmemO + half * (D / 2) + 32 * c, r);
+                tmem_ld32(t_lane + kTO + (DB ? ob * D : 0u) + half * (D / 2) + 32 * c, r);
                 tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
@@ -352,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++uc) {
-            const Unit x = unit_geom(u, p);
+            const Unit x = unit_geom<KT>(u, p);
             const int t = x.t0 + prow;
             const bool row_valid = (t <= x.t1);
             const int lo_t = p.w < 0 ? 0 : max(p.s, t - (p.w - p.s) + 1);
@@ -363,26 +339,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(bar(SL::kSFull), g & 1, &g_prefill_error, abort_flag);
                 tc_fence_after_sync();
                 // this thread's chunks: columns 32*(half + 2i) .. +31, i = 0..3
-                uint32_t sr[4][32];
+                uint32_t sr[NC][32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) tmem_ld32(t_lane + kTmemS + 32 * (half + 2 * i), sr[i]);
+                for (int i = 0; i < NC; ++i) tmem_ld32(t_lane + kTmemS + 32 * (half + 2 * i), sr[i]);
                 // column c of this tile is attended when c is in the band
                 // [c_lo, c_hi] or among the sinks [0, sink_hi)
-                const int key0 = x.lo + kKT * j - p.s_pad;
+                const int key0 = x.lo + KT * j - p.s_pad;
                 int c_lo = max(j == 0 ? p.s_pad : 0, lo_t - key0);
-                int c_hi = min(t - key0, kKT - 1);
+                int c_hi = min(t - key0, KT - 1);
                 int sink_hi = (j == 0) ? min(p.s, t + 1) : 0;
                 if (!row_valid) {
-                    c_lo = kKT;
+                    c_lo = KT;
                     c_hi = -1;
                     sink_hi = 0;
                 }
                 const bool band_ok = c_lo <= c_hi;
                 const unsigned span = band_ok ? static_cast<unsigned>(c_hi - c_lo) : 0u;
                 const int band_from = band_ok ? c_lo : 1 << 20;
-                bool full[4], empty[4];
+                bool full[NC], empty[NC];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < NC; ++i) {
                     const int c0 = 32 * (half + 2 * i);
                     const bool f = band_ok && c_lo <= c0 && c_hi >= c0 + 31;
                     const bool e = (!band_ok || c_hi < c0 || c_lo > c0 + 31) && sink_hi <= c0;
@@ -397,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < NC; ++i) {
                     if (empty[i]) continue;
                     if (!full[i]) {
                         const int x0 = 32 * (half + 2 * i) - band_from;
@@ -433,9 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t sc2 = f32x2(p.scale_log2, p.scale_log2);
                 const uint64_t nm2 = f32x2(neg_m, neg_m);
                 uint64_t l2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
-                uint32_t pk[4][16];
+                uint32_t pk[NC][16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < NC; ++i) {
                     if (empty[i]) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) pk[i][e] = 0u;
@@ -458,23 +434,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 f32x2_split(l2[0], lx, ly);
                 f32x2_split(l2[1], lz, lw);
                 l_half = l_half * alpha + ((lx + ly) + (lz + lw));
-                // P and O may be touched once the previous P V (of this unit,
-                // or the last one of the previous unit) has completed.
-                if (g > 0) mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
+                // The P buffer may be written once the P V that last read it
+                // (tile g-1, or g-2 with two buffers) has completed; with one
+                // O buffer the previous unit's O is read out first.
+                if (DB) {
+                    if (g >= 2)
+                        mbar_wait(bar(SL::kPVDone + (g & 1)), ((g - 2) >> 1) & 1, &g_prefill_error,
+                                  abort_flag);
+                } else if (g > 0) {
+                    mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
+                }
                 tc_fence_after_sync();
-                if (do_epi) {
-                    epilogue(l_prev);
+                if (!DB && do_epi) {
+                    epilogue(l_prev, 0);
                     pend = false;
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) tmem_st16(t_lane + kTmemP + 16 * (half + 2 * i), pk[i]);
+                for (int i = 0; i < NC; ++i)
+                    tmem_st16(t_lane + kTP + (DB ? (g & 1) * 64 : 0u) + 16 * (half + 2 * i), pk[i]);
                 // Rescale O when this warp raised any running max (not on the
-                // first tile: its P V overwrites O).  Each half owns d/2 columns.
+                // first tile: its P V overwrites O), after the previous P V
+                // into it completed.  Each half owns d/2 columns.
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                    if (DB) {
+                        mbar_wait(bar(SL::kPVDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1,
+                                  &g_prefill_error, abort_flag);
+                        tc_fence_after_sync();
+                    }
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t r[32];
-                        const uint32_t ta = t_lane + kTmemO + half * (D / 2) + 32 * c;
+                        const uint32_t ta =
+                            t_lane + kTO + (DB ? (uc & 1) * D : 0u) + half * (D / 2) + 32 * c;
                         tmem_ld32(ta, r);
                         tmem_wait_ld();
 #pragma unroll
@@ -487,6 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(SL::kPFull));
+                // With two O buffers the previous unit's epilogue runs here,
+                // beside this tile's P V, once that unit's last P V is done.
+                if (DB && do_epi) {
+                    mbar_wait(bar(SL::kPVDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1,
+                              &g_prefill_error, abort_flag);
+                    tc_fence_after_sync();
+                    epilogue(l_prev, (uc - 1) & 1);
+                    pend = false;
+                }
             }
             pend = true;
             pend_valid = row_valid;
@@ -499,10 +499,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pend) {  // the last unit's epilogue
             float *rl = redl + ((uc - 1) & 1) * 256;
             rl[half * 128 + row] = pend_l;
-            mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
+            if (DB)
+                mbar_wait(bar(SL::kPVDone + ((g - 1) & 1)), ((g - 1) >> 1) & 1, &g_prefill_error,
+                          abort_flag);
+            else
+                mbar_wait(bar(SL::kPVDone), (g - 1) & 1, &g_prefill_error, abort_flag);
             tc_fence_after_sync();
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            epilogue(rl[row] + rl[128 + row]);
+            epilogue(rl[row] + rl[128 + row], (uc - 1) & 1);
         }
     }
 
@@ -519,30 +523,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 namespace {
 
-bool encode_map(CUtensorMap *m, const void *ptr, int d, int heads, int L, int B, int box_heads,
-                int box_rows) {
-    const cuTensorMapEncodeTiled_fn enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2,
-                             (cuuint64_t)L * heads * d * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-template <int D, int NSK, int NSV>
+template <int D, int KT, int NSK, int NSV>
 swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaStream_t stream) {
-    using SL = PrefillSmem<D, NSK, NSV>;
+    using SL = PrefillSmem<D, KT, NSK, NSV>;
+    static_assert(SL::kAlloc <= 232448, "shared memory per CTA");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(swa_prefill_kernel<D, NSK, NSV>,
+        e = cudaFuncSetAttribute(swa_prefill_kernel<D, KT, NSK, NSV>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
         configured[dev] = true;
@@ -550,45 +540,33 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
     const int sms = device_sm_count();
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const int grid = p.n_units < sms ? p.n_units : sms;
-    swa_prefill_kernel<D, NSK, NSV><<<grid, kThreads, SL::kAlloc, stream>>>(maps, p);
+    swa_prefill_kernel<D, KT, NSK, NSV><<<grid, kThreads, SL::kAlloc, stream>>>(maps, p);
     e = cudaPeekAtLastError();
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_prefill_kernel");
 }
 
 }  // namespace
 
+// Key tiles of 128 columns while the widest unit's key columns fit one of
+// them (narrow windows: deeper K/V rings, no MMA width lost), else 256.
+bool prefill_narrow(const PrefillParams &p) {
+    const long long cols =
+        p.w < 0 ? static_cast<long long>(p.L) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
+    return cols <= SWA_PREFILL_NARROW_MAX_COLS;
+}
+
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                           int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream) {
-    PrefillParams p{};
-    p.B = B;
-    p.L = L;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.G = Hq / Hkv;
-    p.P = 128 / p.G;
-    p.w = w < 0 ? -1 : w;
-    p.s = w < 0 ? 0 : s;
-    p.s_pad = (p.s + 7) & ~7;
-    p.n_qtiles = (L + p.P - 1) / p.P;
-    p.n_units = B * Hkv * p.n_qtiles;
-    p.scale = 1.0f / std::sqrt(static_cast<float>(d));
-    p.scale_log2 = p.scale * 1.4426950408889634f;
-    p.o = static_cast<uint16_t *>(o);
-    p.lse = lse;
-
+    const PrefillParams p = make_prefill_params(o, lse, B, L, Hq, Hkv, d, w, s);
+    const bool narrow = prefill_narrow(p);
     PrefillMaps maps;
-    std::memset(&maps, 0, sizeof(maps));
-    bool ok = encode_map(&maps.q, q, d, Hq, L, B, p.G, p.P) &&
-              encode_map(&maps.k_band, k, d, Hkv, L, B, 1, kKT) &&
-              encode_map(&maps.v_band, v, d, Hkv, L, B, 1, kKT);
-    if (ok && p.s_pad > 0)
-        ok = encode_map(&maps.k_sink, k, d, Hkv, L, B, 1, p.s_pad) &&
-             encode_map(&maps.v_sink, v, d, Hkv, L, B, 1, p.s_pad) &&
-             encode_map(&maps.k_band0, k, d, Hkv, L, B, 1, kKT - p.s_pad) &&
-             encode_map(&maps.v_band0, v, d, Hkv, L, B, 1, kKT - p.s_pad);
-    if (!ok) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    if (d == 128) return launch_prefill<128, 1, 1>(maps, p, stream);
-    return launch_prefill<64, 2, 2>(maps, p, stream);
+    if (!encode_prefill_maps(&maps, q, k, v, p, d, narrow ? 128 : 256))
+        return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    if (d == 128)
+        return narrow ? launch_prefill<128, 128, SWA_PREFILL_NARROW_NSK, SWA_PREFILL_NARROW_NSV>(maps, p, stream)
+                      : launch_prefill<128, 256, 1, 1>(maps, p, stream);
+    return narrow ? launch_prefill<64, 128, 4, 4>(maps, p, stream)
+                  : launch_prefill<64, 256, 2, 2>(maps, p, stream);
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {

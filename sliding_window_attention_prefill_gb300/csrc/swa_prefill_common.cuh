@@ -1,0 +1,130 @@
+// swa_prefill_common.cuh -- work decomposition shared by the two prefill
+// kernels (swa_prefill.cu: one query tile at a time, 256-column key tiles;
+// swa_prefill_pp.cu: two query tiles in flight, 128-column key tiles).
+//
+// A work unit is (sequence b, key/value head kvh, query tile).  Its 128 MMA
+// rows pack the G = Hq/Hkv query heads that share kvh for P = 128/G
+// consecutive positions: row r is position t0 + r/G, head kvh*G + r%G, which
+// is exactly a box of the [B, L, Hq, d] query tensor, so one TMA box loads it.
+// The unit needs the sink keys [0, s) and the band [lo, t1] with
+// lo = max(s, t0-(w-s)+1) (the window of "Sliding-window beats linear
+// attention", section "Prerequisites / Sliding-window attention SWA(w, s)"):
+// its key columns are laid out as [s_pad sink rows | band ...] and cut into
+// key tiles of KT columns, the sink block (s rounded up to 8 rows, so that the
+// band starts on a 1024-byte swizzle atom) sharing the first tile.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "swa_internal.h"
+
+namespace swa {
+
+struct PrefillMaps {
+    CUtensorMap q;                    // box {64, G, P, 1} over [B, L, Hq, d]
+    CUtensorMap k_band, v_band;       // box {64, 1, KT, 1} over [B, L, Hkv, d]
+    CUtensorMap k_sink, v_sink;       // box {64, 1, s_pad, 1}
+    CUtensorMap k_band0, v_band0;     // box {64, 1, KT - s_pad, 1}
+};
+
+struct PrefillParams {
+    int B, L, Hq, Hkv, G, P;  // P: positions per query tile (128 / G)
+    int w, s;                 // w < 0: infinite window (s is then 0)
+    int s_pad;                // sink rows loaded: s rounded up to 8 (0 if s == 0)
+    int n_qtiles, n_units;
+    float scale_log2;         // log2(e) / sqrt(d)
+    float scale;              // 1 / sqrt(d)
+    uint16_t *o;              // [B, L, Hq, d] bf16
+    float *lse;               // optional [B, Hq, L]
+};
+
+struct Unit {
+    int b, kvh, t0, t1, lo, n_cols, n_tiles;
+};
+
+// Geometry of work unit u.  Units run heaviest query tiles first (only
+// matters for the infinite window, where cost grows with the position).
+template <int KT>
+__device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p) {
+    const int bh = p.B * p.Hkv;
+    const int qt_rev = u / bh;
+    const int r = u - qt_rev * bh;
+    Unit x;
+    x.b = r / p.Hkv;
+    x.kvh = r - x.b * p.Hkv;
+    const int qt = p.n_qtiles - 1 - qt_rev;
+    x.t0 = qt * p.P;
+    x.t1 = min(x.t0 + p.P, p.L) - 1;
+    x.lo = p.w < 0 ? 0 : max(p.s, x.t0 - (p.w - p.s) + 1);
+    const int nb = max(0, x.t1 - x.lo + 1);
+    x.n_cols = p.s_pad + nb;
+    x.n_tiles = (x.n_cols + KT - 1) / KT;
+    return x;
+}
+
+// Key columns of tile j, rounded up to the MMA's N granularity of 16.
+template <int KT>
+__device__ __forceinline__ int tile_width(const Unit &x, int j) {
+    const int n = min(KT, x.n_cols - KT * j);
+    return (n + 15) & ~15;
+}
+
+// ------------------------------------------------------------------ host side
+inline PrefillParams make_prefill_params(void *o, float *lse, int B, int L, int Hq, int Hkv, int d,
+                                         int w, int s) {
+    PrefillParams p{};
+    p.B = B;
+    p.L = L;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.P = 128 / p.G;
+    p.w = w < 0 ? -1 : w;
+    p.s = w < 0 ? 0 : s;
+    p.s_pad = (p.s + 7) & ~7;
+    p.n_qtiles = (L + p.P - 1) / p.P;
+    p.n_units = B * Hkv * p.n_qtiles;
+    p.scale = 1.0f / std::sqrt(static_cast<float>(d));
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.o = static_cast<uint16_t *>(o);
+    p.lse = lse;
+    return p;
+}
+
+// 4-D map over a [B, L, heads, d] bf16 tensor, 64-column boxes, 128-byte swizzle.
+static inline bool encode_prefill_map(CUtensorMap *m, const void *ptr, int d, int heads, int L,
+                                      int B, int box_heads, int box_rows) {
+    const cuTensorMapEncodeTiled_fn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2,
+                             (cuuint64_t)L * heads * d * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The maps of one call with key tiles of `kt` columns.
+static inline bool encode_prefill_maps(PrefillMaps *maps, const void *q, const void *k,
+                                       const void *v, const PrefillParams &p, int d, int kt) {
+    std::memset(maps, 0, sizeof(*maps));
+    bool ok = encode_prefill_map(&maps->q, q, d, p.Hq, p.L, p.B, p.G, p.P) &&
+              encode_prefill_map(&maps->k_band, k, d, p.Hkv, p.L, p.B, 1, kt) &&
+              encode_prefill_map(&maps->v_band, v, d, p.Hkv, p.L, p.B, 1, kt);
+    if (ok && p.s_pad > 0)
+        ok = encode_prefill_map(&maps->k_sink, k, d, p.Hkv, p.L, p.B, 1, p.s_pad) &&
+             encode_prefill_map(&maps->v_sink, v, d, p.Hkv, p.L, p.B, 1, p.s_pad) &&
+             encode_prefill_map(&maps->k_band0, k, d, p.Hkv, p.L, p.B, 1, kt - p.s_pad) &&
+             encode_prefill_map(&maps->v_band0, v, d, p.Hkv, p.L, p.B, 1, kt - p.s_pad);
+    return ok;
+}
+
+}  // namespace swa

@@ -43,7 +43,7 @@ def _call(fn, q, cache, pos):
     return o
 
 
-@pytest.mark.parametrize("B,w,s,prompt,cap", [(1, W_INF, 0, 15000, 20000), (64, 512, 4, 4096, None)])
+@pytest.mark.parametrize("B,w,s,prompt,cap", [(1, W_INF, 0, 15000, 20000), (16, 512, 4, 4096, None)])
 def test_noalloc_matches_decode_twice(noalloc, B, w, s, prompt, cap):
     Hq, Hkv, d = 32, 8, 128
     cache = Cache(B, Hkv, d, w, s, max_len=cap)
