@@ -38,8 +38,10 @@
 #include "swa_prefill_common.cuh"
 #include "swa_ptx.cuh"
 
-#ifndef SWA_PREFILL_NARROW_MAX_COLS
-#define SWA_PREFILL_NARROW_MAX_COLS 128
+// 0: pick the key tile width per call (prefill_narrow); 128 or 256: always
+// that width (for measurements).
+#ifndef SWA_PREFILL_FORCE_KT
+#define SWA_PREFILL_FORCE_KT 0
 #endif
 #ifndef SWA_PREFILL_NARROW_NSK
 #define SWA_PREFILL_NARROW_NSK 2
@@ -284,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;      // MMA row == TMEM lane
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t t_lane = tmem + lane_addr;
-        const int prow = row / p.G;               // position offset within the tile
-        const int hrow = row - prow * p.G;        // head offset within the group
+        const int prow = row >> p.g_log2;         // position offset within the tile
+        const int hrow = row & (p.G - 1);         // head offset within the group
         float *red = reinterpret_cast<float *>(gbase + SL::kRed);    // [2][2][128]
         float *redl = reinterpret_cast<float *>(gbase + SL::kRedL);  // [2][2][128]
         uint32_t g = 0, uc = 0;
@@ -295,32 +297,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         // weights are computed while the previous unit's last P V runs, and
         // O is read out just before the new P is written.
         bool pend = false, pend_valid = false;
-        int pend_b = 0, pend_kvh = 0, pend_t = 0;
+        int pend_b = 0, pend_kvh = 0, pend_t = 0, pend_t0 = 0, pend_t1 = 0;
         float pend_m = 0.f, pend_l = 0.f;
         auto epilogue = [&](float l_tot, uint32_t ob) {
             const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-            const bool store = pend_valid && !*abort_flag;
-            uint16_t *orow =
-                p.o + ((static_cast<int64_t>(pend_b) * p.L + pend_t) * p.Hq + pend_kvh * p.G + hrow) * D +
-                half * (D / 2);
+            const bool ok = !*abort_flag;
+            // This thread's half row of O / l as CH 16-byte chunks of bf16.
+            constexpr int CH = D / 16;
+            uint4 ch[CH];
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
                 tmem_ld32(t_lane + kTO + (DB ? ob * D : 0u) + half * (D / 2) + 32 * c, r);
                 tmem_wait_ld();
-                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
-                                        __uint_as_float(r[2 * e + 1]) * inv_l);
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+                for (int v = 0; v < 4; ++v) {
+                    uint32_t w4[4];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int e = 0; e < 4; ++e)
+                        w4[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv_l,
+                                            __uint_as_float(r[8 * v + 2 * e + 1]) * inv_l);
+                    ch[4 * c + v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
-            if (p.lse != nullptr && store && half == 0) {
+            // Transpose the CH x CH chunks within each group of CH lanes
+            // (butterfly over lane bits): afterwards lane CH*k + c holds chunk c
+            // of the warp's rows CH*k + v in ch[v].  Each store below then
+            // writes CH consecutive chunks of one half row -- whole 128-byte
+            // lines -- instead of one chunk in each of 32 lines.
+#pragma unroll
+            for (int dd = CH / 2; dd >= 1; dd >>= 1) {
+                const bool upper = (lane & dd) != 0;
+#pragma unroll
+                for (int lo = 0; lo < CH; ++lo) {
+                    if (lo & dd) continue;
+                    const int hi = lo | dd;
+                    const uint4 snd = upper ? ch[lo] : ch[hi];
+                    uint4 rcv;
+                    rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, dd);
+                    rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, dd);
+                    rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, dd);
+                    rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, dd);
+                    if (upper)
+                        ch[lo] = rcv;
+                    else
+                        ch[hi] = rcv;
+                }
+            }
+            const int kgrp = lane / CH, cpos = lane % CH;
+#pragma unroll
+            for (int v = 0; v < CH; ++v) {
+                const int rr = quarter * 32 + kgrp * CH + v;  // MMA row of ch[v]
+                const int tv = pend_t0 + (rr >> p.g_log2);
+                if (ok && tv <= pend_t1)
+                    *reinterpret_cast<uint4 *>(
+                        p.o + ((static_cast<int64_t>(pend_b) * p.L + tv) * p.Hq + pend_kvh * p.G +
+                               (rr & (p.G - 1))) * D +
+                        half * (D / 2) + cpos * 8) = ch[v];
+            }
+            if (p.lse != nullptr && ok && pend_valid && half == 0) {
                 const int h = pend_kvh * p.G + hrow;
                 p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + pend_t] =
                     pend_m * p.scale + logf(l_tot);
@@ -493,6 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend_b = x.b;
             pend_kvh = x.kvh;
             pend_t = t;
+            pend_t0 = x.t0;
+            pend_t1 = x.t1;
             pend_m = m_run;
             pend_l = l_half;
         }
@@ -547,12 +584,17 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
 
 }  // namespace
 
-// Key tiles of 128 columns while the widest unit's key columns fit one of
-// them (narrow windows: deeper K/V rings, no MMA width lost), else 256.
+// Key tile width for a call: whichever makes the widest unit cheaper, a
+// 128-column tile (two-stage K/V rings, double-buffered P and O) costing
+// about 5/8 of a 256-column one on GB300 (measured for d = 128 at windows
+// 64 .. 2048 and full causal): 128 for SWA(64,4) and SWA(256,4), 256 for
+// SWA(128,4), SWA(512,4) and wider bands.
 bool prefill_narrow(const PrefillParams &p) {
+    if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT == 128;
     const long long cols =
         p.w < 0 ? static_cast<long long>(p.L) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
-    return cols <= SWA_PREFILL_NARROW_MAX_COLS;
+    const long long t128 = (cols + 127) / 128, t256 = (cols + 255) / 256;
+    return 5 * t128 < 8 * t256;
 }
 
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,

@@ -34,6 +34,7 @@ struct PrefillMaps {
 
 struct PrefillParams {
     int B, L, Hq, Hkv, G, P;  // P: positions per query tile (128 / G)
+    int g_log2;               // G is a power of two (row r: position r >> g_log2)
     int w, s;                 // w < 0: infinite window (s is then 0)
     int s_pad;                // sink rows loaded: s rounded up to 8 (0 if s == 0)
     int n_qtiles, n_units;
@@ -84,6 +85,8 @@ inline PrefillParams make_prefill_params(void *o, float *lse, int B, int L, int 
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
     p.P = 128 / p.G;
+    p.g_log2 = 0;
+    while ((1 << p.g_log2) < p.G) ++p.g_log2;
     p.w = w < 0 ? -1 : w;
     p.s = w < 0 ? 0 : s;
     p.s_pad = (p.s + 7) & ~7;

@@ -47,9 +47,9 @@ CASES = [
     (1, 5, 4, 1, 64, 64, 4),         # every position is a sink position
     (1, 1, 8, 2, 128, 64, 4),        # one token
     (3, 129, 4, 4, 64, 33, 1),       # odd window and one sink
-    # Windows around and past the point where prefill switches from the
-    # two-query-tile kernel (128-column key tiles) to the one-tile kernel
-    # (256-column key tiles): a unit of G=4 spans w + 35 key columns.
+    # Long windows (256-column key tiles; a unit of G=4 spans w + 35 key
+    # columns), including one whose last tile is a single 16-column MMA step,
+    # and d=64 with 128-column tiles.
     (1, 2600, 8, 2, 128, 989, 4),
     (1, 2600, 8, 2, 128, 990, 4),
     (1, 5000, 4, 1, 128, 2048, 4),
