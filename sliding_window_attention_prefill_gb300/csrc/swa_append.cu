@@ -12,7 +12,7 @@
 // the latest w-s of them -- so the result is the same as appending one
 // position at a time, no two threads write the same slot, and a long prompt
 // costs O(w) rather than O(n).  Pure copy: 16-byte vectors, one per
-// thread-iteration, coalesced on both sides.
+// thread, coalesced on both sides.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -27,29 +27,37 @@ struct AppendParams {
     uint4 *ck;           // [B, Hkv, cap, d]
     uint4 *cv;
     int64_t pos0;
-    int B, n, Hkv, vpr, cap, w, s;  // vpr: 16-byte vectors per row (d / 8)
+    int B, n, Hkv, vpr, vpr_log2, cap, w, s;  // vpr: 16-byte vectors per row (d / 8)
     int a, b0;  // surviving new positions: j in [0, a) and j in [b0, n)
 };
 
-__global__ void __launch_bounds__(256) swa_append_kernel(const AppendParams p) {
+// Grid (vector blocks, surviving positions, sequences): the threads of the x
+// dimension cover the Hkv * d / 8 vectors of one position; y and z walk the
+// surviving positions and the sequences (grid-stride, so any count fits the
+// 65535 limit of those grid dimensions).  The only integer work per vector is
+// one slot computation.
+constexpr int kAppendThreads = 128;
+
+__global__ void __launch_bounds__(kAppendThreads) swa_append_kernel(const AppendParams p) {
+    const int per_pos = p.Hkv * p.vpr;  // vectors of one position (all kv heads)
+    const int t = blockIdx.x * kAppendThreads + threadIdx.x;
+    if (t >= per_pos) return;
+    const int h = t >> p.vpr_log2;
+    const int vec = t & (p.vpr - 1);
     const int m = p.a + (p.n - p.b0);  // surviving positions per sequence
-    const int64_t total = static_cast<int64_t>(p.B) * m * p.Hkv * p.vpr;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = idx / p.vpr;           // (b * m + jj) * Hkv + h
-        const int vec = static_cast<int>(idx - r * p.vpr);
-        const int h = static_cast<int>(r % p.Hkv);
-        const int64_t bj = r / p.Hkv;
-        const int jj = static_cast<int>(bj % m);
-        const int b = static_cast<int>(bj / m);
-        const int j = jj < p.a ? jj : p.b0 + (jj - p.a);
-        const int64_t pos = p.pos0 + j;
-        const int64_t slot =
-            (p.w < 0 || pos < p.s) ? pos : p.s + (pos - p.s) % static_cast<int64_t>(p.w - p.s);
-        const int64_t src = ((static_cast<int64_t>(b) * p.n + j) * p.Hkv + h) * p.vpr + vec;
-        const int64_t dst = ((static_cast<int64_t>(b) * p.Hkv + h) * p.cap + slot) * p.vpr + vec;
-        p.ck[dst] = p.k_new[src];
-        p.cv[dst] = p.v_new[src];
+    for (int b = blockIdx.z; b < p.B; b += gridDim.z) {
+        for (int jj = blockIdx.y; jj < m; jj += gridDim.y) {
+            const int j = jj < p.a ? jj : p.b0 + (jj - p.a);
+            const int64_t pos = p.pos0 + j;
+            const int64_t slot =
+                (p.w < 0 || pos < p.s) ? pos : p.s + (pos - p.s) % static_cast<int64_t>(p.w - p.s);
+            const int64_t src = (static_cast<int64_t>(b) * p.n + j) * per_pos + t;
+            const int64_t dst = ((static_cast<int64_t>(b) * p.Hkv + h) * p.cap + slot) * p.vpr + vec;
+            const uint4 kv = p.k_new[src];
+            const uint4 vv = p.v_new[src];
+            p.ck[dst] = kv;
+            p.cv[dst] = vv;
+        }
     }
 }
 
@@ -66,6 +74,7 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
     p.n = n;
     p.Hkv = c.Hkv;
     p.vpr = c.d / 8;
+    p.vpr_log2 = p.vpr == 16 ? 4 : 3;  // d is 128 or 64
     p.cap = c.cap;
     p.w = c.w < 0 ? -1 : c.w;
     p.s = c.w < 0 ? 0 : c.s;
@@ -79,14 +88,13 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
         const int64_t b0 = static_cast<int64_t>(n) - (p.w - p.s);
         p.b0 = static_cast<int>(b0 < p.a ? p.a : b0);
     }
-    const int m = p.a + (n - p.b0);
-    const int64_t total = static_cast<int64_t>(p.B) * m * p.Hkv * p.vpr;
-    if (total == 0) return SWA_OK;
-    const int sms = device_sm_count();
-    int64_t blocks = (total + 255) / 256;
-    const int64_t max_blocks = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;
-    if (blocks > max_blocks) blocks = max_blocks;
-    swa_append_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    const int m = p.a + (n - p.b0);  // surviving positions per sequence
+    if (m == 0) return SWA_OK;
+    const int per_pos = p.Hkv * p.vpr;
+    const dim3 grid((per_pos + kAppendThreads - 1) / kAppendThreads,
+                    static_cast<unsigned>(m < 65535 ? m : 65535),
+                    static_cast<unsigned>(c.B < 65535 ? c.B : 65535));
+    swa_append_kernel<<<grid, kAppendThreads, 0, stream>>>(p);
     const cudaError_t e = cudaPeekAtLastError();
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_append_kernel");
 }

@@ -43,6 +43,25 @@ def test_append_bit_exact(w, s, d):
         pos += n
 
 
+def test_append_more_positions_than_a_grid_dimension():
+    """A bulk append whose surviving positions (every one of them, w = inf)
+    outnumber the 65535 limit of a grid's y dimension, into a cache at an
+    offset; plus a finite-window cache from a prompt of the same length."""
+    B, Hkv, d, n = 2, 1, 64, 70000
+    g = inputs.generator(12)
+    kn = inputs.normal_bf16((B, n, Hkv, d), g)
+    vn = inputs.normal_bf16((B, n, Hkv, d), g)
+    orc = oracle.get()
+    for w, s, pos0, cap in [(W_INF, 0, 16, n + 32), (512, 4, 0, None)]:
+        c = Cache(B, Hkv, d, w, s, max_len=cap)
+        hk, hv = _host_cache(c)
+        c.append(kn.cuda(), vn.cuda(), pos0)
+        orc.cache_append(hk, hv, bits(kn), bits(vn), pos0, w, s)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(c.k), hk), f"K, w={w}"
+        assert np.array_equal(bits(c.v), hv), f"V, w={w}"
+
+
 def _decode_case(B, Hq, Hkv, d, w, s, prompt, steps, check, seed=0, max_len=None):
     kp, vp, ks, vs, qs = inputs.decode_stream(B, Hq, Hkv, d, prompt, steps, seed=seed)
     c = Cache(B, Hkv, d, w, s, max_len=max_len)
