@@ -134,29 +134,55 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int row, int cc) {
 }
 
 // One work item: the slots [begin, end) of (sequence b, kv head kvh) that
-// split `split` covers; n_chunks == 0 when there is nothing to do (empty
-// split, or a position outside the cache, which is recorded as an error).
+// split `split` covers, of which those below n_valid = min(pos + 1, cap_eff)
+// are filled.
+//   Finite window: the splits partition [0, w) whatever the position, so an
+//   item's first chunk is known before pos is read; the producer issues it
+//   at once (spec) and reads pos while it is in flight.  Slots at or past
+//   n_valid (a cache not yet full) are masked.
+//   Infinite window: the splits partition [0, n_valid); only split 0's first
+//   chunk (slots 0..63) is known in advance.
+// n_chunks counts the chunks both sides walk: those holding filled slots,
+// and at least the speculative one.  A position outside the cache (bad) is
+// recorded as an error; its chunks are consumed and nothing is written.
 struct DecItem {
-    int b, kvh, split, begin, end, n_chunks;
-    bool bad;
+    int b, kvh, split, begin, end, n_chunks, n_valid;
+    bool bad, spec;
 };
 
-__device__ __forceinline__ DecItem dec_item(int it, const DecodeParams &p) {
+__device__ __forceinline__ DecItem dec_item_head(int it, const DecodeParams &p) {
     DecItem x;
     const int pair = it / p.splits;
     x.split = it - pair * p.splits;
     x.b = pair / p.Hkv;
     x.kvh = pair - x.b * p.Hkv;
-    const int pos = p.pos[x.b];
-    x.bad = pos < 0 || (p.w < 0 && pos >= p.cap);
-    x.begin = x.end = x.n_chunks = 0;
-    if (!x.bad) {
-        const int cap_eff = p.w < 0 ? p.cap : p.w;
+    x.begin = x.end = x.n_chunks = x.n_valid = 0;
+    x.bad = false;
+    if (p.w >= 0) {
         int used;
-        split_range(min(pos + 1, cap_eff), p.splits, x.split, x.begin, x.end, used);
-        if (x.end > x.begin) x.n_chunks = (x.end - x.begin + kDecCH - 1) / kDecCH;
+        split_range(p.w, p.splits, x.split, x.begin, x.end, used);
+        x.spec = x.end > x.begin;
+    } else {
+        x.spec = (x.split == 0);
     }
     return x;
+}
+
+__device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p) {
+    const int pos = p.pos[x.b];
+    x.bad = pos < 0 || (p.w < 0 && pos >= p.cap);
+    const int cap_eff = p.w < 0 ? p.cap : p.w;
+    x.n_valid = x.bad ? 0 : min(pos + 1, cap_eff);
+    if (p.w < 0) {
+        int used;
+        if (x.bad)
+            x.begin = x.end = 0;
+        else
+            split_range(x.n_valid, p.splits, x.split, x.begin, x.end, used);
+    }
+    const int hi = min(x.end, x.n_valid);
+    const int need = hi > x.begin ? (hi - x.begin + kDecCH - 1) / kDecCH : 0;
+    x.n_chunks = max(need, x.spec ? 1 : 0);
 }
 
 // Persistent: each CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...;
@@ -195,17 +221,16 @@ __global__ void __launch_bounds__(kDecThreads)
             int cg = 0;  // chunks issued by this CTA
             bool ok = true;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                const DecItem x = dec_item(it, p);
-                if (x.bad && x.kvh == 0 && x.split == 0) atomicCAS(&g_decode_error, 0, kErrBounds);
+                DecItem x = dec_item_head(it, p);
                 const int row_base = (x.b * p.Hkv + x.kvh) * p.cap;  // row of slot 0
                 const uint16_t *qsrc = p.q + (static_cast<int64_t>(x.b) * p.Hq + x.kvh * G) * D;
-                for (int c = 0; c < x.n_chunks; ++c, ++cg) {
+                // chunk c of the item into the next stage; q rides along with chunk 0
+                auto issue = [&](int c) -> bool {
                     const int st = cg % kDecStages;
-                    ok = mbar_wait(empty(st), ((cg / kDecStages) & 1) ^ 1, &g_decode_error, abort_flag);
-                    if (!ok) break;
+                    if (!mbar_wait(empty(st), ((cg / kDecStages) & 1) ^ 1, &g_decode_error, abort_flag))
+                        return false;
                     const uint32_t stage = sbase + st * SL::kStage;
                     const int row = row_base + x.begin + c * kDecCH;
-                    // q rides along with the first chunk of each item
                     mbar_arrive_expect_tx(full(st), 2 * SL::kChunkBytes + (c == 0 ? SL::kQBytes : 0));
 #pragma unroll
                     for (int r = 0; r < D / 64; ++r) {
@@ -214,7 +239,17 @@ __global__ void __launch_bounds__(kDecThreads)
                                     r * 64, row);
                     }
                     if (c == 0) bulk_load_1d(stage + 2 * SL::kChunkBytes, qsrc, SL::kQBytes, full(st));
+                    ++cg;
+                    return true;
+                };
+                int c = 0;
+                if (x.spec) {
+                    ok = issue(0);
+                    c = 1;
                 }
+                dec_item_pos(x, p);
+                if (x.bad && x.kvh == 0 && x.split == 0) atomicCAS(&g_decode_error, 0, kErrBounds);
+                for (; c < x.n_chunks && ok; ++c) ok = issue(c);
             }
             int no_abort = 0;  // drain the copies this thread started
             for (int i = 0; i < kDecStages && i < cg; ++i) {
@@ -235,7 +270,8 @@ __global__ void __launch_bounds__(kDecThreads)
     int cg = 0;                   // chunks consumed by this CTA
 
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const DecItem x = dec_item(it, p);
+        DecItem x = dec_item_head(it, p);
+        dec_item_pos(x, p);
         if (x.n_chunks == 0) continue;
         float acc[KS][4];  // O^T: d = 16*mt + gq (+8), heads 2tq, 2tq+1
 #pragma unroll
@@ -249,7 +285,8 @@ __global__ void __launch_bounds__(kDecThreads)
         for (int c = 0; c < x.n_chunks; ++c, ++cg) {
             const int st = cg % kDecStages;
             mbar_wait(full(st), (cg / kDecStages) & 1, &g_decode_error, abort_flag);
-            const int rows = min(kDecCH, x.end - (x.begin + c * kDecCH));
+            // filled slots of this chunk (none past n_valid, e.g. a speculative chunk)
+            const int rows = min(kDecCH, min(x.end, x.n_valid) - (x.begin + c * kDecCH));
             const int mine = rows - slot0;  // valid slots among this warp's 16
             if (c == 0) {
                 const uint16_t *qrow = reinterpret_cast<const uint16_t *>(
@@ -375,8 +412,9 @@ __global__ void __launch_bounds__(kDecThreads)
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
-        // over the warps; thread t handles outputs t, t+128, ...
-        for (int idx = threadIdx.x; idx < G * D; idx += kDecWarps * 32) {
+        // over the warps; thread t handles outputs t, t+128, ... (nothing is
+        // written for a position outside the cache)
+        for (int idx = threadIdx.x; idx < (x.bad ? 0 : G * D); idx += kDecWarps * 32) {
             const int h = idx / D, e = idx - h * D;
             float m = -INFINITY;
 #pragma unroll
@@ -415,8 +453,10 @@ __global__ void __launch_bounds__(128) swa_decode_merge_kernel(const DecodeParam
     if (pos < 0 || (p.w < 0 && pos >= p.cap)) return;  // recorded by the split kernel
     const int cap_eff = p.w < 0 ? p.cap : p.w;
     const int n_valid = min(pos + 1, cap_eff);
+    // the splits that wrote partials: those of [0, w) for a finite window
+    // (some may hold no filled slot: m = -inf, l = 0), of [0, n_valid) else
     int begin, end, used;
-    split_range(n_valid, p.splits, 0, begin, end, used);
+    split_range(p.w >= 0 ? p.w : n_valid, p.splits, 0, begin, end, used);
     constexpr int E = D / 32;
     float m = -INFINITY;
     for (int j = 0; j < used; ++j)

@@ -161,3 +161,46 @@ def test_decode_position_out_of_range_is_reported():
     decode(q, c, pos)
     assert device_error() == -7
     assert device_error() == 0
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,w,prompt", [(2, 32, 8, 128, 512, 100), (1, 8, 2, 64, 256, 5)])
+def test_decode_unfilled_slots_are_masked(B, Hq, Hkv, d, w, prompt):
+    """A finite-window cache not yet full: its unfilled slots hold NaN.  The
+    decode reads chunks of those slots (a window's splits cover all w slots,
+    some of them past the filled ones) and must mask every one of them."""
+    s = 4
+    g = inputs.generator(31)
+    kp = inputs.normal_bf16((B, prompt, Hkv, d), g)
+    vp = inputs.normal_bf16((B, prompt, Hkv, d), g)
+    q = inputs.normal_bf16((B, Hq, d), g)
+    c = Cache(B, Hkv, d, w, s)
+    c.k.fill_(float("nan"))
+    c.v.fill_(float("nan"))
+    c.append(kp.cuda(), vp.cuda(), 0)
+    pos = torch.full((B,), prompt - 1, dtype=torch.int32, device="cuda")
+    o = decode(q.cuda(), c, pos).cpu()
+    assert device_error() == 0
+    assert not torch.isnan(o.float()).any()
+    ref = oracle.get().decode(bits(q), bits(kp), bits(vp), [prompt - 1] * B, w, s)
+    assert_close(o, ref, f"filling SWA({w},4) at {prompt - 1}")
+
+
+def test_decode_negative_position_finite_window():
+    """pos < 0 for one sequence of a finite-window cache: SWA_ERR_BOUNDS is
+    recorded, that sequence's output is left alone, the others are exact."""
+    B, Hq, Hkv, d, w, s, prompt = 3, 8, 2, 128, 64, 4, 80
+    g = inputs.generator(32)
+    kp = inputs.normal_bf16((B, prompt, Hkv, d), g)
+    vp = inputs.normal_bf16((B, prompt, Hkv, d), g)
+    q = inputs.normal_bf16((B, Hq, d), g)
+    c = Cache(B, Hkv, d, w, s)
+    c.append(kp.cuda(), vp.cuda(), 0)
+    pos = torch.tensor([prompt - 1, -1, prompt - 1], dtype=torch.int32, device="cuda")
+    out = torch.full((B, Hq, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    decode(q.cuda(), c, pos, out=out)
+    assert device_error() == -7
+    o = out.cpu()
+    assert torch.all(o[1] == 7.0)
+    ref = oracle.get().decode(bits(q), bits(kp), bits(vp), [prompt - 1] * B, w, s)
+    for b in (0, 2):
+        assert_close(o[b:b + 1], ref[b:b + 1], f"b={b}")
