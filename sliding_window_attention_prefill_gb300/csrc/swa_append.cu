@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "swa_internal.h"
+#include "swa_ptx.cuh"
 
 namespace swa {
 
@@ -39,6 +40,8 @@ struct AppendParams {
 constexpr int kAppendThreads = 128;
 
 __global__ void __launch_bounds__(kAppendThreads) swa_append_kernel(const AppendParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int per_pos = p.Hkv * p.vpr;  // vectors of one position (all kv heads)
     const int t = blockIdx.x * kAppendThreads + threadIdx.x;
     if (t >= per_pos) return;
@@ -94,8 +97,7 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
     const dim3 grid((per_pos + kAppendThreads - 1) / kAppendThreads,
                     static_cast<unsigned>(m < 65535 ? m : 65535),
                     static_cast<unsigned>(c.B < 65535 ? c.B : 65535));
-    swa_append_kernel<<<grid, kAppendThreads, 0, stream>>>(p);
-    const cudaError_t e = cudaPeekAtLastError();
+    const cudaError_t e = launch_pdl(swa_append_kernel, grid, dim3(kAppendThreads), 0, stream, p);
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_append_kernel");
 }
 

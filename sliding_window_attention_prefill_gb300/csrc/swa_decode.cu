@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kDecThreads)
     auto full = [&](int st) { return sbase + SL::kBar + 8u * st; };
     auto empty = [&](int st) { return sbase + SL::kBar + 8u * (kDecStages + st); };
     const int n_items = p.B * p.Hkv * p.splits;
+    pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kDecStages; ++st) {
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kDecThreads)
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // the cache, q and pos are the previous kernels' from here on
 
     if (warp == kDecWarps) {
         // ---------------------------------------------------------------- producer
@@ -445,6 +447,8 @@ __global__ void __launch_bounds__(kDecThreads)
 // One warp per (sequence, query head): merge the non-empty splits.
 template <int D>
 __global__ void __launch_bounds__(128) swa_decode_merge_kernel(const DecodeParams p) {
+    pdl_launch_dependents();
+    pdl_wait();  // the split kernel's partials
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= p.B * p.Hq) return;
@@ -534,13 +538,12 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStre
     const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
     const long long cap_ctas = static_cast<long long>(SWA_DEC_CTAS_PER_SM) * sms;
     const int grid = static_cast<int>(items < cap_ctas ? items : cap_ctas);
-    swa_decode_kernel<D, G><<<grid, kDecThreads, SL::kAlloc, stream>>>(maps, p);
-    e = cudaPeekAtLastError();
+    e = launch_pdl(swa_decode_kernel<D, G>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
+                   maps, p);
     if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_kernel");
     if (p.splits > 1) {
         const int rows = p.B * p.Hq;
-        swa_decode_merge_kernel<D><<<(rows + 3) / 4, 128, 0, stream>>>(p);
-        e = cudaPeekAtLastError();
+        e = launch_pdl(swa_decode_merge_kernel<D>, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
         if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_merge_kernel");
     }
     return SWA_OK;

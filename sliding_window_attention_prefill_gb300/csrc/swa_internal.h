@@ -7,6 +7,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "swa.h"
 
@@ -39,6 +40,27 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
                          int64_t pos0, cudaStream_t stream);
 swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,
                          void *workspace, const DecodePlan &plan, cudaStream_t stream);
+
+// Launch with programmatic stream serialization: the kernel's CTAs may be
+// placed while the previous kernel of the stream drains, so its prologue
+// (barrier init, TMEM allocation, tensor-map prefetch) overlaps that tail.
+// Every kernel of the library executes griddepcontrol.wait before it reads
+// or writes global memory, so stream order is kept for the data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Record the CUDA error behind an SWA_ERR_CUDA (per host thread) and return
 // SWA_ERR_CUDA; `where` names the failing call.

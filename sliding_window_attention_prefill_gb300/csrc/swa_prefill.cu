@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SL::kNumBars; ++i) {
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // inputs and outputs are the previous kernels' from here on
 
     // Register split: 3 x 128 threads launched at 168 registers each
     // (64512); the first warpgroup drops to 80 and the softmax warpgroups
@@ -577,8 +579,8 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
     const int sms = device_sm_count();
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const int grid = p.n_units < sms ? p.n_units : sms;
-    swa_prefill_kernel<D, KT, NSK, NSV><<<grid, kThreads, SL::kAlloc, stream>>>(maps, p);
-    e = cudaPeekAtLastError();
+    e = launch_pdl(swa_prefill_kernel<D, KT, NSK, NSV>, dim3(grid), dim3(kThreads), SL::kAlloc,
+                   stream, maps, p);
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_prefill_kernel");
 }
 

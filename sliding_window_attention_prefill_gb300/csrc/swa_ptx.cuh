@@ -101,6 +101,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *er
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Let the next kernel of the stream start launching (its CTAs are placed as
+// this grid's CTAs exit; it still waits below before using our results).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the previous kernel of the stream has completed and its memory
+// operations are visible (returns at once when there is no such dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // proxy fences
 // ---------------------------------------------------------------------------
 // Make this thread's generic-proxy shared-memory writes visible to the async
