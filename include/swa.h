@@ -204,6 +204,17 @@ const char *swa_status_string(swa_status status);
 swa_status swa_get_device_error(swa_stream_t stream);
 
 /*
+ * swa_selftest_wait_timeout -- enqueue a one-CTA kernel whose bounded wait
+ * runs out on purpose: it waits on an mbarrier that nothing arrives on,
+ * through the same bounded wait as every kernel of the library, holding a
+ * TMEM allocation.  After the wait limit (0.2 s) it records SWA_ERR_TIMEOUT,
+ * frees the TMEM and returns, so the context stays usable.  Returns SWA_OK
+ * when the kernel was enqueued; swa_get_device_error then reports
+ * SWA_ERR_TIMEOUT.  For tests of the failure path; no GPU fault is involved.
+ */
+swa_status swa_selftest_wait_timeout(swa_stream_t stream);
+
+/*
  * Host-only argument checks: the validation the calls above run before
  * enqueuing anything, without touching the GPU.  Same return codes.
  */

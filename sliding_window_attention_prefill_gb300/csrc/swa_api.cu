@@ -232,6 +232,10 @@ swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos,
     return swa::decode_launch(q, *cache, pos, Hq, o, workspace, plan, as_cuda(stream));
 }
 
+swa_status swa_selftest_wait_timeout(swa_stream_t stream) {
+    return swa::selftest_wait_launch(as_cuda(stream));
+}
+
 swa_status swa_get_device_error(swa_stream_t stream) {
     const int a = swa::prefill_read_clear_error(as_cuda(stream));
     const int b = swa::decode_read_clear_error(as_cuda(stream));

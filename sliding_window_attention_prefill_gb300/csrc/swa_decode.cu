@@ -607,6 +607,42 @@ int decode_read_clear_error(cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------------------
+// self-test of the wait limit (swa_selftest_wait_timeout)
+// ---------------------------------------------------------------------------
+// One warp holds 32 TMEM columns and waits on an mbarrier that nothing
+// arrives on.  Each lane's bounded wait gives up after SWA_WAIT_LIMIT_NS
+// (the first records SWA_ERR_TIMEOUT and sets the abort flag, the others
+// then return at once); the warp frees the TMEM and the kernel ends.
+__global__ void __launch_bounds__(32) swa_wait_selftest_kernel() {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    tmem_alloc(smem_u32(&tmem_slot), 32);
+    tmem_relinquish();
+    tc_fence_before_sync();
+    __syncwarp();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    const bool ok = mbar_wait(smem_u32(&bar), 0, &g_decode_error, &abort_flag);
+    if (ok) atomicCAS(&g_decode_error, 0, kErrBounds);  // cannot happen: nothing arrives
+    tc_fence_before_sync();
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 32);
+}
+
+swa_status selftest_wait_launch(cudaStream_t stream) {
+    swa_wait_selftest_kernel<<<1, 32, 0, stream>>>();
+    const cudaError_t e = cudaPeekAtLastError();
+    return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_wait_selftest_kernel");
+}
+
+// ---------------------------------------------------------------------------
 // decode without a caller-provided workspace (swa_decode_noalloc)
 // ---------------------------------------------------------------------------
 // Split partials for callers that cannot allocate: a fixed device array owned

@@ -67,6 +67,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 swa_status cuda_fail(cudaError_t e, const char *where);
 const char *last_cuda_error();
 
+// The wait-limit self-test kernel (records SWA_ERR_TIMEOUT in the decode
+// module's error word).
+swa_status selftest_wait_launch(cudaStream_t stream);
+
 // Read and clear each module's device error word (synchronises `stream`).
 // Returns 0 or a negative swa_status value.
 int prefill_read_clear_error(cudaStream_t stream);

@@ -80,6 +80,8 @@ def _declare(L) -> None:
     L.swa_version.restype = ctypes.c_char_p
     L.swa_last_cuda_error.argtypes = []
     L.swa_last_cuda_error.restype = ctypes.c_char_p
+    L.swa_selftest_wait_timeout.argtypes = [_c_p]
+    L.swa_selftest_wait_timeout.restype = _c_int
 
 
 def lib():
@@ -236,6 +238,14 @@ def decode(q: torch.Tensor, cache: Cache, pos: torch.Tensor, out: torch.Tensor |
                           _ptr(ws), nbytes, _stream(q.device))
     _check(st, "swa_decode")
     return o
+
+
+def selftest_wait_timeout(device=None) -> None:
+    """Enqueue the kernel whose bounded wait runs out on purpose (see
+    swa_selftest_wait_timeout in include/swa.h); read the result with
+    device_error()."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    _check(lib().swa_selftest_wait_timeout(_stream(dev)), "swa_selftest_wait_timeout")
 
 
 def device_error(device=None) -> int:
