@@ -43,12 +43,6 @@
 #ifndef SWA_PREFILL_FORCE_KT
 #define SWA_PREFILL_FORCE_KT 0
 #endif
-#ifndef SWA_PREFILL_NARROW_NSK
-#define SWA_PREFILL_NARROW_NSK 2
-#endif
-#ifndef SWA_PREFILL_NARROW_NSV
-#define SWA_PREFILL_NARROW_NSV 2
-#endif
 
 namespace swa {
 
@@ -66,7 +60,11 @@ struct PrefillSmem {
     static constexpr int kQ = 0;                        // 2 Q buffers
     static constexpr int kK = kQ + 2 * kQTile;          // K ring
     static constexpr int kV = kK + NSK * kKTile;        // V ring
-    static constexpr int kRed = kV + NSV * kKTile;      // row max [2 parity][2 half][128]
+    // O tile staged for one TMA store (128-column tiles only: 128 x d bf16,
+    // d/64 slabs of 128 rows x 128 bytes, 128-byte swizzle)
+    static constexpr int kStageO = kV + NSV * kKTile;
+    static constexpr int kStageBytes = (KT == 128) ? 128 * D * 2 : 0;
+    static constexpr int kRed = kStageO + kStageBytes;  // row max [2 parity][2 half][128]
     static constexpr int kRedL = kRed + 2 * 2 * 128 * 4;  // row sum [2 parity][2 half][128]
     static constexpr int kBar = kRedL + 2 * 2 * 128 * 4;
     static constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = 4 + NSK,
@@ -94,6 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // softmax of a tile need not wait for the previous P V to write its P,
     // and a unit's epilogue runs while the next unit's P V goes on.
     constexpr bool DB = (KT == 128);
+    constexpr bool kStageOut = (KT == 128);  // epilogue through shared memory + TMA store
     constexpr uint32_t kTP = DB ? 128u : 256u;
     constexpr uint32_t kTO = DB ? 256u : 384u;
     static_assert(kTO + (DB ? 2 : 1) * D <= kTmemCols, "TMEM columns");
@@ -304,6 +303,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto epilogue = [&](float l_tot, uint32_t ob) {
             const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const bool ok = !*abort_flag;
+            if constexpr (kStageOut) {
+                // Stage O / l as bf16 in the 128-byte-swizzled layout of the
+                // output box (row r = MMA row: position r/G, head r%G) and
+                // store the whole unit with one TMA tensor store per 64-column
+                // slab; rows past the sequence end fall outside the tensor
+                // and are not written.
+                const uint32_t stage = base + SL::kStageO;
+                if (threadIdx.x == 128) tma_store_wait_read_all();  // previous store read it
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_lane + kTO + (DB ? ob * D : 0u) + half * (D / 2) + 32 * c, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w4[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv_l,
+                                                __uint_as_float(r[8 * v + 2 * e + 1]) * inv_l);
+                        const int col = half * (D / 2) + 32 * c + 8 * v;  // first column
+                        const int ci = (col & 63) >> 3;                   // 16-byte chunk in the row
+                        const uint32_t addr = stage + (col >> 6) * (128 * 128) + row * 128 +
+                                              ((ci ^ (row & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                     "r"(w4[0]), "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                                     : "memory");
+                    }
+                }
+                fence_proxy_async_smem();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (threadIdx.x == 128 && ok) {
+#pragma unroll
+                    for (int db = 0; db < D / 64; ++db)
+                        tma_store_4d(&maps.o, stage + db * (128 * 128), db * 64, pend_kvh * p.G,
+                                     pend_t0, pend_b);
+                    tma_store_commit();
+                }
+                if (p.lse != nullptr && ok && pend_valid && half == 0) {
+                    const int h = pend_kvh * p.G + hrow;
+                    p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + pend_t] =
+                        pend_m * p.scale + logf(l_tot);
+                }
+                return;
+            }
             // This thread's half row of O / l as CH 16-byte chunks of bf16.
             constexpr int CH = D / 16;
             uint4 ch[CH];
@@ -547,6 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("bar.sync 1, 256;" ::: "memory");
             epilogue(rl[row] + rl[128 + row], (uc - 1) & 1);
         }
+        // the staged output must be written before the CTA exits
+        if (kStageOut && threadIdx.x == 128) tma_store_wait_all();
     }
 
     tc_fence_before_sync();
@@ -586,17 +633,17 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
 
 }  // namespace
 
-// Key tile width for a call: whichever makes the widest unit cheaper, a
-// 128-column tile (two-stage K/V rings, double-buffered P and O) costing
-// about 5/8 of a 256-column one on GB300 (measured for d = 128 at windows
-// 64 .. 2048 and full causal): 128 for SWA(64,4) and SWA(256,4), 256 for
-// SWA(128,4), SWA(512,4) and wider bands.
+// Key tile width for a call: 128 columns (two-stage K ring, double-buffered
+// P and O, epilogue through shared memory and a TMA store) while the widest
+// unit spans at most 768 key columns, else 256 (one tile fills the MMA's
+// N = 256).  Measured on GB300 at d = 128: 128 is faster for SWA(64..512,4)
+// (unit spans of 99..547 columns), 256 for SWA(1024,4), SWA(2048,4) and full
+// causal.
 bool prefill_narrow(const PrefillParams &p) {
     if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT == 128;
     const long long cols =
         p.w < 0 ? static_cast<long long>(p.L) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
-    const long long t128 = (cols + 127) / 128, t256 = (cols + 255) / 256;
-    return 5 * t128 < 8 * t256;
+    return cols <= 768;
 }
 
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
@@ -607,7 +654,7 @@ swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, 
     if (!encode_prefill_maps(&maps, q, k, v, p, d, narrow ? 128 : 256))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     if (d == 128)
-        return narrow ? launch_prefill<128, 128, SWA_PREFILL_NARROW_NSK, SWA_PREFILL_NARROW_NSV>(maps, p, stream)
+        return narrow ? launch_prefill<128, 128, 2, 1>(maps, p, stream)
                       : launch_prefill<128, 256, 1, 1>(maps, p, stream);
     return narrow ? launch_prefill<64, 128, 4, 4>(maps, p, stream)
                   : launch_prefill<64, 256, 2, 2>(maps, p, stream);

@@ -30,6 +30,7 @@ struct PrefillMaps {
     CUtensorMap k_band, v_band;       // box {64, 1, KT, 1} over [B, L, Hkv, d]
     CUtensorMap k_sink, v_sink;       // box {64, 1, s_pad, 1}
     CUtensorMap k_band0, v_band0;     // box {64, 1, KT - s_pad, 1}
+    CUtensorMap o;                    // box {64, G, P, 1} over the [B, L, Hq, d] output
 };
 
 struct PrefillParams {
@@ -120,6 +121,7 @@ static inline bool encode_prefill_maps(PrefillMaps *maps, const void *q, const v
                                        const void *v, const PrefillParams &p, int d, int kt) {
     std::memset(maps, 0, sizeof(*maps));
     bool ok = encode_prefill_map(&maps->q, q, d, p.Hq, p.L, p.B, p.G, p.P) &&
+              encode_prefill_map(&maps->o, p.o, d, p.Hq, p.L, p.B, p.G, p.P) &&
               encode_prefill_map(&maps->k_band, k, d, p.Hkv, p.L, p.B, 1, kt) &&
               encode_prefill_map(&maps->v_band, v, d, p.Hkv, p.L, p.B, 1, kt);
     if (ok && p.s_pad > 0)
