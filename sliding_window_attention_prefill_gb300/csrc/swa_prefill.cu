@@ -15,7 +15,8 @@
 //   warp 1       tcgen05 issuer; owns the 512-column TMEM allocation
 //                S (256 columns) | P (128 columns, bf16 pairs) | O (d columns)
 //   warp 2       TMA producer for V tiles
-//   warp 3       idle
+//   warp 3       TMA stores of the staged output tile (128-column key tiles;
+//                idle otherwise)
 //   warps 4..11  softmax + epilogue: two threads per MMA row (TMEM lane), each
 //                taking every other 32-column chunk of the key tile
 // Key tiles of 256 columns let S = Q K^T run as N = 256 MMAs (twice the work
@@ -70,7 +71,10 @@ struct PrefillSmem {
     static constexpr int kQFull = 0, kQEmpty = 2, kKFull = 4, kKEmpty = 4 + NSK,
                          kVFull = 4 + 2 * NSK, kVEmpty = 4 + 2 * NSK + NSV,
                          kSFull = 4 + 2 * NSK + 2 * NSV, kSEmpty = kSFull + 1,
-                         kPFull = kSFull + 2, kPVDone = kSFull + 3, kNumBars = kSFull + 5;
+                         kPFull = kSFull + 2, kPVDone = kSFull + 3,
+                         // staged epilogue: O written (one arrive per softmax
+                         // warp), staging buffer read by its stores
+                         kOStaged = kSFull + 5, kOFree = kSFull + 6, kNumBars = kSFull + 7;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SL::kNumBars; ++i) {
-            const bool eight = (i == SL::kSEmpty || i == SL::kPFull);
+            const bool eight = (i == SL::kSEmpty || i == SL::kPFull || i == SL::kOStaged);
             mbar_init(bar(i), eight ? 8u : 1u);
         }
         *abort_flag = 0;
@@ -278,6 +282,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     mbar_wait(bar(SL::kPVDone), last_pv_g & 1, &g_prefill_error, &no_abort);
             }
+        } else if (kStageOut && warp == 3 && lane == 0) {
+            // -------------------------------------------------------- output stores
+            // For each unit in the softmax warps' order: once they have staged
+            // its O tile, store it with TMA, wait until the store has read the
+            // buffer and hand the buffer back.
+            uint32_t e = 0;
+            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++e) {
+                const Unit x = unit_geom<KT>(u, p);
+                const bool staged =
+                    mbar_wait(bar(SL::kOStaged), e & 1, &g_prefill_error, abort_flag);
+                if (staged && !*abort_flag) {
+#pragma unroll
+                    for (int db = 0; db < D / 64; ++db)
+                        tma_store_4d(&maps.o, base + SL::kStageO + db * (128 * 128), db * 64,
+                                     x.kvh * p.G, x.t0, x.b);
+                    tma_store_commit();
+                    tma_store_wait_read_all();
+                }
+                mbar_arrive(bar(SL::kOFree));
+            }
+            tma_store_wait_all();  // the stores are complete before the CTA exits
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
@@ -300,18 +325,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool pend = false, pend_valid = false;
         int pend_b = 0, pend_kvh = 0, pend_t = 0, pend_t0 = 0, pend_t1 = 0;
         float pend_m = 0.f, pend_l = 0.f;
+        uint32_t ep = 0;  // staged epilogues so far
         auto epilogue = [&](float l_tot, uint32_t ob) {
             const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const bool ok = !*abort_flag;
             if constexpr (kStageOut) {
                 // Stage O / l as bf16 in the 128-byte-swizzled layout of the
-                // output box (row r = MMA row: position r/G, head r%G) and
-                // store the whole unit with one TMA tensor store per 64-column
-                // slab; rows past the sequence end fall outside the tensor
-                // and are not written.
+                // output box (row r = MMA row: position r/G, head r%G); warp 3
+                // stores the whole unit with one TMA tensor store per 64-column
+                // slab (rows past the sequence end fall outside the tensor and
+                // are not written), so no softmax warp waits on the store.
                 const uint32_t stage = base + SL::kStageO;
-                if (threadIdx.x == 128) tma_store_wait_read_all();  // previous store read it
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                // the previous unit's stores have read the buffer
+                mbar_wait(bar(SL::kOFree), (ep & 1u) ^ 1u, &g_prefill_error, abort_flag);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     uint32_t r[32];
@@ -334,14 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 fence_proxy_async_smem();
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                if (threadIdx.x == 128 && ok) {
-#pragma unroll
-                    for (int db = 0; db < D / 64; ++db)
-                        tma_store_4d(&maps.o, stage + db * (128 * 128), db * 64, pend_kvh * p.G,
-                                     pend_t0, pend_b);
-                    tma_store_commit();
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(SL::kOStaged));  // warp 3 stores it
+                ++ep;
                 if (p.lse != nullptr && ok && pend_valid && half == 0) {
                     const int h = pend_kvh * p.G + hrow;
                     p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + pend_t] =
@@ -436,8 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sink_hi = 0;
                 }
                 const bool band_ok = c_lo <= c_hi;
-                const unsigned span = band_ok ? static_cast<unsigned>(c_hi - c_lo) : 0u;
-                const int band_from = band_ok ? c_lo : 1 << 20;
                 bool full[NC], empty[NC];
 #pragma unroll
                 for (int i = 0; i < NC; ++i) {
@@ -453,28 +472,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(SL::kSEmpty));
 
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < NC; ++i) {
                     if (empty[i]) continue;
                     if (!full[i]) {
-                        const int x0 = 32 * (half + 2 * i) - band_from;
-                        const int sh = sink_hi - 32 * (half + 2 * i);
+                        // attended columns of this chunk as a bit mask: the band
+                        // [c_lo, c_hi] and the sinks [0, sink_hi), clipped to it
+                        const int c0 = 32 * (half + 2 * i);
+                        const int lo = max(c_lo - c0, 0), hi = min(c_hi - c0, 31);
+                        uint32_t vb = (band_ok && lo <= hi) ? ((0xFFFFFFFFu >> (31 - (hi - lo))) << lo) : 0u;
+                        const int ns = sink_hi - c0;
+                        vb |= ns <= 0 ? 0u : (ns >= 32 ? 0xFFFFFFFFu : ((1u << ns) - 1u));
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
-                            if (!(static_cast<unsigned>(x0 + e) <= span || e < sh))
-                                sr[i][e] = __float_as_uint(-INFINITY);
+                            if (!(vb & (1u << e))) sr[i][e] = __float_as_uint(-INFINITY);
                     }
+                    // elements 0..1, then 2..29 four at a time, then 30..31
+                    float a = __uint_as_float(sr[i][0]), b = __uint_as_float(sr[i][1]);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(sr[i][e]));
+                    for (int e = 2; e < 30; e += 4) {
+                        a = fmax3(a, __uint_as_float(sr[i][e]), __uint_as_float(sr[i][e + 1]));
+                        b = fmax3(b, __uint_as_float(sr[i][e + 2]), __uint_as_float(sr[i][e + 3]));
+                    }
+                    mx_a = fmax3(mx_a, a, __uint_as_float(sr[i][30]));
+                    mx_b = fmax3(mx_b, b, __uint_as_float(sr[i][31]));
                 }
                 // Row max over both halves through shared memory, one barrier
                 // per tile (buffers alternate with the tile parity); the first
                 // tile of a unit also exchanges the previous unit's row sums.
                 float *rm = red + (g & 1) * 256;
                 float *rl = redl + ((uc - 1) & 1) * 256;
-                rm[half * 128 + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                rm[half * 128 + row] = fmaxf(mx_a, mx_b);
                 const bool do_epi = (j == 0 && pend);
                 if (do_epi) rl[half * 128 + row] = pend_l;
                 asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -592,8 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("bar.sync 1, 256;" ::: "memory");
             epilogue(rl[row] + rl[128 + row], (uc - 1) & 1);
         }
-        // the staged output must be written before the CTA exits
-        if (kStageOut && threadIdx.x == 128) tma_store_wait_all();
     }
 
     tc_fence_before_sync();

@@ -33,12 +33,31 @@ struct PrefillMaps {
     CUtensorMap o;                    // box {64, G, P, 1} over the [B, L, Hq, d] output
 };
 
+// Division by a divisor fixed for a call, as a multiply-high and a shift
+// (round-up method): l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (mulhi(m, n) + n) >> l, exact for 0 <= n < 2^31, 1 <= d < 2^31.
+struct FastDiv {
+    uint32_t m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+    return FastDiv{static_cast<uint32_t>(m), l};
+}
+
+__device__ __forceinline__ int fast_div(int n, const FastDiv &f) {
+    return static_cast<int>((__umulhi(f.m, static_cast<uint32_t>(n)) + static_cast<uint32_t>(n)) >> f.l);
+}
+
 struct PrefillParams {
     int B, L, Hq, Hkv, G, P;  // P: positions per query tile (128 / G)
     int g_log2;               // G is a power of two (row r: position r >> g_log2)
     int w, s;                 // w < 0: infinite window (s is then 0)
     int s_pad;                // sink rows loaded: s rounded up to 8 (0 if s == 0)
     int n_qtiles, n_units;
+    FastDiv div_bh, div_hkv;  // by B * Hkv and by Hkv (unit geometry)
     float scale_log2;         // log2(e) / sqrt(d)
     float scale;              // 1 / sqrt(d)
     uint16_t *o;              // [B, L, Hq, d] bf16
@@ -54,10 +73,10 @@ struct Unit {
 template <int KT>
 __device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p) {
     const int bh = p.B * p.Hkv;
-    const int qt_rev = u / bh;
+    const int qt_rev = fast_div(u, p.div_bh);
     const int r = u - qt_rev * bh;
     Unit x;
-    x.b = r / p.Hkv;
+    x.b = fast_div(r, p.div_hkv);
     x.kvh = r - x.b * p.Hkv;
     const int qt = p.n_qtiles - 1 - qt_rev;
     x.t0 = qt * p.P;
@@ -93,6 +112,8 @@ inline PrefillParams make_prefill_params(void *o, float *lse, int B, int L, int 
     p.s_pad = (p.s + 7) & ~7;
     p.n_qtiles = (L + p.P - 1) / p.P;
     p.n_units = B * Hkv * p.n_qtiles;
+    p.div_bh = make_fastdiv(static_cast<uint32_t>(B * Hkv > 0 ? B * Hkv : 1));
+    p.div_hkv = make_fastdiv(static_cast<uint32_t>(Hkv > 0 ? Hkv : 1));
     p.scale = 1.0f / std::sqrt(static_cast<float>(d));
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.o = static_cast<uint16_t *>(o);
