@@ -64,7 +64,7 @@ struct PrefillSmem {
     // O tile staged for one TMA store (128-column tiles only: 128 x d bf16,
     // d/64 slabs of 128 rows x 128 bytes, 128-byte swizzle)
     static constexpr int kStageO = kV + NSV * kKTile;
-    static constexpr int kStageBytes = (KT == 128) ? 128 * D * 2 : 0;
+    static constexpr int kStageBytes = (KT <= 128) ? 128 * D * 2 : 0;
     static constexpr int kRed = kStageO + kStageBytes;  // row max [2 parity][2 half][128]
     static constexpr int kRedL = kRed + 2 * 2 * 128 * 4;  // row sum [2 parity][2 half][128]
     static constexpr int kBar = kRedL + 2 * 2 * 128 * 4;
@@ -89,14 +89,14 @@ template <int D, int KT, int NSK, int NSV>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
     using SL = PrefillSmem<D, KT, NSK, NSV>;
-    constexpr int NC = KT / 64;  // 32-column chunks of a tile per softmax thread
+    constexpr int NC = (KT + 63) / 64;  // 32-column chunks of a tile per softmax thread
     // TMEM columns.  256-column tiles: S [0,256) | P [256,384) | O [384,384+d).
     // 128-column tiles leave room to double-buffer P (by tile) and O (by
     // unit): S [0,128) | P0, P1 [128,256) | O0, O1 [256,256+2d); then the
     // softmax of a tile need not wait for the previous P V to write its P,
     // and a unit's epilogue runs while the next unit's P V goes on.
-    constexpr bool DB = (KT == 128);
-    constexpr bool kStageOut = (KT == 128);  // epilogue through shared memory + TMA store
+    constexpr bool DB = (KT <= 128);
+    constexpr bool kStageOut = (KT <= 128);  // epilogue through shared memory + TMA store
     constexpr uint32_t kTP = DB ? 128u : 256u;
     constexpr uint32_t kTO = DB ? 256u : 384u;
     static_assert(kTO + (DB ? 2 : 1) * D <= kTmemCols, "TMEM columns");
@@ -660,31 +660,37 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
 
 }  // namespace
 
-// Key tile width for a call: 128 columns (two-stage K ring, double-buffered
-// P and O, epilogue through shared memory and a TMA store) while the widest
-// unit spans at most 768 key columns, else 256 (one tile fills the MMA's
-// N = 256).  Measured on GB300 at d = 128: 128 is faster for SWA(64..512,4)
-// (unit spans of 99..547 columns), 256 for SWA(1024,4), SWA(2048,4) and full
-// causal.
-bool prefill_narrow(const PrefillParams &p) {
-    if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT == 128;
+// Key tile width for a call, from the widest unit's span of key columns:
+//   <= 112: one 112-column tile per unit; K and V tiles of 28 KB leave room
+//           for two stages of each beside the staged output tile;
+//   <= 768: 128-column tiles (two-stage K ring, one V stage, double-buffered
+//           P and O, epilogue through shared memory and a TMA store);
+//   else:   256 (one tile fills the MMA's N = 256).
+// Measured on GB300 at d = 128: 128 is faster for SWA(64..512,4) (unit spans
+// of 99..547 columns), 256 for SWA(1024,4), SWA(2048,4) and full causal.
+int prefill_key_tile(const PrefillParams &p) {
+    if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT;
     const long long cols =
         p.w < 0 ? static_cast<long long>(p.L) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
-    return cols <= 768;
+    if (cols <= 112) return 112;
+    return cols <= 768 ? 128 : 256;
 }
 
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                           int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream) {
     const PrefillParams p = make_prefill_params(o, lse, B, L, Hq, Hkv, d, w, s);
-    const bool narrow = prefill_narrow(p);
+    int kt = prefill_key_tile(p);
+    if (d != 128 && kt == 112) kt = 128;  // d = 64 has room for deep rings at 128
     PrefillMaps maps;
-    if (!encode_prefill_maps(&maps, q, k, v, p, d, narrow ? 128 : 256))
+    if (!encode_prefill_maps(&maps, q, k, v, p, d, kt))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    if (d == 128)
-        return narrow ? launch_prefill<128, 128, 2, 1>(maps, p, stream)
-                      : launch_prefill<128, 256, 1, 1>(maps, p, stream);
-    return narrow ? launch_prefill<64, 128, 4, 4>(maps, p, stream)
-                  : launch_prefill<64, 256, 2, 2>(maps, p, stream);
+    if (d == 128) {
+        if (kt == 112) return launch_prefill<128, 112, 2, 2>(maps, p, stream);
+        return kt == 128 ? launch_prefill<128, 128, 2, 1>(maps, p, stream)
+                         : launch_prefill<128, 256, 1, 1>(maps, p, stream);
+    }
+    return kt == 128 ? launch_prefill<64, 128, 4, 4>(maps, p, stream)
+                     : launch_prefill<64, 256, 2, 2>(maps, p, stream);
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {
