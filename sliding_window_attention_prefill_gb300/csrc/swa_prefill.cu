@@ -661,36 +661,37 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
 }  // namespace
 
 // Key tile width for a call, from the widest unit's span of key columns:
-//   <= 112: one 112-column tile per unit; K and V tiles of 28 KB leave room
-//           for two stages of each beside the staged output tile;
-//   <= 768: 128-column tiles (two-stage K ring, one V stage, double-buffered
-//           P and O, epilogue through shared memory and a TMA store);
+//   <= 768: narrow tiles with double-buffered P and O and the output staged
+//           for TMA stores; at d = 128 they are 112 columns, whose 28 KB K and
+//           V tiles leave room for two stages of each beside the 32 KB staged
+//           output tile; at d = 64, 128 columns with four stages of each;
 //   else:   256 (one tile fills the MMA's N = 256).
-// Measured on GB300 at d = 128: 128 is faster for SWA(64..512,4) (unit spans
-// of 99..547 columns), 256 for SWA(1024,4), SWA(2048,4) and full causal.
-int prefill_key_tile(const PrefillParams &p) {
+// Measured on GB300 at d = 128 (TFLOP/s with 112 / 128 / 256-column tiles):
+// SWA(128,4) 509 / 447 / 456, SWA(256,4) 686 / 656 / 569, SWA(512,4)
+// 868 / 841 / 836, SWA(1024,4) 914 / 997 / 1083; full causal is fastest
+// with 256.
+int prefill_key_tile(const PrefillParams &p, int d) {
     if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT;
     const long long cols =
         p.w < 0 ? static_cast<long long>(p.L) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
-    if (cols <= 112) return 112;
-    return cols <= 768 ? 128 : 256;
+    if (cols > 768) return 256;
+    return d == 128 ? 112 : 128;
 }
 
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                           int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream) {
     const PrefillParams p = make_prefill_params(o, lse, B, L, Hq, Hkv, d, w, s);
-    int kt = prefill_key_tile(p);
-    if (d != 128 && kt == 112) kt = 128;  // d = 64 has room for deep rings at 128
+    // the widths that have a kernel: 112 or 256 at d = 128, 128 or 256 at d = 64
+    int kt = prefill_key_tile(p, d);
+    if (kt != 256) kt = (d == 128) ? 112 : 128;
     PrefillMaps maps;
     if (!encode_prefill_maps(&maps, q, k, v, p, d, kt))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    if (d == 128) {
-        if (kt == 112) return launch_prefill<128, 112, 2, 2>(maps, p, stream);
-        return kt == 128 ? launch_prefill<128, 128, 2, 1>(maps, p, stream)
-                         : launch_prefill<128, 256, 1, 1>(maps, p, stream);
-    }
-    return kt == 128 ? launch_prefill<64, 128, 4, 4>(maps, p, stream)
-                     : launch_prefill<64, 256, 2, 2>(maps, p, stream);
+    if (d == 128)
+        return kt == 256 ? launch_prefill<128, 256, 1, 1>(maps, p, stream)
+                         : launch_prefill<128, 112, 2, 2>(maps, p, stream);
+    return kt == 256 ? launch_prefill<64, 256, 2, 2>(maps, p, stream)
+                     : launch_prefill<64, 128, 4, 4>(maps, p, stream);
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {
