@@ -43,17 +43,18 @@ namespace swa {
 
 __device__ int g_decode_error;
 
-#ifndef SWA_DEC_STAGES
-#define SWA_DEC_STAGES 2
-#endif
 #ifndef SWA_DEC_ITEMS_PER_SM
 #define SWA_DEC_ITEMS_PER_SM 4
 #endif
 #ifndef SWA_DEC_CTAS_PER_SM
 #define SWA_DEC_CTAS_PER_SM 2
 #endif
+#ifndef SWA_DEC_CTAS_PER_SM_SINGLE
+#define SWA_DEC_CTAS_PER_SM_SINGLE 4
+#endif
+// persistent CTAs per SM with a 1-stage and a 2-stage chunk ring
+constexpr int kDecCtasPerSm[2] = {SWA_DEC_CTAS_PER_SM_SINGLE, SWA_DEC_CTAS_PER_SM};
 constexpr int kDecCH = 64;              // slots per chunk
-constexpr int kDecStages = SWA_DEC_STAGES;  // chunk ring depth
 constexpr int kDecWarps = 4;            // consumer warps, 16 slots each
 constexpr int kDecThreads = 32 * (kDecWarps + 1);
 
@@ -71,17 +72,19 @@ struct DecodeParams {
     float scale_log2;
 };
 
-template <int D, int G>
+// ST: depth of the chunk ring (2 when items span several chunks; 1 when every
+// item is a single chunk, which halves shared memory so more CTAs fit).
+template <int D, int G, int ST>
 struct DecSmem {
     static constexpr int kRegion = kDecCH * 128;            // 64 rows x 64 columns (bf16)
     static constexpr int kChunkBytes = (D / 64) * kRegion;  // one of K or V
     static constexpr int kQBytes = G * D * 2;               // q of the G heads of the item
     static constexpr int kStage = 2 * kChunkBytes + ((kQBytes + 1023) & ~1023);  // K | V | q
-    static constexpr int kP = kDecStages * kStage;          // [warp][16 slots][8 heads] bf16
+    static constexpr int kP = ST * kStage;          // [warp][16 slots][8 heads] bf16
     static constexpr int kAcc = kP + kDecWarps * 16 * 8 * 2;  // [warp][G][D] f32
     static constexpr int kML = kAcc + kDecWarps * G * D * 4;  // [warp][G][2] f32
     static constexpr int kBar = kML + kDecWarps * G * 2 * 4;  // full[st], empty[st]
-    static constexpr int kAbort = kBar + 2 * kDecStages * 8;
+    static constexpr int kAbort = kBar + 2 * ST * 8;
     static constexpr int kBytes = kAbort + 16;
     static constexpr int kAlloc = kBytes + 1024;              // align the base to 1024
 };
@@ -188,10 +191,11 @@ __device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p) 
 // Persistent: each CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...;
 // the producer streams their chunks back to back, so the latency of the
 // first loads is paid once per CTA rather than once per item.
-template <int D, int G>
+template <int D, int G, int ST>
 __global__ void __launch_bounds__(kDecThreads)
     swa_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
-    using SL = DecSmem<D, G>;
+    using SL = DecSmem<D, G, ST>;
+    constexpr int kDecStages = ST;
     constexpr int KS = D / 16;  // k-steps of S, d-tiles of O
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -520,15 +524,16 @@ bool encode_cache_map(CUtensorMap *m, const void *ptr, int d, uint64_t rows) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G>
+template <int D, int G, int ST>
 swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStream_t stream) {
-    using SL = DecSmem<D, G>;
+    using SL = DecSmem<D, G, ST>;
+    static_assert(kDecCtasPerSm[ST - 1] * (SL::kAlloc + 1024) <= 233472, "CTAs per SM must fit");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(swa_decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(swa_decode_kernel<D, G, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SL::kAlloc);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode)");
         configured[dev] = true;
@@ -536,9 +541,9 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStre
     const int sms = device_sm_count();
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
-    const long long cap_ctas = static_cast<long long>(SWA_DEC_CTAS_PER_SM) * sms;
+    const long long cap_ctas = static_cast<long long>(kDecCtasPerSm[ST - 1]) * sms;
     const int grid = static_cast<int>(items < cap_ctas ? items : cap_ctas);
-    e = launch_pdl(swa_decode_kernel<D, G>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
+    e = launch_pdl(swa_decode_kernel<D, G, ST>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
                    maps, p);
     if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_kernel");
     if (p.splits > 1) {
@@ -575,20 +580,24 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
     if (!encode_cache_map(&maps.k, c.k, c.d, rows) || !encode_cache_map(&maps.v, c.v, c.d, rows))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(cache)");
     const int G = Hq / c.Hkv;
+    // items of one chunk (at most 64 slots per split): one ring stage
+    const long long cap_eff = c.w < 0 ? c.cap : c.w;
+    const long long chunks = (cap_eff + kDecCH - 1) / kDecCH;
+    const bool single = (chunks + plan.splits - 1) / plan.splits <= 1;
     if (c.d == 128) {
         switch (G) {
-            case 1: return launch_decode<128, 1>(maps, p, stream);
-            case 2: return launch_decode<128, 2>(maps, p, stream);
-            case 4: return launch_decode<128, 4>(maps, p, stream);
-            case 8: return launch_decode<128, 8>(maps, p, stream);
+            case 1: return single ? launch_decode<128, 1, 1>(maps, p, stream) : launch_decode<128, 1, 2>(maps, p, stream);
+            case 2: return single ? launch_decode<128, 2, 1>(maps, p, stream) : launch_decode<128, 2, 2>(maps, p, stream);
+            case 4: return single ? launch_decode<128, 4, 1>(maps, p, stream) : launch_decode<128, 4, 2>(maps, p, stream);
+            case 8: return single ? launch_decode<128, 8, 1>(maps, p, stream) : launch_decode<128, 8, 2>(maps, p, stream);
             default: return SWA_ERR_UNSUPPORTED;
         }
     }
     switch (G) {
-        case 1: return launch_decode<64, 1>(maps, p, stream);
-        case 2: return launch_decode<64, 2>(maps, p, stream);
-        case 4: return launch_decode<64, 4>(maps, p, stream);
-        case 8: return launch_decode<64, 8>(maps, p, stream);
+        case 1: return single ? launch_decode<64, 1, 1>(maps, p, stream) : launch_decode<64, 1, 2>(maps, p, stream);
+        case 2: return single ? launch_decode<64, 2, 1>(maps, p, stream) : launch_decode<64, 2, 2>(maps, p, stream);
+        case 4: return single ? launch_decode<64, 4, 1>(maps, p, stream) : launch_decode<64, 4, 2>(maps, p, stream);
+        case 8: return single ? launch_decode<64, 8, 1>(maps, p, stream) : launch_decode<64, 8, 2>(maps, p, stream);
         default: return SWA_ERR_UNSUPPORTED;
     }
 }
