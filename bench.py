@@ -577,6 +577,49 @@ def suite_decode(steps: int, only_w=None, n_steps: int = 1024):
         torch.cuda.empty_cache()
 
 
+def suite_chunk(steps: int):
+    """Chunked prefill from a cache (prefill_chunk) against one prefill of the
+    whole prompt, Llama attention shape (Hq=32, Hkv=8, d=128): SWA(64,4)
+    B=1 L=4096 in chunks of 512, SWA(512,4) B=2 L=32768 in chunks of 4096,
+    and full causal B=1 L=16384 in chunks of 4096.  A step is the whole
+    prompt (all chunks, each gathering, attending and appending); L2 is
+    flushed before each step."""
+    import torch
+
+    import sliding_window_attention_prefill_gb300 as swa
+    from sliding_window_attention_prefill_gb300 import build, inputs
+    build.build()
+    pk = peaks()
+    flush = L2Flush()
+    Hq, Hkv, d = 32, 8, 128
+    for B, L, w, s, n in [(1, 4096, 64, 4, 512), (2, 32768, 512, 4, 4096), (1, 16384, -1, 0, 4096)]:
+        q, k, v = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=0)
+        q, k, v = q.cuda(), k.cuda(), v.cuda()
+        qc = [q[:, i:i + n].contiguous() for i in range(0, L, n)]
+        kc = [k[:, i:i + n].contiguous() for i in range(0, L, n)]
+        vc = [v[:, i:i + n].contiguous() for i in range(0, L, n)]
+        oc = [torch.empty_like(x) for x in qc]
+        cache = swa.Cache(B, Hkv, d, w, s, max_len=(L if w < 0 else None))
+        o = torch.empty_like(q)
+
+        def chunked():
+            for j in range(len(qc)):
+                swa.prefill_chunk(qc[j], kc[j], vc[j], cache, j * n, out=oc[j])
+
+        ms_chunk = _time_graph(chunked, steps, flush)
+        ms_full = _time_graph(lambda: swa.prefill(q, k, v, w, s, out=o), steps, flush)
+        fl = prefill_flops(B, L, Hq, d, w)
+        print(json.dumps({"suite": "chunk", "B": B, "L": L, "w": w if w > 0 else "inf", "s": s,
+                          "chunk": n, "ms_chunked": ms_chunk, "ms_whole": ms_full,
+                          "tflops_chunked": fl / (ms_chunk * 1e-3) / 1e12,
+                          "tok_s_chunked": B * L / (ms_chunk * 1e-3),
+                          "overhead": ms_chunk / ms_full - 1.0,
+                          "frac_tensor_peak_chunked": fl / (ms_chunk * 1e-3) / 1e12 / pk["bf16_tflops"],
+                          "l2": L2_NOTE}), flush=True)
+        del q, k, v, qc, kc, vc, oc, cache, o
+        torch.cuda.empty_cache()
+
+
 CONTEXT_POSITIONS = [1 << e for e in range(7, 19)]  # 128 .. 262144
 CONTEXT_WINDOWS = [64, 128, 256, 512, -1]
 CONTEXT_LAYERS = 4
@@ -672,7 +715,7 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["swa", "reference"], default="swa")
-    ap.add_argument("--suite", choices=["prefill", "decode", "context"], default=None,
+    ap.add_argument("--suite", choices=["prefill", "decode", "context", "chunk"], default=None,
                     help="auxiliary per-config lines instead of the headline step")
     ap.add_argument("--w", type=int, default=None, help="prefill suite: only this window")
     ap.add_argument("--B", type=int, default=None, help="prefill suite: batch override")
@@ -685,6 +728,9 @@ def main():
         return
     if args.suite == "decode":
         suite_decode(max(args.steps // 4, 20), args.w, args.decode_steps)
+        return
+    if args.suite == "chunk":
+        suite_chunk(max(args.steps // 20, 10))
         return
     if args.suite == "context":
         suite_context(max(min(args.steps // 40, 20), 5),

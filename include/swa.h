@@ -204,6 +204,42 @@ const char *swa_status_string(swa_status status);
 swa_status swa_get_device_error(swa_stream_t stream);
 
 /*
+ * swa_prefill_chunk -- prefill one chunk of a prompt that continues from a
+ * cache, then append the chunk to it.  Positions pos0 .. pos0+n-1 attend to
+ * what the cache holds of positions < pos0 (the s sinks and the latest w-s,
+ * or every position for w = SWA_W_INF) and to the chunk itself, which is
+ * exactly their attended set A(t): prefilling a prompt chunk by chunk with
+ * this call gives the outputs of one swa_prefill of the whole prompt, with
+ * memory bounded by the cache for a finite window.  The cache then also
+ * holds the chunk (as swa_cache_append would leave it).
+ *
+ *   q        [B, n, Hq, d] bf16, positions pos0 .. pos0+n-1
+ *   k_new, v_new  [B, n, Hkv, d] bf16, the same positions (position-encoded)
+ *   o        [B, n, Hq, d] bf16 output; lse optional fp32 [B, Hq, n]
+ *   cache    holds positions 0 .. pos0-1 exactly as appends left them; its
+ *            w and s are the window's (w = SWA_W_INF: pos0 + n <= cap)
+ *   workspace  device scratch of swa_prefill_chunk_workspace_bytes(...)
+ *            bytes, 16-byte aligned, caller-owned, contents undefined
+ *            between calls; 0 bytes (may be NULL) for w = SWA_W_INF, which
+ *            reads K and V from the cache in place
+ *
+ * Enqueues on `stream`, in order, a gather of the attended keys into the
+ * workspace (finite window only), the prefill, and the append; the cache must
+ * not be used by other work until they complete.  Returns the swa_prefill /
+ * swa_cache_append codes; SWA_ERR_WORKSPACE when the workspace is missing or
+ * short.
+ *
+ * Source: the window equation of "Sliding-window beats linear attention"
+ * (paper summary page), section "Prerequisites / Sliding-window attention
+ * SWA(w, s)"; the fixed cache and its eviction rule: blog page "Microsoft SWA
+ * paper overturns linear attention", section "What they tested".
+ */
+size_t swa_prefill_chunk_workspace_bytes(int B, int n, int Hkv, int d, int w, int64_t pos0);
+swa_status swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *o,
+                             float *lse, const swa_cache *cache, int n, int64_t pos0, int Hq,
+                             void *workspace, size_t workspace_bytes, swa_stream_t stream);
+
+/*
  * swa_selftest_wait_timeout -- enqueue a one-CTA kernel whose bounded wait
  * runs out on purpose: it waits on an mbarrier that nothing arrives on,
  * through the same bounded wait as every kernel of the library, holding a
@@ -226,6 +262,11 @@ swa_status swa_check_append(const swa_cache *cache, const void *k_new, const voi
 swa_status swa_check_decode(const void *q, const swa_cache *cache, const int32_t *pos, int Hq,
                             int w, int s, const void *o, const void *workspace,
                             size_t workspace_bytes, size_t required_bytes);
+
+swa_status swa_check_prefill_chunk(const void *q, const void *k_new, const void *v_new,
+                                   const void *o, const float *lse, const swa_cache *cache, int n,
+                                   int64_t pos0, int Hq, const void *workspace,
+                                   size_t workspace_bytes);
 
 /* Slot of position p in a cache of window w with s sinks (host helper; -1 if invalid). */
 int64_t swa_cache_slot(int64_t p, int w, int s);

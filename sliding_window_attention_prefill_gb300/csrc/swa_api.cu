@@ -93,6 +93,14 @@ bool decode_group_supported(int d, int G) {
 
 cudaStream_t as_cuda(swa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Chunked prefill: the chunk's queries sit at key position q_off + i of the
+// attended key sequence -- pos0 itself when the cache has not wrapped (and
+// always for an infinite window), else w (s sinks + w-s ring slots).
+int64_t chunk_q_off(int w, int64_t pos0) {
+    if (w == SWA_W_INF) return pos0;
+    return pos0 < w ? pos0 : w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -197,6 +205,90 @@ swa_status swa_check_decode(const void *q, const swa_cache *cache, const int32_t
                                overlap(workspace, required_bytes, cache->v, cb)))
         return SWA_ERR_INVALID_ARG;
     return SWA_OK;
+}
+
+size_t swa_prefill_chunk_workspace_bytes(int B, int n, int Hkv, int d, int w, int64_t pos0) {
+    if (B <= 0 || n <= 0 || Hkv < 1 || (d != 64 && d != 128) || pos0 < 0) return 0;
+    if (w == SWA_W_INF) return 0;
+    const int64_t Lk = chunk_q_off(w, pos0) + n;
+    return static_cast<size_t>(2) * B * Lk * Hkv * d * 2;
+}
+
+swa_status swa_check_prefill_chunk(const void *q, const void *k_new, const void *v_new,
+                                   const void *o, const float *lse, const swa_cache *cache, int n,
+                                   int64_t pos0, int Hq, const void *workspace,
+                                   size_t workspace_bytes) {
+    const swa_status cs = check_cache(cache);
+    if (cs != SWA_OK) return cs;
+    if (n < 0 || pos0 < 0 || Hq < 1 || Hq % cache->Hkv != 0) return SWA_ERR_INVALID_ARG;
+    const int G = Hq / cache->Hkv;
+    if (!pow2(G) || G > 128) return SWA_ERR_UNSUPPORTED;
+    if (cache->w == SWA_W_INF && pos0 + n > cache->cap) return SWA_ERR_INVALID_ARG;
+    const int64_t Lk = chunk_q_off(cache->w, pos0) + n;
+    if (Lk >= (int64_t(1) << 31)) return SWA_ERR_UNSUPPORTED;
+    if (n == 0 || cache->B == 0) return SWA_OK;
+    const int B = cache->B, Hkv = cache->Hkv, d = cache->d;
+    // tensor-map limit: strides below 2^40 bytes
+    if (static_cast<uint64_t>(n) * Hq * d * 2 >= (1ull << 40) ||
+        static_cast<uint64_t>(Lk) * Hkv * d * 2 >= (1ull << 40) ||
+        static_cast<uint64_t>(cache->cap) * Hkv * d * 2 >= (1ull << 40))
+        return SWA_ERR_UNSUPPORTED;
+    if (!q || !k_new || !v_new || !o) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(o))
+        return SWA_ERR_ALIGNMENT;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SWA_ERR_ALIGNMENT;
+    const size_t need = swa_prefill_chunk_workspace_bytes(B, n, Hkv, d, cache->w, pos0);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SWA_ERR_ALIGNMENT;
+    }
+    const size_t qb = static_cast<size_t>(B) * n * Hq * d * 2;
+    const size_t kb = static_cast<size_t>(B) * n * Hkv * d * 2;
+    const size_t cb = static_cast<size_t>(B) * Hkv * cache->cap * d * 2;
+    const size_t lb = lse ? static_cast<size_t>(B) * Hq * n * 4 : 0;
+    const void *outs[2] = {o, lse};
+    const size_t outb[2] = {qb, lb};
+    for (int i = 0; i < 2; ++i) {
+        if (overlap(outs[i], outb[i], q, qb) || overlap(outs[i], outb[i], k_new, kb) ||
+            overlap(outs[i], outb[i], v_new, kb) || overlap(outs[i], outb[i], cache->k, cb) ||
+            overlap(outs[i], outb[i], cache->v, cb) || overlap(outs[i], outb[i], workspace, need))
+            return SWA_ERR_INVALID_ARG;
+    }
+    if (overlap(o, qb, lse, lb)) return SWA_ERR_INVALID_ARG;
+    if (overlap(k_new, kb, cache->k, cb) || overlap(k_new, kb, cache->v, cb) ||
+        overlap(v_new, kb, cache->k, cb) || overlap(v_new, kb, cache->v, cb))
+        return SWA_ERR_INVALID_ARG;
+    if (need > 0 && (overlap(workspace, need, q, qb) || overlap(workspace, need, k_new, kb) ||
+                     overlap(workspace, need, v_new, kb) || overlap(workspace, need, cache->k, cb) ||
+                     overlap(workspace, need, cache->v, cb)))
+        return SWA_ERR_INVALID_ARG;
+    return SWA_OK;
+}
+
+swa_status swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *o,
+                             float *lse, const swa_cache *cache, int n, int64_t pos0, int Hq,
+                             void *workspace, size_t workspace_bytes, swa_stream_t stream) {
+    const swa_status st = swa_check_prefill_chunk(q, k_new, v_new, o, lse, cache, n, pos0, Hq,
+                                                  workspace, workspace_bytes);
+    if (st != SWA_OK || n == 0 || cache->B == 0) return st;
+    const swa_cache &c = *cache;
+    const cudaStream_t cs = as_cuda(stream);
+    const int q_off = static_cast<int>(chunk_q_off(c.w, pos0));
+    if (c.w == SWA_W_INF) {
+        // nothing is evicted: append first, then read K and V in place
+        swa_status r = swa::append_launch(c, k_new, v_new, n, pos0, cs);
+        if (r != SWA_OK) return r;
+        return swa::prefill_launch_offset(q, c.k, c.v, o, lse, c.B, n, Hq, c.Hkv, c.d, c.w, 0,
+                                          q_off, q_off + n, c.cap, cs);
+    }
+    void *wk = workspace;
+    void *wv = static_cast<char *>(workspace) + static_cast<size_t>(c.B) * (q_off + n) * c.Hkv * c.d * 2;
+    swa_status r = swa::chunk_gather_launch(c, k_new, v_new, n, pos0, q_off, wk, wv, cs);
+    if (r != SWA_OK) return r;
+    r = swa::prefill_launch_offset(q, wk, wv, o, lse, c.B, n, Hq, c.Hkv, c.d, c.w, c.s, q_off,
+                                   q_off + n, 0, cs);
+    if (r != SWA_OK) return r;
+    return swa::append_launch(c, k_new, v_new, n, pos0, cs);
 }
 
 swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,

@@ -101,4 +101,84 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_append_kernel");
 }
 
+// ---------------------------------------------------------------------------
+// chunked prefill: the keys a chunk of queries attends to, in one sequence
+// ---------------------------------------------------------------------------
+// A chunk of positions pos0 .. pos0+n-1 of a finite window attends to the
+// sinks and the latest w-s positions before it (what the cache holds) and to
+// itself.  Row j < q_off of the gathered sequence is cache position
+//   j                              if the cache has not wrapped (pos0 <= w)
+//   j (sink) or pos0-(w-s)+(j-s)   otherwise (q_off = w)
+// read from its slot; row q_off + i is chunk row i.  In these coordinates a
+// query at chunk row i sits at position q_off + i and attends to exactly the
+// SWA(w,s) set of that position, so the ordinary prefill runs on them.
+struct GatherParams {
+    const uint4 *ck, *cv;        // cache [B, Hkv, cap, d]
+    const uint4 *k_new, *v_new;  // chunk [B, n, Hkv, d]
+    uint4 *wk, *wv;              // gathered [B, q_off + n, Hkv, d]
+    int64_t pos0;
+    int B, n, Hkv, vpr, vpr_log2, cap, w, s, q_off;
+};
+
+__global__ void __launch_bounds__(kAppendThreads) swa_chunk_gather_kernel(const GatherParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int per_pos = p.Hkv * p.vpr;  // vectors of one row (all kv heads)
+    const int t = blockIdx.x * kAppendThreads + threadIdx.x;
+    if (t >= per_pos) return;
+    const int h = t >> p.vpr_log2;
+    const int vec = t & (p.vpr - 1);
+    const int Lk = p.q_off + p.n;
+    for (int b = blockIdx.z; b < p.B; b += gridDim.z) {
+        for (int j = blockIdx.y; j < Lk; j += gridDim.y) {
+            uint4 kv, vv;
+            if (j < p.q_off) {
+                int64_t pos = j;
+                if (p.pos0 > p.w && j >= p.s) pos = p.pos0 - (p.w - p.s) + (j - p.s);
+                const int64_t slot = pos < p.s ? pos : p.s + (pos - p.s) % (p.w - p.s);
+                const int64_t src = ((static_cast<int64_t>(b) * p.Hkv + h) * p.cap + slot) * p.vpr + vec;
+                kv = p.ck[src];
+                vv = p.cv[src];
+            } else {
+                const int64_t src = (static_cast<int64_t>(b) * p.n + (j - p.q_off)) * per_pos + t;
+                kv = p.k_new[src];
+                vv = p.v_new[src];
+            }
+            const int64_t dst = (static_cast<int64_t>(b) * Lk + j) * per_pos + t;
+            p.wk[dst] = kv;
+            p.wv[dst] = vv;
+        }
+    }
+}
+
+swa_status chunk_gather_launch(const swa_cache &c, const void *k_new, const void *v_new, int n,
+                               int64_t pos0, int q_off, void *wk, void *wv, cudaStream_t stream) {
+    GatherParams p{};
+    p.ck = static_cast<const uint4 *>(c.k);
+    p.cv = static_cast<const uint4 *>(c.v);
+    p.k_new = static_cast<const uint4 *>(k_new);
+    p.v_new = static_cast<const uint4 *>(v_new);
+    p.wk = static_cast<uint4 *>(wk);
+    p.wv = static_cast<uint4 *>(wv);
+    p.pos0 = pos0;
+    p.B = c.B;
+    p.n = n;
+    p.Hkv = c.Hkv;
+    p.vpr = c.d / 8;
+    p.vpr_log2 = p.vpr == 16 ? 4 : 3;
+    p.cap = c.cap;
+    p.w = c.w;
+    p.s = c.s;
+    p.q_off = q_off;
+    const int Lk = q_off + n;
+    if (Lk == 0 || c.B == 0) return SWA_OK;
+    const int per_pos = p.Hkv * p.vpr;
+    const dim3 grid((per_pos + kAppendThreads - 1) / kAppendThreads,
+                    static_cast<unsigned>(Lk < 65535 ? Lk : 65535),
+                    static_cast<unsigned>(c.B < 65535 ? c.B : 65535));
+    const cudaError_t e =
+        launch_pdl(swa_chunk_gather_kernel, grid, dim3(kAppendThreads), 0, stream, p);
+    return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_chunk_gather_kernel");
+}
+
 }  // namespace swa

@@ -36,6 +36,17 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int d, int cap, int w, int sm_cou
 // Launchers (arguments already validated).
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                           int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream);
+// Prefill of L query rows that sit at key positions q_off .. q_off+L-1 of a
+// key sequence of Lk rows: K/V in [B, Lk, Hkv, d], or in a cache's
+// [B, Hkv, kv_cap, d] layout when kv_cap > 0.
+swa_status prefill_launch_offset(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 int B, int L, int Hq, int Hkv, int d, int w, int s, int q_off,
+                                 int Lk, int kv_cap, cudaStream_t stream);
+// Chunked prefill of a finite window: the key rows the chunk's queries need,
+// in one sequence [B, q_off + n, Hkv, d] per tensor -- the cache's sinks and
+// ring in position order, then the chunk.
+swa_status chunk_gather_launch(const swa_cache &c, const void *k_new, const void *v_new, int n,
+                               int64_t pos0, int q_off, void *wk, void *wv, cudaStream_t stream);
 swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_new, int n,
                          int64_t pos0, cudaStream_t stream);
 swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,

@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int db = 0; db < D / 64; ++db)
                         tma_load_4d(base + SL::kQ + qb * SL::kQTile + db * SL::kQRegion, &maps.q,
-                                    bar(SL::kQFull + qb), db * 64, x.kvh * p.G, x.t0, x.b);
+                                    bar(SL::kQFull + qb), db * 64, x.kvh * p.G, x.t0 - p.q_off,
+                                    x.b);
                 }
                 for (int j = 0; j < x.n_tiles; ++j, ++g) {
                     const uint32_t slot = g % ns;
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int db = 0; db < D / 64; ++db)
                         tma_store_4d(&maps.o, base + SL::kStageO + db * (128 * 128), db * 64,
-                                     x.kvh * p.G, x.t0, x.b);
+                                     x.kvh * p.G, x.t0 - p.q_off, x.b);
                     tma_store_commit();
                     tma_store_wait_read_all();
                 }
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ep;
                 if (p.lse != nullptr && ok && pend_valid && half == 0) {
                     const int h = pend_kvh * p.G + hrow;
-                    p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + pend_t] =
+                    p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_t - p.q_off)] =
                         pend_m * p.scale + logf(l_tot);
                 }
                 return;
@@ -419,13 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tv = pend_t0 + (rr >> p.g_log2);
                 if (ok && tv <= pend_t1)
                     *reinterpret_cast<uint4 *>(
-                        p.o + ((static_cast<int64_t>(pend_b) * p.L + tv) * p.Hq + pend_kvh * p.G +
+                        p.o + ((static_cast<int64_t>(pend_b) * p.L + (tv - p.q_off)) * p.Hq + pend_kvh * p.G +
                                (rr & (p.G - 1))) * D +
                         half * (D / 2) + cpos * 8) = ch[v];
             }
             if (p.lse != nullptr && ok && pend_valid && half == 0) {
                 const int h = pend_kvh * p.G + hrow;
-                p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + pend_t] =
+                p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_t - p.q_off)] =
                     pend_m * p.scale + logf(l_tot);
             }
         };
@@ -673,25 +674,31 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
 int prefill_key_tile(const PrefillParams &p, int d) {
     if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT;
     const long long cols =
-        p.w < 0 ? static_cast<long long>(p.L) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
+        p.w < 0 ? static_cast<long long>(p.Lk) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
     if (cols > 768) return 256;
     return d == 128 ? 112 : 128;
 }
 
-swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                          int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream) {
-    const PrefillParams p = make_prefill_params(o, lse, B, L, Hq, Hkv, d, w, s);
+swa_status prefill_launch_offset(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 int B, int L, int Hq, int Hkv, int d, int w, int s, int q_off,
+                                 int Lk, int kv_cap, cudaStream_t stream) {
+    const PrefillParams p = make_prefill_params(o, lse, B, L, Hq, Hkv, d, w, s, q_off, Lk);
     // the widths that have a kernel: 112 or 256 at d = 128, 128 or 256 at d = 64
     int kt = prefill_key_tile(p, d);
     if (kt != 256) kt = (d == 128) ? 112 : 128;
     PrefillMaps maps;
-    if (!encode_prefill_maps(&maps, q, k, v, p, d, kt))
+    if (!encode_prefill_maps(&maps, q, k, v, p, d, kt, kv_cap))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     if (d == 128)
         return kt == 256 ? launch_prefill<128, 256, 1, 1>(maps, p, stream)
                          : launch_prefill<128, 112, 2, 2>(maps, p, stream);
     return kt == 256 ? launch_prefill<64, 256, 2, 2>(maps, p, stream)
                      : launch_prefill<64, 128, 4, 4>(maps, p, stream);
+}
+
+swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                          int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream) {
+    return prefill_launch_offset(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, 0, L, 0, stream);
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {

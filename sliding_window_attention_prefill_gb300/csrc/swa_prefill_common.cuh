@@ -52,7 +52,8 @@ __device__ __forceinline__ int fast_div(int n, const FastDiv &f) {
 }
 
 struct PrefillParams {
-    int B, L, Hq, Hkv, G, P;  // P: positions per query tile (128 / G)
+    int B, L, Hq, Hkv, G, P;  // L: query rows; P: positions per query tile (128 / G)
+    int q_off, Lk;            // query row i sits at key position q_off + i; Lk key rows
     int g_log2;               // G is a power of two (row r: position r >> g_log2)
     int w, s;                 // w < 0: infinite window (s is then 0)
     int s_pad;                // sink rows loaded: s rounded up to 8 (0 if s == 0)
@@ -79,8 +80,8 @@ __device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p) {
     x.b = fast_div(r, p.div_hkv);
     x.kvh = r - x.b * p.Hkv;
     const int qt = p.n_qtiles - 1 - qt_rev;
-    x.t0 = qt * p.P;
-    x.t1 = min(x.t0 + p.P, p.L) - 1;
+    x.t0 = p.q_off + qt * p.P;                      // key-space positions
+    x.t1 = min(x.t0 + p.P, p.q_off + p.L) - 1;
     x.lo = p.w < 0 ? 0 : max(p.s, x.t0 - (p.w - p.s) + 1);
     const int nb = max(0, x.t1 - x.lo + 1);
     x.n_cols = p.s_pad + nb;
@@ -96,11 +97,15 @@ __device__ __forceinline__ int tile_width(const Unit &x, int j) {
 }
 
 // ------------------------------------------------------------------ host side
+// q_off / Lk: the queries are key positions q_off .. q_off+L-1 of a key
+// sequence of Lk rows (a plain prefill: 0 and L).
 inline PrefillParams make_prefill_params(void *o, float *lse, int B, int L, int Hq, int Hkv, int d,
-                                         int w, int s) {
+                                         int w, int s, int q_off = 0, int Lk = -1) {
     PrefillParams p{};
     p.B = B;
     p.L = L;
+    p.q_off = q_off;
+    p.Lk = Lk < 0 ? L : Lk;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
@@ -121,14 +126,21 @@ inline PrefillParams make_prefill_params(void *o, float *lse, int B, int L, int 
     return p;
 }
 
-// 4-D map over a [B, L, heads, d] bf16 tensor, 64-column boxes, 128-byte swizzle.
+// 4-D map (coordinates d, head, position, batch) over a bf16 tensor, 64-column
+// boxes, 128-byte swizzle.  Layout [B, L, heads, d] when bhsd_cap == 0, else
+// [B, heads, bhsd_cap, d] (a cache: positions 0 .. L-1 of cap slots).
 static inline bool encode_prefill_map(CUtensorMap *m, const void *ptr, int d, int heads, int L,
-                                      int B, int box_heads, int box_rows) {
+                                      int B, int box_heads, int box_rows, int bhsd_cap = 0) {
     const cuTensorMapEncodeTiled_fn enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
     cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2,
                              (cuuint64_t)L * heads * d * 2};
+    if (bhsd_cap > 0) {
+        strides[0] = (cuuint64_t)bhsd_cap * d * 2;           // head
+        strides[1] = (cuuint64_t)d * 2;                      // position
+        strides[2] = (cuuint64_t)heads * bhsd_cap * d * 2;   // batch
+    }
     cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
@@ -137,19 +149,21 @@ static inline bool encode_prefill_map(CUtensorMap *m, const void *ptr, int d, in
     return r == CUDA_SUCCESS;
 }
 
-// The maps of one call with key tiles of `kt` columns.
+// The maps of one call with key tiles of `kt` columns; K and V in the
+// [B, Lk, Hkv, d] layout, or [B, Hkv, kv_cap, d] when kv_cap > 0.
 static inline bool encode_prefill_maps(PrefillMaps *maps, const void *q, const void *k,
-                                       const void *v, const PrefillParams &p, int d, int kt) {
+                                       const void *v, const PrefillParams &p, int d, int kt,
+                                       int kv_cap = 0) {
     std::memset(maps, 0, sizeof(*maps));
     bool ok = encode_prefill_map(&maps->q, q, d, p.Hq, p.L, p.B, p.G, p.P) &&
               encode_prefill_map(&maps->o, p.o, d, p.Hq, p.L, p.B, p.G, p.P) &&
-              encode_prefill_map(&maps->k_band, k, d, p.Hkv, p.L, p.B, 1, kt) &&
-              encode_prefill_map(&maps->v_band, v, d, p.Hkv, p.L, p.B, 1, kt);
+              encode_prefill_map(&maps->k_band, k, d, p.Hkv, p.Lk, p.B, 1, kt, kv_cap) &&
+              encode_prefill_map(&maps->v_band, v, d, p.Hkv, p.Lk, p.B, 1, kt, kv_cap);
     if (ok && p.s_pad > 0)
-        ok = encode_prefill_map(&maps->k_sink, k, d, p.Hkv, p.L, p.B, 1, p.s_pad) &&
-             encode_prefill_map(&maps->v_sink, v, d, p.Hkv, p.L, p.B, 1, p.s_pad) &&
-             encode_prefill_map(&maps->k_band0, k, d, p.Hkv, p.L, p.B, 1, kt - p.s_pad) &&
-             encode_prefill_map(&maps->v_band0, v, d, p.Hkv, p.L, p.B, 1, kt - p.s_pad);
+        ok = encode_prefill_map(&maps->k_sink, k, d, p.Hkv, p.Lk, p.B, 1, p.s_pad, kv_cap) &&
+             encode_prefill_map(&maps->v_sink, v, d, p.Hkv, p.Lk, p.B, 1, p.s_pad, kv_cap) &&
+             encode_prefill_map(&maps->k_band0, k, d, p.Hkv, p.Lk, p.B, 1, kt - p.s_pad, kv_cap) &&
+             encode_prefill_map(&maps->v_band0, v, d, p.Hkv, p.Lk, p.B, 1, kt - p.s_pad, kv_cap);
     return ok;
 }
 

@@ -82,6 +82,14 @@ def _declare(L) -> None:
     L.swa_last_cuda_error.restype = ctypes.c_char_p
     L.swa_selftest_wait_timeout.argtypes = [_c_p]
     L.swa_selftest_wait_timeout.restype = _c_int
+    L.swa_prefill_chunk_workspace_bytes.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64]
+    L.swa_prefill_chunk_workspace_bytes.restype = _c_size
+    L.swa_prefill_chunk.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, P(SwaCacheStruct), _c_int, _c_i64,
+                                    _c_int, _c_p, _c_size, _c_p]
+    L.swa_prefill_chunk.restype = _c_int
+    L.swa_check_prefill_chunk.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, P(SwaCacheStruct), _c_int,
+                                          _c_i64, _c_int, _c_p, _c_size]
+    L.swa_check_prefill_chunk.restype = _c_int
 
 
 def lib():
@@ -198,6 +206,48 @@ class Cache:
         st = lib().swa_cache_append(ctypes.byref(c), _ptr(k_new), _ptr(v_new), k_new.shape[1],
                                     int(pos0), _stream(self.k.device))
         _check(st, "swa_cache_append")
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+_chunk_workspaces: dict = {}
+
+
+def prefill_chunk_workspace_bytes(B: int, n: int, Hkv: int, d: int, w: int, pos0: int) -> int:
+    return int(lib().swa_prefill_chunk_workspace_bytes(B, n, Hkv, d, int(w), int(pos0)))
+
+
+def prefill_chunk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cache: "Cache", pos0: int,
+                  out: torch.Tensor | None = None, return_lse: bool = False,
+                  workspace: torch.Tensor | None = None):
+    """Prefill positions pos0 .. pos0+n-1 of a prompt against what ``cache``
+    holds of the earlier positions, then append them to the cache.
+
+    q [B, n, Hq, d], k/v [B, n, Hkv, d] bf16 CUDA tensors; returns o [B, n, Hq, d]
+    (and lse [B, Hq, n] fp32 if ``return_lse``).  Chunk by chunk this equals
+    one prefill of the whole prompt.
+    """
+    _need(q, "q"), _need(k, "k"), _need(v, "v")
+    B, n, Hq, d = q.shape
+    if (B, d) != (cache.B, cache.d) or k.shape != (B, n, cache.Hkv, d) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, cache "
+                         f"B={cache.B} Hkv={cache.Hkv} d={cache.d}")
+    o = torch.empty_like(q) if out is None else out
+    _need(o, "out")
+    lse = torch.empty(B, Hq, n, dtype=torch.float32, device=q.device) if return_lse else None
+    nbytes = prefill_chunk_workspace_bytes(B, n, cache.Hkv, d, cache.w, pos0)
+    ws = workspace
+    if ws is None and nbytes > 0:
+        key = q.device
+        ws = _chunk_workspaces.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+            _chunk_workspaces[key] = ws
+    wbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    c = cache.struct()
+    st = lib().swa_prefill_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), ctypes.byref(c), n,
+                                 int(pos0), Hq, _ptr(ws), wbytes, _stream(q.device))
+    _check(st, "swa_prefill_chunk")
+    return (o, lse) if return_lse else o
 
 
 # ----------------------------------------------------------------------------- decode

@@ -101,6 +101,32 @@ def test_check_decode(L):
     assert c(q, ctypes.byref(cache), None, 8, 64, 4, o, None, 0, 0) == INVALID
 
 
+def test_check_prefill_chunk(L):
+    c, wb = L.swa_check_prefill_chunk, L.swa_prefill_chunk_workspace_bytes
+    q, kn, vn, o, ws = _p(7000), _p(7400), _p(7500), _p(7600), _p(20000)
+    cache = _cache(B=2, Hkv=2, d=128, cap=64, w=64, s=4)
+    # finite window: the gathered keys are the cache (min(pos0, w) rows) + the chunk
+    assert wb(2, 100, 2, 128, 64, 10) == 2 * 2 * (10 + 100) * 2 * 128 * 2
+    assert wb(2, 100, 2, 128, 64, 5000) == 2 * 2 * (64 + 100) * 2 * 128 * 2
+    assert wb(2, 100, 2, 128, INF, 5000) == 0                # read in place
+    need = wb(2, 100, 2, 128, 64, 5000)
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, 5000, 8, ws, need) == OK
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, 5000, 8, ws, need - 16) == WORKSPACE
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, 5000, 8, None, 0) == WORKSPACE
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 0, 5000, 8, None, 0) == OK     # empty chunk
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), -1, 0, 8, ws, need) == INVALID
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, -1, 8, ws, need) == INVALID
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, 5000, 7, ws, need) == INVALID  # Hq % Hkv
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, 5000, 6, ws, need) == UNSUPPORTED  # G=3
+    assert c(q, kn, vn, q, None, ctypes.byref(cache), 100, 5000, 8, ws, need) == INVALID  # o aliases q
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, 5000, 8, _p(7600), need) == INVALID
+    assert c(q, kn, vn, o, None, ctypes.byref(cache), 100, 5000, 8,
+             ctypes.c_void_p(FAKE * 20000 + 8), need) == ALIGN
+    inf = _cache(B=2, Hkv=2, d=128, cap=300, w=INF, s=0)
+    assert c(q, kn, vn, o, None, ctypes.byref(inf), 100, 200, 8, None, 0) == OK
+    assert c(q, kn, vn, o, None, ctypes.byref(inf), 100, 201, 8, None, 0) == INVALID  # past cap
+
+
 def test_slot_map_matches_oracle(L):
     orc = oracle.get()
     for w, s in [(64, 4), (512, 4), (9, 0), (5, 4), (INF, 0), (128, 64)]:
