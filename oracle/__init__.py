@@ -6,8 +6,10 @@ calls it, and this package imports nothing from the CUDA side.
 
 The arithmetic lives in ``swa_oracle.c`` (plain C, fp64, OpenMP over output
 rows); this module compiles it with gcc and wraps it with ctypes.  Inputs are
-bf16 bit patterns (``numpy.uint16``); outputs are float64.  ``W_INF`` (-1)
-stands for an infinite window (full causal attention).
+16-bit floating-point bit patterns (``numpy.uint16``), bf16 or IEEE fp16:
+torch tensors say which by their dtype, bare bit arrays are bf16 unless
+``dtype="f16"`` is passed.  Outputs are float64.  ``W_INF`` (-1) stands for
+an infinite window (full causal attention).
 
 Definition followed: "Sliding-window beats linear attention" (paper summary
 page), section "Prerequisites / Sliding-window attention SWA(w, s)": the window
@@ -27,6 +29,9 @@ SOURCE = os.path.join(_HERE, "swa_oracle.c")
 DEFAULT_LIB = os.path.join(_HERE, "_build", "liboracle_swa.so")
 
 W_INF = -1
+
+# element types (the C source's ORACLE_BF16, ORACLE_F16)
+DTYPES = {"bf16": 0, "f16": 1}
 
 _i64 = ctypes.c_int64
 _int = ctypes.c_int
@@ -51,14 +56,33 @@ def build(force: bool = False) -> str:
     return DEFAULT_LIB
 
 
-def bf16_bits(x) -> np.ndarray:
-    """bf16 bit patterns of a torch bf16 tensor (or pass a uint16 array through)."""
+def bits16(x) -> np.ndarray:
+    """Bit patterns of a torch bf16 or fp16 tensor (or pass a uint16 array through)."""
     if isinstance(x, np.ndarray):
         assert x.dtype == np.uint16
         return np.ascontiguousarray(x)
     import torch
-    assert x.dtype == torch.bfloat16
+    assert x.dtype in (torch.bfloat16, torch.float16)
     return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def bf16_bits(x) -> np.ndarray:
+    """bf16 bit patterns of a torch bf16 tensor (or pass a uint16 array through)."""
+    if not isinstance(x, np.ndarray):
+        import torch
+        assert x.dtype == torch.bfloat16
+    return bits16(x)
+
+
+def dtype_code(x, dtype: str | None = None) -> int:
+    """Element-type code of an input: ``dtype`` if given, else the tensor's
+    dtype (bare uint16 arrays are bf16)."""
+    if dtype is not None:
+        return DTYPES[dtype]
+    if isinstance(x, np.ndarray):
+        return DTYPES["bf16"]
+    import torch
+    return DTYPES["f16"] if x.dtype == torch.float16 else DTYPES["bf16"]
 
 
 def bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -82,15 +106,17 @@ class Oracle:
         L.oracle_cache_slot.restype = _i64
         L.oracle_set_threads.argtypes = [_int]
         L.oracle_get_threads.restype = _int
-        L.oracle_swa_prefill.argtypes = [_p, _p, _p, _p, _p] + [_i64] * 7 + [_p, _p, _int]
+        L.oracle_swa_prefill.argtypes = [_p, _p, _p, _p, _p] + [_i64] * 7 + [_p, _p, _int, _int]
         L.oracle_swa_prefill.restype = _int
-        L.oracle_swa_prefill_rows.argtypes = [_p, _p, _p, _p, _i64, _p, _p] + [_i64] * 7 + [_p, _p, _int]
+        L.oracle_swa_prefill_rows.argtypes = ([_p, _p, _p, _p, _i64, _p, _p] + [_i64] * 7
+                                              + [_p, _p, _int, _int])
         L.oracle_swa_prefill_rows.restype = _int
-        L.oracle_swa_decode.argtypes = [_p, _p, _p, _p, _p] + [_i64] * 7 + [_p, _p, _int]
+        L.oracle_swa_decode.argtypes = [_p, _p, _p, _p, _p] + [_i64] * 7 + [_p, _p, _int, _int]
         L.oracle_swa_decode.restype = _int
         L.oracle_cache_append.argtypes = [_p, _p, _p, _p] + [_i64] * 8
         L.oracle_cache_append.restype = _int
-        L.oracle_swa_decode_cache.argtypes = [_p, _p, _p, _p, _p] + [_i64] * 7 + [_p, _p, _int]
+        L.oracle_swa_decode_cache.argtypes = ([_p, _p, _p, _p, _p] + [_i64] * 7
+                                              + [_p, _p, _int, _int])
         L.oracle_swa_decode_cache.restype = _int
         self.lib = L
 
@@ -108,9 +134,11 @@ class Oracle:
     def threads(self, n: int | None) -> int:
         return n if n and n > 0 else max(1, int(self.lib.oracle_get_threads()))
 
-    def prefill(self, q, k, v, w: int, s: int, threads: int | None = None):
-        """All rows.  q [B,L,Hq,d], k/v [B,L,Hkv,d] bf16 bits -> (o [B,L,Hq,d], lse [B,Hq,L])."""
-        q, k, v = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+    def prefill(self, q, k, v, w: int, s: int, threads: int | None = None,
+                dtype: str | None = None):
+        """All rows.  q [B,L,Hq,d], k/v [B,L,Hkv,d] 16-bit -> (o [B,L,Hq,d], lse [B,Hq,L])."""
+        dt = dtype_code(q, dtype)
+        q, k, v = bits16(q), bits16(k), bits16(v)
         B, L, Hq, d = q.shape
         Hkv = k.shape[2]
         nt = self.threads(threads)
@@ -119,14 +147,16 @@ class Oracle:
         wi = np.empty(nt * max(L, 1), np.int64)
         ws = np.empty(nt * max(L, 1), np.float64)
         rc = self.lib.oracle_swa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                                         B, L, Hq, Hkv, d, w, s, _ptr(wi), _ptr(ws), nt)
+                                         B, L, Hq, Hkv, d, w, s, _ptr(wi), _ptr(ws), nt, dt)
         if rc != 0:
             raise ValueError("oracle_swa_prefill rejected its arguments")
         return o, lse
 
-    def prefill_rows(self, q, k, v, rows, w: int, s: int, threads: int | None = None):
+    def prefill_rows(self, q, k, v, rows, w: int, s: int, threads: int | None = None,
+                     dtype: str | None = None):
         """Selected rows: rows is an (n, 3) int array of (b, t, h) -> (o [n,d], lse [n])."""
-        q, k, v = bf16_bits(q), bf16_bits(k), bf16_bits(v)
+        dt = dtype_code(q, dtype)
+        q, k, v = bits16(q), bits16(k), bits16(v)
         B, L, Hq, d = q.shape
         Hkv = k.shape[2]
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
@@ -138,14 +168,16 @@ class Oracle:
         ws = np.empty(nt * max(L, 1), np.float64)
         rc = self.lib.oracle_swa_prefill_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(rows), n, _ptr(o),
                                               _ptr(lse), B, L, Hq, Hkv, d, w, s, _ptr(wi),
-                                              _ptr(ws), nt)
+                                              _ptr(ws), nt, dt)
         if rc != 0:
             raise ValueError("oracle_swa_prefill_rows rejected its arguments")
         return o, lse
 
-    def decode(self, q, k_hist, v_hist, pos, w: int, s: int, threads: int | None = None):
+    def decode(self, q, k_hist, v_hist, pos, w: int, s: int, threads: int | None = None,
+               dtype: str | None = None):
         """q [B,Hq,d] at positions pos [B] over history k/v [B,P,Hkv,d] -> o [B,Hq,d]."""
-        q, k_hist, v_hist = bf16_bits(q), bf16_bits(k_hist), bf16_bits(v_hist)
+        dt = dtype_code(q, dtype)
+        q, k_hist, v_hist = bits16(q), bits16(k_hist), bits16(v_hist)
         B, Hq, d = q.shape
         P, Hkv = k_hist.shape[1], k_hist.shape[2]
         pos = np.ascontiguousarray(np.asarray(pos, dtype=np.int64).reshape(B))
@@ -154,7 +186,7 @@ class Oracle:
         wi = np.empty(nt * max(P, 1), np.int64)
         ws = np.empty(nt * max(P, 1), np.float64)
         rc = self.lib.oracle_swa_decode(_ptr(q), _ptr(k_hist), _ptr(v_hist), _ptr(pos), _ptr(o),
-                                        B, P, Hq, Hkv, d, w, s, _ptr(wi), _ptr(ws), nt)
+                                        B, P, Hq, Hkv, d, w, s, _ptr(wi), _ptr(ws), nt, dt)
         if rc != 0:
             raise ValueError("oracle_swa_decode rejected its arguments")
         return o
@@ -162,8 +194,9 @@ class Oracle:
     # -- cache --------------------------------------------------------------------
     def cache_append(self, cache_k: np.ndarray, cache_v: np.ndarray, k_new, v_new,
                      pos0: int, w: int, s: int) -> None:
-        """In place: cache [B,Hkv,cap,d] uint16, k_new/v_new [B,n,Hkv,d] bf16 bits."""
-        k_new, v_new = bf16_bits(k_new), bf16_bits(v_new)
+        """In place: cache [B,Hkv,cap,d] uint16, k_new/v_new [B,n,Hkv,d] 16-bit patterns
+        (copied bit for bit, whatever their type)."""
+        k_new, v_new = bits16(k_new), bits16(v_new)
         assert cache_k.dtype == np.uint16 and cache_k.flags.c_contiguous
         assert cache_v.dtype == np.uint16 and cache_v.flags.c_contiguous
         B, Hkv, cap, d = cache_k.shape
@@ -173,9 +206,11 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_cache_append: a slot falls outside the cache")
 
-    def decode_cache(self, q, cache_k, cache_v, pos, w: int, s: int, threads: int | None = None):
+    def decode_cache(self, q, cache_k, cache_v, pos, w: int, s: int, threads: int | None = None,
+                     dtype: str | None = None):
         """q [B,Hq,d] over the filled slots of cache [B,Hkv,cap,d] -> o [B,Hq,d]."""
-        q, cache_k, cache_v = bf16_bits(q), bf16_bits(cache_k), bf16_bits(cache_v)
+        dt = dtype_code(q, dtype)
+        q, cache_k, cache_v = bits16(q), bits16(cache_k), bits16(cache_v)
         B, Hq, d = q.shape
         Hkv, cap = cache_k.shape[1], cache_k.shape[2]
         pos = np.ascontiguousarray(np.asarray(pos, dtype=np.int64).reshape(B))
@@ -185,7 +220,7 @@ class Oracle:
         ws = np.empty(nt * max(cap, 1), np.float64)
         rc = self.lib.oracle_swa_decode_cache(_ptr(q), _ptr(cache_k), _ptr(cache_v), _ptr(pos),
                                               _ptr(o), B, Hq, Hkv, d, cap, w, s, _ptr(wi),
-                                              _ptr(ws), nt)
+                                              _ptr(ws), nt, dt)
         if rc != 0:
             raise ValueError("oracle_swa_decode_cache rejected its arguments")
         return o

@@ -4,7 +4,7 @@
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call
  * this file: only the test suite, the smoke check and the benchmark's CPU
  * baseline leg use it.  It shares no code, header, table or helper with the
- * CUDA library; both sides only see the same seeded bf16 inputs.
+ * CUDA library; both sides only see the same seeded 16-bit inputs.
  *
  * What it computes (the plain definition, fp64 throughout):
  *
@@ -37,7 +37,11 @@
  *     otherwise (for w = infinity, slot = p); appending writes positions in
  *     increasing order, so a later position overwrites an earlier one in the
  *     same slot;
- *   - inputs are bf16 bit patterns, widened exactly to fp64.
+ *   - inputs are 16-bit floating-point bit patterns, bf16 or IEEE binary16
+ *     (fp16, the precision of the pages' own system measurements: paper
+ *     summary page, section "Method steps", step five), widened exactly to
+ *     fp64; every entry point takes the element type as its last argument
+ *     (ORACLE_BF16 or ORACLE_F16).
  *
  * Softmax is the usual two-pass, max-subtracted form, which equals the
  * equation above in exact arithmetic.
@@ -49,13 +53,46 @@
 #include <omp.h>
 #endif
 
-/* Exact widening of a bf16 bit pattern to double. */
+/* Element types of the 16-bit inputs. */
+#define ORACLE_BF16 0
+#define ORACLE_F16 1
+
+typedef double (*widen_fn)(uint16_t bits);
+
+/* Exact widening of a bf16 bit pattern to double: bf16 is the upper half of
+ * an IEEE binary32. */
 static double bf16_bits_to_double(uint16_t bits)
 {
     uint32_t u = ((uint32_t)bits) << 16;
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* Exact widening of an IEEE binary16 bit pattern to double: 1 sign bit, a
+ * 5-bit exponent with bias 15 and a 10-bit fraction.  Exponent 0 holds zero
+ * and the subnormals (fraction x 2^-24); exponent 31 holds the infinities
+ * (fraction 0) and NaN. */
+static double f16_bits_to_double(uint16_t bits)
+{
+    int negative = (bits >> 15) & 1;
+    int e = (bits >> 10) & 31;
+    int f = bits & 1023;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -24);
+    else if (e == 31)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + f), e - 25);   /* (1 + f/1024) 2^(e-15) */
+    return negative ? -mag : mag;
+}
+
+static widen_fn widen_for(int dtype)
+{
+    if (dtype == ORACLE_BF16) return bf16_bits_to_double;
+    if (dtype == ORACLE_F16) return f16_bits_to_double;
+    return 0;
 }
 
 void oracle_set_threads(int n)
@@ -93,14 +130,14 @@ int oracle_in_window(int64_t t, int64_t i, int64_t w, int64_t s)
  */
 static double attend_list(const uint16_t *q, const uint16_t *keys, const uint16_t *vals,
                           const int64_t *idx, int64_t n, int64_t row_stride, int d,
-                          double *score, double *out)
+                          widen_fn widen, double *score, double *out)
 {
     const double scale = 1.0 / sqrt((double)d);
     double m = -INFINITY;
     for (int64_t r = 0; r < n; ++r) {
         const uint16_t *k = keys + idx[r] * row_stride;
         double dot = 0.0;
-        for (int c = 0; c < d; ++c) dot += bf16_bits_to_double(q[c]) * bf16_bits_to_double(k[c]);
+        for (int c = 0; c < d; ++c) dot += widen(q[c]) * widen(k[c]);
         score[r] = dot * scale;
         if (score[r] > m) m = score[r];
     }
@@ -110,7 +147,7 @@ static double attend_list(const uint16_t *q, const uint16_t *keys, const uint16_
         const uint16_t *v = vals + idx[r] * row_stride;
         double p = exp(score[r] - m);
         den += p;
-        for (int c = 0; c < d; ++c) out[c] += p * bf16_bits_to_double(v[c]);
+        for (int c = 0; c < d; ++c) out[c] += p * widen(v[c]);
     }
     for (int c = 0; c < d; ++c) out[c] /= den;
     return m + log(den);
@@ -135,13 +172,13 @@ static int64_t window_indices(int64_t t, int64_t w, int64_t s, int64_t *idx)
 }
 
 /*
- * One output row (b, t, h) of prefill.  q, k, v: bf16 bits, q [B,L,Hq,d],
+ * One output row (b, t, h) of prefill.  q, k, v: 16-bit patterns, q [B,L,Hq,d],
  * k and v [B,L,Hkv,d].  o_row: d doubles.  Returns the row's log-sum-exp.
  * scratch_idx / scratch_score: room for L entries each.
  */
 static double prefill_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                           int64_t b, int64_t t, int64_t h, int64_t L, int64_t Hq,
-                          int64_t Hkv, int d, int64_t w, int64_t s,
+                          int64_t Hkv, int d, int64_t w, int64_t s, widen_fn widen,
                           int64_t *scratch_idx, double *scratch_score, double *o_row)
 {
     int64_t G = Hq / Hkv;
@@ -150,20 +187,23 @@ static double prefill_row(const uint16_t *q, const uint16_t *k, const uint16_t *
     const uint16_t *qrow = q + ((b * L + t) * Hq + h) * d;
     const uint16_t *kbase = k + (b * L * Hkv + kvh) * d;   /* position 0 of (b, kvh) */
     const uint16_t *vbase = v + (b * L * Hkv + kvh) * d;
-    return attend_list(qrow, kbase, vbase, scratch_idx, n, Hkv * d, d, scratch_score, o_row);
+    return attend_list(qrow, kbase, vbase, scratch_idx, n, Hkv * d, d, widen, scratch_score,
+                       o_row);
 }
 
 /*
  * Full prefill: o [B,L,Hq,d] (double), lse [B,Hq,L] (double, may be NULL).
  * Work buffers: work_idx holds nthreads*L int64, work_score nthreads*L
- * doubles; nthreads >= 1 is the number of OpenMP threads used.
+ * doubles; nthreads >= 1 is the number of OpenMP threads used; dtype is
+ * ORACLE_BF16 or ORACLE_F16.
  */
 int oracle_swa_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                        double *o, double *lse, int64_t B, int64_t L, int64_t Hq,
                        int64_t Hkv, int64_t d, int64_t w, int64_t s,
-                       int64_t *work_idx, double *work_score, int nthreads)
+                       int64_t *work_idx, double *work_score, int nthreads, int dtype)
 {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    widen_fn widen = widen_for(dtype);
+    if (!widen || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
     if (w >= 0 && w <= s) return -1;
     int64_t rows = B * L * Hq;
 #pragma omp parallel for schedule(dynamic, 16) num_threads(nthreads)
@@ -176,7 +216,7 @@ int oracle_swa_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         int64_t h = r % Hq;
         int64_t t = (r / Hq) % L;
         int64_t b = r / (Hq * L);
-        double ls = prefill_row(q, k, v, b, t, h, L, Hq, Hkv, (int)d, w, s,
+        double ls = prefill_row(q, k, v, b, t, h, L, Hq, Hkv, (int)d, w, s, widen,
                                 work_idx + (int64_t)tid * L, work_score + (int64_t)tid * L,
                                 o + r * d);
         if (lse) lse[(b * Hq + h) * L + t] = ls;
@@ -192,9 +232,10 @@ int oracle_swa_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t
                             const int64_t *rows, int64_t n, double *o, double *lse,
                             int64_t B, int64_t L, int64_t Hq, int64_t Hkv, int64_t d,
                             int64_t w, int64_t s, int64_t *work_idx, double *work_score,
-                            int nthreads)
+                            int nthreads, int dtype)
 {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    widen_fn widen = widen_for(dtype);
+    if (!widen || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
     if (w >= 0 && w <= s) return -1;
     for (int64_t r = 0; r < n; ++r) {
         int64_t b = rows[3 * r], t = rows[3 * r + 1], h = rows[3 * r + 2];
@@ -208,7 +249,7 @@ int oracle_swa_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t
         int tid = 0;
 #endif
         double ls = prefill_row(q, k, v, rows[3 * r], rows[3 * r + 1], rows[3 * r + 2], L, Hq,
-                                Hkv, (int)d, w, s, work_idx + (int64_t)tid * L,
+                                Hkv, (int)d, w, s, widen, work_idx + (int64_t)tid * L,
                                 work_score + (int64_t)tid * L, o + r * d);
         if (lse) lse[r] = ls;
     }
@@ -223,9 +264,10 @@ int oracle_swa_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t
 int oracle_swa_decode(const uint16_t *q, const uint16_t *k_hist, const uint16_t *v_hist,
                       const int64_t *pos, double *o, int64_t B, int64_t P, int64_t Hq,
                       int64_t Hkv, int64_t d, int64_t w, int64_t s, int64_t *work_idx,
-                      double *work_score, int nthreads)
+                      double *work_score, int nthreads, int dtype)
 {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    widen_fn widen = widen_for(dtype);
+    if (!widen || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
     if (w >= 0 && w <= s) return -1;
     for (int64_t b = 0; b < B; ++b)
         if (pos[b] < 0 || pos[b] >= P) return -1;
@@ -242,7 +284,7 @@ int oracle_swa_decode(const uint16_t *q, const uint16_t *k_hist, const uint16_t 
         int64_t n = window_indices(pos[b], w, s, idx);
         const uint16_t *kbase = k_hist + (b * P * Hkv + kvh) * d;
         const uint16_t *vbase = v_hist + (b * P * Hkv + kvh) * d;
-        attend_list(q + r * d, kbase, vbase, idx, n, Hkv * d, (int)d,
+        attend_list(q + r * d, kbase, vbase, idx, n, Hkv * d, (int)d, widen,
                     work_score + (int64_t)tid * P, o + r * d);
     }
     return 0;
@@ -257,7 +299,8 @@ int64_t oracle_cache_slot(int64_t p, int64_t w, int64_t s)
 
 /*
  * Host simulation of appending positions pos0 .. pos0+n-1 to a cache.
- * cache_k, cache_v: [B,Hkv,cap,d] bf16 bits; k_new, v_new: [B,n,Hkv,d].
+ * cache_k, cache_v: [B,Hkv,cap,d] 16-bit patterns (copied, whatever their
+ * type); k_new, v_new: [B,n,Hkv,d].
  * Positions are written one after the other, so where two positions share a
  * slot the later one is what remains.  Returns -1 if a slot falls outside cap.
  */
@@ -291,9 +334,10 @@ int oracle_cache_append(uint16_t *cache_k, uint16_t *cache_v, const uint16_t *k_
 int oracle_swa_decode_cache(const uint16_t *q, const uint16_t *cache_k, const uint16_t *cache_v,
                             const int64_t *pos, double *o, int64_t B, int64_t Hq, int64_t Hkv,
                             int64_t d, int64_t cap, int64_t w, int64_t s, int64_t *work_idx,
-                            double *work_score, int nthreads)
+                            double *work_score, int nthreads, int dtype)
 {
-    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
+    widen_fn widen = widen_for(dtype);
+    if (!widen || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return -1;
     if (w >= 0 && (w <= s || w > cap)) return -1;
     int64_t G = Hq / Hkv;
     int64_t cap_eff = w < 0 ? cap : w;
@@ -312,7 +356,7 @@ int oracle_swa_decode_cache(const uint16_t *q, const uint16_t *cache_k, const ui
         for (int64_t i = 0; i < n; ++i) idx[i] = i;
         const uint16_t *kbase = cache_k + (b * Hkv + kvh) * cap * d;
         const uint16_t *vbase = cache_v + (b * Hkv + kvh) * cap * d;
-        attend_list(q + r * d, kbase, vbase, idx, n, d, (int)d,
+        attend_list(q + r * d, kbase, vbase, idx, n, d, (int)d, widen,
                     work_score + (int64_t)tid * cap, o + r * d);
     }
     return 0;

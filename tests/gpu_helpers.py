@@ -29,4 +29,6 @@ def assert_close(got, ref: np.ndarray, what: str = "", max_abs: float = MAX_ABS,
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    return oracle.bf16_bits(t.cpu())
+    """Bit patterns of a bf16 or fp16 tensor (pass dtype="f16" to the oracle
+    for fp16)."""
+    return oracle.bits16(t.cpu())

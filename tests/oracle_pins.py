@@ -12,6 +12,9 @@ What pins what:
     "the first s" and "the latest w-s" positions, in numpy;
   * a library routine: torch's scaled_dot_product_attention (fp64, causal),
     which SWA(w,s) must equal when the window covers the whole prefix;
+  * fp16 inputs: every one of the 65536 binary16 bit patterns widened by the
+    oracle equals numpy's float16 -> float64 conversion, and brute force on
+    fp16 inputs (widened by numpy) matches every attention entry point;
   * closed forms: t = 0 gives v_0; q = 0 gives the plain mean of the attended
     values; two keys in d = 1 give a two-term weighted mean;
   * invariants: equal values give that value; permuting the history inside
@@ -39,6 +42,16 @@ def _bf16(x: np.ndarray) -> np.ndarray:
 
 def _rand_bits(rng: np.random.Generator, shape) -> np.ndarray:
     return _bf16(rng.standard_normal(shape).astype(np.float32))
+
+
+def _rand_f16_bits(rng: np.random.Generator, shape) -> np.ndarray:
+    """N(0,1) rounded to IEEE binary16 by numpy, as bit patterns."""
+    return np.ascontiguousarray(rng.standard_normal(shape).astype(np.float16).view(np.uint16))
+
+
+def _f16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """numpy's own binary16 -> float64 conversion of bit patterns."""
+    return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
 
 
 def _parse_ranges(text: str) -> list[int]:
@@ -73,9 +86,9 @@ def _first_and_latest(t: int, w: int, s: int) -> list[int]:
     return sorted(set(first) | set(latest))
 
 
-def _dense_reference(q, k, v, w, s):
+def _dense_reference(q, k, v, w, s, widen=bits_to_f64):
     """Brute-force masked attention: full score matrix, -inf outside the set."""
-    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    qf, kf, vf = widen(q), widen(k), widen(v)
     B, L, Hq, d = qf.shape
     Hkv = kf.shape[2]
     G = Hq // Hkv
@@ -296,6 +309,49 @@ def pin_rows_match_full(orc) -> None:
     assert np.array_equal(rl, lse[rows[:, 0], rows[:, 2], rows[:, 1]])
 
 
+def pin_f16_every_pattern(orc) -> None:
+    """t = 0 attends only to itself, so o = v_0 exactly: with v_0 holding all
+    65536 binary16 bit patterns (q = k = 0), the oracle's fp16 widening must
+    agree with numpy's for each one (zeros, subnormals, normals, infinities,
+    NaN)."""
+    v = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).reshape(1, 1, 1, 1 << 16)
+    z = np.zeros_like(v)
+    o, _ = orc.prefill(z, z, v, W_INF, 0, threads=1, dtype="f16")
+    ref = _f16_to_f64(v)
+    assert np.array_equal(o, ref, equal_nan=True), "fp16 widening"
+    # the same bits read as bf16 give other values: the type argument is used
+    o_bf, _ = orc.prefill(z, z, v, W_INF, 0, threads=1)
+    assert not np.array_equal(o_bf, ref, equal_nan=True)
+
+
+def pin_f16_brute_force(orc) -> None:
+    """fp16 inputs through prefill, prefill_rows, decode and decode over the
+    cache, against dense masked attention on numpy-widened values."""
+    rng = np.random.default_rng(8)
+    for B, L, Hq, Hkv, d, w, s in [(1, 37, 4, 4, 16, 8, 2), (2, 30, 4, 2, 8, W_INF, 0),
+                                   (1, 41, 2, 1, 8, 12, 4)]:
+        q = _rand_f16_bits(rng, (B, L, Hq, d))
+        k = _rand_f16_bits(rng, (B, L, Hkv, d))
+        v = _rand_f16_bits(rng, (B, L, Hkv, d))
+        ref = _dense_reference(q, k, v, w, s, widen=_f16_to_f64)
+        o, _ = orc.prefill(q, k, v, w, s, threads=2, dtype="f16")
+        assert np.abs(o - ref).max() < 1e-12, ("prefill", B, L, w, s)
+        rows = np.array([[b, t, h] for b in range(B) for t in (0, 5, L - 1) for h in range(Hq)])
+        ro, _ = orc.prefill_rows(q, k, v, rows, w, s, threads=2, dtype="f16")
+        assert np.abs(ro - ref[rows[:, 0], rows[:, 1], rows[:, 2]]).max() < 1e-12
+        t = L - 1
+        qt = np.ascontiguousarray(q[:, t])
+        od = orc.decode(qt, k, v, [t] * B, w, s, threads=2, dtype="f16")
+        assert np.abs(od - ref[:, t]).max() < 1e-12, ("decode", B, L, w, s)
+        cap = L if w == W_INF else w
+        ck = np.zeros((B, Hkv, cap, d), np.uint16)
+        cv = np.zeros((B, Hkv, cap, d), np.uint16)
+        orc.cache_append(ck, cv, k, v, 0, w, s)
+        oc = orc.decode_cache(qt, ck, cv, [t] * B, w, s, threads=2, dtype="f16")
+        assert np.abs(oc - ref[:, t]).max() < 1e-12, ("decode_cache", B, L, w, s)
+
+
 ALL_PINS = [pin_golden_sets, pin_window_size, pin_brute_force, pin_causal_library,
             pin_closed_forms, pin_equal_values, pin_decode_history, pin_golden_cache,
-            pin_ring_mapping, pin_decode_cache, pin_rows_match_full]
+            pin_ring_mapping, pin_decode_cache, pin_rows_match_full, pin_f16_every_pattern,
+            pin_f16_brute_force]

@@ -36,6 +36,13 @@ MUTANTS = {
     # the query's own position left out (causal end exclusive)
     "exclusive_end": ("for (int64_t i = lo; i <= t; ++i) idx[n++] = i;",
                       "for (int64_t i = lo; i < t; ++i) idx[n++] = i;"),
+    # fp16: exponent bias off by one
+    "f16_bias": ("mag = ldexp((double)(1024 + f), e - 25);", "mag = ldexp((double)(1024 + f), e - 24);"),
+    # fp16: subnormals read as if they had the implicit leading one
+    "f16_subnormal": ("mag = ldexp((double)f, -24);", "mag = ldexp((double)(1024 + f), -24);"),
+    # fp16 inputs widened as bf16
+    "f16_as_bf16": ("if (dtype == ORACLE_F16) return f16_bits_to_double;",
+                    "if (dtype == ORACLE_F16) return bf16_bits_to_double;"),
 }
 
 CHILD = r"""
