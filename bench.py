@@ -477,8 +477,10 @@ def _time_graph(fn, steps: int, flush, warm: int = 3) -> float:
 
 def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
     """Prefill kernel alone on the prefill configs: B=1 L=4096 SWA(64,4) and
-    B=2 L=32768 SWA(w,4) for w in {128, 256, 512} (Hq=32, Hkv=8, d=128).
-    Also full causal attention (w = infinity) at B=1, L=16384.
+    B=2 L=32768 SWA(w,4) for w in {128, 256, 512} (Hq=32, Hkv=8, d=128, bf16).
+    Also full causal attention (w = infinity) at B=1, L=16384; SWA(512,4) in
+    fp16; and the pages' system-test attention shape (16 heads of 64, fp16,
+    batch 1) at L=32768 for SWA(64,4), SWA(512,4) and full causal.
     only_w / B_ / L_ restrict or resize the list (smaller cases for ncu)."""
     import torch
 
@@ -487,21 +489,27 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
     build.build()
     pk = peaks()
     flush = L2Flush()
-    cases = [(1, 4096, 64, 4), (2, 32768, 128, 0), (2, 32768, 256, 0), (2, 32768, 512, 0),
-             (1, 16384, -1, 0)]
+    llama, paper = (32, 8, 128), (16, 16, 64)
+    cases = [(1, 4096, 64, 4, llama, "bf16"), (2, 32768, 128, 0, llama, "bf16"),
+             (2, 32768, 256, 0, llama, "bf16"), (2, 32768, 512, 0, llama, "bf16"),
+             (1, 16384, -1, 0, llama, "bf16"), (2, 32768, 512, 0, llama, "f16"),
+             (1, 32768, 64, 4, paper, "f16"), (1, 32768, 512, 0, paper, "f16"),
+             (1, 32768, -1, 0, paper, "f16")]
     if only_w is not None:
         cases = [c for c in cases if c[2] == only_w]
-    cases = [(B_ or c[0], L_ or c[1], c[2], c[3]) for c in cases]
-    for B, L, w, sink_rows in cases:
-        Hq, Hkv, d, s = 32, 8, 128, 4
-        q, k, v = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=0, sink_rows=sink_rows)
+    cases = [(B_ or c[0], L_ or c[1]) + c[2:] for c in cases]
+    for B, L, w, sink_rows, (Hq, Hkv, d), dts in cases:
+        s = 4
+        dt = torch.float16 if dts == "f16" else torch.bfloat16
+        q, k, v = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=0, sink_rows=sink_rows, dtype=dt)
         q, k, v = q.cuda(), k.cuda(), v.cuda()
         o = torch.empty_like(q)
         ms = _time_graph(lambda: swa.prefill(q, k, v, w, s, out=o), steps, flush)
         fl, by = prefill_flops(B, L, Hq, d, w), prefill_bytes(B, L, Hq, Hkv, d)
         tf = fl / (ms * 1e-3) / 1e12
         attainable = min(pk["bf16_tflops"], fl / by * pk["hbm_gbs"] / 1e3)
-        print(json.dumps({"suite": "prefill", "B": B, "L": L, "w": w if w > 0 else "inf",
+        print(json.dumps({"suite": "prefill", "dtype": dts, "Hq": Hq, "Hkv": Hkv, "d": d,
+                          "B": B, "L": L, "w": w if w > 0 else "inf",
                           "s": s if w > 0 else 0, "ms": ms,
                           "tflops": tf, "frac_tensor_peak": tf / pk["bf16_tflops"],
                           "frac_attainable": tf / attainable, "attainable_tflops": attainable,
@@ -631,7 +639,16 @@ def context_cache_bytes(B, Hkv, d, cap, layers=CONTEXT_LAYERS) -> int:
     return layers * 2 * B * Hkv * cap * d * 2
 
 
-def context_points(batches=(1, 256)):
+# Attention shapes of the context sweep: the Llama-3.1-8B layer (bf16), and
+# the pages' own system-test model (paper summary page, section "Method
+# steps", step five: D = 1024, 16 heads of 64, batch 1, fp16).
+CONTEXT_SHAPES = {
+    "llama": {"Hq": 32, "Hkv": 8, "d": 128, "dtype": "bf16"},
+    "paper": {"Hq": 16, "Hkv": 16, "d": 64, "dtype": "f16"},
+}
+
+
+def context_points(batches=(1, 256), Hkv: int = 8, d: int = 128):
     """(B, w, pos) of the context sweep whose caches fit the memory budget;
     an infinite window needs pos+1 slots, a finite one w."""
     pts, skipped = [], []
@@ -639,23 +656,24 @@ def context_points(batches=(1, 256)):
         for w in CONTEXT_WINDOWS:
             for P in CONTEXT_POSITIONS:
                 cap = P + 1 if w < 0 else w
-                if context_cache_bytes(B, 8, 128, cap) > CONTEXT_MAX_CACHE_BYTES:
+                if context_cache_bytes(B, Hkv, d, cap) > CONTEXT_MAX_CACHE_BYTES:
                     skipped.append((B, w, P))
                 else:
                     pts.append((B, w, P))
     return pts, skipped
 
 
-def suite_context(steps: int, batches=(1, 256)):
-    """Decode context sweep through a stack of 4 attention layers (Hq=32,
-    Hkv=8, d=128, bf16, N(0,1)).  For each window w in {64,128,256,512} with
-    s=4, and w = infinity (full causal), batch 1 and 256, and position P from
-    128 to 262144: every layer holds a cache in the state reached after P
-    tokens (every slot a decode at P reads holds an N(0,1) value), and one
-    step appends token P and decodes it in each of the 4 layers.  Prints
-    tok/s, the decode kernel's KV read rate and the cache bytes held.
-    Points whose caches exceed 160 GiB are skipped (an infinite window at
-    batch 256 beyond 32768 positions) and listed."""
+def suite_context(steps: int, batches=(1, 256), shape: str = "llama"):
+    """Decode context sweep through a stack of 4 attention layers: the Llama
+    shape (Hq=32, Hkv=8, d=128, bf16) or the pages' system-test shape
+    (Hq=Hkv=16, d=64, fp16), N(0,1) values.  For each window w in
+    {64,128,256,512} with s=4, and w = infinity (full causal), each batch
+    size, and position P from 128 to 262144: every layer holds a cache in the
+    state reached after P tokens (every slot a decode at P reads holds an
+    N(0,1) value), and one step appends token P and decodes it in each of the
+    4 layers.  Prints tok/s, the decode kernel's KV read rate and the cache
+    bytes held.  Points whose caches exceed 160 GiB are skipped (an infinite
+    window at batch 256 beyond 32768 positions) and listed."""
     import torch
 
     import sliding_window_attention_prefill_gb300 as swa
@@ -663,19 +681,22 @@ def suite_context(steps: int, batches=(1, 256)):
     build.build()
     pk = peaks()
     flush = L2Flush()
-    Hq, Hkv, d, s = 32, 8, 128, 4
+    sh = CONTEXT_SHAPES[shape]
+    Hq, Hkv, d, s = sh["Hq"], sh["Hkv"], sh["d"], 4
+    dt = torch.float16 if sh["dtype"] == "f16" else torch.bfloat16
     gen = torch.Generator(device="cuda")
-    pts, skipped = context_points(batches)
+    pts, skipped = context_points(batches, Hkv, d)
     for B, w, P in pts:
         gen.manual_seed(B * 1000003 + P * 7 + (w + 1))
         layers = []
         for _ in range(CONTEXT_LAYERS):
-            c = swa.Cache(B, Hkv, d, w, s if w > 0 else 0, max_len=(P + 1 if w < 0 else None))
+            c = swa.Cache(B, Hkv, d, w, s if w > 0 else 0, max_len=(P + 1 if w < 0 else None),
+                          dtype=dt)
             c.k.normal_(generator=gen)
             c.v.normal_(generator=gen)
-            kn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(torch.bfloat16)
-            vn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(torch.bfloat16)
-            q = torch.randn(B, Hq, d, generator=gen, device="cuda").to(torch.bfloat16)
+            kn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(dt)
+            vn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(dt)
+            q = torch.randn(B, Hq, d, generator=gen, device="cuda").to(dt)
             layers.append((c, kn, vn, q, torch.empty_like(q), swa.workspace_for(c, Hq)))
         pos = torch.full((B,), P, dtype=torch.int32, device="cuda")
 
@@ -694,7 +715,8 @@ def suite_context(steps: int, batches=(1, 256)):
         kv = CONTEXT_LAYERS * 2 * B * Hkv * d * 2 * n_valid
         by = CONTEXT_LAYERS * decode_bytes(B, Hq, Hkv, d, n_valid)
         cap = layers[0][0].cap
-        print(json.dumps({"suite": "context", "B": B, "w": w if w > 0 else "inf",
+        print(json.dumps({"suite": "context", "shape": shape, "dtype": sh["dtype"], "Hq": Hq,
+                          "Hkv": Hkv, "d": d, "B": B, "w": w if w > 0 else "inf",
                           "s": s if w > 0 else 0, "pos": P, "layers": CONTEXT_LAYERS,
                           "ms_step": ms, "tok_s": B / (ms * 1e-3), "ms_decode": ms_dec,
                           "kv_read_gbs": kv / (ms_dec * 1e-3) / 1e9,
@@ -704,7 +726,7 @@ def suite_context(steps: int, batches=(1, 256)):
         del layers, step, decode_only
         torch.cuda.empty_cache()
     if skipped:
-        print(json.dumps({"suite": "context", "skipped": [
+        print(json.dumps({"suite": "context", "shape": shape, "skipped": [
             {"B": B, "w": "inf" if w < 0 else w, "pos": P} for B, w, P in skipped],
             "reason": "caches above 160 GiB"}), flush=True)
 
@@ -722,6 +744,9 @@ def main():
     ap.add_argument("--L", type=int, default=None, help="prefill suite: length override")
     ap.add_argument("--decode-steps", type=int, default=1024, help="decode suite: steps")
     ap.add_argument("--batches", type=str, default="1,256", help="context suite: batch sizes")
+    ap.add_argument("--shape", choices=sorted(CONTEXT_SHAPES), default="llama",
+                    help="context suite: attention shape (llama: 32/8 heads of 128, bf16; "
+                         "paper: 16 heads of 64, fp16)")
     args = ap.parse_args()
     if args.suite == "prefill":
         suite_prefill(max(args.steps // 10, 10), args.w, args.B, args.L)
@@ -734,7 +759,7 @@ def main():
         return
     if args.suite == "context":
         suite_context(max(min(args.steps // 40, 20), 5),
-                      tuple(int(b) for b in args.batches.split(",")))
+                      tuple(int(b) for b in args.batches.split(",")), args.shape)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -20,7 +20,9 @@
  * heads: query head h reads key/value head h / (Hq/Hkv).
  *
  * Conventions for every call:
- *   - tensors are bf16, dense (contiguous) in the stated layout, in device
+ *   - tensors are bf16 -- or fp16 where a call takes an element type
+ *     (swa_prefill_ex; the cache's dtype field for the calls on a cache) --,
+ *     dense (contiguous) in the stated layout, in device
  *     memory of the current device, 16-byte aligned; the caller owns them and
  *     keeps them alive until the stream work completes;
  *   - calls are asynchronous on `stream` (NULL = the legacy default stream);
@@ -58,6 +60,19 @@ typedef enum {
     SWA_ERR_BOUNDS = -7        /* a kernel skipped an out-of-range access (device word)*/
 } swa_status;
 
+/*
+ * Element type of the 16-bit tensors.  bf16 is the default; fp16 is the
+ * precision of the pages' own system measurements ("Sliding-window beats
+ * linear attention", paper summary page, section "Method steps", step five).
+ * Either way the kernels compute scores, the softmax and the output
+ * accumulator in fp32; the attention weights P enter the P.V product rounded
+ * to the element type, and the output is rounded to it (nearest even).
+ */
+typedef enum {
+    SWA_BF16 = 0,
+    SWA_F16 = 1
+} swa_dtype;
+
 /* Infinite window: full causal attention (A(t) = [0, t]); s is then ignored. */
 #define SWA_W_INF (-1)
 
@@ -88,8 +103,18 @@ swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, flo
                        swa_stream_t stream);
 
 /*
- * The fixed-size cache of one layer.  k and v are bf16 [B, Hkv, cap, d] in
- * device memory owned by the caller.  Position p lives in slot
+ * swa_prefill_ex -- swa_prefill with the element type of q, k, v and o given
+ * by `dtype` (SWA_BF16 or SWA_F16; any other value returns
+ * SWA_ERR_INVALID_ARG).  swa_prefill is swa_prefill_ex with SWA_BF16.
+ */
+swa_status swa_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int L, int Hq, int Hkv, int d, int w, int s, swa_dtype dtype,
+                          swa_stream_t stream);
+
+/*
+ * The fixed-size cache of one layer.  k and v are [B, Hkv, cap, d] of element
+ * type `dtype` (SWA_BF16 -- the value of a zero-initialised struct -- or
+ * SWA_F16) in device memory owned by the caller.  Position p lives in slot
  *     slot(p) = p                      if w == SWA_W_INF or p < s,
  *     slot(p) = s + (p - s) mod (w-s)  otherwise,
  * so cap == w for a finite window (s sink slots + a (w-s)-slot ring: the
@@ -103,12 +128,13 @@ typedef struct {
     void *k;
     void *v;
     int32_t B, Hkv, d, cap, w, s;
+    int32_t dtype; /* swa_dtype of k, v, and of q and o in the calls on this cache */
 } swa_cache;
 
 /*
  * swa_cache_append -- write the keys/values of positions pos0 .. pos0+n-1.
  *
- *   k_new, v_new [B, n, Hkv, d] bf16 (device)
+ *   k_new, v_new [B, n, Hkv, d] of the cache's element type (device)
  *
  * Each position is copied bit for bit to slot(p).  When n > w - s several
  * positions share a ring slot; only the latest one is written, so the result
@@ -130,12 +156,13 @@ size_t swa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, int w)
 /*
  * swa_decode -- one new token per sequence attends to the cache.
  *
- *   q   [B, Hq, d] bf16   the query of position pos[b] for each sequence b
+ *   q   [B, Hq, d]        the query of position pos[b] for each sequence b
+ *                          (the cache's element type, as are k, v and o)
  *   pos [B] int32 (device) position of that query; the cache must already
  *                          hold positions 0..pos[b] (append before decode, so
  *                          the token attends to itself: the window equation's
  *                          sum ends at i = t)
- *   o   [B, Hq, d] bf16   output, written
+ *   o   [B, Hq, d]        output, written
  *   workspace              device memory of at least
  *                          swa_decode_workspace_bytes(...) bytes (may be NULL
  *                          when that is 0); contents need no initialisation
@@ -213,9 +240,10 @@ swa_status swa_get_device_error(swa_stream_t stream);
  * memory bounded by the cache for a finite window.  The cache then also
  * holds the chunk (as swa_cache_append would leave it).
  *
- *   q        [B, n, Hq, d] bf16, positions pos0 .. pos0+n-1
- *   k_new, v_new  [B, n, Hkv, d] bf16, the same positions (position-encoded)
- *   o        [B, n, Hq, d] bf16 output; lse optional fp32 [B, Hq, n]
+ *   q        [B, n, Hq, d], positions pos0 .. pos0+n-1
+ *   k_new, v_new  [B, n, Hkv, d], the same positions (position-encoded)
+ *   o        [B, n, Hq, d] output; lse optional fp32 [B, Hq, n]
+ *            (q, k_new, v_new and o of the cache's element type)
  *   cache    holds positions 0 .. pos0-1 exactly as appends left them; its
  *            w and s are the window's (w = SWA_W_INF: pos0 + n <= cap)
  *   workspace  device scratch of swa_prefill_chunk_workspace_bytes(...)

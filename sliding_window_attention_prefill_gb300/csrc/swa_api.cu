@@ -70,8 +70,11 @@ swa_status check_window(int w, int s) {
     return SWA_OK;
 }
 
+bool valid_dtype(int dtype) { return dtype == SWA_BF16 || dtype == SWA_F16; }
+
 swa_status check_cache(const swa_cache *c) {
     if (c == nullptr) return SWA_ERR_INVALID_ARG;
+    if (!valid_dtype(c->dtype)) return SWA_ERR_INVALID_ARG;
     if (c->B < 0 || c->Hkv < 1 || c->cap < 1) return SWA_ERR_INVALID_ARG;
     if (c->d != 64 && c->d != 128) return c->d < 1 ? SWA_ERR_INVALID_ARG : SWA_ERR_UNSUPPORTED;
     const swa_status ws = check_window(c->w, c->s);
@@ -279,23 +282,30 @@ swa_status swa_prefill_chunk(const void *q, const void *k_new, const void *v_new
         swa_status r = swa::append_launch(c, k_new, v_new, n, pos0, cs);
         if (r != SWA_OK) return r;
         return swa::prefill_launch_offset(q, c.k, c.v, o, lse, c.B, n, Hq, c.Hkv, c.d, c.w, 0,
-                                          q_off, q_off + n, c.cap, cs);
+                                          q_off, q_off + n, c.cap, c.dtype, cs);
     }
     void *wk = workspace;
     void *wv = static_cast<char *>(workspace) + static_cast<size_t>(c.B) * (q_off + n) * c.Hkv * c.d * 2;
     swa_status r = swa::chunk_gather_launch(c, k_new, v_new, n, pos0, q_off, wk, wv, cs);
     if (r != SWA_OK) return r;
     r = swa::prefill_launch_offset(q, wk, wv, o, lse, c.B, n, Hq, c.Hkv, c.d, c.w, c.s, q_off,
-                                   q_off + n, 0, cs);
+                                   q_off + n, 0, c.dtype, cs);
     if (r != SWA_OK) return r;
     return swa::append_launch(c, k_new, v_new, n, pos0, cs);
 }
 
-swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                       int L, int Hq, int Hkv, int d, int w, int s, swa_stream_t stream) {
+swa_status swa_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int L, int Hq, int Hkv, int d, int w, int s, swa_dtype dtype,
+                          swa_stream_t stream) {
+    if (!valid_dtype(dtype)) return SWA_ERR_INVALID_ARG;
     const swa_status st = swa_check_prefill(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s);
     if (st != SWA_OK || B == 0 || L == 0) return st;
-    return swa::prefill_launch(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, as_cuda(stream));
+    return swa::prefill_launch(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, dtype, as_cuda(stream));
+}
+
+swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int L, int Hq, int Hkv, int d, int w, int s, swa_stream_t stream) {
+    return swa_prefill_ex(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, SWA_BF16, stream);
 }
 
 swa_status swa_cache_append(const swa_cache *cache, const void *k_new, const void *v_new, int n,

@@ -17,7 +17,7 @@
 // boundaries, into shared memory with 2-D TMA copies (128-byte swizzle,
 // mbarrier ring); q of the item rides along with its first chunk.  Four
 // consumer warps take 16 slots each and use the warp-level tensor-core MMA
-// (mma.sync m16n8k16, bf16 in, fp32 accumulate) for both products with the
+// (mma.sync m16n8k16, bf16 or fp16 in, fp32 accumulate) for both products with the
 // G <= 8 heads as the N = 8 dimension:
 //   S^T [16 slots x 8 heads] = K [16 x d] . Q^T [d x 8]   (K via ldmatrix)
 //   O^T [d x 8 heads]       += V^T [d x 16] . P^T [16 x 8] (V via ldmatrix.trans)
@@ -28,7 +28,6 @@
 // weighted values) and a second kernel merges them: m = max m_j,
 // l = sum l_j 2^(m_j - m), o = sum acc_j 2^(m_j - m) / l.
 #include <cuda.h>
-#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -63,7 +62,7 @@ struct DecodeMaps {
 };
 
 struct DecodeParams {
-    const uint16_t *q;   // [B, Hq, D] bf16
+    const uint16_t *q;   // [B, Hq, D] bf16 or fp16
     const int32_t *pos;  // [B]
     uint16_t *o;         // [B, Hq, D]
     float *ws_acc;       // [B*Hq, splits, D]
@@ -120,14 +119,22 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                  : "r"(addr));
 }
 
-// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+// D (16x8 fp32) += A (16x16, row) * B (16x8, col); A and B bf16 or fp16 (DT).
+template <int DT>
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                           uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    if constexpr (DT == kBf16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // Address of 16-byte chunk `cc` (of the row's d/8) of chunk row `row` in a
@@ -191,7 +198,7 @@ __device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p) 
 // Persistent: each CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...;
 // the producer streams their chunks back to back, so the latency of the
 // first loads is paid once per CTA rather than once per item.
-template <int D, int G, int ST>
+template <int D, int G, int ST, int DT>
 __global__ void __launch_bounds__(kDecThreads)
     swa_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     using SL = DecSmem<D, G, ST>;
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(kDecThreads)
                 for (int ks = 0; ks < KS; ++ks) {
                     uint32_t a[4];
                     ldsm_x4(swz(kst, slot0 + (lane & 15), 2 * ks + (lane >> 4)), a);
-                    mma_16816(s, a, qb[ks][0], qb[ks][1]);
+                    mma_16816<DT>(s, a, qb[ks][0], qb[ks][1]);
                 }
                 // ---- online softmax per head over this warp's 16 slots
                 const bool va = gq < mine, vb_ = gq + 8 < mine;
@@ -364,8 +371,8 @@ __global__ void __launch_bounds__(kDecThreads)
                 l0 += p0 + p2;
                 l1 += p1 + p3;
                 // ---- P^T through shared memory into the B-operand layout
-                *reinterpret_cast<uint32_t *>(psm + gq * 8 + 2 * tq) = pack_bf16x2(p0, p1);
-                *reinterpret_cast<uint32_t *>(psm + (gq + 8) * 8 + 2 * tq) = pack_bf16x2(p2, p3);
+                *reinterpret_cast<uint32_t *>(psm + gq * 8 + 2 * tq) = pack2<DT>(p0, p1);
+                *reinterpret_cast<uint32_t *>(psm + (gq + 8) * 8 + 2 * tq) = pack2<DT>(p2, p3);
                 __syncwarp();
                 const uint32_t pb0 = static_cast<uint32_t>(psm[(2 * tq) * 8 + gq]) |
                                      (static_cast<uint32_t>(psm[(2 * tq + 1) * 8 + gq]) << 16);
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(kDecThreads)
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t a[4];
                     ldsm_x4_t(swz(vst, vrow, 2 * mt + ((lane >> 3) & 1)), a);
-                    mma_16816(acc[mt], a, pb0, pb1);
+                    mma_16816<DT>(acc[mt], a, pb0, pb1);
                 }
                 if (mine < 16) fence_proxy_async_smem();  // zeroed rows before the next TMA fill
             }
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kDecThreads)
             const int64_t orow = static_cast<int64_t>(x.b) * p.Hq + x.kvh * G + h;
             if (p.splits == 1) {
                 const float ov = l > 0.f ? a / l : 0.f;
-                p.o[orow * D + e] = __bfloat16_as_ushort(__float2bfloat16_rn(ov));
+                p.o[orow * D + e] = round16<DT>(ov);
             } else {
                 p.ws_acc[(orow * p.splits + x.split) * D + e] = a;
                 if (e == 0) {
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(kDecThreads)
 }
 
 // One warp per (sequence, query head): merge the non-empty splits.
-template <int D>
+template <int D, int DT>
 __global__ void __launch_bounds__(128) swa_decode_merge_kernel(const DecodeParams p) {
     pdl_launch_dependents();
     pdl_wait();  // the split kernel's partials
@@ -483,8 +490,7 @@ __global__ void __launch_bounds__(128) swa_decode_merge_kernel(const DecodeParam
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e)
-        p.o[static_cast<int64_t>(row) * D + lane * E + e] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(a[e] * inv));
+        p.o[static_cast<int64_t>(row) * D + lane * E + e] = round16<DT>(a[e] * inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -512,19 +518,21 @@ DecodePlan decode_plan(int B, int Hq, int Hkv, int d, int cap, int w, int sm_cou
 
 namespace {
 
-bool encode_cache_map(CUtensorMap *m, const void *ptr, int d, uint64_t rows) {
+bool encode_cache_map(CUtensorMap *m, const void *ptr, int d, uint64_t rows, int dtype) {
     const cuTensorMapEncodeTiled_fn enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)d * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)kDecCH};
     cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+    const CUtensorMapDataType ty =
+        dtype == SWA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return enc(m, ty, 2, const_cast<void *>(ptr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int G, int ST>
+template <int D, int G, int ST, int DT>
 swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStream_t stream) {
     using SL = DecSmem<D, G, ST>;
     static_assert(kDecCtasPerSm[ST - 1] * (SL::kAlloc + 1024) <= 233472, "CTAs per SM must fit");
@@ -533,7 +541,7 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStre
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(swa_decode_kernel<D, G, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(swa_decode_kernel<D, G, ST, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SL::kAlloc);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(decode)");
         configured[dev] = true;
@@ -543,15 +551,38 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStre
     const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
     const long long cap_ctas = static_cast<long long>(kDecCtasPerSm[ST - 1]) * sms;
     const int grid = static_cast<int>(items < cap_ctas ? items : cap_ctas);
-    e = launch_pdl(swa_decode_kernel<D, G, ST>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
+    e = launch_pdl(swa_decode_kernel<D, G, ST, DT>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
                    maps, p);
     if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_kernel");
     if (p.splits > 1) {
         const int rows = p.B * p.Hq;
-        e = launch_pdl(swa_decode_merge_kernel<D>, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
+        e = launch_pdl(swa_decode_merge_kernel<D, DT>, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
         if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_merge_kernel");
     }
     return SWA_OK;
+}
+
+}  // namespace
+
+namespace {
+
+template <int D, int DT>
+swa_status launch_decode_g(const DecodeMaps &maps, const DecodeParams &p, int G, bool single,
+                           cudaStream_t stream) {
+    switch (G) {
+        case 1: return single ? launch_decode<D, 1, 1, DT>(maps, p, stream) : launch_decode<D, 1, 2, DT>(maps, p, stream);
+        case 2: return single ? launch_decode<D, 2, 1, DT>(maps, p, stream) : launch_decode<D, 2, 2, DT>(maps, p, stream);
+        case 4: return single ? launch_decode<D, 4, 1, DT>(maps, p, stream) : launch_decode<D, 4, 2, DT>(maps, p, stream);
+        case 8: return single ? launch_decode<D, 8, 1, DT>(maps, p, stream) : launch_decode<D, 8, 2, DT>(maps, p, stream);
+        default: return SWA_ERR_UNSUPPORTED;
+    }
+}
+
+template <int DT>
+swa_status launch_decode_dt(const DecodeMaps &maps, const DecodeParams &p, int d, int G,
+                            bool single, cudaStream_t stream) {
+    return d == 128 ? launch_decode_g<128, DT>(maps, p, G, single, stream)
+                    : launch_decode_g<64, DT>(maps, p, G, single, stream);
 }
 
 }  // namespace
@@ -577,29 +608,16 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
     DecodeMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     const uint64_t rows = static_cast<uint64_t>(c.B) * c.Hkv * c.cap;
-    if (!encode_cache_map(&maps.k, c.k, c.d, rows) || !encode_cache_map(&maps.v, c.v, c.d, rows))
+    if (!encode_cache_map(&maps.k, c.k, c.d, rows, c.dtype) ||
+        !encode_cache_map(&maps.v, c.v, c.d, rows, c.dtype))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(cache)");
     const int G = Hq / c.Hkv;
     // items of one chunk (at most 64 slots per split): one ring stage
     const long long cap_eff = c.w < 0 ? c.cap : c.w;
     const long long chunks = (cap_eff + kDecCH - 1) / kDecCH;
     const bool single = (chunks + plan.splits - 1) / plan.splits <= 1;
-    if (c.d == 128) {
-        switch (G) {
-            case 1: return single ? launch_decode<128, 1, 1>(maps, p, stream) : launch_decode<128, 1, 2>(maps, p, stream);
-            case 2: return single ? launch_decode<128, 2, 1>(maps, p, stream) : launch_decode<128, 2, 2>(maps, p, stream);
-            case 4: return single ? launch_decode<128, 4, 1>(maps, p, stream) : launch_decode<128, 4, 2>(maps, p, stream);
-            case 8: return single ? launch_decode<128, 8, 1>(maps, p, stream) : launch_decode<128, 8, 2>(maps, p, stream);
-            default: return SWA_ERR_UNSUPPORTED;
-        }
-    }
-    switch (G) {
-        case 1: return single ? launch_decode<64, 1, 1>(maps, p, stream) : launch_decode<64, 1, 2>(maps, p, stream);
-        case 2: return single ? launch_decode<64, 2, 1>(maps, p, stream) : launch_decode<64, 2, 2>(maps, p, stream);
-        case 4: return single ? launch_decode<64, 4, 1>(maps, p, stream) : launch_decode<64, 4, 2>(maps, p, stream);
-        case 8: return single ? launch_decode<64, 8, 1>(maps, p, stream) : launch_decode<64, 8, 2>(maps, p, stream);
-        default: return SWA_ERR_UNSUPPORTED;
-    }
+    return c.dtype == SWA_F16 ? launch_decode_dt<kF16>(maps, p, c.d, G, single, stream)
+                              : launch_decode_dt<kBf16>(maps, p, c.d, G, single, stream);
 }
 
 int decode_read_clear_error(cudaStream_t stream) {

@@ -34,14 +34,16 @@ struct DecodePlan {
 DecodePlan decode_plan(int B, int Hq, int Hkv, int d, int cap, int w, int sm_count);
 
 // Launchers (arguments already validated).
+// dtype: SWA_BF16 or SWA_F16, the type of q, k, v and o.
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                          int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream);
+                          int L, int Hq, int Hkv, int d, int w, int s, int dtype,
+                          cudaStream_t stream);
 // Prefill of L query rows that sit at key positions q_off .. q_off+L-1 of a
 // key sequence of Lk rows: K/V in [B, Lk, Hkv, d], or in a cache's
 // [B, Hkv, kv_cap, d] layout when kv_cap > 0.
 swa_status prefill_launch_offset(const void *q, const void *k, const void *v, void *o, float *lse,
                                  int B, int L, int Hq, int Hkv, int d, int w, int s, int q_off,
-                                 int Lk, int kv_cap, cudaStream_t stream);
+                                 int Lk, int kv_cap, int dtype, cudaStream_t stream);
 // Chunked prefill of a finite window: the key rows the chunk's queries need,
 // in one sequence [B, q_off + n, Hkv, d] per tensor -- the cache's sinks and
 // ring in position order, then the chunk.

@@ -13,7 +13,7 @@
 // Roles (384 threads = three warpgroups, one persistent CTA per SM):
 //   warp 0       TMA producer for Q (double-buffered) and K tiles
 //   warp 1       tcgen05 issuer; owns the 512-column TMEM allocation
-//                S (256 columns) | P (128 columns, bf16 pairs) | O (d columns)
+//                S (256 columns) | P (128 columns, 16-bit pairs) | O (d columns)
 //   warp 2       TMA producer for V tiles
 //   warp 3       TMA stores of the staged output tile (128-column key tiles;
 //                idle otherwise)
@@ -28,6 +28,10 @@
 // registers.  The running max is only raised when it grows by more than 2^8
 // (exact: numerator and denominator share the same stale max), so the O
 // rescale through TMEM is rare.
+//
+// Element type (template DT): bf16 or fp16 for Q, K, V, P and O alike (one
+// kind::f16 MMA takes both operands of one type); scores, the softmax and the
+// O accumulator are fp32 either way.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,7 +43,7 @@
 #include "swa_prefill_common.cuh"
 #include "swa_ptx.cuh"
 
-// 0: pick the key tile width per call (prefill_narrow); 128 or 256: always
+// 0: pick the key tile width per call (prefill_key_tile); 128 or 256: always
 // that width (for measurements).
 #ifndef SWA_PREFILL_FORCE_KT
 #define SWA_PREFILL_FORCE_KT 0
@@ -61,7 +65,7 @@ struct PrefillSmem {
     static constexpr int kQ = 0;                        // 2 Q buffers
     static constexpr int kK = kQ + 2 * kQTile;          // K ring
     static constexpr int kV = kK + NSK * kKTile;        // V ring
-    // O tile staged for one TMA store (128-column tiles only: 128 x d bf16,
+    // O tile staged for one TMA store (128-column tiles only: 128 x d 16-bit,
     // d/64 slabs of 128 rows x 128 bytes, 128-byte swizzle)
     static constexpr int kStageO = kV + NSV * kKTile;
     static constexpr int kStageBytes = (KT <= 128) ? 128 * D * 2 : 0;
@@ -85,7 +89,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 
-template <int D, int KT, int NSK, int NSV>
+template <int D, int KT, int NSK, int NSV, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
     using SL = PrefillSmem<D, KT, NSK, NSV>;
@@ -204,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
-            constexpr uint32_t kIdescS = idesc_bf16_f32(128, 0, false);
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
+            constexpr uint32_t kIdescS = idesc_f16k<DT>(128, 0, false);
+            constexpr uint32_t kIdescPV = idesc_f16k<DT>(128, D, true);
             uint32_t g = 0, uc = 0;
             bool ok = true, have_prev = false, any_pv = false;
             uint32_t prev_g = 0, last_pv_g = 0, prev_ob = 0;
@@ -220,10 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after_sync();
                 const uint32_t vbase = base + SL::kV + vs * SL::kKTile;
                 for (int kk = 0; kk < pn / 16; ++kk) {
-                    // A = P (TMEM, two bf16 per column), B = V (MN-major:
+                    // A = P (TMEM, two 16-bit values per column), B = V (MN-major:
                     // 64-column slabs LBO apart, 8-key groups SBO apart)
                     const uint64_t b = smem_desc_sw128(vbase + kk * 16 * 128, SL::kKRegion, 1024);
-                    mma_bf16_ts(tmem + kTO + (DB ? ob * D : 0u),
+                    mma_f16k_ts(tmem + kTO + (DB ? ob * D : 0u),
                                 tmem + kTP + (DB ? (pg & 1) * 64 : 0u) + kk * 8, b, kIdescPV,
                                 (!first || kk > 0) ? 1u : 0u);
                 }
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             qbase + (kk >> 2) * SL::kQRegion + (kk & 3) * 32, 16, 1024);
                         const uint64_t b = smem_desc_sw128(
                             kbase + (kk >> 2) * SL::kKRegion + (kk & 3) * 32, 16, 1024);
-                        mma_bf16_ss(tmem + kTmemS, a, b, idesc, kk > 0 ? 1u : 0u);
+                        mma_f16k_ss(tmem + kTmemS, a, b, idesc, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(SL::kSFull));
                     mma_commit(bar(SL::kKEmpty + ks));
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *redl = reinterpret_cast<float *>(gbase + SL::kRedL);  // [2][2][128]
         uint32_t g = 0, uc = 0;
 
-        // The epilogue of a unit (O / l -> bf16 -> global, LSE) is deferred
+        // The epilogue of a unit (O / l -> 16-bit -> global, LSE) is deferred
         // into the first tile of the next unit: that tile's scores and
         // weights are computed while the previous unit's last P V runs, and
         // O is read out just before the new P is written.
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const bool ok = !*abort_flag;
             if constexpr (kStageOut) {
-                // Stage O / l as bf16 in the 128-byte-swizzled layout of the
+                // Stage O / l as 16-bit values in the 128-byte-swizzled layout of the
                 // output box (row r = MMA row: position r/G, head r%G); warp 3
                 // stores the whole unit with one TMA tensor store per 64-column
                 // slab (rows past the sequence end fall outside the tensor and
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t w4[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            w4[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv_l,
+                            w4[e] = pack2<DT>(__uint_as_float(r[8 * v + 2 * e]) * inv_l,
                                                 __uint_as_float(r[8 * v + 2 * e + 1]) * inv_l);
                         const int col = half * (D / 2) + 32 * c + 8 * v;  // first column
                         const int ci = (col & 63) >> 3;                   // 16-byte chunk in the row
@@ -371,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return;
             }
-            // This thread's half row of O / l as CH 16-byte chunks of bf16.
+            // This thread's half row of O / l as CH 16-byte chunks of 16-bit values.
             constexpr int CH = D / 16;
             uint4 ch[CH];
 #pragma unroll
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w4[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        w4[e] = pack_bf16x2(__uint_as_float(r[8 * v + 2 * e]) * inv_l,
+                        w4[e] = pack2<DT>(__uint_as_float(r[8 * v + 2 * e]) * inv_l,
                                             __uint_as_float(r[8 * v + 2 * e + 1]) * inv_l);
                     ch[4 * c + v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     a0, a1);
                         a0 = ex2_approx(a0);
                         a1 = ex2_approx(a1);
-                        pk[i][e] = pack_bf16x2(a0, a1);
+                        pk[i][e] = pack2<DT>(a0, a1);
                         l2[e & 1] = add_f32x2(l2[e & 1], f32x2(a0, a1));
                     }
                 }
@@ -637,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 namespace {
 
-template <int D, int KT, int NSK, int NSV>
+template <int D, int KT, int NSK, int NSV, int DT>
 swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaStream_t stream) {
     using SL = PrefillSmem<D, KT, NSK, NSV>;
     static_assert(SL::kAlloc <= 232448, "shared memory per CTA");
@@ -646,7 +650,7 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(swa_prefill_kernel<D, KT, NSK, NSV>,
+        e = cudaFuncSetAttribute(swa_prefill_kernel<D, KT, NSK, NSV, DT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
         configured[dev] = true;
@@ -654,7 +658,7 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
     const int sms = device_sm_count();
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const int grid = p.n_units < sms ? p.n_units : sms;
-    e = launch_pdl(swa_prefill_kernel<D, KT, NSK, NSV>, dim3(grid), dim3(kThreads), SL::kAlloc,
+    e = launch_pdl(swa_prefill_kernel<D, KT, NSK, NSV, DT>, dim3(grid), dim3(kThreads), SL::kAlloc,
                    stream, maps, p);
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_prefill_kernel");
 }
@@ -679,26 +683,38 @@ int prefill_key_tile(const PrefillParams &p, int d) {
     return d == 128 ? 112 : 128;
 }
 
+namespace {
+
+template <int DT>
+swa_status launch_prefill_dt(const PrefillMaps &maps, const PrefillParams &p, int d, int kt,
+                             cudaStream_t stream) {
+    if (d == 128)
+        return kt == 256 ? launch_prefill<128, 256, 1, 1, DT>(maps, p, stream)
+                         : launch_prefill<128, 112, 2, 2, DT>(maps, p, stream);
+    return kt == 256 ? launch_prefill<64, 256, 2, 2, DT>(maps, p, stream)
+                     : launch_prefill<64, 128, 4, 4, DT>(maps, p, stream);
+}
+
+}  // namespace
+
 swa_status prefill_launch_offset(const void *q, const void *k, const void *v, void *o, float *lse,
                                  int B, int L, int Hq, int Hkv, int d, int w, int s, int q_off,
-                                 int Lk, int kv_cap, cudaStream_t stream) {
+                                 int Lk, int kv_cap, int dtype, cudaStream_t stream) {
     const PrefillParams p = make_prefill_params(o, lse, B, L, Hq, Hkv, d, w, s, q_off, Lk);
     // the widths that have a kernel: 112 or 256 at d = 128, 128 or 256 at d = 64
     int kt = prefill_key_tile(p, d);
     if (kt != 256) kt = (d == 128) ? 112 : 128;
     PrefillMaps maps;
-    if (!encode_prefill_maps(&maps, q, k, v, p, d, kt, kv_cap))
+    if (!encode_prefill_maps(&maps, q, k, v, p, d, kt, dtype, kv_cap))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    if (d == 128)
-        return kt == 256 ? launch_prefill<128, 256, 1, 1>(maps, p, stream)
-                         : launch_prefill<128, 112, 2, 2>(maps, p, stream);
-    return kt == 256 ? launch_prefill<64, 256, 2, 2>(maps, p, stream)
-                     : launch_prefill<64, 128, 4, 4>(maps, p, stream);
+    return dtype == SWA_F16 ? launch_prefill_dt<kF16>(maps, p, d, kt, stream)
+                            : launch_prefill_dt<kBf16>(maps, p, d, kt, stream);
 }
 
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                          int L, int Hq, int Hkv, int d, int w, int s, cudaStream_t stream) {
-    return prefill_launch_offset(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, 0, L, 0, stream);
+                          int L, int Hq, int Hkv, int d, int w, int s, int dtype,
+                          cudaStream_t stream) {
+    return prefill_launch_offset(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, 0, L, 0, dtype, stream);
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {

@@ -61,7 +61,7 @@ struct PrefillParams {
     FastDiv div_bh, div_hkv;  // by B * Hkv and by Hkv (unit geometry)
     float scale_log2;         // log2(e) / sqrt(d)
     float scale;              // 1 / sqrt(d)
-    uint16_t *o;              // [B, L, Hq, d] bf16
+    uint16_t *o;              // [B, L, Hq, d] bf16 or fp16
     float *lse;               // optional [B, Hq, L]
 };
 
@@ -126,11 +126,18 @@ inline PrefillParams make_prefill_params(void *o, float *lse, int B, int L, int 
     return p;
 }
 
-// 4-D map (coordinates d, head, position, batch) over a bf16 tensor, 64-column
-// boxes, 128-byte swizzle.  Layout [B, L, heads, d] when bhsd_cap == 0, else
-// [B, heads, bhsd_cap, d] (a cache: positions 0 .. L-1 of cap slots).
+// Tensor-map element type of a swa_dtype value.
+static inline CUtensorMapDataType tensor_map_type(int dtype) {
+    return dtype == SWA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+// 4-D map (coordinates d, head, position, batch) over a 16-bit tensor of type
+// `dtype`, 64-column boxes, 128-byte swizzle.  Layout [B, L, heads, d] when
+// bhsd_cap == 0, else [B, heads, bhsd_cap, d] (a cache: positions 0 .. L-1
+// of cap slots).
 static inline bool encode_prefill_map(CUtensorMap *m, const void *ptr, int d, int heads, int L,
-                                      int B, int box_heads, int box_rows, int bhsd_cap = 0) {
+                                      int B, int box_heads, int box_rows, int dtype,
+                                      int bhsd_cap = 0) {
     const cuTensorMapEncodeTiled_fn enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)L, (cuuint64_t)B};
@@ -143,7 +150,7 @@ static inline bool encode_prefill_map(CUtensorMap *m, const void *ptr, int d, in
     }
     cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+    CUresult r = enc(m, tensor_map_type(dtype), 4, const_cast<void *>(ptr), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -153,17 +160,20 @@ static inline bool encode_prefill_map(CUtensorMap *m, const void *ptr, int d, in
 // [B, Lk, Hkv, d] layout, or [B, Hkv, kv_cap, d] when kv_cap > 0.
 static inline bool encode_prefill_maps(PrefillMaps *maps, const void *q, const void *k,
                                        const void *v, const PrefillParams &p, int d, int kt,
-                                       int kv_cap = 0) {
+                                       int dtype, int kv_cap = 0) {
     std::memset(maps, 0, sizeof(*maps));
-    bool ok = encode_prefill_map(&maps->q, q, d, p.Hq, p.L, p.B, p.G, p.P) &&
-              encode_prefill_map(&maps->o, p.o, d, p.Hq, p.L, p.B, p.G, p.P) &&
-              encode_prefill_map(&maps->k_band, k, d, p.Hkv, p.Lk, p.B, 1, kt, kv_cap) &&
-              encode_prefill_map(&maps->v_band, v, d, p.Hkv, p.Lk, p.B, 1, kt, kv_cap);
+    const int dt = dtype;
+    bool ok = encode_prefill_map(&maps->q, q, d, p.Hq, p.L, p.B, p.G, p.P, dt) &&
+              encode_prefill_map(&maps->o, p.o, d, p.Hq, p.L, p.B, p.G, p.P, dt) &&
+              encode_prefill_map(&maps->k_band, k, d, p.Hkv, p.Lk, p.B, 1, kt, dt, kv_cap) &&
+              encode_prefill_map(&maps->v_band, v, d, p.Hkv, p.Lk, p.B, 1, kt, dt, kv_cap);
     if (ok && p.s_pad > 0)
-        ok = encode_prefill_map(&maps->k_sink, k, d, p.Hkv, p.Lk, p.B, 1, p.s_pad, kv_cap) &&
-             encode_prefill_map(&maps->v_sink, v, d, p.Hkv, p.Lk, p.B, 1, p.s_pad, kv_cap) &&
-             encode_prefill_map(&maps->k_band0, k, d, p.Hkv, p.Lk, p.B, 1, kt - p.s_pad, kv_cap) &&
-             encode_prefill_map(&maps->v_band0, v, d, p.Hkv, p.Lk, p.B, 1, kt - p.s_pad, kv_cap);
+        ok = encode_prefill_map(&maps->k_sink, k, d, p.Hkv, p.Lk, p.B, 1, p.s_pad, dt, kv_cap) &&
+             encode_prefill_map(&maps->v_sink, v, d, p.Hkv, p.Lk, p.B, 1, p.s_pad, dt, kv_cap) &&
+             encode_prefill_map(&maps->k_band0, k, d, p.Hkv, p.Lk, p.B, 1, kt - p.s_pad, dt,
+                                kv_cap) &&
+             encode_prefill_map(&maps->v_band0, v, d, p.Hkv, p.Lk, p.B, 1, kt - p.s_pad, dt,
+                                kv_cap);
     return ok;
 }
 

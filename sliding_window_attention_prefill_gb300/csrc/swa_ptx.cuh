@@ -210,8 +210,9 @@ __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] x B[smem], kind::f16 (bf16 operands, fp32 accumulator).
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] x B[smem], kind::f16 (bf16 or fp16 operands, as the
+// instruction descriptor says; fp32 accumulator).
+__device__ __forceinline__ void mma_f16k_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -222,8 +223,8 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
 }
 
 // D[tmem] (+)= A[tmem] x B[smem], kind::f16: A (M x 16 per k-step) read from
-// tensor memory, row m in lane m, two bf16 values per 32-bit column.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// tensor memory, row m in lane m, two 16-bit values per 32-bit column.
+__device__ __forceinline__ void mma_f16k_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -308,11 +309,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Element type of the 16-bit operands and outputs (the values of swa_dtype).
+constexpr int kBf16 = 0;
+constexpr int kF16 = 1;
+
 // Instruction descriptor for tcgen05.mma kind::f16: fp32 accumulator (bits
-// 4..5 = 1), A and B bf16 (bits 7..9 = 1, 10..12 = 1), A K-major, B K-major
-// or MN-major (bit 16), N >> 3 in bits 17..22, M >> 4 in bits 24..28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// 4..5 = 1), A and B of one type -- bf16 (bits 7..9 = 1, 10..12 = 1) or
+// fp16 (both 0) --, A K-major, B K-major or MN-major (bit 16), N >> 3 in
+// bits 17..22, M >> 4 in bits 24..28.
+template <int DT>
+__host__ __device__ constexpr uint32_t idesc_f16k(uint32_t M, uint32_t N, bool b_mn_major) {
+    constexpr uint32_t ab = (DT == kBf16) ? 1u : 0u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
@@ -356,16 +364,22 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     return d;
 }
 
-// Two floats -> packed bf16x2 (round to nearest even); lo in bits 0..15.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+// Two floats -> packed 16-bit pair of element type DT (round to nearest
+// even); lo in bits 0..15.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    if constexpr (DT == kBf16)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
-__device__ __forceinline__ float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16hi_to_f32(uint32_t v) {
-    return __uint_as_float(v & 0xFFFF0000u);
+// One float -> 16-bit pattern of element type DT (round to nearest even).
+template <int DT>
+__device__ __forceinline__ uint16_t round16(float x) {
+    return static_cast<uint16_t>(pack2<DT>(x, 0.f) & 0xFFFFu);
 }
 
 }  // namespace swa

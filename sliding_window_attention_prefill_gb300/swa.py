@@ -17,6 +17,9 @@ from . import build as _build
 
 W_INF = -1
 
+# swa_dtype codes of the 16-bit element types
+DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1}
+
 _c_int = ctypes.c_int
 _c_i32 = ctypes.c_int32
 _c_i64 = ctypes.c_int64
@@ -27,7 +30,7 @@ _c_p = ctypes.c_void_p
 class SwaCacheStruct(ctypes.Structure):
     """Mirror of ``swa_cache``."""
     _fields_ = [("k", _c_p), ("v", _c_p), ("B", _c_i32), ("Hkv", _c_i32), ("d", _c_i32),
-                ("cap", _c_i32), ("w", _c_i32), ("s", _c_i32)]
+                ("cap", _c_i32), ("w", _c_i32), ("s", _c_i32), ("dtype", _c_i32)]
 
 
 STATUS = {0: "SWA_OK", -1: "SWA_ERR_INVALID_ARG", -2: "SWA_ERR_UNSUPPORTED",
@@ -56,6 +59,8 @@ def _declare(L) -> None:
     P = ctypes.POINTER
     L.swa_prefill.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7 + [_c_p]
     L.swa_prefill.restype = _c_int
+    L.swa_prefill_ex.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 8 + [_c_p]
+    L.swa_prefill_ex.restype = _c_int
     L.swa_cache_append.argtypes = [P(SwaCacheStruct), _c_p, _c_p, _c_int, _c_i64, _c_p]
     L.swa_cache_append.restype = _c_int
     L.swa_decode_workspace_bytes.argtypes = [_c_int] * 6
@@ -129,6 +134,12 @@ def _stream(device: torch.device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def _dtype_code(dtype) -> int:
+    if dtype not in DTYPE_CODES:
+        raise TypeError(f"element type must be torch.bfloat16 or torch.float16, got {dtype}")
+    return DTYPE_CODES[dtype]
+
+
 def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -145,35 +156,42 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: int,
             out: torch.Tensor | None = None, return_lse: bool = False):
     """SWA(w,s) attention of every prompt position.
 
-    q [B, L, Hq, d], k/v [B, L, Hkv, d] bf16 CUDA tensors; returns o [B, L, Hq, d]
-    (and lse [B, Hq, L] fp32 if ``return_lse``).  ``w = W_INF`` is full causal.
+    q [B, L, Hq, d], k/v [B, L, Hkv, d] CUDA tensors, all bf16 or all fp16;
+    returns o [B, L, Hq, d] of the same type (and lse [B, Hq, L] fp32 if
+    ``return_lse``).  ``w = W_INF`` is full causal.
     """
-    _need(q, "q"), _need(k, "k"), _need(v, "v")
+    if not isinstance(q, torch.Tensor):
+        raise TypeError("q must be a torch.Tensor")
+    dt = _dtype_code(q.dtype)
+    _need(q, "q", q.dtype), _need(k, "k", q.dtype), _need(v, "v", q.dtype)
     B, L, Hq, d = q.shape
     if k.shape[:2] != (B, L) or k.shape[3] != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
     Hkv = k.shape[2]
     o = torch.empty_like(q) if out is None else out
-    _need(o, "out")
+    _need(o, "out", q.dtype)
     if o.shape != q.shape:
         raise ValueError("out must have the shape of q")
     lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device) if return_lse else None
-    st = lib().swa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, L, Hq, Hkv, d,
-                           int(w), int(s), _stream(q.device))
-    _check(st, "swa_prefill")
+    st = lib().swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, L, Hq, Hkv, d,
+                              int(w), int(s), dt, _stream(q.device))
+    _check(st, "swa_prefill_ex")
     return (o, lse) if return_lse else o
 
 
 # ----------------------------------------------------------------------------- cache
 class Cache:
-    """One layer's fixed SWA(w,s) cache: k, v bf16 [B, Hkv, cap, d] (torch-owned).
+    """One layer's fixed SWA(w,s) cache: k, v [B, Hkv, cap, d] (torch-owned),
+    bf16 or fp16 (``dtype``; queries and outputs of the calls on the cache
+    have the same type).
 
     cap = w for a finite window (s sink slots + a (w-s)-slot ring), or
     ``max_len`` for ``w = W_INF``.
     """
 
     def __init__(self, B: int, Hkv: int, d: int, w: int, s: int, max_len: int | None = None,
-                 device="cuda"):
+                 device="cuda", dtype=torch.bfloat16):
+        _dtype_code(dtype)
         if w == W_INF:
             if not max_len:
                 raise ValueError("an infinite window needs max_len")
@@ -181,24 +199,27 @@ class Cache:
         else:
             cap = int(w)
         self.B, self.Hkv, self.d, self.w, self.s, self.cap = B, Hkv, d, int(w), int(s), cap
-        self.k = torch.zeros(B, Hkv, cap, d, dtype=torch.bfloat16, device=device)
-        self.v = torch.zeros(B, Hkv, cap, d, dtype=torch.bfloat16, device=device)
+        self.dtype = dtype
+        self.k = torch.zeros(B, Hkv, cap, d, dtype=dtype, device=device)
+        self.v = torch.zeros(B, Hkv, cap, d, dtype=dtype, device=device)
 
     @classmethod
     def from_tensors(cls, k: torch.Tensor, v: torch.Tensor, w: int, s: int) -> "Cache":
-        _need(k, "cache k"), _need(v, "cache v")
+        _dtype_code(k.dtype)
+        _need(k, "cache k", k.dtype), _need(v, "cache v", k.dtype)
         obj = cls.__new__(cls)
+        obj.dtype = k.dtype
         obj.B, obj.Hkv, obj.cap, obj.d = k.shape
         obj.w, obj.s, obj.k, obj.v = int(w), int(s), k, v
         return obj
 
     def struct(self) -> SwaCacheStruct:
         return SwaCacheStruct(self.k.data_ptr(), self.v.data_ptr(), self.B, self.Hkv, self.d,
-                              self.cap, self.w, self.s)
+                              self.cap, self.w, self.s, DTYPE_CODES[self.dtype])
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int) -> None:
         """Write positions pos0 .. pos0+n-1 from k_new/v_new [B, n, Hkv, d]."""
-        _need(k_new, "k_new"), _need(v_new, "v_new")
+        _need(k_new, "k_new", self.dtype), _need(v_new, "v_new", self.dtype)
         if (k_new.shape != v_new.shape or k_new.shape[0] != self.B
                 or tuple(k_new.shape[2:]) != (self.Hkv, self.d)):
             raise ValueError(f"k_new/v_new must be [B, n, Hkv, d], got {tuple(k_new.shape)}")
@@ -222,17 +243,17 @@ def prefill_chunk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cache: "Cac
     """Prefill positions pos0 .. pos0+n-1 of a prompt against what ``cache``
     holds of the earlier positions, then append them to the cache.
 
-    q [B, n, Hq, d], k/v [B, n, Hkv, d] bf16 CUDA tensors; returns o [B, n, Hq, d]
-    (and lse [B, Hq, n] fp32 if ``return_lse``).  Chunk by chunk this equals
-    one prefill of the whole prompt.
+    q [B, n, Hq, d], k/v [B, n, Hkv, d] CUDA tensors of the cache's type;
+    returns o [B, n, Hq, d] (and lse [B, Hq, n] fp32 if ``return_lse``).
+    Chunk by chunk this equals one prefill of the whole prompt.
     """
-    _need(q, "q"), _need(k, "k"), _need(v, "v")
+    _need(q, "q", cache.dtype), _need(k, "k", cache.dtype), _need(v, "v", cache.dtype)
     B, n, Hq, d = q.shape
     if (B, d) != (cache.B, cache.d) or k.shape != (B, n, cache.Hkv, d) or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, cache "
                          f"B={cache.B} Hkv={cache.Hkv} d={cache.d}")
     o = torch.empty_like(q) if out is None else out
-    _need(o, "out")
+    _need(o, "out", cache.dtype)
     lse = torch.empty(B, Hq, n, dtype=torch.float32, device=q.device) if return_lse else None
     nbytes = prefill_chunk_workspace_bytes(B, n, cache.Hkv, d, cache.w, pos0)
     ws = workspace
@@ -273,14 +294,15 @@ def workspace_for(cache: "Cache", Hq: int) -> torch.Tensor | None:
 
 def decode(q: torch.Tensor, cache: Cache, pos: torch.Tensor, out: torch.Tensor | None = None,
            workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """One token per sequence: q [B, Hq, d] at positions pos [B] (int32, device)."""
-    _need(q, "q")
+    """One token per sequence: q [B, Hq, d] (the cache's type) at positions
+    pos [B] (int32, device)."""
+    _need(q, "q", cache.dtype)
     _need(pos, "pos", torch.int32)
     B, Hq, d = q.shape
     if B != cache.B or d != cache.d or pos.numel() != B:
         raise ValueError("q / pos do not match the cache")
     o = torch.empty_like(q) if out is None else out
-    _need(o, "out")
+    _need(o, "out", cache.dtype)
     ws = workspace if workspace is not None else workspace_for(cache, Hq)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     c = cache.struct()

@@ -4,6 +4,7 @@ the device."""
 import ctypes
 
 import pytest
+import torch
 
 import oracle
 from sliding_window_attention_prefill_gb300 import build as swa_build
@@ -61,9 +62,25 @@ def test_check_prefill(L):
     assert c(q, k, v, o, ctypes.c_void_p(FAKE * 5000 + 2), 1, 256, 4, 1, 64, 64, 4) == ALIGN
 
 
-def _cache(B=2, Hkv=2, d=128, cap=64, w=64, s=4, k=None, v=None):
+def _cache(B=2, Hkv=2, d=128, cap=64, w=64, s=4, k=None, v=None, dtype=0):
     return swa.SwaCacheStruct(k if k is not None else FAKE * 10, v if v is not None else FAKE * 900,
-                              B, Hkv, d, cap, w, s)
+                              B, Hkv, d, cap, w, s, dtype)
+
+
+def test_element_types(L):
+    """bf16 (0) and fp16 (1) are the element types; anything else is rejected
+    on the host before any launch."""
+    q, k, v, o = _p(1000), _p(2000), _p(3000), _p(4000)
+    for bad in (2, -1, 7):
+        assert L.swa_prefill_ex(q, k, v, o, None, 1, 256, 4, 1, 64, 64, 4, bad, None) == INVALID
+    kn, vn = _p(5000), _p(6000)
+    assert L.swa_check_append(ctypes.byref(_cache(dtype=1)), kn, vn, 1, 0) == OK
+    assert L.swa_check_append(ctypes.byref(_cache(dtype=2)), kn, vn, 1, 0) == INVALID
+    qd, pos, od = _p(7000), _p(7100), _p(7200)
+    assert L.swa_check_decode(qd, ctypes.byref(_cache(dtype=1)), pos, 8, 64, 4, od, None, 0, 0) == OK
+    assert L.swa_check_decode(qd, ctypes.byref(_cache(dtype=3)), pos, 8, 64, 4, od, None, 0,
+                              0) == INVALID
+    assert swa.DTYPE_CODES == {torch.bfloat16: 0, torch.float16: 1}
 
 
 def test_check_append(L):
