@@ -94,6 +94,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     swa_prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
     using SL = PrefillSmem<D, KT, NSK, NSV>;
     constexpr int NC = (KT + 63) / 64;  // 32-column chunks of a tile per softmax thread
+    // A 112-column tile ends in a 16-column chunk (columns 96..111, taken by
+    // the second half): that chunk's other 16 columns are not computed.
+    constexpr bool kShortTail = (KT % 64 == 48);
     // TMEM columns.  256-column tiles: S [0,256) | P [256,384) | O [384,384+d).
     // 128-column tiles leave room to double-buffer P (by tile) and O (by
     // unit): S [0,128) | P0, P1 [128,256) | O0, O1 [256,256+2d); then the
@@ -463,10 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool band_ok = c_lo <= c_hi;
                 bool full[NC], empty[NC];
+                // this thread's last chunk has only 16 columns (warp-uniform)
+                const bool short_tail = kShortTail && half == 1;
 #pragma unroll
                 for (int i = 0; i < NC; ++i) {
                     const int c0 = 32 * (half + 2 * i);
-                    const bool f = band_ok && c_lo <= c0 && c_hi >= c0 + 31;
+                    const int cw = (short_tail && i == NC - 1) ? 16 : 32;
+                    const bool f = band_ok && c_lo <= c0 && c_hi >= c0 + cw - 1;
                     const bool e = (!band_ok || c_hi < c0 || c_lo > c0 + 31) && sink_hi <= c0;
                     full[i] = __all_sync(0xffffffffu, f);
                     empty[i] = __all_sync(0xffffffffu, e);
@@ -493,15 +499,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 32; ++e)
                             if (!(vb & (1u << e))) sr[i][e] = __float_as_uint(-INFINITY);
                     }
-                    // elements 0..1, then 2..29 four at a time, then 30..31
+                    // elements 0..1, then 2..13 four at a time, then 14..15;
+                    // the same for 16..31 unless the chunk has 16 columns
                     float a = __uint_as_float(sr[i][0]), b = __uint_as_float(sr[i][1]);
 #pragma unroll
-                    for (int e = 2; e < 30; e += 4) {
+                    for (int e = 2; e < 14; e += 4) {
                         a = fmax3(a, __uint_as_float(sr[i][e]), __uint_as_float(sr[i][e + 1]));
                         b = fmax3(b, __uint_as_float(sr[i][e + 2]), __uint_as_float(sr[i][e + 3]));
                     }
-                    mx_a = fmax3(mx_a, a, __uint_as_float(sr[i][30]));
-                    mx_b = fmax3(mx_b, b, __uint_as_float(sr[i][31]));
+                    a = fmax3(a, __uint_as_float(sr[i][14]), __uint_as_float(sr[i][15]));
+                    if (!(short_tail && i == NC - 1)) {
+#pragma unroll
+                        for (int e = 16; e < 32; e += 4) {
+                            a = fmax3(a, __uint_as_float(sr[i][e]), __uint_as_float(sr[i][e + 1]));
+                            b = fmax3(b, __uint_as_float(sr[i][e + 2]), __uint_as_float(sr[i][e + 3]));
+                        }
+                    }
+                    mx_a = fmaxf(mx_a, a);
+                    mx_b = fmaxf(mx_b, b);
                 }
                 // Row max over both halves through shared memory, one barrier
                 // per tile (buffers alternate with the tile parity); the first
@@ -533,8 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 16; ++e) pk[i][e] = 0u;
                         continue;
                     }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
+                    auto pair = [&](int e) {
                         float a0, a1;
                         f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[i][2 * e]),
                                                     __uint_as_float(sr[i][2 * e + 1])),
@@ -544,6 +558,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a1 = ex2_approx(a1);
                         pk[i][e] = pack2<DT>(a0, a1);
                         l2[e & 1] = add_f32x2(l2[e & 1], f32x2(a0, a1));
+                    };
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) pair(e);
+                    if (short_tail && i == NC - 1) {
+#pragma unroll
+                        for (int e = 8; e < 16; ++e) pk[i][e] = 0u;
+                    } else {
+#pragma unroll
+                        for (int e = 8; e < 16; ++e) pair(e);
                     }
                 }
                 float lx, ly, lz, lw;
