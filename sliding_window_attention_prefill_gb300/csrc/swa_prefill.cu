@@ -78,7 +78,9 @@ struct PrefillSmem {
                          kPFull = kSFull + 2, kPVDone = kSFull + 3,
                          // staged epilogue: O written (one arrive per softmax
                          // warp), staging buffer read by its stores
-                         kOStaged = kSFull + 5, kOFree = kSFull + 6, kNumBars = kSFull + 7;
+                         kOStaged = kSFull + 5, kOFree = kSFull + 6,
+                         // P written, for odd tiles (kPFull: even tiles)
+                         kPFull1 = kSFull + 7, kNumBars = kSFull + 8;
     static constexpr int kTmemSlot = kBar + kNumBars * 8;
     static constexpr int kAbort = kTmemSlot + 8;
     static constexpr int kBytes = kAbort + 8;
@@ -121,7 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < SL::kNumBars; ++i) {
-            const bool eight = (i == SL::kSEmpty || i == SL::kPFull || i == SL::kOStaged);
+            const bool eight = (i == SL::kSEmpty || i == SL::kPFull || i == SL::kPFull1 ||
+                                i == SL::kOStaged);
             mbar_init(bar(i), eight ? 8u : 1u);
         }
         *abort_flag = 0;
@@ -221,7 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             auto issue_pv = [&](uint32_t pg, int pn, bool first, uint32_t ob) -> bool {
                 const uint32_t vs = pg % NSV;
-                if (!mbar_wait(bar(SL::kPFull), pg & 1, &g_prefill_error, abort_flag)) return false;
+                // One barrier per tile parity: the softmax may finish tile pg+1
+                // before this warp has waited for tile pg, and a waiter must
+                // not fall two phases behind an mbarrier (its phase parity
+                // would read as not yet complete).
+                if (!mbar_wait(bar((pg & 1) ? SL::kPFull1 : SL::kPFull), (pg >> 1) & 1,
+                               &g_prefill_error, abort_flag))
+                    return false;
                 if (!mbar_wait(bar(SL::kVFull + vs), (pg / NSV) & 1, &g_prefill_error, abort_flag))
                     return false;
                 tc_fence_after_sync();
@@ -616,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(SL::kPFull));
+                if (lane == 0) mbar_arrive(bar((g & 1) ? SL::kPFull1 : SL::kPFull));
                 // With two O buffers the previous unit's epilogue runs here,
                 // beside this tile's P V, once that unit's last P V is done.
                 if (DB && do_epi) {

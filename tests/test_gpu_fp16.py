@@ -126,3 +126,23 @@ def test_mixed_types_are_rejected():
     pos = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(TypeError):
         decode(torch.zeros(1, 2, 64, dtype=torch.bfloat16, device="cuda"), c, pos)
+
+
+def test_prefill_many_units_per_cta_keeps_its_waits():
+    """Many two-tile units per CTA (the pages' shape, L = 32768, SWA(512,4)):
+    repeated launches record no wait timeout, and sampled rows match the
+    oracle.  (An mbarrier waited by one parity bit must not complete twice
+    before it is waited; a fast softmax finishing two tiles before the MMA
+    warp looked at the first would otherwise stall the kernel.)"""
+    B, L, Hq, Hkv, d, w, s = 1, 32768, 16, 16, 64, 512, 4
+    q, k, v = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=12, dtype=F16)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    for _ in range(3):
+        o = prefill(qd, kd, vd, w, s)
+        torch.cuda.synchronize()
+        assert device_error() == 0
+    rng = np.random.default_rng(5)
+    rows = np.stack([np.zeros(64, np.int64), rng.integers(0, L, 64), rng.integers(0, Hq, 64)], 1)
+    ref, _ = oracle.get().prefill_rows(bits(q), bits(k), bits(v), rows, w, s, dtype="f16")
+    got = o.cpu()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got, ref, "sampled rows")
