@@ -628,6 +628,58 @@ def suite_chunk(steps: int):
         torch.cuda.empty_cache()
 
 
+def suite_varlen(steps: int):
+    """Ragged-batch prefill (prefill_varlen) against a padded batch and
+    against one prefill per sequence, Llama attention shape (Hq=32, Hkv=8,
+    d=128): 64 sequences with seeded lengths uniform in [256, 8192]
+    (about 270K tokens), SWA(64,4) and SWA(512,4).  TFLOP/s count only the
+    attended pairs of the real tokens; L2 is flushed before each step."""
+    import numpy as np
+    import torch
+
+    import sliding_window_attention_prefill_gb300 as swa
+    from sliding_window_attention_prefill_gb300 import build, inputs
+    build.build()
+    pk = peaks()
+    flush = L2Flush()
+    Hq, Hkv, d = 32, 8, 128
+    rng = np.random.default_rng(0)
+    lengths = [int(x) for x in rng.integers(256, 8193, 64)]
+    total, max_len = sum(lengths), max(lengths)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device="cuda")
+    q, k, v = inputs.prefill_inputs(1, total, Hq, Hkv, d, seed=0)
+    q, k, v = q[0].cuda(), k[0].cuda(), v[0].cuda()
+    o = torch.empty_like(q)
+    seqs = []
+    for b, n in enumerate(lengths):
+        a = int(cu[b])
+        seqs.append((q[a:a + n].unsqueeze(0), k[a:a + n].unsqueeze(0), v[a:a + n].unsqueeze(0),
+                     o[a:a + n].unsqueeze(0)))
+    qp = torch.zeros(len(lengths), max_len, Hq, d, dtype=q.dtype, device="cuda")
+    kp = torch.zeros(len(lengths), max_len, Hkv, d, dtype=q.dtype, device="cuda")
+    vp = torch.zeros_like(kp)
+    op = torch.empty_like(qp)
+    for w, s in [(64, 4), (512, 4)]:
+        fl = sum(prefill_flops(1, n, Hq, d, w) for n in lengths)
+        ms_var = _time_graph(lambda: swa.prefill_varlen(q, k, v, cu, w, s, max_len=max_len, out=o),
+                             steps, flush)
+        ms_pad = _time_graph(lambda: swa.prefill(qp, kp, vp, w, s, out=op), steps, flush)
+
+        def per_seq():
+            for qs, ks, vs, os_ in seqs:
+                swa.prefill(qs, ks, vs, w, s, out=os_)
+
+        ms_seq = _time_graph(per_seq, steps, flush)
+        tf = fl / (ms_var * 1e-3) / 1e12
+        print(json.dumps({"suite": "varlen", "sequences": len(lengths), "tokens": total,
+                          "max_len": max_len, "w": w, "s": s, "ms_varlen": ms_var,
+                          "ms_padded_batch": ms_pad, "ms_per_sequence_calls": ms_seq,
+                          "tflops_varlen": tf, "tok_s_varlen": total / (ms_var * 1e-3),
+                          "frac_tensor_peak": tf / pk["bf16_tflops"], "l2": L2_NOTE}), flush=True)
+    del q, k, v, o, qp, kp, vp, op, seqs
+    torch.cuda.empty_cache()
+
+
 CONTEXT_POSITIONS = [1 << e for e in range(7, 19)]  # 128 .. 262144
 CONTEXT_WINDOWS = [64, 128, 256, 512, -1]
 CONTEXT_LAYERS = 4
@@ -737,7 +789,7 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["swa", "reference"], default="swa")
-    ap.add_argument("--suite", choices=["prefill", "decode", "context", "chunk"], default=None,
+    ap.add_argument("--suite", choices=["prefill", "decode", "context", "chunk", "varlen"], default=None,
                     help="auxiliary per-config lines instead of the headline step")
     ap.add_argument("--w", type=int, default=None, help="prefill suite: only this window")
     ap.add_argument("--B", type=int, default=None, help="prefill suite: batch override")
@@ -756,6 +808,9 @@ def main():
         return
     if args.suite == "chunk":
         suite_chunk(max(args.steps // 20, 10))
+        return
+    if args.suite == "varlen":
+        suite_varlen(max(args.steps // 20, 10))
         return
     if args.suite == "context":
         suite_context(max(min(args.steps // 40, 20), 5),

@@ -268,6 +268,46 @@ swa_status swa_prefill_chunk(const void *q, const void *k_new, const void *v_new
                              void *workspace, size_t workspace_bytes, swa_stream_t stream);
 
 /*
+ * swa_prefill_varlen -- swa_prefill of B sequences of different lengths in
+ * one call (a ragged batch, as a serving system packs it).  The sequences are
+ * packed one after the other:
+ *
+ *   q          [total, Hq,  d]  queries; sequence b is rows
+ *                               cu_seqlens[b] .. cu_seqlens[b+1]-1
+ *   k, v       [total, Hkv, d]  keys and values, packed the same way
+ *   o          [total, Hq,  d]  output; lse optional fp32 [Hq, total]
+ *   cu_seqlens [B+1] int32, DEVICE memory: 0 = cu_seqlens[0] <= ... <=
+ *              cu_seqlens[B] = total (empty sequences allowed)
+ *   max_len    an upper bound of the sequence lengths (host); it only picks
+ *              the key tile width for w = SWA_W_INF
+ *   workspace  device scratch of swa_prefill_varlen_workspace_bytes(B, total,
+ *              Hq, Hkv) bytes, 16-byte aligned, contents undefined between
+ *              calls
+ *
+ * Each position attends to its attended set A(t) within its own sequence
+ * (positions counted from the sequence's first row; the sinks are its first
+ * s tokens), exactly as swa_prefill of that sequence alone.  cu_seqlens is
+ * read on the device: a cu_seqlens that is not such a partition of
+ * [0, total) makes the call compute nothing and record SWA_ERR_BOUNDS in the
+ * device error word.  Other requirements and codes as swa_prefill_ex.
+ *
+ * Source: the same window equation ("Sliding-window beats linear
+ * attention", paper summary page, section "Prerequisites / Sliding-window
+ * attention SWA(w, s)"); the pages' own system measurements run batch 1
+ * (same page, section "Method steps", step five).
+ */
+size_t swa_prefill_varlen_workspace_bytes(int B, int total, int Hq, int Hkv);
+swa_status swa_prefill_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int B, int total, int max_len, int Hq,
+                              int Hkv, int d, int w, int s, swa_dtype dtype, void *workspace,
+                              size_t workspace_bytes, swa_stream_t stream);
+swa_status swa_check_prefill_varlen(const void *q, const void *k, const void *v, const void *o,
+                                    const float *lse, const int32_t *cu_seqlens, int B, int total,
+                                    int max_len, int Hq, int Hkv, int d, int w, int s,
+                                    swa_dtype dtype, const void *workspace,
+                                    size_t workspace_bytes);
+
+/*
  * swa_selftest_wait_timeout -- enqueue a one-CTA kernel whose bounded wait
  * runs out on purpose: it waits on an mbarrier that nothing arrives on,
  * through the same bounded wait as every kernel of the library, holding a

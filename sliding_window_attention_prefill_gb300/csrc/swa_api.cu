@@ -308,6 +308,51 @@ swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, flo
     return swa_prefill_ex(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, SWA_BF16, stream);
 }
 
+size_t swa_prefill_varlen_workspace_bytes(int B, int total, int Hq, int Hkv) {
+    if (B < 1 || total < 0 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0) return 0;
+    return swa::varlen_workspace_bytes(B, total, Hq, Hkv);
+}
+
+swa_status swa_check_prefill_varlen(const void *q, const void *k, const void *v, const void *o,
+                                    const float *lse, const int32_t *cu_seqlens, int B, int total,
+                                    int max_len, int Hq, int Hkv, int d, int w, int s,
+                                    swa_dtype dtype, const void *workspace,
+                                    size_t workspace_bytes) {
+    if (!valid_dtype(dtype)) return SWA_ERR_INVALID_ARG;
+    if (B < 1 || total < 0 || max_len < 0) return SWA_ERR_INVALID_ARG;
+    // the packed tensors as one sequence of `total` rows (shapes, window,
+    // alignment, overlaps)
+    const swa_status st = swa_check_prefill(q, k, v, o, lse, 1, total, Hq, Hkv, d, w, s);
+    if (st != SWA_OK) return st;
+    if (!cu_seqlens) return SWA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) return SWA_ERR_ALIGNMENT;
+    const size_t need = swa::varlen_workspace_bytes(B, total, Hq, Hkv);
+    if (!workspace || workspace_bytes < need) return SWA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SWA_ERR_ALIGNMENT;
+    const size_t qb = static_cast<size_t>(total) * Hq * d * 2;
+    const size_t kb = static_cast<size_t>(total) * Hkv * d * 2;
+    const size_t lb = lse ? static_cast<size_t>(total) * Hq * 4 : 0;
+    const size_t cb = (static_cast<size_t>(B) + 1) * 4;
+    if (overlap(workspace, need, q, qb) || overlap(workspace, need, k, kb) ||
+        overlap(workspace, need, v, kb) || overlap(workspace, need, o, qb) ||
+        overlap(workspace, need, lse, lb) || overlap(workspace, need, cu_seqlens, cb) ||
+        overlap(o, qb, cu_seqlens, cb) || overlap(lse, lb, cu_seqlens, cb))
+        return SWA_ERR_INVALID_ARG;
+    return SWA_OK;
+}
+
+swa_status swa_prefill_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int B, int total, int max_len, int Hq,
+                              int Hkv, int d, int w, int s, swa_dtype dtype, void *workspace,
+                              size_t workspace_bytes, swa_stream_t stream) {
+    const swa_status st = swa_check_prefill_varlen(q, k, v, o, lse, cu_seqlens, B, total, max_len,
+                                                   Hq, Hkv, d, w, s, dtype, workspace,
+                                                   workspace_bytes);
+    if (st != SWA_OK || total == 0) return st;
+    return swa::prefill_varlen_launch(q, k, v, o, lse, cu_seqlens, B, total, max_len, Hq, Hkv, d, w,
+                                      w == SWA_W_INF ? 0 : s, dtype, workspace, as_cuda(stream));
+}
+
 swa_status swa_cache_append(const swa_cache *cache, const void *k_new, const void *v_new, int n,
                             int64_t pos0, swa_stream_t stream) {
     const swa_status st = swa_check_append(cache, k_new, v_new, n, pos0);

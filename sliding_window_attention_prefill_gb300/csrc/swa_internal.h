@@ -44,6 +44,14 @@ swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, 
 swa_status prefill_launch_offset(const void *q, const void *k, const void *v, void *o, float *lse,
                                  int B, int L, int Hq, int Hkv, int d, int w, int s, int q_off,
                                  int Lk, int kv_cap, int dtype, cudaStream_t stream);
+// Variable-length prefill: B sequences packed in [total, heads, d] tensors,
+// sequence b at rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (device array);
+// workspace of varlen_workspace_bytes(B, total, Hq, Hkv) bytes.
+size_t varlen_workspace_bytes(int B, int total, int Hq, int Hkv);
+swa_status prefill_varlen_launch(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 const int32_t *cu_seqlens, int B, int total, int max_len, int Hq,
+                                 int Hkv, int d, int w, int s, int dtype, void *workspace,
+                                 cudaStream_t stream);
 // Chunked prefill of a finite window: the key rows the chunk's queries need,
 // in one sequence [B, q_off + n, Hkv, d] per tensor -- the cache's sinks and
 // ring in position order, then the chunk.

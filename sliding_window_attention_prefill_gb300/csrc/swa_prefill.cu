@@ -91,7 +91,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 
-template <int D, int KT, int NSK, int NSV, int DT>
+template <int D, int KT, int NSK, int NSV, int DT, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     swa_prefill_kernel(const __grid_constant__ PrefillMaps maps, const PrefillParams p) {
     using SL = PrefillSmem<D, KT, NSK, NSV>;
@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     pdl_wait();  // inputs and outputs are the previous kernels' from here on
+    const int n_units = prefill_units<VL>(p);
 
     // Register split: 3 x 128 threads launched at 168 registers each
     // (64512); the first warpgroup drops to 80 and the softmax warpgroups
@@ -163,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ring = base + (kq ? SL::kK : SL::kV);
             uint32_t g = 0, uc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
-                const Unit x = unit_geom<KT>(u, p);
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+                const Unit x = unit_geom<KT, VL>(u, p, n_units);
                 if (kq) {
                     const uint32_t qb = uc & 1;
                     ok = mbar_wait(bar(SL::kQEmpty + qb), ((uc >> 1) & 1) ^ 1, &g_prefill_error,
@@ -174,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int db = 0; db < D / 64; ++db)
                         tma_load_4d(base + SL::kQ + qb * SL::kQTile + db * SL::kQRegion, &maps.q,
-                                    bar(SL::kQFull + qb), db * 64, x.kvh * p.G, x.t0 - p.q_off,
-                                    x.b);
+                                    bar(SL::kQFull + qb), db * 64, x.kvh * p.G,
+                                    x.r0 + x.t0 - p.q_off, x.b);
                 }
                 for (int j = 0; j < x.n_tiles; ++j, ++g) {
                     const uint32_t slot = g % ns;
@@ -190,10 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int db = 0; db < D / 64; ++db) {
                         const uint32_t dst = dst0 + db * SL::kKRegion;
                         if (j == 0 && p.s_pad > 0) {
-                            tma_load_4d(dst, m_sink, fb, db * 64, x.kvh, 0, x.b);
-                            tma_load_4d(dst + p.s_pad * 128, m_band0, fb, db * 64, x.kvh, x.lo, x.b);
+                            tma_load_4d(dst, m_sink, fb, db * 64, x.kvh, x.r0, x.b);
+                            tma_load_4d(dst + p.s_pad * 128, m_band0, fb, db * 64, x.kvh,
+                                        x.r0 + x.lo, x.b);
                         } else {
-                            tma_load_4d(dst, m_band, fb, db * 64, x.kvh, key0, x.b);
+                            tma_load_4d(dst, m_band, fb, db * 64, x.kvh, x.r0 + key0, x.b);
                         }
                     }
                 }
@@ -250,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
 
-            for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
-                const Unit x = unit_geom<KT>(u, p);
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+                const Unit x = unit_geom<KT, VL>(u, p, n_units);
                 const uint32_t qb = uc & 1;
                 ok = mbar_wait(bar(SL::kQFull + qb), (uc >> 1) & 1, &g_prefill_error, abort_flag);
                 if (!ok) break;
@@ -299,27 +301,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     mbar_wait(bar(SL::kPVDone), last_pv_g & 1, &g_prefill_error, &no_abort);
             }
-        } else if (kStageOut && warp == 3 && lane == 0) {
+        } else if (kStageOut && warp == 3) {
             // -------------------------------------------------------- output stores
             // For each unit in the softmax warps' order: once they have staged
             // its O tile, store it with TMA, wait until the store has read the
-            // buffer and hand the buffer back.
+            // buffer and hand the buffer back.  A varlen unit at the end of
+            // its sequence is copied row by row instead (its box would reach
+            // into the next sequence's rows).
             uint32_t e = 0;
-            for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++e) {
-                const Unit x = unit_geom<KT>(u, p);
-                const bool staged =
-                    mbar_wait(bar(SL::kOStaged), e & 1, &g_prefill_error, abort_flag);
-                if (staged && !*abort_flag) {
+            for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++e) {
+                const Unit x = unit_geom<KT, VL>(u, p, n_units);
+                bool staged = false;
+                if (lane == 0)
+                    staged = mbar_wait(bar(SL::kOStaged), e & 1, &g_prefill_error, abort_flag) &&
+                             !*abort_flag;
+                staged = __shfl_sync(0xffffffffu, staged ? 1 : 0, 0) != 0;
+                const int nrows = (x.t1 - x.t0 + 1) << p.g_log2;  // valid MMA rows
+                if (staged && (!VL || nrows >= 128)) {
+                    if (lane == 0) {
 #pragma unroll
-                    for (int db = 0; db < D / 64; ++db)
-                        tma_store_4d(&maps.o, base + SL::kStageO + db * (128 * 128), db * 64,
-                                     x.kvh * p.G, x.t0 - p.q_off, x.b);
-                    tma_store_commit();
-                    tma_store_wait_read_all();
+                        for (int db = 0; db < D / 64; ++db)
+                            tma_store_4d(&maps.o, base + SL::kStageO + db * (128 * 128), db * 64,
+                                         x.kvh * p.G, x.r0 + x.t0 - p.q_off, x.b);
+                        tma_store_commit();
+                        tma_store_wait_read_all();
+                    }
+                } else if (VL && staged) {
+                    constexpr int kChunks = D / 8;  // 16-byte chunks of a row
+                    for (int c = lane; c < nrows * kChunks; c += 32) {
+                        const int r = c / kChunks, col = (c % kChunks) * 8;
+                        const int ci = (col & 63) >> 3;
+                        const uint32_t src = base + SL::kStageO + (col >> 6) * (128 * 128) + r * 128 +
+                                             ((ci ^ (r & 7)) << 4);
+                        uint4 v4;
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(v4.x), "=r"(v4.y), "=r"(v4.z), "=r"(v4.w)
+                                     : "r"(src));
+                        const int64_t grow = x.r0 + x.t0 + (r >> p.g_log2) - p.q_off;
+                        *reinterpret_cast<uint4 *>(
+                            p.o + (grow * p.Hq + x.kvh * p.G + (r & (p.G - 1))) * D + col) = v4;
+                    }
                 }
-                mbar_arrive(bar(SL::kOFree));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(SL::kOFree));
             }
-            tma_store_wait_all();  // the stores are complete before the CTA exits
+            if (lane == 0) tma_store_wait_all();  // the stores are complete before the CTA exits
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
@@ -340,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // weights are computed while the previous unit's last P V runs, and
         // O is read out just before the new P is written.
         bool pend = false, pend_valid = false;
-        int pend_b = 0, pend_kvh = 0, pend_t = 0, pend_t0 = 0, pend_t1 = 0;
+        int pend_b = 0, pend_kvh = 0, pend_t = 0, pend_t0 = 0, pend_t1 = 0, pend_r0 = 0;
         float pend_m = 0.f, pend_l = 0.f;
         uint32_t ep = 0;  // staged epilogues so far
         auto epilogue = [&](float l_tot, uint32_t ob) {
@@ -382,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ep;
                 if (p.lse != nullptr && ok && pend_valid && half == 0) {
                     const int h = pend_kvh * p.G + hrow;
-                    p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_t - p.q_off)] =
+                    p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_r0 + pend_t - p.q_off)] =
                         pend_m * p.scale + logf(l_tot);
                 }
                 return;
@@ -436,19 +462,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tv = pend_t0 + (rr >> p.g_log2);
                 if (ok && tv <= pend_t1)
                     *reinterpret_cast<uint4 *>(
-                        p.o + ((static_cast<int64_t>(pend_b) * p.L + (tv - p.q_off)) * p.Hq + pend_kvh * p.G +
+                        p.o + ((static_cast<int64_t>(pend_b) * p.L + (pend_r0 + tv - p.q_off)) * p.Hq + pend_kvh * p.G +
                                (rr & (p.G - 1))) * D +
                         half * (D / 2) + cpos * 8) = ch[v];
             }
             if (p.lse != nullptr && ok && pend_valid && half == 0) {
                 const int h = pend_kvh * p.G + hrow;
-                p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_t - p.q_off)] =
+                p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_r0 + pend_t - p.q_off)] =
                     pend_m * p.scale + logf(l_tot);
             }
         };
 
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++uc) {
-            const Unit x = unit_geom<KT>(u, p);
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
+            const Unit x = unit_geom<KT, VL>(u, p, n_units);
             const int t = x.t0 + prow;
             const bool row_valid = (t <= x.t1);
             const int lo_t = p.w < 0 ? 0 : max(p.s, t - (p.w - p.s) + 1);
@@ -639,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pend = true;
             pend_valid = row_valid;
             pend_b = x.b;
+            pend_r0 = x.r0;
             pend_kvh = x.kvh;
             pend_t = t;
             pend_t0 = x.t0;
@@ -673,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 namespace {
 
-template <int D, int KT, int NSK, int NSV, int DT>
+template <int D, int KT, int NSK, int NSV, int DT, bool VL>
 swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaStream_t stream) {
     using SL = PrefillSmem<D, KT, NSK, NSV>;
     static_assert(SL::kAlloc <= 232448, "shared memory per CTA");
@@ -682,7 +709,7 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     static bool configured[64] = {};
     if (dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(swa_prefill_kernel<D, KT, NSK, NSV, DT>,
+        e = cudaFuncSetAttribute(swa_prefill_kernel<D, KT, NSK, NSV, DT, VL>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
         configured[dev] = true;
@@ -690,7 +717,7 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
     const int sms = device_sm_count();
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const int grid = p.n_units < sms ? p.n_units : sms;
-    e = launch_pdl(swa_prefill_kernel<D, KT, NSK, NSV, DT>, dim3(grid), dim3(kThreads), SL::kAlloc,
+    e = launch_pdl(swa_prefill_kernel<D, KT, NSK, NSV, DT, VL>, dim3(grid), dim3(kThreads), SL::kAlloc,
                    stream, maps, p);
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_prefill_kernel");
 }
@@ -717,30 +744,144 @@ int prefill_key_tile(const PrefillParams &p, int d) {
 
 namespace {
 
-template <int DT>
+template <int DT, bool VL>
 swa_status launch_prefill_dt(const PrefillMaps &maps, const PrefillParams &p, int d, int kt,
                              cudaStream_t stream) {
     if (d == 128)
-        return kt == 256 ? launch_prefill<128, 256, 1, 1, DT>(maps, p, stream)
-                         : launch_prefill<128, 112, 2, 2, DT>(maps, p, stream);
-    return kt == 256 ? launch_prefill<64, 256, 2, 2, DT>(maps, p, stream)
-                     : launch_prefill<64, 128, 4, 4, DT>(maps, p, stream);
+        return kt == 256 ? launch_prefill<128, 256, 1, 1, DT, VL>(maps, p, stream)
+                         : launch_prefill<128, 112, 2, 2, DT, VL>(maps, p, stream);
+    return kt == 256 ? launch_prefill<64, 256, 2, 2, DT, VL>(maps, p, stream)
+                     : launch_prefill<64, 128, 4, 4, DT, VL>(maps, p, stream);
 }
 
 }  // namespace
+
+namespace {
+
+// The widths that have a kernel: 112 or 256 at d = 128, 128 or 256 at d = 64.
+int kernel_key_tile(const PrefillParams &p, int d) {
+    const int kt = prefill_key_tile(p, d);
+    return kt == 256 ? 256 : (d == 128 ? 112 : 128);
+}
+
+// ---------------------------------------------------------------------------
+// varlen planning: one CTA checks cu_seqlens and writes the query-tile records
+// ---------------------------------------------------------------------------
+// tile_off[b] = query tiles of sequences 0..b-1 (tile_off[B]: all of them, or
+// 0 when cu_seqlens is not a valid partition of [0, total) or the tiles
+// exceed tiles_max, which also records SWA_ERR_BOUNDS); tile_rec[T] =
+// {b, tile index in b, first row of b, length of b}.
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) swa_varlen_plan_kernel(
+    const int *cu, int B, int total, int P, int tiles_max, int *tile_off, int4 *tile_rec) {
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ int s_warp[kPlanThreads / 32];
+    __shared__ int s_carry, s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) {
+        s_carry = 0;
+        s_bad = (cu[0] != 0 || cu[B] != total) ? 1 : 0;
+    }
+    __syncthreads();
+    for (int b0 = 0; b0 < B; b0 += kPlanThreads) {
+        const int b = b0 + tid;
+        int tiles = 0;
+        if (b < B) {
+            const int len = cu[b + 1] - cu[b];
+            if (len < 0) s_bad = 1;
+            tiles = len > 0 ? (len + P - 1) / P : 0;
+        }
+        // inclusive scan of tiles over the block: within warps, then of warp sums
+        int incl = tiles;
+#pragma unroll
+        for (int dd = 1; dd < 32; dd <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, dd);
+            if (lane >= dd) incl += y;
+        }
+        if (lane == 31) s_warp[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int ws = s_warp[lane];
+#pragma unroll
+            for (int dd = 1; dd < 32; dd <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ws, dd);
+                if (lane >= dd) ws += y;
+            }
+            s_warp[lane] = ws;  // inclusive warp prefix
+        }
+        __syncthreads();
+        const int before = s_carry + (wid > 0 ? s_warp[wid - 1] : 0) + incl - tiles;
+        if (b < B) tile_off[b] = before;
+        __syncthreads();
+        if (tid == kPlanThreads - 1) s_carry = before + tiles;
+        __syncthreads();
+    }
+    const bool ok = !s_bad && s_carry <= tiles_max;
+    if (tid == 0) {
+        tile_off[B] = ok ? s_carry : 0;
+        if (!ok) atomicCAS(&g_prefill_error, 0, kErrBounds);
+    }
+    if (!ok) return;
+    __syncthreads();  // tile_off is written (global memory, same CTA)
+    // one warp per sequence writes its records
+    for (int b = wid; b < B; b += kPlanThreads / 32) {
+        const int off = tile_off[b], row0 = cu[b], len = cu[b + 1] - row0;
+        const int tiles = len > 0 ? (len + P - 1) / P : 0;
+        for (int qt = lane; qt < tiles; qt += 32) tile_rec[off + qt] = make_int4(b, qt, row0, len);
+    }
+}
+
+}  // namespace
+
+size_t varlen_workspace_bytes(int B, int total, int Hq, int Hkv) {
+    if (B < 1 || total < 0 || Hkv < 1 || Hq < Hkv) return 0;
+    const int P = 128 / (Hq / Hkv);
+    const size_t off_bytes = (static_cast<size_t>(B) + 1) * 4;
+    const size_t tiles_max = static_cast<size_t>(B) + (static_cast<size_t>(total) + P - 1) / P;
+    return ((off_bytes + 15) & ~static_cast<size_t>(15)) + tiles_max * 16;
+}
+
+swa_status prefill_varlen_launch(const void *q, const void *k, const void *v, void *o, float *lse,
+                                 const int32_t *cu_seqlens, int B, int total, int max_len, int Hq,
+                                 int Hkv, int d, int w, int s, int dtype, void *workspace,
+                                 cudaStream_t stream) {
+    PrefillParams p = make_prefill_params(o, lse, 1, total, Hq, Hkv, d, w, s, 0, total);
+    const size_t off_bytes = ((static_cast<size_t>(B) + 1) * 4 + 15) & ~static_cast<size_t>(15);
+    int *tile_off = static_cast<int *>(workspace);
+    int4 *tile_rec = reinterpret_cast<int4 *>(static_cast<char *>(workspace) + off_bytes);
+    const int tiles_max = B + (total + p.P - 1) / p.P;
+    p.varlen = 1;
+    p.tile_count = tile_off + B;
+    p.tile_rec = tile_rec;
+    p.n_units = tiles_max * Hkv;  // an upper bound, for the grid
+    p.n_qtiles = 0;
+    cudaError_t e = launch_pdl(swa_varlen_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream,
+                               reinterpret_cast<const int *>(cu_seqlens), B, total, p.P, tiles_max,
+                               tile_off, tile_rec);
+    if (e != cudaSuccess) return cuda_fail(e, "launch swa_varlen_plan_kernel");
+    // key tile width from the widest unit (max_len bounds it for w = infinity)
+    PrefillParams span = p;
+    span.Lk = max_len;
+    const int kt = kernel_key_tile(span, d);
+    PrefillMaps maps;
+    if (!encode_prefill_maps(&maps, q, k, v, p, d, kt, dtype, 0))
+        return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    return dtype == SWA_F16 ? launch_prefill_dt<kF16, true>(maps, p, d, kt, stream)
+                            : launch_prefill_dt<kBf16, true>(maps, p, d, kt, stream);
+}
 
 swa_status prefill_launch_offset(const void *q, const void *k, const void *v, void *o, float *lse,
                                  int B, int L, int Hq, int Hkv, int d, int w, int s, int q_off,
                                  int Lk, int kv_cap, int dtype, cudaStream_t stream) {
     const PrefillParams p = make_prefill_params(o, lse, B, L, Hq, Hkv, d, w, s, q_off, Lk);
-    // the widths that have a kernel: 112 or 256 at d = 128, 128 or 256 at d = 64
-    int kt = prefill_key_tile(p, d);
-    if (kt != 256) kt = (d == 128) ? 112 : 128;
+    const int kt = kernel_key_tile(p, d);
     PrefillMaps maps;
     if (!encode_prefill_maps(&maps, q, k, v, p, d, kt, dtype, kv_cap))
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    return dtype == SWA_F16 ? launch_prefill_dt<kF16>(maps, p, d, kt, stream)
-                            : launch_prefill_dt<kBf16>(maps, p, d, kt, stream);
+    return dtype == SWA_F16 ? launch_prefill_dt<kF16, false>(maps, p, d, kt, stream)
+                            : launch_prefill_dt<kBf16, false>(maps, p, d, kt, stream);
 }
 
 swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, float *lse, int B,

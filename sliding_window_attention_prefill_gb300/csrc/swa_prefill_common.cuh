@@ -1,6 +1,6 @@
-// swa_prefill_common.cuh -- work decomposition shared by the two prefill
-// kernels (swa_prefill.cu: one query tile at a time, 256-column key tiles;
-// swa_prefill_pp.cu: two query tiles in flight, 128-column key tiles).
+// swa_prefill_common.cuh -- work decomposition of the prefill kernel
+// (swa_prefill.cu): work units, their key columns and key tiles, and the
+// tensor maps.
 //
 // A work unit is (sequence b, key/value head kvh, query tile).  Its 128 MMA
 // rows pack the G = Hq/Hkv query heads that share kvh for P = 128/G
@@ -12,6 +12,12 @@
 // its key columns are laid out as [s_pad sink rows | band ...] and cut into
 // key tiles of KT columns, the sink block (s rounded up to 8 rows, so that the
 // band starts on a 1024-byte swizzle atom) sharing the first tile.
+//
+// Variable-length batches (varlen): the sequences are packed one after the
+// other in [1, total, heads, d] tensors; sequence b holds rows
+// cu_seqlens[b] .. cu_seqlens[b+1]-1.  A small planning kernel writes one
+// record per query tile ({b, tile index, first row, length}); unit u is
+// (tile record, kv head) and its TMA coordinates add the first row.
 #pragma once
 
 #include <cuda.h>
@@ -63,22 +69,51 @@ struct PrefillParams {
     float scale;              // 1 / sqrt(d)
     uint16_t *o;              // [B, L, Hq, d] bf16 or fp16
     float *lse;               // optional [B, Hq, L]
+    // varlen: B sequences packed in L rows; the planning kernel's output
+    int varlen;
+    const int *tile_count;    // number of query tiles (0 if cu_seqlens is invalid)
+    const int4 *tile_rec;     // per query tile: {b, tile index, first row, length}
 };
 
+// A work unit.  b is the batch coordinate of the tensor maps and r0 the row
+// of position 0 of the unit's sequence (0 unless varlen, where b is 0).
 struct Unit {
-    int b, kvh, t0, t1, lo, n_cols, n_tiles;
+    int b, kvh, t0, t1, lo, n_cols, n_tiles, r0;
 };
 
-// Geometry of work unit u.  Units run heaviest query tiles first (only
-// matters for the infinite window, where cost grows with the position).
-template <int KT>
-__device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p) {
+// Work units of the call (read from the planning kernel's output for varlen).
+template <bool VL>
+__device__ __forceinline__ int prefill_units(const PrefillParams &p) {
+    if constexpr (VL) return *p.tile_count * p.Hkv;
+    return p.n_units;
+}
+
+// Geometry of work unit u of n_units.  Units run heaviest query tiles first
+// (only matters for the infinite window, where cost grows with the position);
+// varlen units run in reverse order of their tile records.
+template <int KT, bool VL>
+__device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p, int n_units) {
+    Unit x;
+    if constexpr (VL) {
+        const int tr = fast_div(u, p.div_hkv);
+        x.kvh = u - tr * p.Hkv;
+        const int4 rec = p.tile_rec[fast_div(n_units, p.div_hkv) - 1 - tr];
+        x.b = 0;
+        x.r0 = rec.z;
+        x.t0 = rec.y * p.P;
+        x.t1 = min(x.t0 + p.P, rec.w) - 1;
+        x.lo = p.w < 0 ? 0 : max(p.s, x.t0 - (p.w - p.s) + 1);
+        const int nb = max(0, x.t1 - x.lo + 1);
+        x.n_cols = p.s_pad + nb;
+        x.n_tiles = (x.n_cols + KT - 1) / KT;
+        return x;
+    } else {
     const int bh = p.B * p.Hkv;
     const int qt_rev = fast_div(u, p.div_bh);
     const int r = u - qt_rev * bh;
-    Unit x;
     x.b = fast_div(r, p.div_hkv);
     x.kvh = r - x.b * p.Hkv;
+    x.r0 = 0;
     const int qt = p.n_qtiles - 1 - qt_rev;
     x.t0 = p.q_off + qt * p.P;                      // key-space positions
     x.t1 = min(x.t0 + p.P, p.q_off + p.L) - 1;
@@ -87,6 +122,7 @@ __device__ __forceinline__ Unit unit_geom(int u, const PrefillParams &p) {
     x.n_cols = p.s_pad + nb;
     x.n_tiles = (x.n_cols + KT - 1) / KT;
     return x;
+    }
 }
 
 // Key columns of tile j, rounded up to the MMA's N granularity of 16.

@@ -95,6 +95,12 @@ def _declare(L) -> None:
     L.swa_check_prefill_chunk.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, P(SwaCacheStruct), _c_int,
                                           _c_i64, _c_int, _c_p, _c_size]
     L.swa_check_prefill_chunk.restype = _c_int
+    L.swa_prefill_varlen_workspace_bytes.argtypes = [_c_int] * 4
+    L.swa_prefill_varlen_workspace_bytes.restype = _c_size
+    L.swa_prefill_varlen.argtypes = ([_c_p] * 6 + [_c_int] * 9 + [_c_p, _c_size, _c_p])
+    L.swa_prefill_varlen.restype = _c_int
+    L.swa_check_prefill_varlen.argtypes = ([_c_p] * 6 + [_c_int] * 9 + [_c_p, _c_size])
+    L.swa_check_prefill_varlen.restype = _c_int
 
 
 def lib():
@@ -176,6 +182,55 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: int,
     st = lib().swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, L, Hq, Hkv, d,
                               int(w), int(s), dt, _stream(q.device))
     _check(st, "swa_prefill_ex")
+    return (o, lse) if return_lse else o
+
+
+# ----------------------------------------------------------------------------- varlen prefill
+_varlen_workspaces: dict = {}
+
+
+def prefill_varlen_workspace_bytes(B: int, total: int, Hq: int, Hkv: int) -> int:
+    return int(lib().swa_prefill_varlen_workspace_bytes(B, total, Hq, Hkv))
+
+
+def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                   w: int, s: int, max_len: int | None = None, out: torch.Tensor | None = None,
+                   return_lse: bool = False, workspace: torch.Tensor | None = None):
+    """SWA(w,s) prefill of a ragged batch packed along the first dimension.
+
+    q [total, Hq, d], k/v [total, Hkv, d] CUDA tensors (bf16 or fp16);
+    cu_seqlens int32 CUDA tensor [B+1] (sequence b is rows cu_seqlens[b] ..
+    cu_seqlens[b+1]-1).  Returns o [total, Hq, d] (and lse [Hq, total] fp32
+    if ``return_lse``).  ``max_len`` bounds the sequence lengths (default:
+    total); it only picks the key tile width for w = W_INF.
+    """
+    if not isinstance(q, torch.Tensor):
+        raise TypeError("q must be a torch.Tensor")
+    dt = _dtype_code(q.dtype)
+    _need(q, "q", q.dtype), _need(k, "k", q.dtype), _need(v, "v", q.dtype)
+    _need(cu_seqlens, "cu_seqlens", torch.int32)
+    if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
+        raise ValueError(f"q must be [total, Hq, d] and k, v [total, Hkv, d]: {tuple(q.shape)}, {tuple(k.shape)}")
+    total, Hq, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    if B < 1:
+        raise ValueError("cu_seqlens needs at least two entries")
+    o = torch.empty_like(q) if out is None else out
+    _need(o, "out", q.dtype)
+    lse = torch.empty(Hq, total, dtype=torch.float32, device=q.device) if return_lse else None
+    nbytes = prefill_varlen_workspace_bytes(B, total, Hq, Hkv)
+    ws = workspace
+    if ws is None:
+        key = q.device
+        ws = _varlen_workspaces.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+            _varlen_workspaces[key] = ws
+    st = lib().swa_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), B,
+                                  total, int(max_len if max_len is not None else total), Hq, Hkv, d,
+                                  int(w), int(s), dt, _ptr(ws), ws.numel(), _stream(q.device))
+    _check(st, "swa_prefill_varlen")
     return (o, lse) if return_lse else o
 
 

@@ -151,3 +151,24 @@ def test_slot_map_matches_oracle(L):
             assert L.swa_cache_slot(p, w, s) == orc.cache_slot(p, w, s), (w, s, p)
     assert L.swa_cache_slot(-1, 64, 4) == -1
     assert L.swa_cache_slot(3, 4, 4) == -1
+
+
+def test_check_prefill_varlen(L):
+    c, wb = L.swa_check_prefill_varlen, L.swa_prefill_varlen_workspace_bytes
+    q, k, v, o, cu, ws = _p(1000), _p(2000), _p(3000), _p(4000), _p(5000), _p(20000)
+    # B=3 sequences, 1000 rows, Hq=32, Hkv=8 (G=4: 32 positions per tile)
+    need = wb(3, 1000, 32, 8)
+    assert need == 16 + 16 * (3 + (1000 + 31) // 32)
+    assert wb(0, 1000, 32, 8) == 0 and wb(3, 1000, 30, 8) == 0
+    args = (3, 1000, 600, 32, 8, 128, 64, 4, 0)
+    assert c(q, k, v, o, None, cu, *args, ws, need) == OK
+    assert c(q, k, v, o, None, cu, *args, ws, need - 16) == WORKSPACE
+    assert c(q, k, v, o, None, cu, *args, None, 0) == WORKSPACE
+    assert c(q, k, v, o, None, None, *args, ws, need) == INVALID
+    assert c(q, k, v, o, None, ctypes.c_void_p(FAKE * 5000 + 2), *args, ws, need) == ALIGN
+    assert c(q, k, v, o, None, cu, 0, 1000, 600, 32, 8, 128, 64, 4, 0, ws, need) == INVALID  # B
+    assert c(q, k, v, o, None, cu, 3, 1000, 600, 32, 8, 128, 64, 4, 2, ws, need) == INVALID  # dtype
+    assert c(q, k, v, o, None, cu, 3, 1000, 600, 32, 8, 96, 64, 4, 0, ws, need) == UNSUPPORTED  # d
+    assert c(q, k, v, o, None, cu, 3, 1000, 600, 32, 8, 128, 4, 4, 0, ws, need) == INVALID  # w <= s
+    assert c(q, k, v, q, None, cu, *args, ws, need) == INVALID                # o aliases q
+    assert c(q, k, v, o, None, cu, *args, _p(1000), need) == INVALID          # workspace aliases q
