@@ -118,6 +118,11 @@ class Oracle:
         L.oracle_swa_decode_cache.argtypes = ([_p, _p, _p, _p, _p] + [_i64] * 7
                                               + [_p, _p, _int, _int])
         L.oracle_swa_decode_cache.restype = _int
+        L.oracle_hybrid_decode.argtypes = ([_p, _p, _p, _p, _p, _p] + [_i64] * 8
+                                           + [_p, _p, _int, _int])
+        L.oracle_hybrid_decode.restype = _int
+        L.oracle_hybrid_state.argtypes = [_p, _p, _p, _p, _p] + [_i64] * 7 + [_p, _int, _int]
+        L.oracle_hybrid_state.restype = _int
         self.lib = L
 
     # -- set and slot definitions -------------------------------------------------
@@ -224,6 +229,50 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_swa_decode_cache rejected its arguments")
         return o
+
+
+    # -- hybrid window + linear attention -----------------------------------------
+    def hybrid_decode(self, q, k_hist, v_hist, W, pos, w: int, s: int,
+                      threads: int | None = None, dtype: str | None = None):
+        """q [B,Hq,d] at positions pos [B] over history k/v [B,P,Hkv,d] with the
+        feature weights W [Hkv,d,df] -> o [B,Hq,d] (softmax over A(t) plus the
+        linear part over the earlier positions outside it)."""
+        dt = dtype_code(q, dtype)
+        q, k_hist, v_hist = bits16(q), bits16(k_hist), bits16(v_hist)
+        W = np.ascontiguousarray(np.asarray(W, np.float64))
+        B, Hq, d = q.shape
+        P, Hkv = k_hist.shape[1], k_hist.shape[2]
+        df = W.shape[2]
+        pos = np.ascontiguousarray(np.asarray(pos, dtype=np.int64).reshape(B))
+        nt = self.threads(threads)
+        o = np.empty((B, Hq, d), np.float64)
+        wi = np.empty(nt * max(P, 1), np.int64)
+        ws = np.empty(nt * (max(P, 1) + 4 * df), np.float64)
+        rc = self.lib.oracle_hybrid_decode(_ptr(q), _ptr(k_hist), _ptr(v_hist), _ptr(W), _ptr(pos),
+                                           _ptr(o), B, P, Hq, Hkv, d, df, w, s, _ptr(wi), _ptr(ws),
+                                           nt, dt)
+        if rc != 0:
+            raise ValueError("oracle_hybrid_decode rejected its arguments")
+        return o
+
+    def hybrid_state(self, k_hist, v_hist, W, w: int, s: int, threads: int | None = None,
+                     dtype: str | None = None):
+        """Linear state after positions 0..P-1 of k/v [B,P,Hkv,d] were appended:
+        S [B,Hkv,2df,d] and z [B,Hkv,2df] (sums over the evicted positions)."""
+        dt = dtype_code(k_hist, dtype)
+        k_hist, v_hist = bits16(k_hist), bits16(v_hist)
+        W = np.ascontiguousarray(np.asarray(W, np.float64))
+        B, P, Hkv, d = k_hist.shape
+        df = W.shape[2]
+        nt = self.threads(threads)
+        S = np.empty((B, Hkv, 2 * df, d), np.float64)
+        z = np.empty((B, Hkv, 2 * df), np.float64)
+        ws = np.empty(nt * 2 * df, np.float64)
+        rc = self.lib.oracle_hybrid_state(_ptr(k_hist), _ptr(v_hist), _ptr(W), _ptr(S), _ptr(z), B, P,
+                                          Hkv, d, df, w, s, _ptr(ws), nt, dt)
+        if rc != 0:
+            raise ValueError("oracle_hybrid_state rejected its arguments")
+        return S, z
 
 
 _default: Oracle | None = None

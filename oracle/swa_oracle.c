@@ -361,3 +361,147 @@ int oracle_swa_decode_cache(const uint16_t *q, const uint16_t *cache_k, const ui
     }
     return 0;
 }
+
+
+/*
+ * Hybrid window + linear attention (LoLCATs-style; NEXT of the scope).
+ *
+ * Linear attention -- "Sliding-window beats linear attention" (paper summary
+ * page), section "Prerequisites / Linear attention": a feature map phi
+ * replaces exp(q k^T) by phi(q) phi(k)^T, and the output of query t is
+ * phi(q_t) s_t / (phi(q_t) z_t) with s_t = sum_i phi(k_i)^T v_i and
+ * z_t = sum_i phi(k_i)^T.  Feature map -- same page, section "Post-training
+ * linearisation and LoLCATs": the Hedgehog map phi(x) = (exp(f(x)),
+ * exp(-f(x))), mixed with a sliding window.
+ *
+ * Readings (the pages give no formula for the mixture): f(x) = x W with W a
+ * d x df matrix per key/value head (synthetic: an input, no training), so
+ * phi(x) has F = 2 df features; the softmax part covers the attended set
+ * A(t) of SWA(w,s) and the linear part every earlier position outside it
+ * (the tokens the fixed cache has evicted), with one shared normaliser:
+ *
+ *   y_t = ( sum_{i in A(t)} exp(c q.k_i) v_i + sum_{i <= t, i not in A(t)} phi(q).phi(k_i) v_i )
+ *       / ( sum_{i in A(t)} exp(c q.k_i)     + sum_{i <= t, i not in A(t)} phi(q).phi(k_i) ).
+ *
+ * This is the direct sum; the library keeps the running state instead.
+ */
+
+/* phi(x) for one row x of d 16-bit values: out[0..df) = exp(f), out[df..2df) = exp(-f). */
+static void hedgehog_phi(const uint16_t *x, const double *W, int d, int df, widen_fn widen,
+                         double *out)
+{
+    for (int j = 0; j < df; ++j) {
+        double f = 0.0;
+        for (int c = 0; c < d; ++c) f += widen(x[c]) * W[(int64_t)c * df + j];
+        out[j] = exp(f);
+        out[df + j] = exp(-f);
+    }
+}
+
+/*
+ * Hybrid decode over the full history: q [B,Hq,d], k_hist/v_hist [B,P,Hkv,d]
+ * (16-bit patterns), W [Hkv,d,df] doubles, pos [B] (< P), o [B,Hq,d]
+ * doubles.  Work buffers: nthreads * (P + 2*F) doubles and nthreads * P
+ * indices.
+ */
+int oracle_hybrid_decode(const uint16_t *q, const uint16_t *k_hist, const uint16_t *v_hist,
+                         const double *W, const int64_t *pos, double *o, int64_t B, int64_t P,
+                         int64_t Hq, int64_t Hkv, int64_t d, int64_t df, int64_t w, int64_t s,
+                         int64_t *work_idx, double *work, int nthreads, int dtype)
+{
+    widen_fn widen = widen_for(dtype);
+    if (!widen || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || df <= 0) return -1;
+    if (w >= 0 && w <= s) return -1;
+    for (int64_t b = 0; b < B; ++b)
+        if (pos[b] < 0 || pos[b] >= P) return -1;
+    const int64_t G = Hq / Hkv, F = 2 * df;
+    const double scale = 1.0 / sqrt((double)d);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t r = 0; r < B * Hq; ++r) {
+#ifdef _OPENMP
+        int tid = omp_get_thread_num();
+#else
+        int tid = 0;
+#endif
+        const int64_t b = r / Hq, h = r % Hq, kvh = h / G, t = pos[b];
+        int64_t *idx = work_idx + (int64_t)tid * P;
+        double *score = work + (int64_t)tid * (P + 2 * F);
+        double *phq = score + P, *phk = phq + F;
+        const double *Wh = W + kvh * d * df;
+        const uint16_t *qrow = q + r * d;
+        const int64_t n = window_indices(t, w, s, idx);
+        /* softmax part over A(t), max-subtracted */
+        double m = -INFINITY;
+        for (int64_t i = 0; i < n; ++i) {
+            const uint16_t *kr = k_hist + ((b * P + idx[i]) * Hkv + kvh) * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += widen(qrow[c]) * widen(kr[c]);
+            score[i] = dot * scale;
+            if (score[i] > m) m = score[i];
+        }
+        double *out = o + r * d;
+        for (int c = 0; c < d; ++c) out[c] = 0.0;
+        double den = 0.0;
+        for (int64_t i = 0; i < n; ++i) {
+            const uint16_t *vr = v_hist + ((b * P + idx[i]) * Hkv + kvh) * d;
+            const double p = exp(score[i] - m);
+            den += p;
+            for (int c = 0; c < d; ++c) out[c] += p * widen(vr[c]);
+        }
+        /* linear part over the earlier positions outside A(t), scaled by e^-m */
+        hedgehog_phi(qrow, Wh, (int)d, (int)df, widen, phq);
+        const double em = exp(-m);
+        for (int64_t i = 0; i <= t; ++i) {
+            if (oracle_in_window(t, i, w, s)) continue;
+            const uint16_t *kr = k_hist + ((b * P + i) * Hkv + kvh) * d;
+            const uint16_t *vr = v_hist + ((b * P + i) * Hkv + kvh) * d;
+            hedgehog_phi(kr, Wh, (int)d, (int)df, widen, phk);
+            double wt = 0.0;
+            for (int64_t f = 0; f < F; ++f) wt += phq[f] * phk[f];
+            den += em * wt;
+            for (int c = 0; c < d; ++c) out[c] += em * wt * widen(vr[c]);
+        }
+        for (int c = 0; c < d; ++c) out[c] /= den;
+    }
+    return 0;
+}
+
+/*
+ * The linear state after positions 0 .. P-1 have been appended to an SWA(w,s)
+ * cache: S [B,Hkv,F,d] = sum over evicted positions i of phi(k_i)^T v_i and
+ * z [B,Hkv,F] = sum of phi(k_i), evicted = s <= i <= P-1-(w-s) (nothing for
+ * w = infinity).  k_hist/v_hist [B,P,Hkv,d] 16-bit patterns, W [Hkv,d,df].
+ */
+int oracle_hybrid_state(const uint16_t *k_hist, const uint16_t *v_hist, const double *W,
+                        double *S, double *z, int64_t B, int64_t P, int64_t Hkv, int64_t d,
+                        int64_t df, int64_t w, int64_t s, double *work, int nthreads, int dtype)
+{
+    widen_fn widen = widen_for(dtype);
+    if (!widen || Hkv <= 0 || d <= 0 || df <= 0) return -1;
+    if (w >= 0 && w <= s) return -1;
+    const int64_t F = 2 * df;
+    const int64_t last = w < 0 ? -1 : P - 1 - (w - s); /* last evicted position */
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+    for (int64_t r = 0; r < B * Hkv; ++r) {
+#ifdef _OPENMP
+        int tid = omp_get_thread_num();
+#else
+        int tid = 0;
+#endif
+        const int64_t b = r / Hkv, kvh = r % Hkv;
+        double *phk = work + (int64_t)tid * F;
+        double *Sr = S + r * F * d, *zr = z + r * F;
+        for (int64_t i = 0; i < F * d; ++i) Sr[i] = 0.0;
+        for (int64_t f = 0; f < F; ++f) zr[f] = 0.0;
+        for (int64_t i = s; i <= last; ++i) {
+            const uint16_t *kr = k_hist + ((b * P + i) * Hkv + kvh) * d;
+            const uint16_t *vr = v_hist + ((b * P + i) * Hkv + kvh) * d;
+            hedgehog_phi(kr, W + kvh * d * df, (int)d, (int)df, widen, phk);
+            for (int64_t f = 0; f < F; ++f) {
+                zr[f] += phk[f];
+                for (int c = 0; c < d; ++c) Sr[f * d + c] += phk[f] * widen(vr[c]);
+            }
+        }
+    }
+    return 0;
+}

@@ -15,6 +15,10 @@ What pins what:
   * fp16 inputs: every one of the 65536 binary16 bit patterns widened by the
     oracle equals numpy's float16 -> float64 conversion, and brute force on
     fp16 inputs (widened by numpy) matches every attention entry point;
+  * the hybrid window + linear decode: a numpy restatement of its definition
+    with dense masks, the no-eviction case (equal to SWA decode), W = 0 (a
+    closed form: every linear weight is the feature count), and the state
+    form (S, z) giving the same outputs as the direct sum;
   * closed forms: t = 0 gives v_0; q = 0 gives the plain mean of the attended
     values; two keys in d = 1 give a two-term weighted mean;
   * invariants: equal values give that value; permuting the history inside
@@ -351,7 +355,106 @@ def pin_f16_brute_force(orc) -> None:
         assert np.abs(oc - ref[:, t]).max() < 1e-12, ("decode_cache", B, L, w, s)
 
 
+def _hedgehog(x, W):
+    """phi(x) = (exp(xW), exp(-xW)) for rows x [..., d], W [d, df] (numpy)."""
+    f = x @ W
+    return np.concatenate([np.exp(f), np.exp(-f)], axis=-1)
+
+
+def _hybrid_dense(q, k, v, W, pos, w, s):
+    """Hybrid decode by dense masks in numpy: softmax weights exp(c q.k) on
+    A(t), linear weights phi(q).phi(k) on the earlier positions outside it,
+    one normaliser."""
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    B, Hq, d = qf.shape
+    Hkv = kf.shape[2]
+    G = Hq // Hkv
+    out = np.zeros_like(qf)
+    for b in range(B):
+        t = pos[b]
+        inside = np.zeros(t + 1, bool)
+        inside[_first_and_latest(t, w, s)] = True
+        for h in range(Hq):
+            kk, vv = kf[b, :t + 1, h // G], vf[b, :t + 1, h // G]
+            sc = kk @ qf[b, h] / math.sqrt(d)
+            m = sc[inside].max()
+            wt = np.where(inside, np.exp(sc - m),
+                          np.exp(-m) * (_hedgehog(kk, W[h // G]) @ _hedgehog(qf[b, h], W[h // G])))
+            out[b, h] = wt @ vv / wt.sum()
+    return out
+
+
+def pin_hybrid_dense(orc) -> None:
+    rng = np.random.default_rng(9)
+    for B, P, Hq, Hkv, d, df, w, s in [(2, 40, 4, 2, 8, 4, 8, 2), (1, 33, 2, 1, 16, 8, 12, 0),
+                                       (1, 25, 4, 4, 8, 2, 6, 5)]:
+        q = _rand_bits(rng, (B, Hq, d))
+        k = _rand_bits(rng, (B, P, Hkv, d))
+        v = _rand_bits(rng, (B, P, Hkv, d))
+        W = 0.2 * rng.standard_normal((Hkv, d, df))
+        pos = [P - 1 - 3 * b for b in range(B)]
+        got = orc.hybrid_decode(q, k, v, W, pos, w, s, threads=2)
+        ref = _hybrid_dense(q, k, v, W, pos, w, s)
+        assert np.abs(got - ref).max() < 1e-12, (B, P, w, s)
+
+
+def pin_hybrid_special_cases(orc) -> None:
+    rng = np.random.default_rng(10)
+    B, P, Hq, Hkv, d, df, w, s = 2, 50, 4, 2, 8, 4, 10, 3
+    q = _rand_bits(rng, (B, Hq, d))
+    k = _rand_bits(rng, (B, P, Hkv, d))
+    v = _rand_bits(rng, (B, P, Hkv, d))
+    W = 0.3 * rng.standard_normal((Hkv, d, df))
+    # nothing evicted yet (t < w): exactly the SWA decode
+    for t in (0, 4, w - 1):
+        a = orc.hybrid_decode(q, k, v, W, [t] * B, w, s, threads=1)
+        b = orc.decode(q, k, v, [t] * B, w, s, threads=1)
+        assert np.abs(a - b).max() < 1e-13, t
+    # W = 0: phi = all ones, every linear weight is F = 2 df (closed form)
+    t = P - 1
+    o = orc.hybrid_decode(q, k, v, np.zeros_like(W), [t] * B, w, s, threads=1)
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    inside = _first_and_latest(t, w, s)
+    outside = [i for i in range(t + 1) if i not in inside]
+    for bb in range(B):
+        for h in range(Hq):
+            sc = kf[bb, inside, h // 2] @ qf[bb, h] / math.sqrt(d)
+            e = np.exp(sc)
+            num = e @ vf[bb, inside, h // 2] + 2 * df * vf[bb, outside, h // 2].sum(axis=0)
+            den = e.sum() + 2 * df * len(outside)
+            assert np.abs(o[bb, h] - num / den).max() < 1e-12, (bb, h)
+
+
+def pin_hybrid_state(orc) -> None:
+    """The state (S, z) after a prefix reproduces the decode's linear part:
+    (window part + e^-m phi(q) S) / (... + e^-m phi(q).z) equals hybrid_decode."""
+    rng = np.random.default_rng(11)
+    B, P, Hq, Hkv, d, df, w, s = 2, 45, 4, 2, 8, 4, 9, 2
+    q = _rand_bits(rng, (B, Hq, d))
+    k = _rand_bits(rng, (B, P, Hkv, d))
+    v = _rand_bits(rng, (B, P, Hkv, d))
+    W = 0.25 * rng.standard_normal((Hkv, d, df))
+    S, z = orc.hybrid_state(k, v, W, w, s, threads=2)
+    t = P - 1
+    ref = orc.hybrid_decode(q, k, v, W, [t] * B, w, s, threads=2)
+    qf, kf, vf = bits_to_f64(q), bits_to_f64(k), bits_to_f64(v)
+    inside = _first_and_latest(t, w, s)
+    for bb in range(B):
+        for h in range(Hq):
+            g = h // 2
+            sc = kf[bb, inside, g] @ qf[bb, h] / math.sqrt(d)
+            m = sc.max()
+            e = np.exp(sc - m)
+            ph = _hedgehog(qf[bb, h], W[g])
+            num = e @ vf[bb, inside, g] + np.exp(-m) * (ph @ S[bb, g])
+            den = e.sum() + np.exp(-m) * (ph @ z[bb, g])
+            assert np.abs(num / den - ref[bb, h]).max() < 1e-12, (bb, h)
+    # infinite window: nothing is ever evicted
+    S0, z0 = orc.hybrid_state(k, v, W, W_INF, 0, threads=1)
+    assert not S0.any() and not z0.any()
+
+
 ALL_PINS = [pin_golden_sets, pin_window_size, pin_brute_force, pin_causal_library,
             pin_closed_forms, pin_equal_values, pin_decode_history, pin_golden_cache,
             pin_ring_mapping, pin_decode_cache, pin_rows_match_full, pin_f16_every_pattern,
-            pin_f16_brute_force]
+            pin_f16_brute_force, pin_hybrid_dense, pin_hybrid_special_cases, pin_hybrid_state]

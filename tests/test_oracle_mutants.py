@@ -43,6 +43,14 @@ MUTANTS = {
     # fp16 inputs widened as bf16
     "f16_as_bf16": ("if (dtype == ORACLE_F16) return f16_bits_to_double;",
                     "if (dtype == ORACLE_F16) return bf16_bits_to_double;"),
+    # hybrid: the second half of the feature map with the wrong sign
+    "phi_sign": ("out[df + j] = exp(-f);", "out[df + j] = exp(f);"),
+    # hybrid: the linear part not brought to the softmax part's scale
+    "linear_unscaled": ("const double em = exp(-m);", "const double em = 1.0;"),
+    # hybrid: the last evicted position left out of the state
+    "state_off_by_one": ("for (int64_t i = s; i <= last; ++i) {", "for (int64_t i = s; i < last; ++i) {"),
+    # hybrid: W read transposed
+    "w_transposed": ("f += widen(x[c]) * W[(int64_t)c * df + j];", "f += widen(x[c]) * W[(int64_t)j * d + c];"),
 }
 
 CHILD = r"""
