@@ -715,7 +715,7 @@ def context_points(batches=(1, 256), Hkv: int = 8, d: int = 128):
     return pts, skipped
 
 
-def suite_context(steps: int, batches=(1, 256), shape: str = "llama"):
+def suite_context(steps: int, batches=(1, 256), shape: str = "llama", hybrid: bool = False):
     """Decode context sweep through a stack of 4 attention layers: the Llama
     shape (Hq=32, Hkv=8, d=128, bf16) or the pages' system-test shape
     (Hq=Hkv=16, d=64, fp16), N(0,1) values.  For each window w in
@@ -725,7 +725,11 @@ def suite_context(steps: int, batches=(1, 256), shape: str = "llama"):
     N(0,1) value), and one step appends token P and decodes it in each of the
     4 layers.  Prints tok/s, the decode kernel's KV read rate and the cache
     bytes held.  Points whose caches exceed 160 GiB are skipped (an infinite
-    window at batch 256 beyond 32768 positions) and listed."""
+    window at batch 256 beyond 32768 positions) and listed.  With ``hybrid``
+    the layers are instead the LoLCATs-style mixture the pages compare
+    against: a 256-token window without sinks plus a linear-attention state
+    of the evicted tokens (df = d/2 Hedgehog features per half), each step
+    a hybrid append and a hybrid decode."""
     import torch
 
     import sliding_window_attention_prefill_gb300 as swa
@@ -738,42 +742,61 @@ def suite_context(steps: int, batches=(1, 256), shape: str = "llama"):
     dt = torch.float16 if sh["dtype"] == "f16" else torch.bfloat16
     gen = torch.Generator(device="cuda")
     pts, skipped = context_points(batches, Hkv, d)
+    if hybrid:
+        pts = [(B, 256, P) for B in batches for P in CONTEXT_POSITIONS]
+        skipped = []
+    df = d // 2
     for B, w, P in pts:
         gen.manual_seed(B * 1000003 + P * 7 + (w + 1))
         layers = []
         for _ in range(CONTEXT_LAYERS):
-            c = swa.Cache(B, Hkv, d, w, s if w > 0 else 0, max_len=(P + 1 if w < 0 else None),
-                          dtype=dt)
+            c = swa.Cache(B, Hkv, d, w, (s if w > 0 else 0) if not hybrid else 0,
+                          max_len=(P + 1 if w < 0 else None), dtype=dt)
             c.k.normal_(generator=gen)
             c.v.normal_(generator=gen)
             kn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(dt)
             vn = torch.randn(B, 1, Hkv, d, generator=gen, device="cuda").to(dt)
             q = torch.randn(B, Hq, d, generator=gen, device="cuda").to(dt)
-            layers.append((c, kn, vn, q, torch.empty_like(q), swa.workspace_for(c, Hq)))
+            st = None
+            if hybrid:
+                Wf = torch.randn(Hkv, d, df, generator=gen, device="cuda") * (0.3 / d ** 0.5)
+                st = swa.LinearState(c, Wf)
+            layers.append((c, kn, vn, q, torch.empty_like(q), swa.workspace_for(c, Hq), st))
         pos = torch.full((B,), P, dtype=torch.int32, device="cuda")
 
         def step():
-            for c, kn, vn, q, o, ws in layers:
-                c.append(kn, vn, P)
-                swa.decode(q, c, pos, out=o, workspace=ws)
+            for c, kn, vn, q, o, ws, st in layers:
+                if hybrid:
+                    swa.hybrid_append(c, st, kn, vn, P)
+                    swa.hybrid_decode(q, c, st, pos, out=o)
+                else:
+                    c.append(kn, vn, P)
+                    swa.decode(q, c, pos, out=o, workspace=ws)
 
         def decode_only():
-            for c, kn, vn, q, o, ws in layers:
-                swa.decode(q, c, pos, out=o, workspace=ws)
+            for c, kn, vn, q, o, ws, st in layers:
+                if hybrid:
+                    swa.hybrid_decode(q, c, st, pos, out=o)
+                else:
+                    swa.decode(q, c, pos, out=o, workspace=ws)
 
         ms = _time_graph(step, steps, flush)
         ms_dec = _time_graph(decode_only, steps, flush)
         n_valid = P + 1 if w < 0 else min(P + 1, w)
         kv = CONTEXT_LAYERS * 2 * B * Hkv * d * 2 * n_valid
         by = CONTEXT_LAYERS * decode_bytes(B, Hq, Hkv, d, n_valid)
+        if hybrid:  # the state S, z of every (sequence, kv head) is read too
+            by += CONTEXT_LAYERS * B * Hkv * (2 * df) * (d + 1) * 4
         cap = layers[0][0].cap
-        print(json.dumps({"suite": "context", "shape": shape, "dtype": sh["dtype"], "Hq": Hq,
+        state_bytes = CONTEXT_LAYERS * B * Hkv * (2 * df) * (d + 1) * 4 if hybrid else 0
+        print(json.dumps({"suite": "context", "mode": "hybrid" if hybrid else "swa",
+                          "shape": shape, "dtype": sh["dtype"], "Hq": Hq,
                           "Hkv": Hkv, "d": d, "B": B, "w": w if w > 0 else "inf",
                           "s": s if w > 0 else 0, "pos": P, "layers": CONTEXT_LAYERS,
                           "ms_step": ms, "tok_s": B / (ms * 1e-3), "ms_decode": ms_dec,
                           "kv_read_gbs": kv / (ms_dec * 1e-3) / 1e9,
                           "frac_hbm": by / (ms_dec * 1e-3) / 1e9 / pk["hbm_gbs"],
-                          "cache_bytes_held": context_cache_bytes(B, Hkv, d, cap),
+                          "cache_bytes_held": context_cache_bytes(B, Hkv, d, cap) + state_bytes,
                           "cache_bytes_read": kv}), flush=True)
         del layers, step, decode_only
         torch.cuda.empty_cache()
@@ -796,6 +819,8 @@ def main():
     ap.add_argument("--L", type=int, default=None, help="prefill suite: length override")
     ap.add_argument("--decode-steps", type=int, default=1024, help="decode suite: steps")
     ap.add_argument("--batches", type=str, default="1,256", help="context suite: batch sizes")
+    ap.add_argument("--hybrid", action="store_true",
+                    help="context suite: the window + linear mixture instead of SWA(w,4)")
     ap.add_argument("--shape", choices=sorted(CONTEXT_SHAPES), default="llama",
                     help="context suite: attention shape (llama: 32/8 heads of 128, bf16; "
                          "paper: 16 heads of 64, fp16)")
@@ -814,7 +839,7 @@ def main():
         return
     if args.suite == "context":
         suite_context(max(min(args.steps // 40, 20), 5),
-                      tuple(int(b) for b in args.batches.split(",")), args.shape)
+                      tuple(int(b) for b in args.batches.split(",")), args.shape, args.hybrid)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

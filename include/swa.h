@@ -308,6 +308,53 @@ swa_status swa_check_prefill_varlen(const void *q, const void *k, const void *v,
                                     size_t workspace_bytes);
 
 /*
+ * Hybrid window + linear attention (the LoLCATs-style mixture the pages
+ * compare SWA(w,s) against: "Sliding-window beats linear attention", paper
+ * summary page, sections "Prerequisites / Linear attention" and
+ * "Post-training linearisation and LoLCATs").  The cache keeps the attended
+ * set A(t) as for SWA(w,s); every token the cache evicts is folded into a
+ * linear-attention state instead of being dropped, and decode mixes both:
+ *
+ *   y_t = ( sum_{i in A(t)} exp(c q.k_i) v_i + phi(q) S ) / ( sum_{i in A(t)} exp(c q.k_i) + phi(q).z )
+ *
+ * with S = sum of phi(k_i)^T v_i and z = sum of phi(k_i) over the evicted
+ * positions (i <= t, i not in A(t)), and the Hedgehog feature map
+ * phi(x) = (exp(x W), exp(-x W)) of 2 df features, W a d x df matrix per
+ * key/value head (an input: the pages train it, this library takes it as
+ * given).  The linear state of one layer:
+ */
+typedef struct {
+    float *S;        /* [B, Hkv, 2*df, d] fp32, device, caller-owned; zero before the first token */
+    float *z;        /* [B, Hkv, 2*df] fp32, device, caller-owned; zero before the first token */
+    const float *W;  /* [Hkv, d, df] fp32, device: f(x) = x W */
+    int32_t B, Hkv, d, df;  /* df in {32, 64}; B, Hkv, d equal to the cache's */
+} swa_linear_state;
+
+/*
+ * swa_hybrid_append -- swa_cache_append that first folds the positions the
+ * append evicts from the ring (from the cache, or from k_new/v_new when a
+ * bulk append evicts its own early tokens) into the state.  Appending a
+ * prompt of P tokens leaves S, z = the sums over positions s .. P-1-(w-s).
+ * Same arguments and codes as swa_cache_append; the state must match the
+ * cache (B, Hkv, d) and be 16-byte aligned.  Nothing is evicted for
+ * w = SWA_W_INF.
+ */
+swa_status swa_hybrid_append(const swa_cache *cache, const swa_linear_state *state,
+                             const void *k_new, const void *v_new, int n, int64_t pos0,
+                             swa_stream_t stream);
+
+/*
+ * swa_hybrid_decode -- swa_decode with the linear part of the evicted
+ * positions mixed in (the formula above).  Workspace:
+ * swa_hybrid_decode_workspace_bytes(...) bytes (never 0).  Same arguments and
+ * codes as swa_decode otherwise.
+ */
+size_t swa_hybrid_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, int w);
+swa_status swa_hybrid_decode(const void *q, const swa_cache *cache, const swa_linear_state *state,
+                             const int32_t *pos, int Hq, int w, int s, void *o, void *workspace,
+                             size_t workspace_bytes, swa_stream_t stream);
+
+/*
  * swa_selftest_wait_timeout -- enqueue a one-CTA kernel whose bounded wait
  * runs out on purpose: it waits on an mbarrier that nothing arrives on,
  * through the same bounded wait as every kernel of the library, holding a

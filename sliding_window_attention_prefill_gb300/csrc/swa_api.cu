@@ -379,6 +379,67 @@ swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos,
     return swa::decode_launch(q, *cache, pos, Hq, o, workspace, plan, as_cuda(stream));
 }
 
+namespace {
+
+// The linear state belongs to the cache: same B, Hkv, d; df in {32, 64};
+// 16-byte aligned buffers that overlap neither each other nor the cache.
+swa_status check_linear_state(const swa_linear_state *st, const swa_cache *c) {
+    if (st == nullptr) return SWA_ERR_INVALID_ARG;
+    if (st->B != c->B || st->Hkv != c->Hkv || st->d != c->d) return SWA_ERR_INVALID_ARG;
+    if (st->df != 32 && st->df != 64) return st->df < 1 ? SWA_ERR_INVALID_ARG : SWA_ERR_UNSUPPORTED;
+    if (c->B == 0) return SWA_OK;
+    if (!st->S || !st->z || !st->W) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(st->S) || !aligned16(st->z) || !aligned16(st->W)) return SWA_ERR_ALIGNMENT;
+    const size_t F = 2 * static_cast<size_t>(st->df);
+    const size_t sb = static_cast<size_t>(c->B) * c->Hkv * F * c->d * 4;
+    const size_t zb = static_cast<size_t>(c->B) * c->Hkv * F * 4;
+    const size_t wb = static_cast<size_t>(c->Hkv) * c->d * st->df * 4;
+    const size_t cb = static_cast<size_t>(c->B) * c->Hkv * c->cap * c->d * 2;
+    if (overlap(st->S, sb, st->z, zb) || overlap(st->S, sb, st->W, wb) ||
+        overlap(st->z, zb, st->W, wb) || overlap(st->S, sb, c->k, cb) ||
+        overlap(st->S, sb, c->v, cb) || overlap(st->z, zb, c->k, cb) || overlap(st->z, zb, c->v, cb))
+        return SWA_ERR_INVALID_ARG;
+    return SWA_OK;
+}
+
+}  // namespace
+
+swa_status swa_hybrid_append(const swa_cache *cache, const swa_linear_state *state,
+                             const void *k_new, const void *v_new, int n, int64_t pos0,
+                             swa_stream_t stream) {
+    swa_status st = swa_check_append(cache, k_new, v_new, n, pos0);
+    if (st != SWA_OK) return st;
+    st = check_linear_state(state, cache);
+    if (st != SWA_OK || n == 0 || cache->B == 0) return st;
+    bool appended = false;
+    st = swa::hybrid_fold_launch(*cache, *state, k_new, v_new, n, pos0, as_cuda(stream), &appended);
+    if (st != SWA_OK || appended) return st;
+    return swa::append_launch(*cache, k_new, v_new, n, pos0, as_cuda(stream));
+}
+
+size_t swa_hybrid_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, int w) {
+    if (B <= 0 || Hq < 1 || Hkv < 1 || cap < 1 || (d != 64 && d != 128)) return 0;
+    const swa::DecodePlan plan = swa::decode_plan(B, Hq, Hkv, d, cap, w, swa::device_sm_count());
+    return static_cast<size_t>(B) * Hq * plan.splits * (d + 2) * sizeof(float);
+}
+
+swa_status swa_hybrid_decode(const void *q, const swa_cache *cache, const swa_linear_state *state,
+                             const int32_t *pos, int Hq, int w, int s, void *o, void *workspace,
+                             size_t workspace_bytes, swa_stream_t stream) {
+    if (cache == nullptr) return SWA_ERR_INVALID_ARG;
+    const int sms = swa::device_sm_count();
+    if (sms <= 0) return swa::cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
+    const swa::DecodePlan plan =
+        swa::decode_plan(cache->B, Hq, cache->Hkv, cache->d, cache->cap, cache->w, sms);
+    const size_t need = static_cast<size_t>(cache->B) * Hq * plan.splits * (cache->d + 2) * 4;
+    swa_status st =
+        swa_check_decode(q, cache, pos, Hq, w, s, o, workspace, workspace_bytes, need);
+    if (st != SWA_OK) return st;
+    st = check_linear_state(state, cache);
+    if (st != SWA_OK || cache->B == 0) return st;
+    return swa::decode_launch(q, *cache, pos, Hq, o, workspace, plan, as_cuda(stream), state);
+}
+
 swa_status swa_selftest_wait_timeout(swa_stream_t stream) {
     return swa::selftest_wait_launch(as_cuda(stream));
 }

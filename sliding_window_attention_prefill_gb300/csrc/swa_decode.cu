@@ -69,6 +69,11 @@ struct DecodeParams {
     float *ws_ml;        // [B*Hq, splits, 2]
     int B, Hq, Hkv, cap, w, splits;
     float scale_log2;
+    // hybrid window + linear decode: partials even with one split, and the
+    // linear state the merge adds (S [B*Hkv, 2 df, D], z [B*Hkv, 2 df],
+    // feature weights W [Hkv, D, df])
+    int partials;
+    const float *S, *z, *W;
 };
 
 // ST: depth of the chunk ring (2 when items span several chunks; 1 when every
@@ -441,7 +446,7 @@ __global__ void __launch_bounds__(kDecThreads)
                 a = fmaf(wacc[(w * G + h) * D + e], f, a);
             }
             const int64_t orow = static_cast<int64_t>(x.b) * p.Hq + x.kvh * G + h;
-            if (p.splits == 1) {
+            if (p.splits == 1 && !p.partials) {
                 const float ov = l > 0.f ? a / l : 0.f;
                 p.o[orow * D + e] = round16<DT>(ov);
             } else {
@@ -493,6 +498,104 @@ __global__ void __launch_bounds__(128) swa_decode_merge_kernel(const DecodeParam
         p.o[static_cast<int64_t>(row) * D + lane * E + e] = round16<DT>(a[e] * inv);
 }
 
+// Hybrid window + linear decode, one CTA per (sequence, query head): the
+// softmax partials of the window splits merged with the linear part of the
+// evicted positions, phi(q) S and phi(q).z with phi(x) = (exp(xW), exp(-xW)),
+// over one normaliser.  In the merge the linear part is a partial with
+// m = 0 (in the base-2 exponent of the scores):
+//   M = max(m_1, .., m_n, 0), l = sum l_j 2^(m_j - M) + (phi(q).z) 2^-M,
+//   o = (sum acc_j 2^(m_j - M) + phi(q) S 2^-M) / l.
+// The state is read once with every load in flight at the same time: thread
+// t sums rows f = t / D (mod NT / D) of column t % D of S, and the row groups
+// are added in shared memory.
+constexpr int kHybThreads = 256;
+
+template <int D, int DF, int DT>
+__global__ void __launch_bounds__(kHybThreads) swa_hybrid_merge_kernel(const DecodeParams p) {
+    constexpr int F = 2 * DF, RG = kHybThreads / D, RPT = F / RG;  // row groups, rows per thread
+    constexpr int kPre = 8;  // window partials read ahead (more are read in a loop)
+    static_assert(F % RG == 0 && F <= kHybThreads, "row split");
+    __shared__ float s_phi[F];
+    __shared__ float s_b[RG][D];
+    __shared__ float s_z[F];
+    pdl_launch_dependents();
+    pdl_wait();  // the split kernel's partials
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int b = row / p.Hq, h = row - b * p.Hq;
+    const int kvh = h / (p.Hq / p.Hkv);
+    const int pos = p.pos[b];
+    if (pos < 0 || (p.w < 0 && pos >= p.cap)) return;  // recorded by the split kernel
+    const int64_t sr = static_cast<int64_t>(b) * p.Hkv + kvh;
+    const int c = tid % D, g = tid / D;
+    // Every global read is issued before any of them is used: the state rows
+    // of this thread, z, q . W for phi(q), and the window partials.
+    const float *Sc = p.S + sr * F * D + c;
+    float sreg[RPT];
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) sreg[i] = __ldg(Sc + static_cast<int64_t>(g + RG * i) * D);
+    float zv = tid < F ? __ldg(p.z + sr * F + tid) : 0.f;
+    float fx = 0.f;
+    if (tid < DF) {
+        const uint16_t *qrow = p.q + static_cast<int64_t>(row) * D;
+        const float *Wh = p.W + static_cast<int64_t>(kvh) * D * DF + tid;
+#pragma unroll
+        for (int cc = 0; cc < D; ++cc) fx = fmaf(widen16<DT>(__ldg(qrow + cc)), __ldg(Wh + cc * DF), fx);
+    }
+    const int cap_eff = p.w < 0 ? p.cap : p.w;
+    const int n_valid = min(pos + 1, cap_eff);
+    int begin, end, used;
+    split_range(p.w >= 0 ? p.w : n_valid, p.splits, 0, begin, end, used);
+    float pm[kPre], pl[kPre], pa[kPre];
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+        const int64_t base = static_cast<int64_t>(row) * p.splits + j;
+        const bool have = j < used && tid < D;
+        pm[j] = have ? p.ws_ml[base * 2] : -INFINITY;
+        pl[j] = have ? p.ws_ml[base * 2 + 1] : 0.f;
+        pa[j] = have ? p.ws_acc[base * D + c] : 0.f;
+    }
+    if (tid < DF) {
+        s_phi[tid] = expf(fx);
+        s_phi[DF + tid] = expf(-fx);
+    }
+    if (tid < F) s_z[tid] = zv;
+    __syncthreads();
+    float acc_b = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) acc_b = fmaf(s_phi[g + RG * i], sreg[i], acc_b);
+    s_b[g][c] = acc_b;
+    __syncthreads();
+    if (tid >= D) return;
+    float bl = 0.f;
+#pragma unroll
+    for (int gg = 0; gg < RG; ++gg) bl += s_b[gg][c];
+    float a_lin = 0.f;
+#pragma unroll 8
+    for (int f = 0; f < F; ++f) a_lin = fmaf(s_phi[f], s_z[f], a_lin);
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) m = fmaxf(m, pm[j]);
+    for (int j = kPre; j < used; ++j)
+        m = fmaxf(m, p.ws_ml[(static_cast<int64_t>(row) * p.splits + j) * 2]);
+    const float flin = ex2_approx(-m);
+    float l = a_lin * flin, acc = bl * flin;
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+        const float f = (pm[j] == -INFINITY) ? 0.f : ex2_approx(pm[j] - m);
+        l = fmaf(pl[j], f, l);
+        acc = fmaf(pa[j], f, acc);
+    }
+    for (int j = kPre; j < used; ++j) {
+        const int64_t base = static_cast<int64_t>(row) * p.splits + j;
+        const float mj = p.ws_ml[base * 2];
+        const float f = (mj == -INFINITY) ? 0.f : ex2_approx(mj - m);
+        l = fmaf(p.ws_ml[base * 2 + 1], f, l);
+        acc = fmaf(p.ws_acc[base * D + c], f, acc);
+    }
+    p.o[static_cast<int64_t>(row) * D + c] = round16<DT>(l > 0.f ? acc / l : 0.f);
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -533,7 +636,8 @@ bool encode_cache_map(CUtensorMap *m, const void *ptr, int d, uint64_t rows, int
 }
 
 template <int D, int G, int ST, int DT>
-swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStream_t stream) {
+swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, int df,
+                         cudaStream_t stream) {
     using SL = DecSmem<D, G, ST>;
     static_assert(kDecCtasPerSm[ST - 1] * (SL::kAlloc + 1024) <= 233472, "CTAs per SM must fit");
     int dev = 0;
@@ -554,7 +658,14 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, cudaStre
     e = launch_pdl(swa_decode_kernel<D, G, ST, DT>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
                    maps, p);
     if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_kernel");
-    if (p.splits > 1) {
+    if (p.partials) {  // hybrid: merge with the linear part
+        const int rows = p.B * p.Hq;
+        e = df == 32 ? launch_pdl(swa_hybrid_merge_kernel<D, 32, DT>, dim3(rows),
+                                  dim3(kHybThreads), 0, stream, p)
+                     : launch_pdl(swa_hybrid_merge_kernel<D, 64, DT>, dim3(rows),
+                                  dim3(kHybThreads), 0, stream, p);
+        if (e != cudaSuccess) return cuda_fail(e, "launch swa_hybrid_merge_kernel");
+    } else if (p.splits > 1) {
         const int rows = p.B * p.Hq;
         e = launch_pdl(swa_decode_merge_kernel<D, DT>, dim3((rows + 3) / 4), dim3(128), 0, stream, p);
         if (e != cudaSuccess) return cuda_fail(e, "launch swa_decode_merge_kernel");
@@ -568,27 +679,28 @@ namespace {
 
 template <int D, int DT>
 swa_status launch_decode_g(const DecodeMaps &maps, const DecodeParams &p, int G, bool single,
-                           cudaStream_t stream) {
+                           int df, cudaStream_t stream) {
     switch (G) {
-        case 1: return single ? launch_decode<D, 1, 1, DT>(maps, p, stream) : launch_decode<D, 1, 2, DT>(maps, p, stream);
-        case 2: return single ? launch_decode<D, 2, 1, DT>(maps, p, stream) : launch_decode<D, 2, 2, DT>(maps, p, stream);
-        case 4: return single ? launch_decode<D, 4, 1, DT>(maps, p, stream) : launch_decode<D, 4, 2, DT>(maps, p, stream);
-        case 8: return single ? launch_decode<D, 8, 1, DT>(maps, p, stream) : launch_decode<D, 8, 2, DT>(maps, p, stream);
+        case 1: return single ? launch_decode<D, 1, 1, DT>(maps, p, df, stream) : launch_decode<D, 1, 2, DT>(maps, p, df, stream);
+        case 2: return single ? launch_decode<D, 2, 1, DT>(maps, p, df, stream) : launch_decode<D, 2, 2, DT>(maps, p, df, stream);
+        case 4: return single ? launch_decode<D, 4, 1, DT>(maps, p, df, stream) : launch_decode<D, 4, 2, DT>(maps, p, df, stream);
+        case 8: return single ? launch_decode<D, 8, 1, DT>(maps, p, df, stream) : launch_decode<D, 8, 2, DT>(maps, p, df, stream);
         default: return SWA_ERR_UNSUPPORTED;
     }
 }
 
 template <int DT>
 swa_status launch_decode_dt(const DecodeMaps &maps, const DecodeParams &p, int d, int G,
-                            bool single, cudaStream_t stream) {
-    return d == 128 ? launch_decode_g<128, DT>(maps, p, G, single, stream)
-                    : launch_decode_g<64, DT>(maps, p, G, single, stream);
+                            bool single, int df, cudaStream_t stream) {
+    return d == 128 ? launch_decode_g<128, DT>(maps, p, G, single, df, stream)
+                    : launch_decode_g<64, DT>(maps, p, G, single, df, stream);
 }
 
 }  // namespace
 
 swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,
-                         void *workspace, const DecodePlan &plan, cudaStream_t stream) {
+                         void *workspace, const DecodePlan &plan, cudaStream_t stream,
+                         const swa_linear_state *lin) {
     if (c.B == 0) return SWA_OK;
     DecodeParams p{};
     p.q = static_cast<const uint16_t *>(q);
@@ -600,7 +712,13 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
     p.cap = c.cap;
     p.w = c.w < 0 ? -1 : c.w;
     p.splits = plan.splits;
-    if (plan.splits > 1) {
+    if (lin != nullptr) {  // hybrid: every split writes partials for the merge
+        p.partials = 1;
+        p.S = lin->S;
+        p.z = lin->z;
+        p.W = lin->W;
+    }
+    if (plan.splits > 1 || lin != nullptr) {
         p.ws_acc = static_cast<float *>(workspace);
         p.ws_ml = p.ws_acc + static_cast<size_t>(c.B) * Hq * plan.splits * c.d;
     }
@@ -616,8 +734,9 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
     const long long cap_eff = c.w < 0 ? c.cap : c.w;
     const long long chunks = (cap_eff + kDecCH - 1) / kDecCH;
     const bool single = (chunks + plan.splits - 1) / plan.splits <= 1;
-    return c.dtype == SWA_F16 ? launch_decode_dt<kF16>(maps, p, c.d, G, single, stream)
-                              : launch_decode_dt<kBf16>(maps, p, c.d, G, single, stream);
+    const int df = lin != nullptr ? lin->df : 0;
+    return c.dtype == SWA_F16 ? launch_decode_dt<kF16>(maps, p, c.d, G, single, df, stream)
+                              : launch_decode_dt<kBf16>(maps, p, c.d, G, single, df, stream);
 }
 
 int decode_read_clear_error(cudaStream_t stream) {

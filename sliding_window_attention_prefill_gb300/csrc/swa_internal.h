@@ -59,8 +59,18 @@ swa_status chunk_gather_launch(const swa_cache &c, const void *k_new, const void
                                int64_t pos0, int q_off, void *wk, void *wv, cudaStream_t stream);
 swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_new, int n,
                          int64_t pos0, cudaStream_t stream);
+// lin != nullptr: hybrid window + linear decode (workspace of
+// hybrid_workspace_bytes, partials written even with one split).
 swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,
-                         void *workspace, const DecodePlan &plan, cudaStream_t stream);
+                         void *workspace, const DecodePlan &plan, cudaStream_t stream,
+                         const swa_linear_state *lin = nullptr);
+// Fold the positions an append of n tokens at pos0 evicts from the ring into
+// the linear state (before the append overwrites them).  *appended: the
+// kernel has also written the tokens (a one-token append), so no append
+// kernel is needed.
+swa_status hybrid_fold_launch(const swa_cache &c, const swa_linear_state &lin, const void *k_new,
+                              const void *v_new, int n, int64_t pos0, cudaStream_t stream,
+                              bool *appended);
 
 // Launch with programmatic stream serialization: the kernel's CTAs may be
 // placed while the previous kernel of the stream drains, so its prologue

@@ -376,6 +376,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return r;
 }
 
+// A 16-bit value of element type DT -> float (exact).
+template <int DT>
+__device__ __forceinline__ float widen16(uint16_t x) {
+    if constexpr (DT == kBf16) {
+        return __uint_as_float(static_cast<uint32_t>(x) << 16);
+    } else {
+        float f;
+        asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(x));
+        return f;
+    }
+}
+
 // One float -> 16-bit pattern of element type DT (round to nearest even).
 template <int DT>
 __device__ __forceinline__ uint16_t round16(float x) {

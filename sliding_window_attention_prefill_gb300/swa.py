@@ -33,6 +33,12 @@ class SwaCacheStruct(ctypes.Structure):
                 ("cap", _c_i32), ("w", _c_i32), ("s", _c_i32), ("dtype", _c_i32)]
 
 
+class SwaLinearStateStruct(ctypes.Structure):
+    """Mirror of ``swa_linear_state``."""
+    _fields_ = [("S", _c_p), ("z", _c_p), ("W", _c_p), ("B", _c_i32), ("Hkv", _c_i32), ("d", _c_i32),
+                ("df", _c_i32)]
+
+
 STATUS = {0: "SWA_OK", -1: "SWA_ERR_INVALID_ARG", -2: "SWA_ERR_UNSUPPORTED",
           -3: "SWA_ERR_ALIGNMENT", -4: "SWA_ERR_WORKSPACE", -5: "SWA_ERR_CUDA",
           -6: "SWA_ERR_TIMEOUT", -7: "SWA_ERR_BOUNDS"}
@@ -95,6 +101,14 @@ def _declare(L) -> None:
     L.swa_check_prefill_chunk.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, P(SwaCacheStruct), _c_int,
                                           _c_i64, _c_int, _c_p, _c_size]
     L.swa_check_prefill_chunk.restype = _c_int
+    L.swa_hybrid_append.argtypes = [P(SwaCacheStruct), P(SwaLinearStateStruct), _c_p, _c_p, _c_int,
+                                    _c_i64, _c_p]
+    L.swa_hybrid_append.restype = _c_int
+    L.swa_hybrid_decode_workspace_bytes.argtypes = [_c_int] * 6
+    L.swa_hybrid_decode_workspace_bytes.restype = _c_size
+    L.swa_hybrid_decode.argtypes = [_c_p, P(SwaCacheStruct), P(SwaLinearStateStruct), _c_p, _c_int,
+                                    _c_int, _c_int, _c_p, _c_p, _c_size, _c_p]
+    L.swa_hybrid_decode.restype = _c_int
     L.swa_prefill_varlen_workspace_bytes.argtypes = [_c_int] * 4
     L.swa_prefill_varlen_workspace_bytes.restype = _c_size
     L.swa_prefill_varlen.argtypes = ([_c_p] * 6 + [_c_int] * 9 + [_c_p, _c_size, _c_p])
@@ -364,6 +378,69 @@ def decode(q: torch.Tensor, cache: Cache, pos: torch.Tensor, out: torch.Tensor |
     st = lib().swa_decode(_ptr(q), ctypes.byref(c), _ptr(pos), Hq, cache.w, cache.s, _ptr(o),
                           _ptr(ws), nbytes, _stream(q.device))
     _check(st, "swa_decode")
+    return o
+
+
+# ----------------------------------------------------------------------------- hybrid
+class LinearState:
+    """The linear-attention state of a hybrid window + linear layer: S fp32
+    [B, Hkv, 2 df, d], z fp32 [B, Hkv, 2 df] (zero: nothing evicted yet) and
+    the feature weights W fp32 [Hkv, d, df] of phi(x) = (exp(xW), exp(-xW))."""
+
+    def __init__(self, cache: "Cache", W: torch.Tensor):
+        _need(W, "W", torch.float32)
+        if W.dim() != 3 or W.shape[0] != cache.Hkv or W.shape[1] != cache.d:
+            raise ValueError(f"W must be [Hkv, d, df], got {tuple(W.shape)}")
+        self.df = int(W.shape[2])
+        self.W = W
+        F = 2 * self.df
+        self.S = torch.zeros(cache.B, cache.Hkv, F, cache.d, dtype=torch.float32, device=W.device)
+        self.z = torch.zeros(cache.B, cache.Hkv, F, dtype=torch.float32, device=W.device)
+        self.B, self.Hkv, self.d = cache.B, cache.Hkv, cache.d
+
+    def struct(self) -> SwaLinearStateStruct:
+        return SwaLinearStateStruct(self.S.data_ptr(), self.z.data_ptr(), self.W.data_ptr(), self.B,
+                                    self.Hkv, self.d, self.df)
+
+
+def hybrid_append(cache: "Cache", state: LinearState, k_new: torch.Tensor, v_new: torch.Tensor,
+                  pos0: int) -> None:
+    """Cache.append that first folds the positions it evicts into ``state``."""
+    _need(k_new, "k_new", cache.dtype), _need(v_new, "v_new", cache.dtype)
+    if (k_new.shape != v_new.shape or k_new.shape[0] != cache.B
+            or tuple(k_new.shape[2:]) != (cache.Hkv, cache.d)):
+        raise ValueError(f"k_new/v_new must be [B, n, Hkv, d], got {tuple(k_new.shape)}")
+    c, st = cache.struct(), state.struct()
+    _check(lib().swa_hybrid_append(ctypes.byref(c), ctypes.byref(st), _ptr(k_new), _ptr(v_new),
+                                   k_new.shape[1], int(pos0), _stream(cache.k.device)),
+           "swa_hybrid_append")
+
+
+_hybrid_workspaces: dict = {}
+
+
+def hybrid_decode(q: torch.Tensor, cache: "Cache", state: LinearState, pos: torch.Tensor,
+                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """decode with the linear part of the evicted positions mixed in."""
+    _need(q, "q", cache.dtype)
+    _need(pos, "pos", torch.int32)
+    B, Hq, d = q.shape
+    if B != cache.B or d != cache.d or pos.numel() != B:
+        raise ValueError("q / pos do not match the cache")
+    o = torch.empty_like(q) if out is None else out
+    _need(o, "out", cache.dtype)
+    n = int(lib().swa_hybrid_decode_workspace_bytes(B, Hq, cache.Hkv, d, cache.cap, cache.w))
+    ws = workspace
+    if ws is None:
+        key = (q.device, n)
+        ws = _hybrid_workspaces.get(key)
+        if ws is None:
+            ws = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+            _hybrid_workspaces[key] = ws
+    c, st = cache.struct(), state.struct()
+    _check(lib().swa_hybrid_decode(_ptr(q), ctypes.byref(c), ctypes.byref(st), _ptr(pos), Hq, cache.w,
+                                   cache.s, _ptr(o), _ptr(ws), ws.numel() * ws.element_size(),
+                                   _stream(q.device)), "swa_hybrid_decode")
     return o
 
 
