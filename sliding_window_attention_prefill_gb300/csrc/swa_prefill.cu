@@ -11,19 +11,23 @@
 // a unit's columns into key tiles of up to 256 and runs one unit at a time.
 //
 // Roles (384 threads = three warpgroups, one persistent CTA per SM):
-//   warp 0       TMA producer for Q (double-buffered) and K tiles
-//   warp 1       tcgen05 issuer; owns the 512-column TMEM allocation
-//                S (256 columns) | P (128 columns, 16-bit pairs) | O (d columns)
-//   warp 2       TMA producer for V tiles
+//   warp 0       TMA producer for Q (double-buffered), K and V tiles
+//   warp 1       tcgen05 issuer of S = Q K^T; owns the 512-column TMEM
+//                allocation S (256 columns) | P (128 columns, 16-bit pairs) |
+//                O (d columns)
+//   warp 2       tcgen05 issuer of O += P V (one issuing thread per product,
+//                so that each one's waits and commits overlap the other's
+//                MMAs: an issuing thread stays only a couple of MMAs ahead
+//                of the tensor pipe)
 //   warp 3       TMA stores of the staged output tile (128-column key tiles;
 //                idle otherwise)
 //   warps 4..11  softmax + epilogue: two threads per MMA row (TMEM lane), each
 //                taking every other 32-column chunk of the key tile
 // Key tiles of 256 columns let S = Q K^T run as N = 256 MMAs (twice the work
 // per instruction of N = 128 at a similar issue cost on this part), and P
-// lives in its own TMEM columns, so the MMA warp issues S_{g+1} as soon as
-// the softmax has read S_g -- while the softmax of tile g is still running --
-// and O += P_g V_g afterwards.  The first warpgroup hands registers to the
+// lives in its own TMEM columns, so S_{g+1} is issued as soon as the softmax
+// has read S_g -- while the softmax of tile g is still running -- and
+// O += P_g V_g once P_g is written.  The first warpgroup hands registers to the
 // two softmax warpgroups (setmaxnreg) so a thread keeps its 128 scores in
 // registers.  The running max is only raised when it grows by more than 2^8
 // (exact: numerator and denominator share the same stale max), so the O
@@ -146,112 +150,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rise to 208: 80*128 + 2*208*128 = 63488 <= 64512.
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
-        if ((warp == 0 || warp == 2) && lane == 0) {
-            // -------------------------------------------------------- producers
-            const bool kq = (warp == 0);
-            if (kq) {
-                tma_prefetch_desc(&maps.q);
-                tma_prefetch_desc(&maps.k_band);
-            } else {
-                tma_prefetch_desc(&maps.v_band);
-            }
-            const CUtensorMap *m_sink = kq ? &maps.k_sink : &maps.v_sink;
-            const CUtensorMap *m_band0 = kq ? &maps.k_band0 : &maps.v_band0;
-            const CUtensorMap *m_band = kq ? &maps.k_band : &maps.v_band;
-            const uint32_t ns = kq ? NSK : NSV;
-            const int full0 = kq ? SL::kKFull : SL::kVFull;
-            const int empty0 = kq ? SL::kKEmpty : SL::kVEmpty;
-            const uint32_t ring = base + (kq ? SL::kK : SL::kV);
-            uint32_t g = 0, uc = 0;
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- producer
+            // Q, K and V tiles, with K one tile ahead of V: K_{g+1} then
+            // V_g, the order in which their slots come free (S_{g-1} = Q K^T
+            // completes before P V_{g-2}), so neither waits behind the other.
+            tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(&maps.k_band);
+            tma_prefetch_desc(&maps.v_band);
+            uint32_t gk = 0, gv = 0, uc = 0;
             bool ok = true;
+            // one K (kq) or V tile: tile j of unit x, ring position g
+            auto load_tile = [&](bool kq, const Unit &x, int j, uint32_t g) -> bool {
+                const uint32_t ns = kq ? NSK : NSV;
+                const uint32_t slot = g % ns;
+                if (!mbar_wait(bar((kq ? SL::kKEmpty : SL::kVEmpty) + slot), ((g / ns) & 1) ^ 1,
+                               &g_prefill_error, abort_flag))
+                    return false;
+                const uint32_t dst0 = base + (kq ? SL::kK : SL::kV) + slot * SL::kKTile;
+                const int key0 = x.lo + KT * j - p.s_pad;  // key of column 0 (band)
+                const uint32_t fb = bar((kq ? SL::kKFull : SL::kVFull) + slot);
+                mbar_arrive_expect_tx(fb, SL::kKTile);
+#pragma unroll
+                for (int db = 0; db < D / 64; ++db) {
+                    const uint32_t dst = dst0 + db * SL::kKRegion;
+                    if (j == 0 && p.s_pad > 0) {
+                        tma_load_4d(dst, kq ? &maps.k_sink : &maps.v_sink, fb, db * 64, x.kvh,
+                                    x.r0, x.b);
+                        tma_load_4d(dst + p.s_pad * 128, kq ? &maps.k_band0 : &maps.v_band0, fb,
+                                    db * 64, x.kvh, x.r0 + x.lo, x.b);
+                    } else {
+                        tma_load_4d(dst, kq ? &maps.k_band : &maps.v_band, fb, db * 64, x.kvh,
+                                    x.r0 + key0, x.b);
+                    }
+                }
+                return true;
+            };
+            Unit xv{};   // the unit of the next V tile
+            int jv = 0;  // and its tile
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
                 const Unit x = unit_geom<KT, VL>(u, p, n_units);
-                if (kq) {
-                    const uint32_t qb = uc & 1;
-                    ok = mbar_wait(bar(SL::kQEmpty + qb), ((uc >> 1) & 1) ^ 1, &g_prefill_error,
-                                   abort_flag);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(bar(SL::kQFull + qb), SL::kQTile);
+                const uint32_t qb = uc & 1;
+                ok = mbar_wait(bar(SL::kQEmpty + qb), ((uc >> 1) & 1) ^ 1, &g_prefill_error,
+                               abort_flag);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(SL::kQFull + qb), SL::kQTile);
 #pragma unroll
-                    for (int db = 0; db < D / 64; ++db)
-                        tma_load_4d(base + SL::kQ + qb * SL::kQTile + db * SL::kQRegion, &maps.q,
-                                    bar(SL::kQFull + qb), db * 64, x.kvh * p.G,
-                                    x.r0 + x.t0 - p.q_off, x.b);
-                }
-                for (int j = 0; j < x.n_tiles; ++j, ++g) {
-                    const uint32_t slot = g % ns;
-                    ok = mbar_wait(bar(empty0 + slot), ((g / ns) & 1) ^ 1, &g_prefill_error,
-                                   abort_flag);
+                for (int db = 0; db < D / 64; ++db)
+                    tma_load_4d(base + SL::kQ + qb * SL::kQTile + db * SL::kQRegion, &maps.q,
+                                bar(SL::kQFull + qb), db * 64, x.kvh * p.G, x.r0 + x.t0 - p.q_off,
+                                x.b);
+                if (uc == 0) xv = x;
+                for (int j = 0; j < x.n_tiles && ok; ++j) {
+                    ok = load_tile(true, x, j, gk);
                     if (!ok) break;
-                    const uint32_t dst0 = ring + slot * SL::kKTile;
-                    const int key0 = x.lo + KT * j - p.s_pad;  // key of column 0 (band)
-                    const uint32_t fb = bar(full0 + slot);
-                    mbar_arrive_expect_tx(fb, SL::kKTile);
-#pragma unroll
-                    for (int db = 0; db < D / 64; ++db) {
-                        const uint32_t dst = dst0 + db * SL::kKRegion;
-                        if (j == 0 && p.s_pad > 0) {
-                            tma_load_4d(dst, m_sink, fb, db * 64, x.kvh, x.r0, x.b);
-                            tma_load_4d(dst + p.s_pad * 128, m_band0, fb, db * 64, x.kvh,
-                                        x.r0 + x.lo, x.b);
-                        } else {
-                            tma_load_4d(dst, m_band, fb, db * 64, x.kvh, x.r0 + key0, x.b);
+                    ++gk;
+                    if (gk >= 2) {  // V of the tile before this one
+                        ok = load_tile(false, xv, jv, gv);
+                        if (!ok) break;
+                        ++gv;
+                        if (++jv == xv.n_tiles) {
+                            xv = x;
+                            jv = 0;
                         }
                     }
                 }
+            }
+            if (ok && gv < gk) {  // the last V
+                if (load_tile(false, xv, jv, gv)) ++gv;
             }
             // Drain: every copy this thread started has landed before exit
             // (bounded waits that ignore the abort flag; in the normal path the
             // consumers already saw these phases complete).
             int no_abort = 0;
-            for (uint32_t i = 0; i < ns && i < g; ++i) {
-                const uint32_t gl = g - 1 - i;
-                mbar_wait(bar(full0 + gl % ns), (gl / ns) & 1, &g_prefill_error, &no_abort);
+            for (uint32_t i = 0; i < NSK && i < gk; ++i) {
+                const uint32_t gl = gk - 1 - i;
+                mbar_wait(bar(SL::kKFull + gl % NSK), (gl / NSK) & 1, &g_prefill_error, &no_abort);
             }
-            if (kq)
-                for (uint32_t i = 0; i < 2 && i < uc; ++i) {
-                    const uint32_t ul = uc - 1 - i;
-                    mbar_wait(bar(SL::kQFull + (ul & 1)), (ul >> 1) & 1, &g_prefill_error,
-                              &no_abort);
-                }
+            for (uint32_t i = 0; i < NSV && i < gv; ++i) {
+                const uint32_t gl = gv - 1 - i;
+                mbar_wait(bar(SL::kVFull + gl % NSV), (gl / NSV) & 1, &g_prefill_error, &no_abort);
+            }
+            for (uint32_t i = 0; i < 2 && i < uc; ++i) {
+                const uint32_t ul = uc - 1 - i;
+                mbar_wait(bar(SL::kQFull + (ul & 1)), (ul >> 1) & 1, &g_prefill_error, &no_abort);
+            }
         } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
+            // -------------------------------------------------------- S = Q K^T issuer
+            // S_{g+1} goes to the tensor core as soon as the softmax has read
+            // S_g (and K_{g+1} has landed), independently of the P V issuer.
             constexpr uint32_t kIdescS = idesc_f16k<DT>(128, 0, false);
-            constexpr uint32_t kIdescPV = idesc_f16k<DT>(128, D, true);
             uint32_t g = 0, uc = 0;
-            bool ok = true, have_prev = false, any_pv = false;
-            uint32_t prev_g = 0, last_pv_g = 0, prev_ob = 0;
-            int prev_n = 0;
-            bool prev_first = false;
-
-            auto issue_pv = [&](uint32_t pg, int pn, bool first, uint32_t ob) -> bool {
-                const uint32_t vs = pg % NSV;
-                // One barrier per tile parity: the softmax may finish tile pg+1
-                // before this warp has waited for tile pg, and a waiter must
-                // not fall two phases behind an mbarrier (its phase parity
-                // would read as not yet complete).
-                if (!mbar_wait(bar((pg & 1) ? SL::kPFull1 : SL::kPFull), (pg >> 1) & 1,
-                               &g_prefill_error, abort_flag))
-                    return false;
-                if (!mbar_wait(bar(SL::kVFull + vs), (pg / NSV) & 1, &g_prefill_error, abort_flag))
-                    return false;
-                tc_fence_after_sync();
-                const uint32_t vbase = base + SL::kV + vs * SL::kKTile;
-                for (int kk = 0; kk < pn / 16; ++kk) {
-                    // A = P (TMEM, two 16-bit values per column), B = V (MN-major:
-                    // 64-column slabs LBO apart, 8-key groups SBO apart)
-                    const uint64_t b = smem_desc_sw128(vbase + kk * 16 * 128, SL::kKRegion, 1024);
-                    mma_f16k_ts(tmem + kTO + (DB ? ob * D : 0u),
-                                tmem + kTP + (DB ? (pg & 1) * 64 : 0u) + kk * 8, b, kIdescPV,
-                                (!first || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(SL::kPVDone + (DB ? (pg & 1) : 0)));
-                mma_commit(bar(SL::kVEmpty + vs));
-                any_pv = true;
-                last_pv_g = pg;
-                return true;
-            };
-
+            bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
                 const Unit x = unit_geom<KT, VL>(u, p, n_units);
                 const uint32_t qb = uc & 1;
@@ -268,38 +258,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     const int n = tile_width<KT>(x, j);
                     const uint32_t idesc = kIdescS | (static_cast<uint32_t>(n >> 3) << 17);
-                    const uint32_t kbase = base + SL::kK + ks * SL::kKTile;
+                    // Descriptors built once per tile; k-step kk (16 columns of d)
+                    // is 32 bytes into a 64-column slab, slab kk/4 a region on
+                    // (offsets added to the start-address field, in 16 bytes).
+                    const uint64_t a0 = smem_desc_sw128(qbase, 16, 1024);
+                    const uint64_t b0 = smem_desc_sw128(base + SL::kK + ks * SL::kKTile, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t a = smem_desc_sw128(
-                            qbase + (kk >> 2) * SL::kQRegion + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(
-                            kbase + (kk >> 2) * SL::kKRegion + (kk & 3) * 32, 16, 1024);
-                        mma_f16k_ss(tmem + kTmemS, a, b, idesc, kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_f16k_ss(tmem + kTmemS,
+                                    a0 + static_cast<uint64_t>(((kk >> 2) * SL::kQRegion + (kk & 3) * 32) >> 4),
+                                    b0 + static_cast<uint64_t>(((kk >> 2) * SL::kKRegion + (kk & 3) * 32) >> 4),
+                                    idesc, kk > 0 ? 1u : 0u);
                     mma_commit(bar(SL::kSFull));
                     mma_commit(bar(SL::kKEmpty + ks));
                     if (j == x.n_tiles - 1) mma_commit(bar(SL::kQEmpty + qb));
-                    if (have_prev) {
-                        ok = issue_pv(prev_g, prev_n, prev_first, prev_ob);
-                        if (!ok) break;
-                    }
-                    have_prev = true;
-                    prev_g = g;
-                    prev_n = n;
-                    prev_first = (j == 0);
-                    prev_ob = uc & 1;
                 }
             }
-            if (ok && have_prev) issue_pv(prev_g, prev_n, prev_first, prev_ob);
-            // Drain: all issued MMAs complete before TMEM is released.
-            if (any_pv) {
+            // Drain: the last S has landed before TMEM is released.
+            if (g > 0) {
                 int no_abort = 0;
+                mbar_wait(bar(SL::kSFull), (g - 1) & 1, &g_prefill_error, &no_abort);
+            }
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------------------- O += P V issuer
+            constexpr uint32_t kIdescPV = idesc_f16k<DT>(128, D, true);
+            uint32_t g = 0, uc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+                const Unit x = unit_geom<KT, VL>(u, p, n_units);
+                const uint32_t ob = uc & 1;
+                for (int j = 0; j < x.n_tiles; ++j, ++g) {
+                    const uint32_t vs = g % NSV;
+                    // One barrier per tile parity: the softmax may finish tile
+                    // g+1 before this thread has waited for tile g, and a
+                    // waiter must not fall two phases behind an mbarrier (its
+                    // phase parity would read as not yet complete).
+                    ok = mbar_wait(bar((g & 1) ? SL::kPFull1 : SL::kPFull), (g >> 1) & 1,
+                                   &g_prefill_error, abort_flag) &&
+                         mbar_wait(bar(SL::kVFull + vs), (g / NSV) & 1, &g_prefill_error,
+                                   abort_flag);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const int n = tile_width<KT>(x, j);
+                    // A = P (TMEM, two 16-bit values per column), B = V (MN-major:
+                    // 64-column slabs LBO apart, 8-key groups SBO apart).  The
+                    // descriptor is built once per tile; a k-step of 16 keys
+                    // (2048 bytes) adds 2048 >> 4 to its start-address field.
+                    const uint64_t b0 =
+                        smem_desc_sw128(base + SL::kV + vs * SL::kKTile, SL::kKRegion, 1024);
+                    const uint32_t d_o = tmem + kTO + (DB ? ob * D : 0u);
+                    const uint32_t a_p = tmem + kTP + (DB ? (g & 1) * 64 : 0u);
+                    mma_f16k_ts(d_o, a_p, b0, kIdescPV, j == 0 ? 0u : 1u);
+                    for (int kk = 1; kk < n / 16; ++kk)
+                        mma_f16k_ts(d_o, a_p + kk * 8, b0 + static_cast<uint64_t>(kk * 128),
+                                    kIdescPV, 1u);
+                    mma_commit(bar(SL::kPVDone + (DB ? (g & 1) : 0)));
+                    mma_commit(bar(SL::kVEmpty + vs));
+                }
+            }
+            // Drain: all issued MMAs complete before TMEM is released.
+            if (g > 0) {
+                int no_abort = 0;
+                const uint32_t gl = g - 1;
                 if (DB)
-                    mbar_wait(bar(SL::kPVDone + (last_pv_g & 1)), (last_pv_g >> 1) & 1,
-                              &g_prefill_error, &no_abort);
+                    mbar_wait(bar(SL::kPVDone + (gl & 1)), (gl >> 1) & 1, &g_prefill_error,
+                              &no_abort);
                 else
-                    mbar_wait(bar(SL::kPVDone), last_pv_g & 1, &g_prefill_error, &no_abort);
+                    mbar_wait(bar(SL::kPVDone), gl & 1, &g_prefill_error, &no_abort);
             }
         } else if (kStageOut && warp == 3) {
             // -------------------------------------------------------- output stores
