@@ -11,7 +11,8 @@
 // a unit's columns into key tiles of up to 256 and runs one unit at a time.
 //
 // Roles (384 threads = three warpgroups, one persistent CTA per SM):
-//   warp 0       TMA producer for Q (double-buffered), K and V tiles
+//   warp 0       TMA producer for Q (double-buffered), K and V tiles (V in
+//                warp 3 for 256-column tiles)
 //   warp 1       tcgen05 issuer of S = Q K^T; owns the 512-column TMEM
 //                allocation S (256 columns) | P (128 columns, 16-bit pairs) |
 //                O (d columns)
@@ -19,8 +20,8 @@
 //                so that each one's waits and commits overlap the other's
 //                MMAs: an issuing thread stays only a couple of MMAs ahead
 //                of the tensor pipe)
-//   warp 3       TMA stores of the staged output tile (128-column key tiles;
-//                idle otherwise)
+//   warp 3       TMA stores of the staged output tile (narrow key tiles), or
+//                the V producer (256-column tiles)
 //   warps 4..11  softmax + epilogue: two threads per MMA row (TMEM lane), each
 //                taking every other 32-column chunk of the key tile
 // Key tiles of 256 columns let S = Q K^T run as N = 256 MMAs (twice the work
@@ -150,14 +151,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rise to 208: 80*128 + 2*208*128 = 63488 <= 64512.
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
-        if (warp == 0 && lane == 0) {
-            // -------------------------------------------------------- producer
-            // Q, K and V tiles, with K one tile ahead of V: K_{g+1} then
-            // V_g, the order in which their slots come free (S_{g-1} = Q K^T
-            // completes before P V_{g-2}), so neither waits behind the other.
-            tma_prefetch_desc(&maps.q);
-            tma_prefetch_desc(&maps.k_band);
-            tma_prefetch_desc(&maps.v_band);
+        if ((warp == 0 || (!kStageOut && warp == 3)) && lane == 0) {
+            // -------------------------------------------------------- producers
+            // Narrow tiles: one thread loads Q, K and V, K one tile ahead of
+            // V (K_{g+1} then V_g, the order in which their slots come free:
+            // S_{g-1} = Q K^T completes before P V_{g-2}), so neither waits
+            // behind the other.  256-column tiles (one stage of each, where V
+            // is the latency-critical load): warp 0 loads Q and K, and warp
+            // 3, which has no output to store, loads V.
+            const bool do_k = (warp == 0);
+            const bool do_v = kStageOut || warp == 3;
+            if (do_k) {
+                tma_prefetch_desc(&maps.q);
+                tma_prefetch_desc(&maps.k_band);
+            }
+            if (do_v) tma_prefetch_desc(&maps.v_band);
             uint32_t gk = 0, gv = 0, uc = 0;
             bool ok = true;
             // one K (kq) or V tile: tile j of unit x, ring position g
@@ -190,6 +198,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int jv = 0;  // and its tile
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
                 const Unit x = unit_geom<KT, VL>(u, p, n_units);
+                if (!do_k) {  // V alone, in tile order
+                    for (int j = 0; j < x.n_tiles && ok; ++j) {
+                        ok = load_tile(false, x, j, gv);
+                        if (ok) ++gv;
+                    }
+                    continue;
+                }
                 const uint32_t qb = uc & 1;
                 ok = mbar_wait(bar(SL::kQEmpty + qb), ((uc >> 1) & 1) ^ 1, &g_prefill_error,
                                abort_flag);
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = load_tile(true, x, j, gk);
                     if (!ok) break;
                     ++gk;
-                    if (gk >= 2) {  // V of the tile before this one
+                    if (do_v && gk >= 2) {  // V of the tile before this one
                         ok = load_tile(false, xv, jv, gv);
                         if (!ok) break;
                         ++gv;
@@ -216,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (ok && gv < gk) {  // the last V
+            if (ok && do_k && do_v && gv < gk) {  // the last V
                 if (load_tile(false, xv, jv, gv)) ++gv;
             }
             // Drain: every copy this thread started has landed before exit
@@ -231,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t gl = gv - 1 - i;
                 mbar_wait(bar(SL::kVFull + gl % NSV), (gl / NSV) & 1, &g_prefill_error, &no_abort);
             }
-            for (uint32_t i = 0; i < 2 && i < uc; ++i) {
+            for (uint32_t i = 0; do_k && i < 2 && i < uc; ++i) {
                 const uint32_t ul = uc - 1 - i;
                 mbar_wait(bar(SL::kQFull + (ul & 1)), (ul >> 1) & 1, &g_prefill_error, &no_abort);
             }
@@ -750,20 +765,21 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
 }  // namespace
 
 // Key tile width for a call, from the widest unit's span of key columns:
-//   <= 768: narrow tiles with double-buffered P and O and the output staged
-//           for TMA stores; at d = 128 they are 112 columns, whose 28 KB K and
-//           V tiles leave room for two stages of each beside the 32 KB staged
+//   narrow: tiles with double-buffered P and O and the output staged for TMA
+//           stores; at d = 128 they are 112 columns, whose 28 KB K and V
+//           tiles leave room for two stages of each beside the 32 KB staged
 //           output tile; at d = 64, 128 columns with four stages of each;
 //   else:   256 (one tile fills the MMA's N = 256).
-// Measured on GB300 at d = 128 (TFLOP/s with 112 / 128 / 256-column tiles):
-// SWA(128,4) 509 / 447 / 456, SWA(256,4) 686 / 656 / 569, SWA(512,4)
-// 868 / 841 / 836, SWA(1024,4) 914 / 997 / 1083; full causal is fastest
-// with 256.
+// Narrow up to 1280 columns at d = 128 and 768 at d = 64.  Measured on GB300
+// (TFLOP/s, narrow / 256-column tiles): d = 128, Hq 32, Hkv 8: SWA(512,4)
+// 990 / 825, SWA(768,4) 1018 / 968, SWA(1024,4) 1097 / 1055, SWA(2048,4)
+// 1196 / 1239, full causal 1219 / 1412; d = 64, 16 heads: SWA(1024,4)
+// 529 / 581, full causal 703 / 781.
 int prefill_key_tile(const PrefillParams &p, int d) {
     if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT;
     const long long cols =
         p.w < 0 ? static_cast<long long>(p.Lk) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
-    if (cols > 768) return 256;
+    if (cols > (d == 128 ? 1280 : 768)) return 256;
     return d == 128 ? 112 : 128;
 }
 

@@ -33,7 +33,7 @@ PREFILL_CASES = [
     (1, 1500, 16, 16, 64, 512, 4),     # same shape, SWA(512,4), ragged tail
     (1, 1000, 16, 16, 64, W_INF, 0),   # same shape, full causal
     (2, 300, 8, 2, 128, 64, 4),        # d = 128, G = 4, two sequences
-    (1, 600, 4, 1, 128, 1000, 4),      # 256-column key tiles at d = 128
+    (1, 1600, 4, 1, 128, 1400, 4),     # 256-column key tiles at d = 128
     (1, 700, 8, 8, 64, 900, 4),        # 256-column key tiles at d = 64
     (1, 90, 4, 1, 128, 16, 12),        # 12 sinks, tiny ring
 ]

@@ -47,11 +47,15 @@ CASES = [
     (1, 5, 4, 1, 64, 64, 4),         # every position is a sink position
     (1, 1, 8, 2, 128, 64, 4),        # one token
     (3, 129, 4, 4, 64, 33, 1),       # odd window and one sink
-    # Long windows (256-column key tiles; a unit of G=4 spans w + 35 key
-    # columns), including one whose last tile is a single 16-column MMA step,
-    # and d=64 with 128-column tiles.
+    # Long windows (a unit of G=4 spans w + 35 key columns): 112-column
+    # tiles up to 1280 columns at d=128, ending in a 16-column MMA step
+    # (w=989) or a 17-column one rounded to 32 (w=990); 256-column tiles
+    # beyond, ending in a single column (w=1246) or exactly (w=1501); d=64
+    # with 128-column tiles.
     (1, 2600, 8, 2, 128, 989, 4),
     (1, 2600, 8, 2, 128, 990, 4),
+    (1, 2600, 8, 2, 128, 1246, 4),
+    (1, 2600, 8, 2, 128, 1501, 4),
     (1, 5000, 4, 1, 128, 2048, 4),
     (2, 700, 8, 2, 64, 300, 4),      # d=64 on the two-tile kernel, two sequences
 ]

@@ -29,7 +29,7 @@ CASES = [
     (1, 8, 2, 128, 64, 4, [40, 40, 40, 41]),          # starts before w, then wraps
     (2, 4, 4, 64, 16, 12, [7, 30, 5, 100]),           # G = 1, d = 64, 12 sinks of 16
     (1, 16, 2, 64, 96, 0, [128, 128, 77]),            # G = 8, no sinks
-    (1, 8, 2, 128, 1000, 4, [600, 700]),              # 256-column key tiles
+    (1, 8, 2, 128, 1400, 4, [900, 700]),              # 256-column key tiles
     (1, 8, 2, 64, W_INF, 0, [128, 300, 272]),         # infinite window, in place
     (2, 32, 8, 128, W_INF, 0, [500, 1, 523]),         # infinite window, d = 128
 ]

@@ -55,7 +55,7 @@ CASES = [
     ([5, 128, 129, 400], 4, 4, 64, 96, 0),                     # G=1 (128 positions per tile)
     ([17, 200, 3, 64], 16, 2, 128, W_INF, 0),                  # G=8, full causal
     ([1500, 10, 700], 32, 8, 128, 512, 4),                     # several key tiles per unit
-    ([1200, 50], 8, 2, 128, 1000, 4),                          # 256-column key tiles
+    ([1600, 50], 8, 2, 128, 1400, 4),                          # 256-column key tiles
     ([3, 9, 2], 8, 2, 64, 16, 12),                             # 12 sinks, sequences shorter than s
 ]
 
