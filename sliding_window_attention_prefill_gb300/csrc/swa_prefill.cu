@@ -54,8 +54,8 @@
 #define SWA_PREFILL_FORCE_KT 0
 #endif
 
-// Epilogue warpgroup (narrow key tiles): 0 never, 1 for calls of at least 16
-// units per SM, 2 always (for measurements).
+// Epilogue warpgroup (narrow key tiles): 0 never, 1 for units of several key
+// tiles or calls of at least 64 units per SM, 2 always (for measurements).
 #ifndef SWA_PREFILL_EPI_WG
 #define SWA_PREFILL_EPI_WG 1
 #endif
@@ -925,19 +925,24 @@ int kernel_key_tile(const PrefillParams &p, int d) {
     return kt == 256 ? 256 : (d == 128 ? 112 : 128);
 }
 
-// The epilogue warpgroup for narrow tiles when the call has at least 16
-// units per SM: it takes the unit epilogue (about 0.3 µs per unit) off the
-// softmax warps, but adds a stage to each unit's pipeline, which only pays
-// when the ramp and the tail are a small part of a CTA's work.  Measured on
-// GB300 (without / with): SWA(512,4) B=2 L=32768 Hq=32 Hkv=8 990 / 1061
-// TFLOP/s, SWA(64,4) the same 207.9 / 202.8 µs; 16 heads of 64, fp16,
-// L=32768: SWA(64,4) 67.6 / 61.4 µs, SWA(512,4) 161.8 / 151.6 µs; but
-// SWA(64,4) B=1 L=4096 Hq=32 Hkv=8 (6.7 units per SM) 20.5 / 22.5 µs.
+// The epilogue warpgroup for narrow tiles: it takes the unit epilogue
+// (about 0.3 µs per unit) off the softmax warps, which pays when units span
+// several key tiles; with single-tile units its extra stage per unit costs
+// more than it saves unless a CTA runs very many of them.  Measured on GB300
+// (without / with; Hq=32 Hkv=8 d=128 unless noted):
+//   SWA(512,4): L=6144 61.5 / 58.9 µs, L=12288 113.0 / 106.5 µs, B=2
+//     L=32768 990 / 1061 TFLOP/s; 16 heads of 64, fp16: L=8192 49.2 / 45.4
+//     µs, L=32768 161.8 / 151.6 µs;
+//   SWA(64,4), one tile per unit: L=4096 20.5 / 22.5 µs, L=12288 43.0 /
+//     45.1 µs, B=2 L=32768 (108 units per SM) 207.9 / 202.8 µs.
 bool use_epilogue_wg(const PrefillParams &p, int kt) {
     if (kt == 256 || SWA_PREFILL_EPI_WG == 0) return false;
     if (SWA_PREFILL_EPI_WG == 2) return true;
+    const long long cols =
+        p.w < 0 ? static_cast<long long>(p.Lk) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
+    if (cols > kt) return true;  // several key tiles per unit
     const int sms = device_sm_count();
-    return sms > 0 && static_cast<long long>(p.n_units) >= 16ll * sms;
+    return sms > 0 && static_cast<long long>(p.n_units) >= 64ll * sms;
 }
 
 // ---------------------------------------------------------------------------
