@@ -345,47 +345,87 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     mean_pre = sum(pre_ms) / len(pre_ms)
     mean_dec = sum(dec_ms) / len(dec_ms)
 
-    # ---- end to end: pinned host buffers, copies inside the timed region
-    host = {n: t.pin_memory() for n, t in
-            dict(q=q_h, k=k_h, v=v_h, k1=k1_h, v1=v1_h, q1=q1_h).items()}
-    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    od_host = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = o_host.numel() * 2 + od_host.numel() * 2
+    # ---- end to end: pinned host buffers, copies inside the timed region.
+    # Each step copies its inputs up (q, k, v of the prompt, the decode
+    # token's k, v, q), runs the library calls and copies both outputs back.
+    # Host <-> device copies run at about 200 GB/s per direction here, so
+    # they dominate; as a serving loop with double-buffered I/O does, the
+    # steps overlap: step i+1's inputs go up on one stream while step i
+    # computes and its outputs come back on another (two sets of device and
+    # host buffers).  value = steps / total time; every step's copies are in
+    # the timed region.  The serial figure (one step at a time, synchronised
+    # after each) is reported beside it.
+    names = ("q", "k", "v", "k1", "v1", "q1")
+    src = dict(q=q_h, k=k_h, v=v_h, k1=k1_h, v1=v1_h, q1=q1_h)
+    host = [{n: src[n].pin_memory() for n in names} for _ in range(2)]
+    devb = [dict(q=q, k=k, v=v, k1=k1, v1=v1, q1=q1, o=o, od=od),
+            {**{n: torch.empty_like(src[n], device=dev) for n in names},
+             "o": torch.empty_like(o), "od": torch.empty_like(od)}]
+    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    od_host = [torch.empty(od.shape, dtype=od.dtype, pin_memory=True) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = o_host[0].numel() * 2 + od_host[0].numel() * 2
+    up, down, comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.current_stream(dev)
 
-    def e2e_step():
-        q.copy_(host["q"], non_blocking=True)
-        k.copy_(host["k"], non_blocking=True)
-        v.copy_(host["v"], non_blocking=True)
-        k1.copy_(host["k1"], non_blocking=True)
-        v1.copy_(host["v1"], non_blocking=True)
-        q1.copy_(host["q1"], non_blocking=True)
-        swa.prefill(q, k, v, w, s, out=o)
-        cache.append(k, v, 0)
-        cache.append(k1, v1, L)
-        swa.decode(q1, cache, pos, out=od)
-        o_host.copy_(o, non_blocking=True)
-        od_host.copy_(od, non_blocking=True)
+    def e2e_step(i, done):
+        # done[j] = (inputs consumed, outputs read back) events of step j
+        b, hb = devb[i & 1], host[i & 1]
+        if i >= 2:  # this buffer set was step i-2's
+            up.wait_event(done[i - 2][0])
+        with torch.cuda.stream(up):
+            for n in names:
+                b[n].copy_(hb[n], non_blocking=True)
+        e_up = torch.cuda.Event()
+        e_up.record(up)
+        comp.wait_event(e_up)
+        if i >= 2:
+            comp.wait_event(done[i - 2][1])
+        swa.prefill(b["q"], b["k"], b["v"], w, s, out=b["o"])
+        cache.append(b["k"], b["v"], 0)
+        cache.append(b["k1"], b["v1"], L)
+        swa.decode(b["q1"], cache, pos, out=b["od"])
+        e_comp = torch.cuda.Event()
+        e_comp.record(comp)
+        down.wait_event(e_comp)
+        with torch.cuda.stream(down):
+            o_host[i & 1].copy_(b["o"], non_blocking=True)
+            od_host[i & 1].copy_(b["od"], non_blocking=True)
+        e_down = torch.cuda.Event()
+        e_down.record(down)
+        done.append((e_comp, e_down))
 
     for _ in range(max(3, min(args.warmup, 10))):
-        e2e_step()
-    torch.cuda.synchronize()
-    n_e2e = max(3, min(args.steps, 200))
-    e2e_ms = []
-    for i in range(n_e2e):
-        flush(i)
+        e2e_step(0, [])
+        torch.cuda.synchronize()
+    n_e2e = max(4, min(args.steps, 200))
+    # serial: one step at a time
+    serial_ms = []
+    for i in range(min(n_e2e, 20)):
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        e2e_step()
-        b_.record()
+        a.record(up)
+        e2e_step(0, [])
+        down.wait_stream(comp)
+        b_.record(down)
         b_.synchronize()
-        e2e_ms.append(a.elapsed_time(b_))
-    mean_e2e = sum(e2e_ms) / len(e2e_ms)
+        serial_ms.append(a.elapsed_time(b_))
+    mean_e2e_serial = sum(serial_ms) / len(serial_ms)
+    # overlapped: n_e2e steps back to back
+    torch.cuda.synchronize()
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(up)
+    done = []
+    for i in range(n_e2e):
+        e2e_step(i, done)
+    up.wait_stream(down)
+    up.wait_stream(comp)
+    b_.record(up)
+    b_.synchronize()
+    mean_e2e = a.elapsed_time(b_) / n_e2e
 
     # ---- max over ranks
     if world > 1:
-        mean_step, mean_pre, mean_dec, mean_e2e = max_over_ranks(
-            [mean_step, mean_pre, mean_dec, mean_e2e], dev)
+        mean_step, mean_pre, mean_dec, mean_e2e, mean_e2e_serial = max_over_ranks(
+            [mean_step, mean_pre, mean_dec, mean_e2e, mean_e2e_serial], dev)
 
     if rank != 0:
         return
@@ -420,7 +460,11 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         "decode": {"ms_append_and_decode": mean_dec, "tok_s": B * world / (mean_dec * 1e-3),
                    "kv_bytes": dbytes, "note": "one token after the prompt; B=1 is latency-bound"},
         "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e},
+                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e,
+                "timing": f"{n_e2e} steps back to back, the copies of consecutive steps "
+                          "overlapping (double-buffered host and device buffers)",
+                "serial": {"value": tokens / (mean_e2e_serial * 1e-3), "ms_per_step": mean_e2e_serial,
+                           "timing": "one step at a time, synchronised after each"}},
         "clocks": clocks,
     }
     if cpu:
