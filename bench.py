@@ -281,10 +281,9 @@ def run_swa(args, rank: int, world: int, local_rank: int):
 
     def cache_decode_part():
         cache.append(k, v, 0)
-        cache.append(k1, v1, L)
-        swa.decode(q1, cache, pos, out=od)
+        swa.append_decode(q1, k1, v1, cache, pos, out=od)  # the token's append + its decode
 
-    launches_per_step = 1 + 2 + 1 + (1 if swa.decode_workspace_bytes(B, Hq, Hkv, d, cache.cap, w) else 0)
+    launches_per_step = 1 + 1 + 1 + (1 if swa.decode_workspace_bytes(B, Hq, Hkv, d, cache.cap, w) else 0)
     stream = torch.cuda.current_stream(dev)
     # warm up once outside capture (sets kernel attributes), then capture
     prefill_part()
@@ -382,8 +381,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
             comp.wait_event(done[i - 2][1])
         swa.prefill(b["q"], b["k"], b["v"], w, s, out=b["o"])
         cache.append(b["k"], b["v"], 0)
-        cache.append(b["k1"], b["v1"], L)
-        swa.decode(b["q1"], cache, pos, out=b["od"])
+        swa.append_decode(b["q1"], b["k1"], b["v1"], cache, pos, out=b["od"])
         e_comp = torch.cuda.Event()
         e_comp.record(comp)
         down.wait_event(e_comp)
@@ -565,9 +563,9 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
 def suite_decode(steps: int, only_w=None, n_steps: int = 1024):
     """Decode configuration: B=64, Hq=32, Hkv=8, d=128, SWA(w,4) for w in
     {64, 512}; the cache is filled from a 4096-token N(0,1) prompt, then
-    `n_steps` decode steps each append one N(0,1) token and decode it.  Every
-    step is its own captured CUDA graph (its position is a launch argument);
-    L2 is flushed before each step.  Also times the decode kernel alone."""
+    `n_steps` decode steps each append one N(0,1) token and decode it (one
+    append_decode call).  Every step is its own captured CUDA graph; L2 is
+    flushed before each step.  Also times the decode kernel alone."""
     import torch
 
     import sliding_window_attention_prefill_gb300 as swa
@@ -588,8 +586,7 @@ def suite_decode(steps: int, only_w=None, n_steps: int = 1024):
         ws = swa.workspace_for(c, Hq)
 
         def step(i):
-            c.append(ks[i], vs[i], prompt + i)
-            swa.decode(qs[i], c, pos[i], out=od, workspace=ws)
+            swa.append_decode(qs[i], ks[i], vs[i], c, pos[i], out=od, workspace=ws)
 
         step(0)  # kernel attributes are set outside capture
         torch.cuda.synchronize()
@@ -814,8 +811,7 @@ def suite_context(steps: int, batches=(1, 256), shape: str = "llama", hybrid: bo
                     swa.hybrid_append(c, st, kn, vn, P)
                     swa.hybrid_decode(q, c, st, pos, out=o)
                 else:
-                    c.append(kn, vn, P)
-                    swa.decode(q, c, pos, out=o, workspace=ws)
+                    swa.append_decode(q, kn, vn, c, pos, out=o, workspace=ws)
 
         def decode_only():
             for c, kn, vn, q, o, ws, st in layers:

@@ -180,6 +180,32 @@ swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos,
                       int w, int s, void *o, void *workspace, size_t workspace_bytes,
                       swa_stream_t stream);
 
+/*
+ * swa_append_decode -- the decode step of one new token per sequence in one
+ * kernel: swa_cache_append of that token at position pos[b], then
+ * swa_decode at pos[b] (the operation is the same as the two calls; the
+ * window equation of "Sliding-window beats linear attention", paper summary
+ * page, section "Prerequisites / Sliding-window attention SWA(w, s)", with
+ * the cache's sink + ring slots).
+ *
+ *   q            [B, Hq, d]   queries of position pos[b]
+ *   k_new, v_new [B, Hkv, d]  the token's key and value (a [B, 1, Hkv, d]
+ *                             append input is the same memory); written to
+ *                             slot(pos[b]) of the cache
+ *   pos          [B] int32 (device); the cache must hold positions
+ *                0..pos[b]-1 (those still in the window)
+ *   o, workspace as for swa_decode (same workspace size)
+ *
+ * Results, the cache afterwards and the errors are those of the two calls
+ * (a pos[b] outside [0, cap) for SWA_W_INF records SWA_ERR_BOUNDS and that
+ * sequence's slot and output are left untouched).  pos is read on the
+ * device, so a captured graph can be replayed with new positions.  k_new and
+ * v_new must be 16-byte aligned and overlap neither the cache nor o.
+ */
+swa_status swa_append_decode(const void *q, const void *k_new, const void *v_new,
+                             const swa_cache *cache, const int32_t *pos, int Hq, int w, int s,
+                             void *o, void *workspace, size_t workspace_bytes, swa_stream_t stream);
+
 /* Size of the device scratch built into the library for swa_decode_noalloc. */
 #define SWA_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -379,6 +379,30 @@ swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos,
     return swa::decode_launch(q, *cache, pos, Hq, o, workspace, plan, as_cuda(stream));
 }
 
+swa_status swa_append_decode(const void *q, const void *k_new, const void *v_new,
+                             const swa_cache *cache, const int32_t *pos, int Hq, int w, int s,
+                             void *o, void *workspace, size_t workspace_bytes,
+                             swa_stream_t stream) {
+    if (cache == nullptr) return SWA_ERR_INVALID_ARG;
+    const int sms = swa::device_sm_count();
+    if (sms <= 0) return swa::cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
+    const swa::DecodePlan plan =
+        swa::decode_plan(cache->B, Hq, cache->Hkv, cache->d, cache->cap, cache->w, sms);
+    const swa_status st =
+        swa_check_decode(q, cache, pos, Hq, w, s, o, workspace, workspace_bytes, plan.workspace);
+    if (st != SWA_OK || cache->B == 0) return st;
+    if (!k_new || !v_new) return SWA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return SWA_ERR_ALIGNMENT;
+    const size_t nb = static_cast<size_t>(cache->B) * cache->Hkv * cache->d * 2;
+    const size_t qb = static_cast<size_t>(cache->B) * Hq * cache->d * 2;
+    const size_t cb = static_cast<size_t>(cache->B) * cache->Hkv * cache->cap * cache->d * 2;
+    for (const void *t : {k_new, v_new})
+        if (overlap(t, nb, cache->k, cb) || overlap(t, nb, cache->v, cb) || overlap(t, nb, o, qb))
+            return SWA_ERR_INVALID_ARG;
+    return swa::decode_launch(q, *cache, pos, Hq, o, workspace, plan, as_cuda(stream), nullptr,
+                              k_new, v_new);
+}
+
 namespace {
 
 // The linear state belongs to the cache: same B, Hkv, d; df in {32, 64};

@@ -74,6 +74,11 @@ struct DecodeParams {
     // feature weights W [Hkv, D, df])
     int partials;
     const float *S, *z, *W;
+    // append + decode: the new token of each sequence ([B, Hkv, D]) goes to
+    // its slot of the cache (kc, vc) and into the staged chunk that holds it
+    const uint16_t *k_new, *v_new;
+    uint16_t *kc, *vc;
+    int s;
 };
 
 // ST: depth of the chunk ring (2 when items span several chunks; 1 when every
@@ -162,6 +167,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int row, int cc) {
 // recorded as an error; its chunks are consumed and nothing is written.
 struct DecItem {
     int b, kvh, split, begin, end, n_chunks, n_valid;
+    int snew;  // append + decode: the new token's slot, else -1
     bool bad, spec;
 };
 
@@ -172,6 +178,7 @@ __device__ __forceinline__ DecItem dec_item_head(int it, const DecodeParams &p) 
     x.b = pair / p.Hkv;
     x.kvh = pair - x.b * p.Hkv;
     x.begin = x.end = x.n_chunks = x.n_valid = 0;
+    x.snew = -1;
     x.bad = false;
     if (p.w >= 0) {
         int used;
@@ -198,6 +205,12 @@ __device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p) 
     const int hi = min(x.end, x.n_valid);
     const int need = hi > x.begin ? (hi - x.begin + kDecCH - 1) / kDecCH : 0;
     x.n_chunks = max(need, x.spec ? 1 : 0);
+    if (p.k_new != nullptr && !x.bad) {
+        // slot(pos): the position itself below s (or for an infinite window),
+        // else s + (pos - s) mod (w - s); this item holds it if it is in range
+        const int sl = (p.w < 0 || pos < p.s) ? pos : p.s + (pos - p.s) % (p.w - p.s);
+        if (sl >= x.begin && sl < hi) x.snew = sl;
+    }
 }
 
 // Persistent: each CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...;
@@ -316,6 +329,27 @@ __global__ void __launch_bounds__(kDecThreads)
                     qb[ks][1] = gq < G ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tq) : 0u;
                 }
             }
+            // append + decode: the warp whose 16 slots hold the new token puts
+            // its k and v into the staged chunk (over what the copy read) and
+            // into the cache (warp-uniform test)
+            const int rnew = x.snew - (x.begin + c * kDecCH);
+            const bool patch = x.snew >= 0 && rnew >= slot0 && rnew < slot0 + 16 && rnew < rows;
+            if (patch) {
+                if (lane < D / 8) {
+                    const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
+                    const int64_t dst =
+                        ((static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * p.cap + x.snew) * D + lane * 8;
+                    const uint4 kk = *reinterpret_cast<const uint4 *>(p.k_new + src);
+                    const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src);
+                    const int off = (lane >> 3) * SL::kRegion + rnew * 128 +
+                                    (((lane & 7) ^ (rnew & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + off) = kk;
+                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + SL::kChunkBytes + off) = vv;
+                    *reinterpret_cast<uint4 *>(p.kc + dst) = kk;
+                    *reinterpret_cast<uint4 *>(p.vc + dst) = vv;
+                }
+                __syncwarp();
+            }
             if (mine > 0) {
                 const uint32_t kst = sbase + st * SL::kStage;
                 const uint32_t vst = kst + SL::kChunkBytes;
@@ -391,7 +425,8 @@ __global__ void __launch_bounds__(kDecThreads)
                     ldsm_x4_t(swz(vst, vrow, 2 * mt + ((lane >> 3) & 1)), a);
                     mma_16816<DT>(acc[mt], a, pb0, pb1);
                 }
-                if (mine < 16) fence_proxy_async_smem();  // zeroed rows before the next TMA fill
+                // zeroed or patched rows before the next TMA fill of this stage
+                if (mine < 16 || patch) fence_proxy_async_smem();
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(st));
@@ -700,7 +735,7 @@ swa_status launch_decode_dt(const DecodeMaps &maps, const DecodeParams &p, int d
 
 swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,
                          void *workspace, const DecodePlan &plan, cudaStream_t stream,
-                         const swa_linear_state *lin) {
+                         const swa_linear_state *lin, const void *k_new, const void *v_new) {
     if (c.B == 0) return SWA_OK;
     DecodeParams p{};
     p.q = static_cast<const uint16_t *>(q);
@@ -723,6 +758,13 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
         p.ws_ml = p.ws_acc + static_cast<size_t>(c.B) * Hq * plan.splits * c.d;
     }
     p.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(c.d));
+    if (k_new != nullptr) {
+        p.k_new = static_cast<const uint16_t *>(k_new);
+        p.v_new = static_cast<const uint16_t *>(v_new);
+        p.kc = static_cast<uint16_t *>(c.k);
+        p.vc = static_cast<uint16_t *>(c.v);
+        p.s = c.w < 0 ? 0 : c.s;
+    }
     DecodeMaps maps;
     std::memset(&maps, 0, sizeof(maps));
     const uint64_t rows = static_cast<uint64_t>(c.B) * c.Hkv * c.cap;

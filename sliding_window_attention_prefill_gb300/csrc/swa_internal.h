@@ -61,9 +61,12 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
                          int64_t pos0, cudaStream_t stream);
 // lin != nullptr: hybrid window + linear decode (workspace of
 // hybrid_workspace_bytes, partials written even with one split).
+// k_new, v_new != nullptr ([B, Hkv, d]): append + decode -- each sequence's
+// new token is written to its slot of position pos[b] and attended at once.
 swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, int Hq, void *o,
                          void *workspace, const DecodePlan &plan, cudaStream_t stream,
-                         const swa_linear_state *lin = nullptr);
+                         const swa_linear_state *lin = nullptr, const void *k_new = nullptr,
+                         const void *v_new = nullptr);
 // Fold the positions an append of n tokens at pos0 evicts from the ring into
 // the linear state (before the append overwrites them).  *appended: the
 // kernel has also written the tokens (a one-token append), so no append

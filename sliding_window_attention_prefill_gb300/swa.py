@@ -74,6 +74,9 @@ def _declare(L) -> None:
     L.swa_decode.argtypes = [_c_p, P(SwaCacheStruct), _c_p, _c_int, _c_int, _c_int, _c_p, _c_p,
                              _c_size, _c_p]
     L.swa_decode.restype = _c_int
+    L.swa_append_decode.argtypes = [_c_p, _c_p, _c_p, P(SwaCacheStruct), _c_p, _c_int, _c_int,
+                                    _c_int, _c_p, _c_p, _c_size, _c_p]
+    L.swa_append_decode.restype = _c_int
     L.swa_status_string.argtypes = [_c_int]
     L.swa_status_string.restype = ctypes.c_char_p
     L.swa_get_device_error.argtypes = [_c_p]
@@ -378,6 +381,33 @@ def decode(q: torch.Tensor, cache: Cache, pos: torch.Tensor, out: torch.Tensor |
     st = lib().swa_decode(_ptr(q), ctypes.byref(c), _ptr(pos), Hq, cache.w, cache.s, _ptr(o),
                           _ptr(ws), nbytes, _stream(q.device))
     _check(st, "swa_decode")
+    return o
+
+
+def append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cache: Cache,
+                  pos: torch.Tensor, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """One decode step in one kernel: the new token of each sequence (k_new,
+    v_new [B, 1, Hkv, d] or [B, Hkv, d]) goes to its cache slot at position
+    pos [B] (int32, device), and q [B, Hq, d] at that position attends to the
+    cache -- the same as ``cache.append`` then ``decode``."""
+    _need(q, "q", cache.dtype)
+    _need(k_new, "k_new", cache.dtype), _need(v_new, "v_new", cache.dtype)
+    _need(pos, "pos", torch.int32)
+    B, Hq, d = q.shape
+    if B != cache.B or d != cache.d or pos.numel() != B:
+        raise ValueError("q / pos do not match the cache")
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        if t.numel() != B * cache.Hkv * d or t.shape[0] != B or t.shape[-1] != d:
+            raise ValueError(f"{n} must be [B, 1, Hkv, d] or [B, Hkv, d], got {tuple(t.shape)}")
+    o = torch.empty_like(q) if out is None else out
+    _need(o, "out", cache.dtype)
+    ws = workspace if workspace is not None else workspace_for(cache, Hq)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    c = cache.struct()
+    st = lib().swa_append_decode(_ptr(q), _ptr(k_new), _ptr(v_new), ctypes.byref(c), _ptr(pos), Hq,
+                                 cache.w, cache.s, _ptr(o), _ptr(ws), nbytes, _stream(q.device))
+    _check(st, "swa_append_decode")
     return o
 
 
