@@ -10,7 +10,8 @@
 // key columns [sink block | band]): swa_prefill_common.cuh.  This kernel cuts
 // a unit's columns into key tiles of up to 256 and runs one unit at a time.
 //
-// Roles (384 threads = three warpgroups, one persistent CTA per SM):
+// Roles (384 threads = three warpgroups, one persistent CTA per SM; 512 with
+// the epilogue warpgroup):
 //   warp 0       TMA producer for Q (double-buffered), K and V tiles (V in
 //                warp 3 for 256-column tiles)
 //   warp 1       tcgen05 issuer of S = Q K^T; owns the 512-column TMEM
@@ -24,6 +25,9 @@
 //                the V producer (256-column tiles)
 //   warps 4..11  softmax + epilogue: two threads per MMA row (TMEM lane), each
 //                taking every other 32-column chunk of the key tile
+//   warps 12..15 epilogue warpgroup (narrow tiles, chosen per call by
+//                use_epilogue_wg): O / l of a finished unit out of TMEM into
+//                the staging tile while the softmax warps go on
 // Key tiles of 256 columns let S = Q K^T run as N = 256 MMAs (twice the work
 // per instruction of N = 128 at a similar issue cost on this part), and P
 // lives in its own TMEM columns, so S_{g+1} is issued as soon as the softmax
@@ -589,7 +593,7 @@ __global__ void __launch_bounds__(prefill_threads(EW), 1)
                     empty[i] = __all_sync(0xffffffffu, e);
                 }
                 tmem_wait_ld();
-                // S has been read: the MMA warp may compute the next S now.
+                // S has been read: the S issuer may compute the next S now.
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(SL::kSEmpty));
