@@ -216,8 +216,10 @@ __device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p) 
 // Persistent: each CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...;
 // the producer streams their chunks back to back, so the latency of the
 // first loads is paid once per CTA rather than once per item.
+// The minimum CTAs per SM of the launch bounds keeps the registers within
+// what that many CTAs can hold (the grid assumes they are all resident).
 template <int D, int G, int ST, int DT>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm[ST - 1])
     swa_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     using SL = DecSmem<D, G, ST>;
     constexpr int kDecStages = ST;
