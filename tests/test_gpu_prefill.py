@@ -58,6 +58,10 @@ CASES = [
     (1, 2600, 8, 2, 128, 1501, 4),
     (1, 5000, 4, 1, 128, 2048, 4),
     (2, 700, 8, 2, 64, 300, 4),      # d=64 on the two-tile kernel, two sequences
+    # Large groups over several key tiles (the epilogue warpgroup's row ->
+    # position / head mapping): G=16 (8 positions per unit) and G=8 at d=64.
+    (1, 600, 32, 2, 128, 300, 4),
+    (2, 400, 16, 2, 64, 300, 4),
 ]
 
 
