@@ -6,7 +6,6 @@ own batch; only the timings meet, as a max over ranks.
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
