@@ -306,6 +306,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm[ST - 1])
         DecItem x = dec_item_head(it, p);
         dec_item_pos(x, p);
         if (x.n_chunks == 0) continue;
+        // append + decode: the warp whose 16 slots will hold the new token
+        // prefetches its k and v now, so that their load overlaps the chunk
+        // copy instead of following it
+        const int onew = x.snew - x.begin;  // the new slot's offset in the item
+        if (x.snew >= 0 && onew >= 0 && onew < x.end - x.begin && ((onew % kDecCH) >> 4) == warp &&
+            lane < D / 8) {
+            const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
+            prefetch_l1(p.k_new + src);
+            prefetch_l1(p.v_new + src);
+        }
         float acc[KS][4];  // O^T: d = 16*mt + gq (+8), heads 2tq, 2tq+1
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt)

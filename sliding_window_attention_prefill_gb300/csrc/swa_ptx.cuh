@@ -125,6 +125,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ---------------------------------------------------------------------------
 // TMA: tiled bulk tensor copies (4-D maps; coordinates innermost first)
 // ---------------------------------------------------------------------------
+// Bring the line holding p into this SM's L1 (a hint: no register is tied
+// up, and a later load of the line merges with it or hits).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
