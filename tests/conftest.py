@@ -7,4 +7,4 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
-    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (run on the GPU box)")
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a)")
