@@ -51,6 +51,17 @@ MUTANTS = {
     "state_off_by_one": ("for (int64_t i = s; i <= last; ++i) {", "for (int64_t i = s; i < last; ++i) {"),
     # hybrid: W read transposed
     "w_transposed": ("f += widen(x[c]) * W[(int64_t)c * df + j];", "f += widen(x[c]) * W[(int64_t)j * d + c];"),
+    # the log-sum-exp without the running max added back
+    "lse_without_max": ("return m + log(den);", "return log(den);"),
+    # decode over the cache: the newest filled slot left out
+    "cache_decode_drops_newest": ("int64_t n = pos[b] + 1 < cap_eff ? pos[b] + 1 : cap_eff;",
+                                  "int64_t n = pos[b] < cap_eff ? pos[b] : cap_eff;"),
+    # decode over the cache: the wrong key/value head for a query head
+    "cache_decode_gqa_modulo": ("kvh = h / G;\n        int64_t n = pos[b] + 1 < cap_eff",
+                                "kvh = h % Hkv;\n        int64_t n = pos[b] + 1 < cap_eff"),
+    # cache append: positions written last-first, so an earlier position that
+    # shares a ring slot with a later one is what remains
+    "append_reverse_order": ("for (int64_t j = 0; j < n; ++j) {", "for (int64_t j = n - 1; j >= 0; --j) {"),
 }
 
 CHILD = r"""
