@@ -180,8 +180,9 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- oracle arm
 def oracle_step_rate(sample_positions: int, seed: int = 0):
-    """Time the oracle on the step restricted to `sample_positions` prompt
-    positions (all heads) + the decode token.  Returns (seconds, tokens)."""
+    """The oracle's step restricted to `sample_positions` prompt positions (all
+    heads) + the decode token.  Returns (run, tokens, oracle, k history,
+    v history): run() performs one such step, `tokens` is what it counts."""
     import numpy as np
 
     import oracle
@@ -219,12 +220,12 @@ def run_reference(args, rank: int):
     oracle.build()
     orc = oracle.get()
     cores = orc.threads(None)
-    # size the sample so the whole run stays within ~2 minutes
+    # size the sample so the whole run stays within about --ref-seconds
     calib_run, calib_tok, *_ = oracle_step_rate(64)
     t = time.perf_counter()
     calib_run()
     per_pos = (time.perf_counter() - t) / 64
-    budget = 120.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     S = int(max(16, min(WORK["L"], budget / max(per_pos, 1e-9))))
     run, tokens, *_ = oracle_step_rate(S)
     for _ in range(args.warmup):
@@ -892,6 +893,8 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["swa", "reference"], default="swa")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: oracle time for the whole run (sizes its sample)")
     ap.add_argument("--suite", choices=["prefill", "decode", "context", "chunk", "varlen"], default=None,
                     help="auxiliary per-config lines instead of the headline step")
     ap.add_argument("--w", type=int, default=None, help="prefill suite: only this window")
