@@ -174,6 +174,20 @@ def _need(t: torch.Tensor, name: str, dtype=torch.bfloat16) -> None:
         raise ValueError(f"{name} must be contiguous")
 
 
+def _out(out, q: torch.Tensor, dtype) -> torch.Tensor:
+    """The output tensor: a new one like q, or `out` checked to have q's shape
+    (the kernels write that many elements through a plain pointer) and the
+    type, device and layout every call needs."""
+    if out is None:
+        return torch.empty_like(q)
+    if not isinstance(out, torch.Tensor):
+        raise TypeError("out must be a torch.Tensor")
+    if out.shape != q.shape:
+        raise ValueError(f"out must have the shape of q {tuple(q.shape)}, got {tuple(out.shape)}")
+    _need(out, "out", dtype)
+    return out
+
+
 # ----------------------------------------------------------------------------- prefill
 def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: int,
             out: torch.Tensor | None = None, return_lse: bool = False):
@@ -191,10 +205,7 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, w: int, s: int,
     if k.shape[:2] != (B, L) or k.shape[3] != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
     Hkv = k.shape[2]
-    o = torch.empty_like(q) if out is None else out
-    _need(o, "out", q.dtype)
-    if o.shape != q.shape:
-        raise ValueError("out must have the shape of q")
+    o = _out(out, q, q.dtype)
     lse = torch.empty(B, Hq, L, dtype=torch.float32, device=q.device) if return_lse else None
     st = lib().swa_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, L, Hq, Hkv, d,
                               int(w), int(s), dt, _stream(q.device))
@@ -233,8 +244,7 @@ def prefill_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens
     B = cu_seqlens.numel() - 1
     if B < 1:
         raise ValueError("cu_seqlens needs at least two entries")
-    o = torch.empty_like(q) if out is None else out
-    _need(o, "out", q.dtype)
+    o = _out(out, q, q.dtype)
     lse = torch.empty(Hq, total, dtype=torch.float32, device=q.device) if return_lse else None
     nbytes = prefill_varlen_workspace_bytes(B, total, Hq, Hkv)
     ws = workspace
@@ -324,8 +334,7 @@ def prefill_chunk(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cache: "Cac
     if (B, d) != (cache.B, cache.d) or k.shape != (B, n, cache.Hkv, d) or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, cache "
                          f"B={cache.B} Hkv={cache.Hkv} d={cache.d}")
-    o = torch.empty_like(q) if out is None else out
-    _need(o, "out", cache.dtype)
+    o = _out(out, q, cache.dtype)
     lse = torch.empty(B, Hq, n, dtype=torch.float32, device=q.device) if return_lse else None
     nbytes = prefill_chunk_workspace_bytes(B, n, cache.Hkv, d, cache.w, pos0)
     ws = workspace
@@ -373,8 +382,7 @@ def decode(q: torch.Tensor, cache: Cache, pos: torch.Tensor, out: torch.Tensor |
     B, Hq, d = q.shape
     if B != cache.B or d != cache.d or pos.numel() != B:
         raise ValueError("q / pos do not match the cache")
-    o = torch.empty_like(q) if out is None else out
-    _need(o, "out", cache.dtype)
+    o = _out(out, q, cache.dtype)
     ws = workspace if workspace is not None else workspace_for(cache, Hq)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     c = cache.struct()
@@ -400,8 +408,7 @@ def append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cac
     for t, n in ((k_new, "k_new"), (v_new, "v_new")):
         if t.numel() != B * cache.Hkv * d or t.shape[0] != B or t.shape[-1] != d:
             raise ValueError(f"{n} must be [B, 1, Hkv, d] or [B, Hkv, d], got {tuple(t.shape)}")
-    o = torch.empty_like(q) if out is None else out
-    _need(o, "out", cache.dtype)
+    o = _out(out, q, cache.dtype)
     ws = workspace if workspace is not None else workspace_for(cache, Hq)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     c = cache.struct()
@@ -457,8 +464,7 @@ def hybrid_decode(q: torch.Tensor, cache: "Cache", state: LinearState, pos: torc
     B, Hq, d = q.shape
     if B != cache.B or d != cache.d or pos.numel() != B:
         raise ValueError("q / pos do not match the cache")
-    o = torch.empty_like(q) if out is None else out
-    _need(o, "out", cache.dtype)
+    o = _out(out, q, cache.dtype)
     n = int(lib().swa_hybrid_decode_workspace_bytes(B, Hq, cache.Hkv, d, cache.cap, cache.w))
     ws = workspace
     if ws is None:
