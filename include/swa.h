@@ -28,6 +28,9 @@
  *   - calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     the library never allocates device memory and never synchronises, except
  *     swa_get_device_error, which synchronises `stream`;
+ *   - per device, the first launch of each kernel sets its attributes and
+ *     the library keeps that state for the life of the process: do not reset
+ *     a device (cudaDeviceReset) between calls;
  *   - errors are return codes; nothing aborts the process.  Argument errors
  *     are detected on the host before anything is enqueued.  Kernels that hit
  *     an internal wait limit record an error code on the device, read with
@@ -225,7 +228,9 @@ swa_status swa_append_decode(const void *q, const void *k_new, const void *v_new
  * until the process exits.  Nothing is allocated and no allocating routine is
  * called.  The first call on each device looks up the array's device address
  * (once, with that device current); make that first call before any stream
- * capture.  If the decode plan for the shape needs more scratch than
+ * capture.  The address is kept for the life of the process, so a device
+ * reset (cudaDeviceReset) between calls is not supported: the kept address
+ * would point into the released context.  If the decode plan for the shape needs more scratch than
  * SWA_NOALLOC_SCRATCH_BYTES, returns SWA_ERR_WORKSPACE before launching
  * anything (on a 152-SM GB300 every supported shape fits).
  *

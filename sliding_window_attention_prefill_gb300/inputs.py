@@ -30,6 +30,21 @@ def normal16(shape, gen: torch.Generator, dtype=torch.bfloat16) -> torch.Tensor:
     return torch.randn(*shape, generator=gen, dtype=torch.float32).to(dtype)
 
 
+def device_generator(seed: int, device="cuda") -> torch.Generator:
+    """A torch generator on ``device``, for inputs too large to draw on the CPU
+    in a test's time (multi-GB caches); the draws differ from the CPU
+    generator's, so a test that uses it copies what it checks to the host."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def normal16_on(shape, gen: torch.Generator, dtype=torch.bfloat16) -> torch.Tensor:
+    """float32 N(0,1) drawn from ``gen`` on the generator's device, rounded to
+    ``dtype`` (bf16 or fp16)."""
+    return torch.randn(*shape, generator=gen, device=gen.device, dtype=torch.float32).to(dtype)
+
+
 def normal_bf16(shape, gen: torch.Generator) -> torch.Tensor:
     """float32 N(0,1) drawn from ``gen``, rounded to bf16 (CPU tensor)."""
     return normal16(shape, gen, torch.bfloat16)
