@@ -1,26 +1,34 @@
 #!/usr/bin/env python3
 """Benchmark of the SWA(w,s) hot path on GB300.
 
-One step = the whole path over one batch of synthetic input:
-  prefill of a 4096-token prompt (sliding-window attention with sinks, SWA(64,4),
-  Llama-3.1-8B attention shape: 32 query heads, 8 key/value heads, d = 128,
-  first 4 key rows x8), bulk append of the prompt's keys/values into a fixed
-  SWA(64,4) cache, then one decode token (append + decode).
+The line measures the metric on the configurations it is quoted on
+(Llama-3.1-8B attention shape: 32 query heads, 8 key/value heads, d = 128,
+bf16, N(0,1) inputs, s = 4 sinks):
+  decode  B=64, SWA(w,4) for w in {64, 512}: a cache filled by the bulk
+          append of a 4096-token prompt, then 1024 steps that each append one
+          token per sequence and decode it (one append_decode call);
+  prefill B=2, L=32768, SWA(w,4) for w in {128, 256, 512}.
+One step is one pass over all of it: the three prefills, and for each decode
+window the prompt's bulk append and the 1024 decode steps.  Every launch is
+timed alone with CUDA events on its stream, with L2 flushed before it
+(256 MiB written, then another 256 MiB read).  `value` is decoded tokens/s:
+the pass's 2 x 64 x 1024 decoded tokens over the device time of its decode
+steps; `prefill` holds the TFLOP/s, `decode` the KV-read GB/s, `rooflines`
+every kernel against the measured peaks, `flatness` the 4-layer decode sweep
+over 1K..256K positions, `small_prefill` the 4096-token SWA(64,4) prefill.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl swa|reference]
 Under torchrun each rank runs its own batch on its own GPU (no data exchange;
-weak scaling) and rank 0 prints one JSON line.
-
-`value` is tokens/s of the whole step (prompt tokens + decoded tokens), device
-time from CUDA events on the launching stream, inputs resident in HBM, L2
-flushed (256 MiB written, another 256 MiB read) before every timed step.  `e2e` is the same metric
-through the C ABI with pinned host buffers, copies inside the timed region.
-`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
-workload on the host cores.
+weak scaling) and rank 0 prints one JSON line.  `e2e` is the decode stream
+through the public API with pinned host buffers, every step's h2d of its
+inputs and d2h of its output inside the timed region.  `--impl reference`
+times the fp64 CPU oracle on a bounded sample of the same decode workload on
+the host cores.
 """
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import math
@@ -33,20 +41,34 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORK = dict(B=1, L=4096, Hq=32, Hkv=8, d=128, w=64, s=4, sink_rows=4)
 METRIC = "SWA(w,4) decode tok/s + KV-read GB/s vs HBM peak; prefill TFLOP/s vs tensor peak"
-WORKLOAD_NAME = ("prefill SWA(64,4) B=1 L=4096 Hq=32 Hkv=8 d=128 (first 4 key rows x8) "
-                 "+ bulk cache append + 1 decode token")
+# The configurations the metric is quoted on.
+PREFILL_CFG = dict(B=2, L=32768, Hq=32, Hkv=8, d=128, s=4, windows=(128, 256, 512))
+DECODE_CFG = dict(B=64, Hq=32, Hkv=8, d=128, s=4, windows=(64, 512), prompt=4096, steps=1024)
+# The 4096-token prompt of one sequence, SWA(64,4), first 4 key rows x8.
+SMALL_PREFILL = dict(B=1, L=4096, Hq=32, Hkv=8, d=128, w=64, s=4, sink_rows=4)
+WORKLOAD_NAME = ("decode SWA(w,4) w in {64,512}: B=64 Hq=32 Hkv=8 d=128 bf16, cache filled from a "
+                 "4096-token N(0,1) prompt, then 1024 steps each appending one N(0,1) token and "
+                 "decoding it; prefill SWA(w,4) w in {128,256,512}: B=2 L=32768 Hq=32 Hkv=8 d=128 "
+                 "bf16 N(0,1)")
 L2_FLUSH_BYTES = 256 << 20
-L2_NOTE = (f"flushed before each step: {L2_FLUSH_BYTES >> 20} MiB written, then another "
-           f"{L2_FLUSH_BYTES >> 20} MiB read, so the timed kernels start on a cold L2 that holds "
-           f"no dirty lines of the flush")
+L2_NOTE = (f"flushed before every timed launch: {L2_FLUSH_BYTES >> 20} MiB written, then another "
+           f"{L2_FLUSH_BYTES >> 20} MiB read, so each launch starts on a cold L2 that holds no "
+           f"dirty lines of the flush")
+# Decode context sweep of the flatness key: 4 attention layers, positions
+# 1K .. 256K, every finite window at batch 1 and 256; full causal at batch 1
+# for contrast.
+FLAT_POSITIONS = [1 << e for e in range(10, 19, 2)]
+FLAT_WINDOWS = (64, 128, 256, 512)
+FLAT_BATCHES = (1, 256)
+FLAT_LAYERS = 4
+CPU_DECODE_STEPS = 16
 
 
 class L2Flush:
     """Evicts the timed kernels' data from L2 (129 MB on GB300): write one
     buffer larger than L2, then read a second one, which also writes the
-    first buffer's dirty lines back before the timed region starts."""
+    first buffer's dirty lines back before the timed launch starts."""
 
     def __init__(self, device="cuda"):
         import torch
@@ -78,6 +100,17 @@ def decode_bytes(B, Hq, Hkv, d, n_valid) -> float:
     return B * (2 * Hq * d * 2 + 4 * Hkv * d * 2 + 2 * Hkv * d * 2 * n_valid)
 
 
+def kv_read_bytes(B, Hkv, d, n_valid) -> float:
+    """K and V bytes of the attended slots that one decode step reads."""
+    return 2.0 * B * Hkv * d * 2 * n_valid
+
+
+def decoded_tokens_per_step(world: int) -> int:
+    """Tokens all ranks decode in one step: each decode window's batch, every step."""
+    C = DECODE_CFG
+    return len(C["windows"]) * C["B"] * C["steps"] * world
+
+
 def peaks() -> dict:
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -88,31 +121,64 @@ def peaks() -> dict:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def prefill_traffic():
-    """dram bytes per prefill launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "prefill_traffic.json")
-    src = os.path.join(ROOT, "sliding_window_attention_prefill_gb300", "csrc", "swa_prefill.cu")
+def roofline_entry(kernel: str, ms: float, flops: float, nbytes: float, pk: dict) -> dict:
+    """The kernel against its bound: tensor if its intensity reaches the ridge
+    of the two measured peaks, else HBM; achieved = algorithmic work per
+    launch / the launch's mean CUDA-event time."""
+    secs = ms * 1e-3
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    tflops, gbs = flops / secs / 1e12, nbytes / secs / 1e9
+    if flops / nbytes >= ridge:
+        e = {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+             "frac": tflops / pk["bf16_tflops"],
+             "peak_source": pk["source"] + " bf16_tflops (burst: each launch is timed alone)"}
+    else:
+        e = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+             "frac": gbs / pk["hbm_gbs"], "peak_source": pk["source"] + " hbm_gbs (copy)"}
+    attainable = min(pk["bf16_tflops"], flops / nbytes * pk["hbm_gbs"] / 1e3)
+    e.update({"kernel": kernel, "ms": ms, "algorithmic_flops_per_launch": flops,
+              "algorithmic_bytes_per_launch": nbytes, "flop_per_byte": flops / nbytes,
+              "tflops": tflops, "gbs": gbs, "frac_of_attainable": tflops / attainable,
+              "attainable_tflops": attainable})
+    return e
+
+
+def kernel_traffic(source: str, workload: str):
+    """DRAM bytes per launch from the committed ncu records (profiles/traffic.json)
+    for this workload, if they were taken on the current kernel source (the
+    file's sha256); else None."""
+    src = os.path.join(ROOT, "sliding_window_attention_prefill_gb300", "csrc", source)
     try:
-        with open(path) as f:
-            rec = json.load(f)
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            recs = json.load(f)["records"]
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if rec.get("kernel_sha256") == h and rec.get("workload") == WORKLOAD_NAME:
-            return float(rec["dram_bytes_per_launch"])
+        for rec in recs:
+            if (rec.get("source") == source and rec.get("kernel_sha256") == h
+                    and rec.get("workload") == workload):
+                return float(rec["dram_bytes_per_launch"])
     except Exception:
         pass
     return None
+
+
+def prefill_workload(w: int) -> str:
+    P = PREFILL_CFG
+    return f"prefill SWA({w},4) B={P['B']} L={P['L']} Hq={P['Hq']} Hkv={P['Hkv']} d={P['d']} bf16"
+
+
+def decode_workload(w: int) -> str:
+    D = DECODE_CFG
+    return (f"append_decode SWA({w},4) B={D['B']} Hq={D['Hq']} Hkv={D['Hkv']} d={D['d']} bf16, "
+            f"positions {D['prompt']}..{D['prompt'] + D['steps'] - 1}")
+
+
+SMALL_WORKLOAD = "prefill SWA(64,4) B=1 L=4096 Hq=32 Hkv=8 d=128 bf16, first 4 key rows x8"
 
 
 # ----------------------------------------------------------------------------- ranks
 def rank_seed(rank: int) -> int:
     """Each rank draws its own batch (weak scaling: independent sequences)."""
     return 1000 * rank
-
-
-def tokens_per_step(world: int) -> int:
-    """Tokens all ranks process in one step: every rank's prompt + decoded token."""
-    return WORK["B"] * (WORK["L"] + 1) * world
 
 
 def max_over_ranks(values, device):
@@ -123,15 +189,28 @@ def max_over_ranks(values, device):
     return t.tolist()
 
 
+def line_config(world: int) -> dict:
+    """The `config` of both arms' lines (identical, so the two compare)."""
+    P, D = PREFILL_CFG, DECODE_CFG
+    return {"workload": WORKLOAD_NAME, "global_batch": D["B"] * world,
+            "decode": {k: (list(v) if isinstance(v, tuple) else v) for k, v in D.items()},
+            "prefill": {k: (list(v) if isinstance(v, tuple) else v) for k, v in P.items()},
+            "seq_len": P["L"], "sinks": D["s"], "l2": L2_NOTE,
+            "parallelism": f"replicas x{world} (independent batches)"}
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi samples every 50 ms for the whole run; summaries per named
+    window of wall-clock time (start/stop marks)."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.t0 = self.t1 = None
+        self.marks = {}
+        self.rows = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -141,19 +220,19 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.4)
 
-    def mark_start(self):
-        self.t0 = time.time()
+    def start(self, name: str):
+        self.marks[name] = [time.time(), None]
 
-    def mark_end(self):
-        self.t1 = time.time()
+    def stop(self, name: str):
+        self.marks[name][1] = time.time()
 
-    def result(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _collect(self):
+        if self.rows is not None or self.proc is None:
+            return
         time.sleep(0.15)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        rows = []
+        self.rows = []
         for line in out.splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 10:
@@ -161,56 +240,85 @@ class ClockSampler:
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                self.rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]), parts[6:10]))
             except Exception:
                 continue
-        inside = [r for r in rows if self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
-        used = inside if inside else rows
+
+    def result(self, name: str) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self._collect()
+        t0, t1 = self.marks[name]
+        inside = [r for r in self.rows if t0 - 0.06 <= r[0] <= t1 + 0.06]
+        used = inside if inside else self.rows
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in used:
-            for n, v in zip(names, r[3]):
+            for n, v in zip(names, r[4]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median([r[1] for r in used]) if used else None,
                 "sm_max_mhz": max(r[2] for r in used) if used else None,
-                "reasons": sorted(reasons), "samples": len(used),
+                "power_w_max": max(r[3] for r in used) if used else None,
+                "reasons": sorted(reasons), "samples": len(used), "seconds": t1 - t0,
                 "window": "timed region" if inside else "around the timed region"}
 
 
-# ----------------------------------------------------------------------------- oracle arm
-def oracle_step_rate(sample_positions: int, seed: int = 0):
-    """The oracle's step restricted to `sample_positions` prompt positions (all
-    heads) + the decode token.  Returns (run, tokens, oracle, k history,
-    v history): run() performs one such step, `tokens` is what it counts."""
+# ----------------------------------------------------------------------------- oracle legs
+def oracle_decode_state(kp, vp, w: int):
+    """The oracle's cache after the prompt's bulk append (host bit patterns)."""
     import numpy as np
 
     import oracle
-    from sliding_window_attention_prefill_gb300 import inputs
-    W = WORK
-    q, k, v = inputs.prefill_inputs(W["B"], W["L"], W["Hq"], W["Hkv"], W["d"], seed=seed,
-                                    sink_rows=W["sink_rows"])
+    D = DECODE_CFG
     orc = oracle.get()
-    qb, kb, vb = oracle.bf16_bits(q), oracle.bf16_bits(k), oracle.bf16_bits(v)
-    L = W["L"]
-    ts = np.linspace(0, L - 1, sample_positions).astype(np.int64)
-    rows = np.array([[b, t, h] for b in range(W["B"]) for t in ts for h in range(W["Hq"])], np.int64)
-    g = inputs.generator(seed + 1)
-    k1 = oracle.bf16_bits(inputs.normal_bf16((W["B"], 1, W["Hkv"], W["d"]), g))
-    v1 = oracle.bf16_bits(inputs.normal_bf16((W["B"], 1, W["Hkv"], W["d"]), g))
-    q1 = oracle.bf16_bits(inputs.normal_bf16((W["B"], W["Hq"], W["d"]), g))
-    hist_k = np.concatenate([kb, k1], axis=1)
-    hist_v = np.concatenate([vb, v1], axis=1)
-    ck = np.zeros((W["B"], W["Hkv"], W["w"], W["d"]), np.uint16)
+    ck = np.zeros((D["B"], D["Hkv"], w, D["d"]), np.uint16)
     cv = np.zeros_like(ck)
+    orc.cache_append(ck, cv, kp, vp, 0, w, D["s"])
+    return ck, cv
 
-    def run():
-        orc.prefill_rows(qb, kb, vb, rows, W["w"], W["s"])
-        orc.cache_append(ck, cv, kb, vb, 0, W["w"], W["s"])
-        orc.cache_append(ck, cv, k1, v1, L, W["w"], W["s"])
-        orc.decode_cache(q1, ck, cv, [L] * W["B"], W["w"], W["s"])
 
-    return run, W["B"] * (sample_positions + 1), orc, hist_k, hist_v
+def oracle_decode_steps(state, ks, vs, qs, w: int, n: int, threads=None) -> float:
+    """Seconds the oracle takes for decode steps 0..n-1 of the stream (each:
+    append the step's token, decode its query over the cache), on a copy of
+    the post-prompt cache state."""
+    import oracle
+    D = DECODE_CFG
+    orc = oracle.get()
+    ck, cv = state[0].copy(), state[1].copy()
+    t0 = time.perf_counter()
+    for i in range(n):
+        p = D["prompt"] + i
+        orc.cache_append(ck, cv, ks[i], vs[i], p, w, D["s"])
+        orc.decode_cache(qs[i], ck, cv, [p] * D["B"], w, D["s"], threads=threads)
+    return time.perf_counter() - t0
+
+
+def host_prompt(seed: int):
+    """The decode workload's prompt as host bit patterns: k, v [B, 4096, Hkv, d]
+    (CPU generator)."""
+    import oracle
+    from sliding_window_attention_prefill_gb300 import inputs
+    D = DECODE_CFG
+    g = inputs.generator(seed)
+    kp = inputs.normal_bf16((D["B"], D["prompt"], D["Hkv"], D["d"]), g)
+    vp = inputs.normal_bf16((D["B"], D["prompt"], D["Hkv"], D["d"]), g)
+    return oracle.bits16(kp), oracle.bits16(vp)
+
+
+def host_steps(n_steps: int, seed: int):
+    """n_steps decode steps as host bit patterns: k, v [B, 1, Hkv, d] and
+    q [B, Hq, d] per step (CPU generator)."""
+    import oracle
+    from sliding_window_attention_prefill_gb300 import inputs
+    D = DECODE_CFG
+    g = inputs.generator(seed)
+    ks = inputs.normal_bf16((n_steps, D["B"], 1, D["Hkv"], D["d"]), g)
+    vs = inputs.normal_bf16((n_steps, D["B"], 1, D["Hkv"], D["d"]), g)
+    qs = inputs.normal_bf16((n_steps, D["B"], D["Hq"], D["d"]), g)
+    b = oracle.bits16
+    return [b(ks[i]) for i in range(n_steps)], [b(vs[i]) for i in range(n_steps)], \
+        [b(qs[i]) for i in range(n_steps)]
 
 
 def run_reference(args, rank: int):
@@ -220,35 +328,99 @@ def run_reference(args, rank: int):
     oracle.build()
     orc = oracle.get()
     cores = orc.threads(None)
-    # size the sample so the whole run stays within about --ref-seconds
-    calib_run, calib_tok, *_ = oracle_step_rate(64)
-    t = time.perf_counter()
-    calib_run()
-    per_pos = (time.perf_counter() - t) / 64
+    D = DECODE_CFG
+    # size the sample (decode steps per window per bench step) to --ref-seconds
+    calib = 2
+    kp, vp = host_prompt(rank_seed(0))
+    states = {w: oracle_decode_state(kp, vp, w) for w in D["windows"]}
+    ks, vs, qs = host_steps(calib, rank_seed(0) + 1)
+    t_step = sum(oracle_decode_steps(states[w], ks, vs, qs, w, calib) for w in D["windows"]) / calib
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
-    S = int(max(16, min(WORK["L"], budget / max(per_pos, 1e-9))))
-    run, tokens, *_ = oracle_step_rate(S)
+    n = int(max(1, min(D["steps"], budget / max(t_step, 1e-9))))
+    if n > calib:
+        ks, vs, qs = host_steps(n, rank_seed(0) + 1)
     for _ in range(args.warmup):
-        run()
+        for w in D["windows"]:
+            oracle_decode_steps(states[w], ks, vs, qs, w, n)
     times = []
     for _ in range(args.steps):
-        t = time.perf_counter()
-        run()
-        times.append(time.perf_counter() - t)
+        times.append(sum(oracle_decode_steps(states[w], ks, vs, qs, w, n) for w in D["windows"]))
     mean = sum(times) / len(times)
+    tokens = len(D["windows"]) * D["B"] * n
     value = tokens / mean
-    sample = (f"{S} of {WORK['L']} prompt positions (all {WORK['Hq']} heads, evenly spaced) + "
-              f"the cache append + 1 decode token per step")
+    sample = (f"decode steps 0..{n - 1} of the {D['steps']}-step stream in each window "
+              f"(B={D['B']}, each step: the token's cache append + the decode of its query), "
+              f"after the prompt's bulk append (untimed); no prefill")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAME, "oracle": "fp64 C, OpenMP over rows"},
+            "config": line_config(1),
+            "oracle": "fp64 C (gcc -O2, OpenMP over output rows)",
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(kp, vp, ks, vs, qs, pre3) -> dict:
+    """The oracle on bounded samples of the workload, all cores and one
+    thread: the decode stream's first 16 steps per window (the headline
+    unit), the 4096-token SWA(64,4) prompt in full, and 4096 sampled output
+    rows (b, t, h) of the B=2 L=32768 prefill per window."""
+    import numpy as np
+
+    import oracle
+    from sliding_window_attention_prefill_gb300 import inputs
+    oracle.build()
+    orc = oracle.get()
+    D, P, S = DECODE_CFG, PREFILL_CFG, SMALL_PREFILL
+    cores = orc.threads(None)
+    n = CPU_DECODE_STEPS
+    out = {"kind": "oracle", "unit": "tok/s", "cores": cores, "nproc": os.cpu_count()}
+    dec = {}
+    for th, key, nn in ((None, "all_cores", n), (1, "one_thread", max(1, n // 4))):
+        secs = 0.0
+        for w in D["windows"]:
+            st = oracle_decode_state(kp, vp, w)
+            t = oracle_decode_steps(st, ks, vs, qs, w, nn, threads=th)
+            dec[f"w{w}_{key}_ms_per_step"] = t / nn * 1e3
+            secs += t
+        dec[key] = len(D["windows"]) * D["B"] * nn / secs
+        dec[f"{key}_steps_per_window"] = nn
+    out["value"] = dec["all_cores"]
+    out["one_thread"] = dec["one_thread"]
+    out["decode"] = dec
+    out["sample"] = (f"decode: steps 0..{n - 1} of the 1024-step stream in each window "
+                     f"(B={D['B']}; append + decode per step), value over all {cores} threads; "
+                     f"one thread over steps 0..{max(1, n // 4) - 1}")
+    # the 4096-token prompt, in full
+    q, k, v = inputs.prefill_inputs(S["B"], S["L"], S["Hq"], S["Hkv"], S["d"], seed=0,
+                                    sink_rows=S["sink_rows"])
+    small = {}
+    for th, key in ((None, "all_cores"), (1, "one_thread")):
+        t0 = time.perf_counter()
+        orc.prefill(q, k, v, S["w"], S["s"], threads=th)
+        small[f"{key}_s"] = time.perf_counter() - t0
+        small[f"{key}_tok_s"] = S["B"] * S["L"] / small[f"{key}_s"]
+    out["small_prefill_full"] = small
+    # the L=32768 prefill: 4096 sampled rows per window
+    q3, k3, v3 = pre3
+    rows_total = P["B"] * P["L"] * P["Hq"]
+    nr = 4096
+    idx = np.linspace(0, rows_total - 1, nr).astype(np.int64)
+    rows = np.stack([idx // (P["L"] * P["Hq"]), (idx // P["Hq"]) % P["L"], idx % P["Hq"]], 1)
+    big = {"rows_sampled": nr, "row": "one (b, t, h) output row of d values"}
+    for w in P["windows"]:
+        for th, key in ((None, "all_cores"), (1, "one_thread")):
+            t0 = time.perf_counter()
+            orc.prefill_rows(q3, k3, v3, rows, w, P["s"], threads=th)
+            dt = time.perf_counter() - t0
+            big[f"w{w}_{key}_rows_s"] = nr / dt
+            big[f"w{w}_{key}_full_s_extrapolated"] = rows_total / (nr / dt)
+    out["prefill_L32768_sample"] = big
+    return out
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -257,280 +429,318 @@ def run_swa(args, rank: int, world: int, local_rank: int):
 
     import sliding_window_attention_prefill_gb300 as swa
     from sliding_window_attention_prefill_gb300 import build, inputs
-
     build.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    W = WORK
-    B, L, Hq, Hkv, d, w, s = W["B"], W["L"], W["Hq"], W["Hkv"], W["d"], W["w"], W["s"]
-    seed = rank_seed(rank)
-    q_h, k_h, v_h = inputs.prefill_inputs(B, L, Hq, Hkv, d, seed=seed, sink_rows=W["sink_rows"])
-    g = inputs.generator(seed + 1)
-    k1_h = inputs.normal_bf16((B, 1, Hkv, d), g)
-    v1_h = inputs.normal_bf16((B, 1, Hkv, d), g)
-    q1_h = inputs.normal_bf16((B, Hq, d), g)
-    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
-    k1, v1, q1 = k1_h.to(dev), v1_h.to(dev), q1_h.to(dev)
-    o = torch.empty_like(q)
-    od = torch.empty_like(q1)
-    cache = swa.Cache(B, Hkv, d, w, s, device=dev)
-    pos = torch.full((B,), L, dtype=torch.int32, device=dev)
+    P, D, S = PREFILL_CFG, DECODE_CFG, SMALL_PREFILL
+    pk = peaks()
+    gen = inputs.device_generator(rank_seed(rank) + 7, dev)
+    # prefill inputs (B=2, L=32768)
+    q3 = inputs.normal16_on((P["B"], P["L"], P["Hq"], P["d"]), gen)
+    k3 = inputs.normal16_on((P["B"], P["L"], P["Hkv"], P["d"]), gen)
+    v3 = inputs.normal16_on((P["B"], P["L"], P["Hkv"], P["d"]), gen)
+    o3 = torch.empty_like(q3)
+    # decode inputs: the prompt and the 1024 steps
+    B, Hq, Hkv, d, s = D["B"], D["Hq"], D["Hkv"], D["d"], D["s"]
+    prompt, nsteps = D["prompt"], D["steps"]
+    kp = inputs.normal16_on((B, prompt, Hkv, d), gen)
+    vp = inputs.normal16_on((B, prompt, Hkv, d), gen)
+    ks = inputs.normal16_on((nsteps, B, 1, Hkv, d), gen)
+    vs = inputs.normal16_on((nsteps, B, 1, Hkv, d), gen)
+    qs = inputs.normal16_on((nsteps, B, Hq, d), gen)
+    pos = (prompt + torch.arange(nsteps, dtype=torch.int32, device=dev))[:, None]
+    pos = pos.expand(nsteps, B).contiguous()
+    caches = {w: swa.Cache(B, Hkv, d, w, s, device=dev) for w in D["windows"]}
+    wsp = {w: swa.workspace_for(caches[w], Hq) for w in D["windows"]}
+    od = {w: torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev) for w in D["windows"]}
     flush = L2Flush(dev)
 
-    side = torch.cuda.Stream(dev)  # the prompt's cache append, beside the prefill
+    # the launches of one step, in order: (kind, window, call, kernels it launches)
+    units = []
+    for w in P["windows"]:
+        units.append(("prefill", w, functools.partial(swa.prefill, q3, k3, v3, w, P["s"], out=o3), 1))
+    for w in D["windows"]:
+        c = caches[w]
+        units.append(("append", w, functools.partial(c.append, kp, vp, 0), 1))
+        nl = 1 + (1 if wsp[w] is not None else 0)
+        for i in range(nsteps):
+            units.append(("decode", w, functools.partial(
+                swa.append_decode, qs[i], ks[i], vs[i], c, pos[i], out=od[w], workspace=wsp[w]), nl))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in units]
 
-    def prefill_part():
-        # The prefill and the prompt's cache append read the same k, v and
-        # nothing of each other: the append runs on a second stream beside
-        # the prefill (joined before the decode token, which needs it).
-        cur = torch.cuda.current_stream(dev)
-        fork = torch.cuda.Event()
-        fork.record(cur)
-        side.wait_event(fork)
-        swa.prefill(q, k, v, w, s, out=o)
-        with torch.cuda.stream(side):
-            cache.append(k, v, 0)
-        join = torch.cuda.Event()
-        join.record(side)
-        cur.wait_event(join)
-
-    def cache_decode_part():
-        swa.append_decode(q1, k1, v1, cache, pos, out=od)  # the token's append + its decode
-
-    def step_part():
-        prefill_part()
-        cache_decode_part()
-
-    launches_per_step = 1 + 1 + 1 + (1 if swa.decode_workspace_bytes(B, Hq, Hkv, d, cache.cap, w) else 0)
-    stream = torch.cuda.current_stream(dev)
-    # Warm up once outside capture (sets kernel attributes), then capture the
-    # whole step as one CUDA graph (the timed step), and its two halves as
-    # graphs of their own (the kernel timings: events between graphs; timing
-    # events recorded inside a graph add nodes that slow it down).
-    step_part()
-    torch.cuda.synchronize()
-    graph, g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    cs = torch.cuda.Stream(dev)
-    cs.wait_stream(stream)
-    with torch.cuda.stream(cs):
-        with torch.cuda.graph(graph, stream=cs):
-            step_part()
-        with torch.cuda.graph(g1, stream=cs, pool=graph.pool()):
-            prefill_part()
-        with torch.cuda.graph(g2, stream=cs, pool=graph.pool()):
-            cache_decode_part()
-    stream.wait_stream(cs)
-    torch.cuda.synchronize()
-
-    # flush time, to stretch the timed region so clock samples land in it
-    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev_a.record()
-    for _ in range(5):
-        flush(1)
-    ev_b.record()
-    torch.cuda.synchronize()
-    t_flush = ev_a.elapsed_time(ev_b) / 5e3
-    flush_reps = max(1, math.ceil((0.6 / max(args.steps, 1)) / max(t_flush, 1e-6)))
-    flush_reps = min(flush_reps, 64)
+    def run_step():
+        for j, u in enumerate(units):
+            flush(j)
+            ev[j][0].record()
+            u[2]()
+            ev[j][1].record()
 
     for _ in range(args.warmup):
-        flush(1)
-        graph.replay()
-        flush(1)
-        g1.replay()
-        g2.replay()
+        run_step()
     torch.cuda.synchronize()
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     if sampler:
-        sampler.mark_start()
-    for i in range(args.steps):  # the timed steps
-        for _ in range(flush_reps):
-            flush(i)
-        ev[i][0].record()
-        graph.replay()
-        ev[i][1].record()
+        sampler.start("step")
+    per_step = []  # [step][unit] ms
+    for _ in range(args.steps):  # the timed steps
+        run_step()
+        torch.cuda.synchronize()
+        per_step.append([a.elapsed_time(b) for a, b in ev])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    for i in range(args.steps):  # the same steps in two halves: kernel times
-        for _ in range(flush_reps):
-            flush(i)
-        evk[i][0].record()
-        g1.replay()
-        evk[i][1].record()
-        g2.replay()
-        evk[i][2].record()
+    if sampler:
+        sampler.stop("step")
+
+    def mean_of(kind, w):
+        js = [j for j, u in enumerate(units) if u[0] == kind and u[1] == w]
+        return sum(t[j] for t in per_step for j in js) / (len(per_step) * len(js))
+
+    step_ms = sum(sum(t) for t in per_step) / len(per_step)
+    dec_ms = sum(sum(t[j] for j, u in enumerate(units) if u[0] == "decode")
+                 for t in per_step) / len(per_step)
+    pre_ms = {w: mean_of("prefill", w) for w in P["windows"]}
+    app_ms = {w: mean_of("append", w) for w in D["windows"]}
+    tok_ms = {w: mean_of("decode", w) for w in D["windows"]}
+
+    # ---- the 4096-token SWA(64,4) prefill (one sequence), launches timed alone
+    sq, sk, sv = inputs.prefill_inputs(S["B"], S["L"], S["Hq"], S["Hkv"], S["d"], seed=rank_seed(rank),
+                                       sink_rows=S["sink_rows"])
+    sq, sk, sv = sq.to(dev), sk.to(dev), sv.to(dev)
+    so = torch.empty_like(sq)
+    n_small = max(20, args.steps)
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_small)]
+    for i in range(3):
+        flush(i)
+        swa.prefill(sq, sk, sv, S["w"], S["s"], out=so)
+    if sampler:
+        sampler.start("small")
+    for i in range(n_small):
+        flush(i)
+        sev[i][0].record()
+        swa.prefill(sq, sk, sv, S["w"], S["s"], out=so)
+        sev[i][1].record()
     torch.cuda.synchronize()
     if sampler:
-        sampler.mark_end()
-    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    pre_ms = [e[0].elapsed_time(e[1]) for e in evk]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evk]
-    mean_step = sum(step_ms) / len(step_ms)
-    mean_pre = sum(pre_ms) / len(pre_ms)
-    mean_dec = sum(dec_ms) / len(dec_ms)
+        sampler.stop("small")
+    small_ms = sum(a.elapsed_time(b) for a, b in sev) / n_small
 
-    # ---- end to end: pinned host buffers, copies inside the timed region.
-    # Each step copies its inputs up (q, k, v of the prompt, the decode
-    # token's k, v, q), runs the library calls and copies both outputs back.
-    # Host <-> device copies run at about 200 GB/s per direction here, so
-    # they dominate; as a serving loop with double-buffered I/O does, the
-    # steps overlap: step i+1's inputs go up on one stream while step i
-    # computes and its outputs come back on another (two sets of device and
-    # host buffers).  value = steps / total time; every step's copies are in
-    # the timed region.  The serial figure (one step at a time, synchronised
-    # after each) is reported beside it.
-    names = ("q", "k", "v", "k1", "v1", "q1")
-    src = dict(q=q_h, k=k_h, v=v_h, k1=k1_h, v1=v1_h, q1=q1_h)
-    host = [{n: src[n].pin_memory() for n in names} for _ in range(2)]
-    devb = [dict(q=q, k=k, v=v, k1=k1, v1=v1, q1=q1, o=o, od=od),
-            {**{n: torch.empty_like(src[n], device=dev) for n in names},
-             "o": torch.empty_like(o), "od": torch.empty_like(od)}]
-    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
-    od_host = [torch.empty(od.shape, dtype=od.dtype, pin_memory=True) for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
-    d2h = o_host[0].numel() * 2 + od_host[0].numel() * 2
+    # ---- end to end: the decode stream through the public API with host
+    # buffers.  Each step's inputs (q, k, v packed in one pinned host row)
+    # go up, append_decode runs, its output comes back; consecutive steps
+    # overlap (step i+1's copy up while step i computes and step i-1's output
+    # comes down: double-buffered device buffers).  Every copy is inside the
+    # timed region.
+    nq, nkv = B * Hq * d, B * Hkv * d
+    host_in = torch.empty(nsteps, nq + 2 * nkv, dtype=torch.bfloat16, pin_memory=True)
+    host_in[:, :nq] = qs.reshape(nsteps, nq).cpu()
+    host_in[:, nq:nq + nkv] = ks.reshape(nsteps, nkv).cpu()
+    host_in[:, nq + nkv:] = vs.reshape(nsteps, nkv).cpu()
+    host_out = torch.empty(nsteps, B, Hq, d, dtype=torch.bfloat16, pin_memory=True)
+    dev_in = [torch.empty(nq + 2 * nkv, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    views = [(b[:nq].view(B, Hq, d), b[nq:nq + nkv].view(B, 1, Hkv, d), b[nq + nkv:].view(B, 1, Hkv, d))
+             for b in dev_in]
+    dev_out = [torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     up, down, comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.current_stream(dev)
 
-    def e2e_step(i, done):
-        # done[j] = (inputs consumed, outputs read back) events of step j
-        b, hb = devb[i & 1], host[i & 1]
-        if i >= 2:  # this buffer set was step i-2's
-            up.wait_event(done[i - 2][0])
-        with torch.cuda.stream(up):
-            for n in names:
-                b[n].copy_(hb[n], non_blocking=True)
-        e_up = torch.cuda.Event()
-        e_up.record(up)
-        comp.wait_event(e_up)
-        if i >= 2:
-            comp.wait_event(done[i - 2][1])
-        fork = torch.cuda.Event()
-        fork.record(comp)
-        side.wait_event(fork)
-        swa.prefill(b["q"], b["k"], b["v"], w, s, out=b["o"])
-        with torch.cuda.stream(side):
-            cache.append(b["k"], b["v"], 0)
-        join = torch.cuda.Event()
-        join.record(side)
-        comp.wait_event(join)
-        swa.append_decode(b["q1"], b["k1"], b["v1"], cache, pos, out=b["od"])
-        e_comp = torch.cuda.Event()
-        e_comp.record(comp)
-        down.wait_event(e_comp)
-        with torch.cuda.stream(down):
-            o_host[i & 1].copy_(b["o"], non_blocking=True)
-            od_host[i & 1].copy_(b["od"], non_blocking=True)
-        e_down = torch.cuda.Event()
-        e_down.record(down)
-        done.append((e_comp, e_down))
-
-    for _ in range(max(3, min(args.warmup, 10))):
-        e2e_step(0, [])
+    def e2e_stream(w):
+        c = caches[w]
+        c.append(kp, vp, 0)  # back to the post-prompt state (device inputs; untimed)
         torch.cuda.synchronize()
-    n_e2e = max(4, min(args.steps, 200))
-    # serial: one step at a time
-    serial_ms = []
-    for i in range(min(n_e2e, 20)):
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(up)
-        e2e_step(0, [])
-        down.wait_stream(comp)
-        b_.record(down)
+        done = []
+        for i in range(nsteps):
+            j = i & 1
+            if i >= 2:  # dev_in[j] was read by step i-2's kernel
+                up.wait_event(done[i - 2][0])
+            with torch.cuda.stream(up):
+                dev_in[j].copy_(host_in[i], non_blocking=True)
+            e_up = torch.cuda.Event()
+            e_up.record(up)
+            comp.wait_event(e_up)
+            if i >= 2:  # dev_out[j] was read back by step i-2's copy
+                comp.wait_event(done[i - 2][1])
+            qv, kv, vv = views[j]
+            swa.append_decode(qv, kv, vv, c, pos[i], out=dev_out[j], workspace=wsp[w])
+            e_comp = torch.cuda.Event()
+            e_comp.record(comp)
+            down.wait_event(e_comp)
+            with torch.cuda.stream(down):
+                host_out[i].copy_(dev_out[j], non_blocking=True)
+            e_down = torch.cuda.Event()
+            e_down.record(down)
+            done.append((e_comp, e_down))
+        up.wait_stream(down)
+        up.wait_stream(comp)
+        b_.record(up)
         b_.synchronize()
-        serial_ms.append(a.elapsed_time(b_))
-    mean_e2e_serial = sum(serial_ms) / len(serial_ms)
-    # overlapped: n_e2e steps back to back
-    torch.cuda.synchronize()
-    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(up)
-    done = []
-    for i in range(n_e2e):
-        e2e_step(i, done)
-    up.wait_stream(down)
-    up.wait_stream(comp)
-    b_.record(up)
-    b_.synchronize()
-    mean_e2e = a.elapsed_time(b_) / n_e2e
+        return a.elapsed_time(b_)
 
-    # ---- max over ranks
+    for w in D["windows"]:  # warm-up
+        e2e_stream(w)
+    if sampler:
+        sampler.start("e2e")
+    e2e_ms = sum(e2e_stream(w) for w in D["windows"])
+    if sampler:
+        sampler.stop("e2e")
+    h2d = len(D["windows"]) * nsteps * (nq + 2 * nkv) * 2
+    d2h = len(D["windows"]) * nsteps * nq * 2
+
+    # ---- flatness: the decode context sweep
+    flat = flatness_sweep(dev, flush, sampler)
+
+    vals = [step_ms, dec_ms, small_ms, e2e_ms] + [pre_ms[w] for w in P["windows"]] + \
+        [app_ms[w] for w in D["windows"]] + [tok_ms[w] for w in D["windows"]]
     if world > 1:
-        mean_step, mean_pre, mean_dec, mean_e2e, mean_e2e_serial = max_over_ranks(
-            [mean_step, mean_pre, mean_dec, mean_e2e, mean_e2e_serial], dev)
-
+        vals = max_over_ranks(vals, dev)
+    step_ms, dec_ms, small_ms, e2e_ms = vals[:4]
+    rest = vals[4:]
+    pre_ms = dict(zip(P["windows"], rest[:len(P["windows"])]))
+    rest = rest[len(P["windows"]):]
+    app_ms = dict(zip(D["windows"], rest[:len(D["windows"])]))
+    tok_ms = dict(zip(D["windows"], rest[len(D["windows"]):]))
     if rank != 0:
         return
-    tokens = tokens_per_step(world)
-    value = tokens / (mean_step * 1e-3)
-    pk = peaks()
-    pbytes = prefill_bytes(B, L, Hq, Hkv, d)
-    pflops = prefill_flops(B, L, Hq, d, w)
-    n_valid = min(L + 1, w)
-    dbytes = decode_bytes(B, Hq, Hkv, d, n_valid)
-    achieved_gbs = pbytes / (mean_pre * 1e-3) / 1e9
-    tflops = pflops / (mean_pre * 1e-3) / 1e12
-    clocks = sampler.result() if sampler else None
-    cpu = None
-    if world == 1:
-        cpu = cpu_baseline()
+
+    tokens = decoded_tokens_per_step(world)
+    value = tokens / (dec_ms * 1e-3)
+    rl, shares = {}, {}
+    prefill_key = {}
+    for w in P["windows"]:
+        fl = prefill_flops(P["B"], P["L"], P["Hq"], P["d"], w)
+        by = prefill_bytes(P["B"], P["L"], P["Hq"], P["Hkv"], P["d"])
+        e = roofline_entry("swa_prefill_kernel", pre_ms[w], fl, by, pk)
+        e["traffic"] = kernel_traffic("swa_prefill.cu", prefill_workload(w))
+        e["workload"] = prefill_workload(w)
+        rl[f"prefill_w{w}"] = e
+        shares[f"prefill_w{w}"] = pre_ms[w] / step_ms
+        prefill_key[f"w{w}"] = {"ms": pre_ms[w], "tflops": e["tflops"],
+                                "frac_tensor_peak": e["tflops"] / pk["bf16_tflops"],
+                                "frac_attainable": e["frac_of_attainable"],
+                                "attainable_tflops": e["attainable_tflops"], "gbs": e["gbs"],
+                                "algorithmic_gflop": fl / 1e9}
+    decode_key = {}
+    for w in D["windows"]:
+        nv = min(prompt + 1, w)
+        by = decode_bytes(B, Hq, Hkv, d, nv)
+        kv = kv_read_bytes(B, Hkv, d, nv)
+        e = roofline_entry("swa_decode_kernel (append_decode)", tok_ms[w], 4.0 * d * Hq * B * nv, by, pk)
+        e["traffic"] = kernel_traffic("swa_decode.cu", decode_workload(w))
+        e["workload"] = decode_workload(w)
+        rl[f"decode_w{w}"] = e
+        shares[f"decode_w{w}"] = tok_ms[w] * nsteps / step_ms
+        shares[f"append_w{w}"] = app_ms[w] / step_ms
+        decode_key[f"w{w}"] = {"ms_step": tok_ms[w], "tok_s": B * world / (tok_ms[w] * 1e-3),
+                               "kv_read_gbs": kv / (tok_ms[w] * 1e-3) / 1e9,
+                               "frac_hbm": e["frac"], "bytes_per_step": by,
+                               "kv_bytes_per_step": kv, "cache_bytes": 2 * B * Hkv * w * d * 2,
+                               "prompt_append_ms": app_ms[w]}
+    dom = max((k for k in rl), key=lambda k: shares[k])
+    roof = {k: rl[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+    roof.update({"traffic": rl[dom]["traffic"], "kernel": rl[dom]["kernel"], "which": dom,
+                 "workload": rl[dom]["workload"],
+                 "share_of_step": shares[dom],
+                 "algorithmic_bytes_per_launch": rl[dom]["algorithmic_bytes_per_launch"],
+                 "peak_source": rl[dom]["peak_source"]})
+    sb = prefill_bytes(S["B"], S["L"], S["Hq"], S["Hkv"], S["d"])
+    sf = prefill_flops(S["B"], S["L"], S["Hq"], S["d"], S["w"])
+    small_rl = roofline_entry("swa_prefill_kernel", small_ms, sf, sb, pk)
+    small_rl["traffic"] = kernel_traffic("swa_prefill.cu", SMALL_WORKLOAD)
+    launches = sum(u[3] for u in units) * args.steps
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, "global_batch": B * world, "seq_len": L,
-                   "window": w, "sinks": s, "l2": L2_NOTE,
-                   "timing": "CUDA events around the replay of the step, captured as one CUDA graph; the prefill and decode times from the same steps replayed as two graphs, events between them"},
-        "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved_gbs / pk["hbm_gbs"],
-                     "traffic": prefill_traffic(), "kernel": "swa_prefill_kernel",
-                     "algorithmic_bytes_per_launch": pbytes,
-                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
-        "prefill": {"ms": mean_pre, "tflops": tflops, "frac_tensor_peak": tflops / pk["bf16_tflops"],
-                    "gbs": achieved_gbs, "algorithmic_gflop": pflops / 1e9},
-        "decode": {"ms_append_and_decode": mean_dec, "tok_s": B * world / (mean_dec * 1e-3),
-                   "kv_bytes": dbytes,
-                   "note": "one token after the prompt (one append_decode; the prompt's cache "
-                           "append runs beside the prefill); B=1 is latency-bound"},
-        "e2e": {"value": tokens / (mean_e2e * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": mean_e2e,
-                "timing": f"{n_e2e} steps back to back, the copies of consecutive steps "
-                          "overlapping (double-buffered host and device buffers)",
-                "serial": {"value": tokens / (mean_e2e_serial * 1e-3), "ms_per_step": mean_e2e_serial,
-                           "timing": "one step at a time, synchronised after each"}},
-        "clocks": clocks,
+        "config": line_config(world),
+        "timing": ("every launch of the step timed alone: CUDA events on its stream around it, "
+                   "L2 flushed before it; ms_per_step = the step's summed launch times; value = "
+                   "decoded_tokens_per_step / ms_decode_per_step"),
+        "decoded_tokens_per_step": tokens, "ms_decode_per_step": dec_ms,
+        "gpu_launches": launches,
+        "roofline": roof,
+        "decode": decode_key,
+        "prefill": prefill_key,
+        "rooflines": rl,
+        "time_shares": shares,
+        "small_prefill": {"workload": SMALL_WORKLOAD, "ms": small_ms, "roofline": small_rl,
+                          "tok_s": S["B"] * S["L"] / (small_ms * 1e-3),
+                          "clocks": sampler.result("small") if sampler else None},
+        "flatness": flat,
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "timing": "the 1024-step decode stream of each window through the Python API "
+                          "(append_decode): every step's q, k, v copied up from pinned host "
+                          "memory and its output copied back, steps overlapped (double-buffered "
+                          "device buffers), events around the whole stream",
+                "clocks": sampler.result("e2e") if sampler else None},
+        "clocks": sampler.result("step") if sampler else None,
     }
-    if cpu:
-        line["cpu_baseline"] = cpu
+    if world == 1:
+        from oracle import bits16
+        line["cpu_baseline"] = cpu_baseline(
+            bits16(kp), bits16(vp), [bits16(ks[i]) for i in range(CPU_DECODE_STEPS)],
+            [bits16(vs[i]) for i in range(CPU_DECODE_STEPS)],
+            [bits16(qs[i]) for i in range(CPU_DECODE_STEPS)], (bits16(q3), bits16(k3), bits16(v3)))
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline() -> dict:
-    """The oracle on a bounded sample of the same step (about 10-20 s of CPU work)."""
-    import oracle
-    oracle.build()
-    S = 512
-    run, tokens, orc, *_ = oracle_step_rate(S)
-    t0 = time.perf_counter()
-    n = 0
-    while True:
-        run()
-        n += 1
-        if time.perf_counter() - t0 > 10.0 or n >= 50:
-            break
-    dt = (time.perf_counter() - t0) / n
-    return {"value": tokens / dt, "unit": "tok/s", "cores": orc.threads(None), "kind": "oracle",
-            "sample": f"{S} of {WORK['L']} prompt positions (all heads) + cache append + 1 decode "
-                      f"token per step, {n} steps"}
+def flatness_sweep(dev, flush, sampler) -> dict:
+    """Decode tok/s of a 4-layer attention-only stack at positions 1K .. 256K
+    (every layer's cache in the state a prompt of that length leaves, N(0,1)
+    values; one step appends the token and decodes it in each layer, replayed
+    as one CUDA graph, L2 flushed before each replay).  Reports tok/s per
+    point and max/min over the positions for each finite window at batch 1
+    and 256; full causal at batch 1 for contrast."""
+    import torch
+
+    import sliding_window_attention_prefill_gb300 as swa
+    D = DECODE_CFG
+    Hq, Hkv, d, s = D["Hq"], D["Hkv"], D["d"], D["s"]
+    gen = torch.Generator(device=dev)
+    out = {"positions": FLAT_POSITIONS, "layers": FLAT_LAYERS, "reps_per_point": 20}
+    if sampler:
+        sampler.start("flatness")
+    pts = [(B, w) for B in FLAT_BATCHES for w in FLAT_WINDOWS] + [(1, -1)]
+    for B, w in pts:
+        toks = []
+        for P in FLAT_POSITIONS:
+            gen.manual_seed(B * 1000003 + P * 7 + (w + 1))
+            layers = []
+            for _ in range(FLAT_LAYERS):
+                c = swa.Cache(B, Hkv, d, w, s if w > 0 else 0, max_len=(P + 1 if w < 0 else None),
+                              device=dev)
+                c.k.normal_(generator=gen)
+                c.v.normal_(generator=gen)
+                kn = torch.randn(B, 1, Hkv, d, generator=gen, device=dev).to(torch.bfloat16)
+                vn = torch.randn(B, 1, Hkv, d, generator=gen, device=dev).to(torch.bfloat16)
+                q = torch.randn(B, Hq, d, generator=gen, device=dev).to(torch.bfloat16)
+                layers.append((c, kn, vn, q, torch.empty_like(q), swa.workspace_for(c, Hq)))
+            pos = torch.full((B,), P, dtype=torch.int32, device=dev)
+
+            def step():
+                for c, kn, vn, q, o, ws in layers:
+                    swa.append_decode(q, kn, vn, c, pos, out=o, workspace=ws)
+
+            ms = _time_graph(step, out["reps_per_point"], flush)
+            toks.append(B / (ms * 1e-3))
+            del layers, step
+            torch.cuda.empty_cache()
+        key = f"B{B}_w{w}" if w > 0 else f"B{B}_full_causal"
+        out[key] = {"tok_s": toks, "max_over_min": max(toks) / min(toks)}
+    finite = [out[f"B{B}_w{w}"]["max_over_min"] for B in FLAT_BATCHES for w in FLAT_WINDOWS]
+    out["worst_max_over_min_finite_w"] = max(finite)
+    if sampler:
+        sampler.stop("flatness")
+        out["clocks"] = sampler.result("flatness")
+    return out
 
 
-# ----------------------------------------------------------------------------- suites
 def _time_graph(fn, steps: int, flush, warm: int = 3) -> float:
     """Mean ms of `fn` replayed as a CUDA graph, L2 flushed before each replay."""
     import torch
@@ -890,13 +1100,14 @@ def suite_context(steps: int, batches=(1, 256), shape: str = "llama", hybrid: bo
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["swa", "reference"], default="swa")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="reference arm: oracle time for the whole run (sizes its sample)")
     ap.add_argument("--suite", choices=["prefill", "decode", "context", "chunk", "varlen"], default=None,
                     help="auxiliary per-config lines instead of the headline step")
+    ap.add_argument("--reps", type=int, default=40, help="suites: timed replays per case")
     ap.add_argument("--w", type=int, default=None, help="prefill suite: only this window")
     ap.add_argument("--B", type=int, default=None, help="prefill suite: batch override")
     ap.add_argument("--L", type=int, default=None, help="prefill suite: length override")
@@ -909,19 +1120,19 @@ def main():
                          "paper: 16 heads of 64, fp16)")
     args = ap.parse_args()
     if args.suite == "prefill":
-        suite_prefill(max(args.steps // 10, 10), args.w, args.B, args.L)
+        suite_prefill(args.reps, args.w, args.B, args.L)
         return
     if args.suite == "decode":
-        suite_decode(max(args.steps // 4, 20), args.w, args.decode_steps)
+        suite_decode(args.reps, args.w, args.decode_steps)
         return
     if args.suite == "chunk":
-        suite_chunk(max(args.steps // 20, 10))
+        suite_chunk(max(args.reps // 2, 10))
         return
     if args.suite == "varlen":
-        suite_varlen(max(args.steps // 20, 10))
+        suite_varlen(max(args.reps // 2, 10))
         return
     if args.suite == "context":
-        suite_context(max(min(args.steps // 40, 20), 5),
+        suite_context(max(min(args.reps // 2, 20), 5),
                       tuple(int(b) for b in args.batches.split(",")), args.shape, args.hybrid)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -47,10 +47,36 @@ def test_decode_bytes():
 
 
 def test_the_bench_workload_figures():
-    """Prefill SWA(64,4), B=1, L=4096, 32 query and 8 key/value heads of 128:
-    Q and O of 32 MiB, K and V of 8 MiB; 4.26 GFLOP over the window."""
-    W = bench.WORK
-    assert bench.prefill_bytes(W["B"], W["L"], W["Hq"], W["Hkv"], W["d"]) == 83886080
-    assert bench.window_sum(W["L"], W["w"]) == 64 * 65 // 2 + (4096 - 64) * 64
-    assert bench.prefill_flops(W["B"], W["L"], W["Hq"], W["d"], W["w"]) == 4261937152
-    assert bench.tokens_per_step(1) == 4097
+    """The configurations the line measures, Llama attention shape (32 query
+    and 8 key/value heads of 128, bf16).
+    Prefill B=2, L=32768: Q and O of 512 MiB, K and V of 128 MiB; 137.2,
+    273.8 and 545.5 GFLOP over the windows 128, 256, 512.
+    Decode B=64 after a 4096-token prompt: the cache holds w slots, each
+    step reads K and V of all of them (128 MiB at w=512) and 2 x 64 x 1024
+    tokens are decoded per step.
+    The 4096-token SWA(64,4) prompt: Q and O of 32 MiB, K and V of 8 MiB."""
+    P, D, S = bench.PREFILL_CFG, bench.DECODE_CFG, bench.SMALL_PREFILL
+    assert bench.prefill_bytes(P["B"], P["L"], P["Hq"], P["Hkv"], P["d"]) == 1342177280
+    gf = [bench.prefill_flops(P["B"], P["L"], P["Hq"], P["d"], w) / 1e9 for w in P["windows"]]
+    assert [round(x, 1) for x in gf] == [137.2, 273.8, 545.5]
+    assert bench.window_sum(P["L"], 512) == 512 * 513 // 2 + (32768 - 512) * 512
+    assert bench.kv_read_bytes(D["B"], D["Hkv"], D["d"], 512) == 128 << 20
+    assert bench.decode_bytes(D["B"], D["Hq"], D["Hkv"], D["d"], 512) == 135790592
+    assert bench.decoded_tokens_per_step(1) == 131072
+    assert bench.prefill_bytes(S["B"], S["L"], S["Hq"], S["Hkv"], S["d"]) == 83886080
+    assert bench.prefill_flops(S["B"], S["L"], S["Hq"], S["d"], S["w"]) == 4261937152
+
+
+def test_roofline_entry_picks_the_bound_by_intensity():
+    pk = {"hbm_gbs": 6794.5, "bf16_tflops": 1924.1, "source": "measured"}
+    P = bench.PREFILL_CFG
+    by = bench.prefill_bytes(P["B"], P["L"], P["Hq"], P["Hkv"], P["d"])
+    for w, bound in [(128, "hbm"), (256, "hbm"), (512, "tensor")]:
+        fl = bench.prefill_flops(P["B"], P["L"], P["Hq"], P["d"], w)
+        e = bench.roofline_entry("k", 1.0, fl, by, pk)
+        assert e["bound"] == bound
+        if bound == "tensor":
+            assert abs(e["achieved"] - fl / 1e-3 / 1e12) < 1e-6 * e["achieved"]
+        else:
+            assert abs(e["achieved"] - by / 1e-3 / 1e9) < 1e-6 * e["achieved"]
+        assert abs(e["frac"] - e["achieved"] / e["peak"]) < 1e-12

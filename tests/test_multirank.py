@@ -47,5 +47,6 @@ def test_max_over_ranks_and_seeds():
 
 
 def test_tokens_scale_with_ranks():
-    assert bench.tokens_per_step(4) == 4 * bench.tokens_per_step(1)
-    assert bench.tokens_per_step(1) == bench.WORK["B"] * (bench.WORK["L"] + 1)
+    assert bench.decoded_tokens_per_step(4) == 4 * bench.decoded_tokens_per_step(1)
+    D = bench.DECODE_CFG
+    assert bench.decoded_tokens_per_step(1) == len(D["windows"]) * D["B"] * D["steps"]
