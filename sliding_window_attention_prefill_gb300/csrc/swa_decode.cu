@@ -89,10 +89,10 @@ struct DecSmem {
     static constexpr int kChunkBytes = (D / 64) * kRegion;  // one of K or V
     static constexpr int kQBytes = G * D * 2;               // q of the G heads of the item
     static constexpr int kStage = 2 * kChunkBytes + ((kQBytes + 1023) & ~1023);  // K | V | q
-    static constexpr int kP = ST * kStage;          // [warp][16 slots][8 heads] bf16
-    static constexpr int kAcc = kP + kDecWarps * 16 * 8 * 2;  // [warp][G][D] f32
-    static constexpr int kML = kAcc + kDecWarps * G * D * 4;  // [warp][G][2] f32
-    static constexpr int kBar = kML + kDecWarps * G * 2 * 4;  // full[st], empty[st]
+    static constexpr int kSxRow = kDecCH + 8;       // one head's scores of a chunk (padded)
+    static constexpr int kSx = ST * kStage;         // [2 chunk parity][8 heads][kSxRow] f32
+    static constexpr int kOst = kSx + 2 * 8 * kSxRow * 4;  // [warp][G][D / 4] 16-bit output
+    static constexpr int kBar = kOst + kDecWarps * G * (D / kDecWarps) * 2;  // full[st], empty[st]
     static constexpr int kAbort = kBar + 2 * ST * 8;
     static constexpr int kBytes = kAbort + 16;
     static constexpr int kAlloc = kBytes + 1024;              // align the base to 1024
@@ -294,12 +294,20 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm[ST - 1])
     }
 
     // -------------------------------------------------------------------- consumers
-    const int gq = lane >> 2;  // mma group id: slot row g (and g+8), head g of B
-    const int tq = lane & 3;   // thread in group: heads 2t, 2t+1; k pairs 2t
-    uint16_t *psm = reinterpret_cast<uint16_t *>(sm + SL::kP) + warp * 16 * 8;
-    float *wacc = reinterpret_cast<float *>(sm + SL::kAcc);
-    float *wml = reinterpret_cast<float *>(sm + SL::kML);
-    const int slot0 = warp * 16;  // this warp's slots within a chunk
+    // Warp w computes the scores of slots 16w .. 16w+15 of each chunk (S^T =
+    // K Q^T on the tensor cores) and puts them, scaled to base 2, in shared
+    // memory.  After one barrier every warp runs the softmax over all 64 slots
+    // of the chunk -- lane (g, t) for head g -- and accumulates the d rows
+    // [D/4 w, D/4 (w+1)) of O^T over them, so that at the end of an item each
+    // warp holds the finished rows of its quarter of d: no merge across warps.
+    constexpr int MW = D / 64;          // m16 tiles of O^T per warp
+    constexpr int DW = D / kDecWarps;   // d rows per warp
+    constexpr int SXR = SL::kSxRow;
+    const int gq = lane >> 2;  // mma group id: slot row g (and g+8); softmax head g
+    const int tq = lane & 3;   // thread in group: heads 2t, 2t+1 of S^T and O^T; k pairs 2t
+    float *sx = reinterpret_cast<float *>(sm + SL::kSx);
+    uint16_t *ost = reinterpret_cast<uint16_t *>(sm + SL::kOst) + warp * G * DW;
+    const int slot0 = warp * 16;  // this warp's slots within a chunk (scores)
     int cg = 0;                   // chunks consumed by this CTA
 
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -316,13 +324,12 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm[ST - 1])
             prefetch_l1(p.k_new + src);
             prefetch_l1(p.v_new + src);
         }
-        float acc[KS][4];  // O^T: d = 16*mt + gq (+8), heads 2tq, 2tq+1
+        float acc[MW][4];  // O^T: d = DW*warp + 16*mt + gq (+8), heads 2tq, 2tq+1
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt)
+        for (int mt = 0; mt < MW; ++mt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY;  // running max, heads 2tq and 2tq+1
-        float l0 = 0.f, l1 = 0.f;              // this thread's share of the sums
+        float m_run = -INFINITY, l_run = 0.f;  // running max and sum of head gq (base 2)
         uint32_t qb[KS][2];                    // Q^T fragments; heads gq >= G are zero columns
 
         for (int c = 0; c < x.n_chunks; ++c, ++cg) {
@@ -362,146 +369,167 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm[ST - 1])
                 }
                 __syncwarp();
             }
-            if (mine > 0) {
-                const uint32_t kst = sbase + st * SL::kStage;
-                const uint32_t vst = kst + SL::kChunkBytes;
-                if (mine < 16) {
-                    // rows past the range hold whatever the cache has there: zero
-                    // the V rows so that 0-weights never meet a non-finite value
-                    uint8_t *vb = sm + st * SL::kStage + SL::kChunkBytes;
-                    for (int i = lane; i < (16 - mine) * (D / 8); i += 32) {
-                        const int r = slot0 + mine + i / (D / 8), cc = i % (D / 8);
-                        *reinterpret_cast<uint4 *>(vb + (cc >> 3) * SL::kRegion + r * 128 +
-                                                   ((cc & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    __syncwarp();
+            const uint32_t kst = sbase + st * SL::kStage;
+            const uint32_t vst = kst + SL::kChunkBytes;
+            if (mine < 16) {
+                // Every warp reads the V rows of all 64 slots: the rows of this
+                // warp's slots past the filled ones hold whatever the cache has
+                // there, so zero them (0-weights never meet a non-finite value).
+                uint8_t *vb = sm + st * SL::kStage + SL::kChunkBytes;
+                const int first = mine > 0 ? mine : 0;
+                for (int i = lane; i < (16 - first) * (D / 8); i += 32) {
+                    const int r = slot0 + first + i / (D / 8), cc = i % (D / 8);
+                    *reinterpret_cast<uint4 *>(vb + (cc >> 3) * SL::kRegion + r * 128 +
+                                               ((cc & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
-                // ---- S^T = K Q^T
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
+            }
+            // ---- S^T = K Q^T for this warp's 16 slots, into the exchange buffer
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            if (mine > 0) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     uint32_t a[4];
                     ldsm_x4(swz(kst, slot0 + (lane & 15), 2 * ks + (lane >> 4)), a);
                     mma_16816<DT>(s, a, qb[ks][0], qb[ks][1]);
                 }
-                // ---- online softmax per head over this warp's 16 slots
-                const bool va = gq < mine, vb_ = gq + 8 < mine;
-                const float s0 = va ? s[0] * p.scale_log2 : -INFINITY;   // slot g,   head 2t
-                const float s1 = va ? s[1] * p.scale_log2 : -INFINITY;   // slot g,   head 2t+1
-                const float s2 = vb_ ? s[2] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t
-                const float s3 = vb_ ? s[3] * p.scale_log2 : -INFINITY;  // slot g+8, head 2t+1
-                float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
-#pragma unroll
-                for (int msk = 4; msk < 32; msk <<= 1) {
-                    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, msk));
-                    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, msk));
-                }
-                float a0 = 1.f, a1 = 1.f;
-                if (x0 > m0 && (m0 == -INFINITY || x0 - m0 > 8.f)) {
-                    a0 = ex2_approx(m0 - x0);
-                    m0 = x0;
-                }
-                if (x1 > m1 && (m1 == -INFINITY || x1 - m1 > 8.f)) {
-                    a1 = ex2_approx(m1 - x1);
-                    m1 = x1;
-                }
-                if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
-                    l0 *= a0;
-                    l1 *= a1;
-#pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        acc[mt][0] *= a0;
-                        acc[mt][2] *= a0;
-                        acc[mt][1] *= a1;
-                        acc[mt][3] *= a1;
-                    }
-                }
-                const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
-                const float p0 = ex2_approx(s0 - u0), p1 = ex2_approx(s1 - u1);
-                const float p2 = ex2_approx(s2 - u0), p3 = ex2_approx(s3 - u1);
-                l0 += p0 + p2;
-                l1 += p1 + p3;
-                // ---- P^T through shared memory into the B-operand layout
-                *reinterpret_cast<uint32_t *>(psm + gq * 8 + 2 * tq) = pack2<DT>(p0, p1);
-                *reinterpret_cast<uint32_t *>(psm + (gq + 8) * 8 + 2 * tq) = pack2<DT>(p2, p3);
-                __syncwarp();
-                const uint32_t pb0 = static_cast<uint32_t>(psm[(2 * tq) * 8 + gq]) |
-                                     (static_cast<uint32_t>(psm[(2 * tq + 1) * 8 + gq]) << 16);
-                const uint32_t pb1 = static_cast<uint32_t>(psm[(2 * tq + 8) * 8 + gq]) |
-                                     (static_cast<uint32_t>(psm[(2 * tq + 9) * 8 + gq]) << 16);
-                // ---- O^T += V^T P^T
-                const int vrow = slot0 + ((lane >> 4) << 3) + (lane & 7);
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    uint32_t a[4];
-                    ldsm_x4_t(swz(vst, vrow, 2 * mt + ((lane >> 3) & 1)), a);
-                    mma_16816<DT>(acc[mt], a, pb0, pb1);
-                }
-                // zeroed or patched rows before the next TMA fill of this stage
-                if (mine < 16 || patch) fence_proxy_async_smem();
             }
+            float *sxb = sx + (cg & 1) * 8 * SXR;
+            {
+                const bool va = gq < mine, vb_ = gq + 8 < mine;
+                const int h0 = 2 * tq, h1 = 2 * tq + 1;
+                if (h0 < G) {
+                    sxb[h0 * SXR + slot0 + gq] = va ? s[0] * p.scale_log2 : -INFINITY;
+                    sxb[h0 * SXR + slot0 + gq + 8] = vb_ ? s[2] * p.scale_log2 : -INFINITY;
+                }
+                if (h1 < G) {
+                    sxb[h1 * SXR + slot0 + gq] = va ? s[1] * p.scale_log2 : -INFINITY;
+                    sxb[h1 * SXR + slot0 + gq + 8] = vb_ ? s[3] * p.scale_log2 : -INFINITY;
+                }
+            }
+            // scores, patched and zeroed rows of all four warps are in place
+            asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+            // ---- online softmax of head gq over the chunk's 64 slots: this
+            // lane takes slots 16kk + {2t, 2t+1, 2t+8, 2t+9}, kk = 0..3 (the
+            // ones its P^T fragments need); lanes 4g .. 4g+3 share head g
+            float v[16];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                float2 lo = make_float2(-INFINITY, -INFINITY), hi = lo;
+                if (gq < G) {
+                    lo = *reinterpret_cast<const float2 *>(sxb + gq * SXR + 16 * kk + 2 * tq);
+                    hi = *reinterpret_cast<const float2 *>(sxb + gq * SXR + 16 * kk + 2 * tq + 8);
+                }
+                v[4 * kk] = lo.x;
+                v[4 * kk + 1] = lo.y;
+                v[4 * kk + 2] = hi.x;
+                v[4 * kk + 3] = hi.y;
+            }
+            float xm = fmax3(v[0], v[1], v[2]);
+#pragma unroll
+            for (int i = 3; i < 15; i += 2) xm = fmax3(xm, v[i], v[i + 1]);
+            xm = fmaxf(xm, v[15]);
+            xm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, 1));
+            xm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, 2));
+            float alpha = 1.f;
+            if (xm > m_run && (m_run == -INFINITY || xm - m_run > 8.f)) {
+                alpha = ex2_approx(m_run - xm);
+                m_run = xm;
+            }
+            const float u = m_run == -INFINITY ? 0.f : m_run;
+            float ls = 0.f;
+            uint32_t pb[4][2];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float p0 = ex2_approx(v[4 * kk] - u), p1 = ex2_approx(v[4 * kk + 1] - u);
+                const float p2 = ex2_approx(v[4 * kk + 2] - u), p3 = ex2_approx(v[4 * kk + 3] - u);
+                ls += (p0 + p1) + (p2 + p3);
+                pb[kk][0] = pack2<DT>(p0, p1);
+                pb[kk][1] = pack2<DT>(p2, p3);
+            }
+            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+            l_run = l_run * alpha + ls;
+            // the O^T columns of this lane are heads 2t and 2t+1: their factors
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * tq) * 4);
+                const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * tq + 1) * 4);
+#pragma unroll
+                for (int mt = 0; mt < MW; ++mt) {
+                    acc[mt][0] *= a0;
+                    acc[mt][2] *= a0;
+                    acc[mt][1] *= a1;
+                    acc[mt][3] *= a1;
+                }
+            }
+            // ---- O^T rows of this warp += V^T P^T over the 64 slots
+            const int vrow = ((lane >> 4) << 3) + (lane & 7);
+#pragma unroll
+            for (int mt = 0; mt < MW; ++mt) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    uint32_t a[4];
+                    ldsm_x4_t(swz(vst, 16 * kk + vrow, 2 * (warp * MW + mt) + ((lane >> 3) & 1)), a);
+                    mma_16816<DT>(acc[mt], a, pb[kk][0], pb[kk][1]);
+                }
+            }
+            // zeroed or patched rows before the next TMA fill of this stage
+            if (mine < 16 || patch) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(st));
         }
 
-        // ---------------------------------------------------------------- merge
-        // sums over the 8 row groups of the warp (lanes with equal tq)
-#pragma unroll
-        for (int msk = 4; msk < 32; msk <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
-        }
-        // every consumer has finished reading the previous item's buffers
-        asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+        // ---------------------------------------------------------------- output
+        // Heads 2t and 2t+1 of this lane's O^T columns: their sums and maxima
+        // are held by lanes 8t and 8t+4.  Nothing is written for a position
+        // outside the cache.
+        const float l0 = __shfl_sync(0xffffffffu, l_run, (2 * tq) * 4);
+        const float l1 = __shfl_sync(0xffffffffu, l_run, (2 * tq + 1) * 4);
         const int h0 = 2 * tq, h1 = 2 * tq + 1;
+        const int64_t orow0 = static_cast<int64_t>(x.b) * p.Hq + x.kvh * G;  // first head's row
+        if (x.bad) continue;
+        if (p.splits == 1 && !p.partials) {
+            const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int d0 = 16 * mt + gq;
-            if (h0 < G) {
-                wacc[(warp * G + h0) * D + d0] = acc[mt][0];
-                wacc[(warp * G + h0) * D + d0 + 8] = acc[mt][2];
-            }
-            if (h1 < G) {
-                wacc[(warp * G + h1) * D + d0] = acc[mt][1];
-                wacc[(warp * G + h1) * D + d0 + 8] = acc[mt][3];
-            }
-        }
-        if (gq == 0) {
-            if (h0 < G) {
-                wml[(warp * G + h0) * 2 + 0] = m0;
-                wml[(warp * G + h0) * 2 + 1] = l0;
-            }
-            if (h1 < G) {
-                wml[(warp * G + h1) * 2 + 0] = m1;
-                wml[(warp * G + h1) * 2 + 1] = l1;
-            }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
-        // over the warps; thread t handles outputs t, t+128, ... (nothing is
-        // written for a position outside the cache)
-        for (int idx = threadIdx.x; idx < (x.bad ? 0 : G * D); idx += kDecWarps * 32) {
-            const int h = idx / D, e = idx - h * D;
-            float m = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, wml[(w * G + h) * 2]);
-            float l = 0.f, a = 0.f;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) {
-                const float wm = wml[(w * G + h) * 2];
-                const float f = (wm == -INFINITY) ? 0.f : ex2_approx(wm - m);
-                l = fmaf(wml[(w * G + h) * 2 + 1], f, l);
-                a = fmaf(wacc[(w * G + h) * D + e], f, a);
-            }
-            const int64_t orow = static_cast<int64_t>(x.b) * p.Hq + x.kvh * G + h;
-            if (p.splits == 1 && !p.partials) {
-                const float ov = l > 0.f ? a / l : 0.f;
-                p.o[orow * D + e] = round16<DT>(ov);
-            } else {
-                p.ws_acc[(orow * p.splits + x.split) * D + e] = a;
-                if (e == 0) {
-                    p.ws_ml[(orow * p.splits + x.split) * 2 + 0] = m;
-                    p.ws_ml[(orow * p.splits + x.split) * 2 + 1] = l;
+            for (int mt = 0; mt < MW; ++mt) {
+                const int dl = 16 * mt + gq;  // d row within this warp's quarter
+                if (h0 < G) {
+                    ost[h0 * DW + dl] = round16<DT>(acc[mt][0] * i0);
+                    ost[h0 * DW + dl + 8] = round16<DT>(acc[mt][2] * i0);
                 }
+                if (h1 < G) {
+                    ost[h1 * DW + dl] = round16<DT>(acc[mt][1] * i1);
+                    ost[h1 * DW + dl + 8] = round16<DT>(acc[mt][3] * i1);
+                }
+            }
+            __syncwarp();
+            // G heads x DW values of 16 bits as 16-byte vectors
+            constexpr int kVec = G * DW / 8;
+            if (lane < kVec) {
+                const int h = lane / (DW / 8), j = lane % (DW / 8);
+                *reinterpret_cast<uint4 *>(p.o + (orow0 + h) * D + DW * warp + 8 * j) =
+                    *reinterpret_cast<const uint4 *>(ost + h * DW + 8 * j);
+            }
+            __syncwarp();
+        } else {
+            // split partials: unnormalised O^T rows, and (max, sum) per head
+#pragma unroll
+            for (int mt = 0; mt < MW; ++mt) {
+                const int d0 = DW * warp + 16 * mt + gq;
+                if (h0 < G) {
+                    float *a0 = p.ws_acc + ((orow0 + h0) * p.splits + x.split) * D;
+                    a0[d0] = acc[mt][0];
+                    a0[d0 + 8] = acc[mt][2];
+                }
+                if (h1 < G) {
+                    float *a1 = p.ws_acc + ((orow0 + h1) * p.splits + x.split) * D;
+                    a1[d0] = acc[mt][1];
+                    a1[d0 + 8] = acc[mt][3];
+                }
+            }
+            if (warp == 0 && tq == 0 && gq < G) {
+                float *ml = p.ws_ml + ((orow0 + gq) * p.splits + x.split) * 2;
+                ml[0] = m_run;
+                ml[1] = l_run;
             }
         }
     }
