@@ -98,8 +98,8 @@ typedef enum {
  * w == SWA_W_INF or 0 <= s < w with s <= SWA_MAX_SINKS.  o and lse must not
  * overlap the inputs.  The band of keys a query tile needs is the sink block
  * plus the latest w-s keys before the tile ("Sliding-window beats linear
- * attention", section "Core method": zero new operators, only the mask
- * changes).
+ * attention", section "Core method": the method adds no operator and
+ * changes only the mask).
  */
 swa_status swa_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
                        int B, int L, int Hq, int Hkv, int d, int w, int s,

@@ -271,6 +271,7 @@ swa_status swa_check_prefill_chunk(const void *q, const void *k_new, const void 
 swa_status swa_prefill_chunk(const void *q, const void *k_new, const void *v_new, void *o,
                              float *lse, const swa_cache *cache, int n, int64_t pos0, int Hq,
                              void *workspace, size_t workspace_bytes, swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_prefill_chunk");
     const swa_status st = swa_check_prefill_chunk(q, k_new, v_new, o, lse, cache, n, pos0, Hq,
                                                   workspace, workspace_bytes);
     if (st != SWA_OK || n == 0 || cache->B == 0) return st;
@@ -297,6 +298,7 @@ swa_status swa_prefill_chunk(const void *q, const void *k_new, const void *v_new
 swa_status swa_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                           int B, int L, int Hq, int Hkv, int d, int w, int s, swa_dtype dtype,
                           swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_prefill_ex");
     if (!valid_dtype(dtype)) return SWA_ERR_INVALID_ARG;
     const swa_status st = swa_check_prefill(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s);
     if (st != SWA_OK || B == 0 || L == 0) return st;
@@ -345,6 +347,7 @@ swa_status swa_prefill_varlen(const void *q, const void *k, const void *v, void 
                               const int32_t *cu_seqlens, int B, int total, int max_len, int Hq,
                               int Hkv, int d, int w, int s, swa_dtype dtype, void *workspace,
                               size_t workspace_bytes, swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_prefill_varlen");
     const swa_status st = swa_check_prefill_varlen(q, k, v, o, lse, cu_seqlens, B, total, max_len,
                                                    Hq, Hkv, d, w, s, dtype, workspace,
                                                    workspace_bytes);
@@ -355,6 +358,7 @@ swa_status swa_prefill_varlen(const void *q, const void *k, const void *v, void 
 
 swa_status swa_cache_append(const swa_cache *cache, const void *k_new, const void *v_new, int n,
                             int64_t pos0, swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_cache_append");
     const swa_status st = swa_check_append(cache, k_new, v_new, n, pos0);
     if (st != SWA_OK) return st;
     return swa::append_launch(*cache, k_new, v_new, n, pos0, as_cuda(stream));
@@ -368,6 +372,7 @@ size_t swa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, int w)
 swa_status swa_decode(const void *q, const swa_cache *cache, const int32_t *pos, int Hq, int w,
                       int s, void *o, void *workspace, size_t workspace_bytes,
                       swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_decode");
     if (cache == nullptr) return SWA_ERR_INVALID_ARG;
     const int sms = swa::device_sm_count();
     if (sms <= 0) return swa::cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
@@ -383,6 +388,7 @@ swa_status swa_append_decode(const void *q, const void *k_new, const void *v_new
                              const swa_cache *cache, const int32_t *pos, int Hq, int w, int s,
                              void *o, void *workspace, size_t workspace_bytes,
                              swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_append_decode");
     if (cache == nullptr) return SWA_ERR_INVALID_ARG;
     const int sms = swa::device_sm_count();
     if (sms <= 0) return swa::cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
@@ -431,6 +437,7 @@ swa_status check_linear_state(const swa_linear_state *st, const swa_cache *c) {
 swa_status swa_hybrid_append(const swa_cache *cache, const swa_linear_state *state,
                              const void *k_new, const void *v_new, int n, int64_t pos0,
                              swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_hybrid_append");
     swa_status st = swa_check_append(cache, k_new, v_new, n, pos0);
     if (st != SWA_OK) return st;
     st = check_linear_state(state, cache);
@@ -450,6 +457,7 @@ size_t swa_hybrid_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int cap,
 swa_status swa_hybrid_decode(const void *q, const swa_cache *cache, const swa_linear_state *state,
                              const int32_t *pos, int Hq, int w, int s, void *o, void *workspace,
                              size_t workspace_bytes, swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_hybrid_decode");
     if (cache == nullptr) return SWA_ERR_INVALID_ARG;
     const int sms = swa::device_sm_count();
     if (sms <= 0) return swa::cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
@@ -465,10 +473,12 @@ swa_status swa_hybrid_decode(const void *q, const swa_cache *cache, const swa_li
 }
 
 swa_status swa_selftest_wait_timeout(swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_selftest_wait_timeout");
     return swa::selftest_wait_launch(as_cuda(stream));
 }
 
 swa_status swa_get_device_error(swa_stream_t stream) {
+    SWA_NVTX_RANGE("swa_get_device_error");
     const int a = swa::prefill_read_clear_error(as_cuda(stream));
     const int b = swa::decode_read_clear_error(as_cuda(stream));
     if (a == SWA_ERR_CUDA || b == SWA_ERR_CUDA) return SWA_ERR_CUDA;

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -18,6 +19,17 @@ typedef CUresult (*cuTensorMapEncodeTiled_fn)(CUtensorMap *, CUtensorMapDataType
                                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 namespace swa {
+
+// One NVTX range around each call of the C ABI that enqueues GPU work, named
+// after the call, so a profiler timeline shows which call launched which
+// kernels.  With no tool attached an NVTX call only tests a function pointer.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define SWA_NVTX_RANGE(name) const ::swa::NvtxRange swa_nvtx_range_(name)
 
 // Driver entry point for tensor-map encoding (resolved once through the
 // runtime, so the library needs no link-time dependency on libcuda).
