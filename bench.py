@@ -811,9 +811,9 @@ def suite_prefill(steps: int, only_w=None, B_=None, L_=None):
         torch.cuda.empty_cache()
 
 
-def suite_decode(steps: int, only_w=None, n_steps: int = 1024):
-    """Decode configuration: B=64, Hq=32, Hkv=8, d=128, SWA(w,4) for w in
-    {64, 512}; the cache is filled from a 4096-token N(0,1) prompt, then
+def suite_decode(steps: int, only_w=None, n_steps: int = 1024, B_=None):
+    """Decode configuration: B=64 (or B_), Hq=32, Hkv=8, d=128, SWA(w,4) for w
+    in {64, 512}; the cache is filled from a 4096-token N(0,1) prompt, then
     `n_steps` decode steps each append one N(0,1) token and decode it (one
     append_decode call).  Every step is its own captured CUDA graph; L2 is
     flushed before each step.  Also times the decode kernel alone."""
@@ -824,13 +824,17 @@ def suite_decode(steps: int, only_w=None, n_steps: int = 1024):
     build.build()
     pk = peaks()
     flush = L2Flush()
-    B, Hq, Hkv, d, s, prompt = 64, 32, 8, 128, 4, 4096
+    B, Hq, Hkv, d, s, prompt = B_ or 64, 32, 8, 128, 4, 4096
     for w in [x for x in (64, 512) if only_w is None or x == only_w]:
-        kp, vp, ks, vs, qs = inputs.decode_stream(B, Hq, Hkv, d, prompt, n_steps, seed=0)
+        gen = inputs.device_generator(0)
+        kp = inputs.normal16_on((B, prompt, Hkv, d), gen)
+        vp = inputs.normal16_on((B, prompt, Hkv, d), gen)
+        ks = inputs.normal16_on((n_steps, B, 1, Hkv, d), gen)
+        vs = inputs.normal16_on((n_steps, B, 1, Hkv, d), gen)
+        qs = inputs.normal16_on((n_steps, B, Hq, d), gen)
         c = swa.Cache(B, Hkv, d, w, s)
-        c.append(kp.cuda(), vp.cuda(), 0)
+        c.append(kp, vp, 0)
         del kp, vp
-        ks, vs, qs = ks.cuda(), vs.cuda(), qs.cuda()
         pos = (prompt + torch.arange(n_steps, dtype=torch.int32, device="cuda"))[:, None]
         pos = pos.expand(n_steps, B).contiguous()
         od = torch.empty_like(qs[0])
@@ -1109,7 +1113,7 @@ def main():
                     help="auxiliary per-config lines instead of the headline step")
     ap.add_argument("--reps", type=int, default=40, help="suites: timed replays per case")
     ap.add_argument("--w", type=int, default=None, help="prefill suite: only this window")
-    ap.add_argument("--B", type=int, default=None, help="prefill suite: batch override")
+    ap.add_argument("--B", type=int, default=None, help="prefill and decode suites: batch override")
     ap.add_argument("--L", type=int, default=None, help="prefill suite: length override")
     ap.add_argument("--decode-steps", type=int, default=1024, help="decode suite: steps")
     ap.add_argument("--batches", type=str, default="1,256", help="context suite: batch sizes")
@@ -1123,7 +1127,7 @@ def main():
         suite_prefill(args.reps, args.w, args.B, args.L)
         return
     if args.suite == "decode":
-        suite_decode(args.reps, args.w, args.decode_steps)
+        suite_decode(args.reps, args.w, args.decode_steps, args.B)
         return
     if args.suite == "chunk":
         suite_chunk(max(args.reps // 2, 10))
