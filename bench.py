@@ -500,6 +500,18 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         js = [j for j, u in enumerate(units) if u[0] == kind and u[1] == w]
         return sum(t[j] for t in per_step for j in js) / (len(per_step) * len(js))
 
+    # The cost of the measurement itself: an event pair with nothing between
+    # it, after a flush, timed the same way (reported beside the results;
+    # every figure above still includes it).
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(200)]
+    for i, (a, b_) in enumerate(eev):
+        flush(i)
+        a.record()
+        b_.record()
+    torch.cuda.synchronize()
+    event_pair_ms = sorted(a.elapsed_time(b_) for a, b_ in eev)[len(eev) // 2]
+
     step_ms = sum(sum(t) for t in per_step) / len(per_step)
     dec_ms = sum(sum(t[j] for j, u in enumerate(units) if u[0] == "decode")
                  for t in per_step) / len(per_step)
@@ -548,12 +560,12 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     dev_out = [torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     up, down, comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.current_stream(dev)
 
-    def e2e_stream(w):
+    def enqueue_stream(w, comp):
+        """Enqueue the window's 1024 steps (copy up, append_decode, copy down)
+        on comp and the two copy streams, forked from and joined back to comp."""
         c = caches[w]
-        c.append(kp, vp, 0)  # back to the post-prompt state (device inputs; untimed)
-        torch.cuda.synchronize()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(up)
+        up.wait_stream(comp)
+        down.wait_stream(comp)
         done = []
         for i in range(nsteps):
             j = i & 1
@@ -576,31 +588,70 @@ def run_swa(args, rank: int, world: int, local_rank: int):
             e_down = torch.cuda.Event()
             e_down.record(down)
             done.append((e_comp, e_down))
-        up.wait_stream(down)
-        up.wait_stream(comp)
-        b_.record(up)
+        comp.wait_stream(up)
+        comp.wait_stream(down)
+
+    def e2e_eager(w):
+        caches[w].append(kp, vp, 0)  # back to the post-prompt state (device inputs; untimed)
+        torch.cuda.synchronize()
+        comp = torch.cuda.current_stream(dev)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(comp)
+        enqueue_stream(w, comp)
+        b_.record(comp)
+        b_.synchronize()
+        return a.elapsed_time(b_)
+
+    # The same stream captured once as a CUDA graph per window (the calls are
+    # graph-replayable: positions and buffers live on the device) and
+    # replayed: the host's per-call overhead leaves the loop, every step's
+    # copies stay in it.
+    cap = torch.cuda.Stream(dev)
+    graphs = {}
+    for w in D["windows"]:
+        enqueue_stream(w, torch.cuda.current_stream(dev))  # warm-up outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                enqueue_stream(w, cap)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        torch.cuda.synchronize()
+        graphs[w] = g
+
+    def e2e_graph(w):
+        caches[w].append(kp, vp, 0)  # back to the post-prompt state (device inputs; untimed)
+        torch.cuda.synchronize()
+        comp = torch.cuda.current_stream(dev)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(comp)
+        graphs[w].replay()
+        b_.record(comp)
         b_.synchronize()
         return a.elapsed_time(b_)
 
     for w in D["windows"]:  # warm-up
-        e2e_stream(w)
+        e2e_graph(w)
     if sampler:
         sampler.start("e2e")
-    e2e_ms = sum(e2e_stream(w) for w in D["windows"])
+    e2e_ms = sum(e2e_graph(w) for w in D["windows"])
     if sampler:
         sampler.stop("e2e")
+    e2e_eager_ms = sum(e2e_eager(w) for w in D["windows"])
+    del graphs
     h2d = len(D["windows"]) * nsteps * (nq + 2 * nkv) * 2
     d2h = len(D["windows"]) * nsteps * nq * 2
 
     # ---- flatness: the decode context sweep
     flat = flatness_sweep(dev, flush, sampler)
 
-    vals = [step_ms, dec_ms, small_ms, e2e_ms] + [pre_ms[w] for w in P["windows"]] + \
+    vals = [step_ms, dec_ms, small_ms, e2e_ms, event_pair_ms, e2e_eager_ms] + [pre_ms[w] for w in P["windows"]] + \
         [app_ms[w] for w in D["windows"]] + [tok_ms[w] for w in D["windows"]]
     if world > 1:
         vals = max_over_ranks(vals, dev)
-    step_ms, dec_ms, small_ms, e2e_ms = vals[:4]
-    rest = vals[4:]
+    step_ms, dec_ms, small_ms, e2e_ms, event_pair_ms, e2e_eager_ms = vals[:6]
+    rest = vals[6:]
     pre_ms = dict(zip(P["windows"], rest[:len(P["windows"])]))
     rest = rest[len(P["windows"]):]
     app_ms = dict(zip(D["windows"], rest[:len(D["windows"])]))
@@ -631,6 +682,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         by = decode_bytes(B, Hq, Hkv, d, nv)
         kv = kv_read_bytes(B, Hkv, d, nv)
         e = roofline_entry("swa_decode_kernel (append_decode)", tok_ms[w], 4.0 * d * Hq * B * nv, by, pk)
+        e["frac_without_event_pair"] = by / ((tok_ms[w] - event_pair_ms) * 1e-3) / 1e9 / pk["hbm_gbs"]
         e["traffic"] = kernel_traffic("swa_decode.cu", decode_workload(w))
         e["workload"] = decode_workload(w)
         rl[f"decode_w{w}"] = e
@@ -662,6 +714,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
                    "L2 flushed before it; ms_per_step = the step's summed launch times; value = "
                    "decoded_tokens_per_step / ms_decode_per_step"),
         "decoded_tokens_per_step": tokens, "ms_decode_per_step": dec_ms,
+        "event_pair_us": event_pair_ms * 1e3,
         "gpu_launches": launches,
         "roofline": roof,
         "decode": decode_key,
@@ -675,9 +728,12 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "timing": "the 1024-step decode stream of each window through the Python API "
-                          "(append_decode): every step's q, k, v copied up from pinned host "
-                          "memory and its output copied back, steps overlapped (double-buffered "
-                          "device buffers), events around the whole stream",
+                          "(append_decode), captured once as a CUDA graph and replayed: every "
+                          "step's q, k, v copied up from pinned host memory and its output "
+                          "copied back, steps overlapped (double-buffered device buffers, "
+                          "copies on two streams of their own), events around the replay",
+                "eager": {"value": tokens / (e2e_eager_ms * 1e-3), "ms_per_step": e2e_eager_ms,
+                          "timing": "the same stream issued call by call from Python"},
                 "clocks": sampler.result("e2e") if sampler else None},
         "clocks": sampler.result("step") if sampler else None,
     }
@@ -694,7 +750,9 @@ def flatness_sweep(dev, flush, sampler) -> dict:
     """Decode tok/s of a 4-layer attention-only stack at positions 1K .. 256K
     (every layer's cache in the state a prompt of that length leaves, N(0,1)
     values; one step appends the token and decodes it in each layer, replayed
-    as one CUDA graph, L2 flushed before each replay).  Reports tok/s per
+    as one CUDA graph, L2 flushed before each replay; the median of 50
+    replays per point, since a batch-1 step of ~70 µs is launch-bound and a
+    mean would carry the launch jitter).  Reports tok/s per
     point and max/min over the positions for each finite window at batch 1
     and 256; full causal at batch 1 for contrast."""
     import torch
@@ -703,7 +761,8 @@ def flatness_sweep(dev, flush, sampler) -> dict:
     D = DECODE_CFG
     Hq, Hkv, d, s = D["Hq"], D["Hkv"], D["d"], D["s"]
     gen = torch.Generator(device=dev)
-    out = {"positions": FLAT_POSITIONS, "layers": FLAT_LAYERS, "reps_per_point": 20}
+    out = {"positions": FLAT_POSITIONS, "layers": FLAT_LAYERS, "reps_per_point": 50,
+           "statistic": "median of the replays"}
     if sampler:
         sampler.start("flatness")
     pts = [(B, w) for B in FLAT_BATCHES for w in FLAT_WINDOWS] + [(1, -1)]
@@ -727,7 +786,7 @@ def flatness_sweep(dev, flush, sampler) -> dict:
                 for c, kn, vn, q, o, ws in layers:
                     swa.append_decode(q, kn, vn, c, pos, out=o, workspace=ws)
 
-            ms = _time_graph(step, out["reps_per_point"], flush)
+            ms = _time_graph(step, out["reps_per_point"], flush, stat="median")
             toks.append(B / (ms * 1e-3))
             del layers, step
             torch.cuda.empty_cache()
@@ -741,8 +800,9 @@ def flatness_sweep(dev, flush, sampler) -> dict:
     return out
 
 
-def _time_graph(fn, steps: int, flush, warm: int = 3) -> float:
-    """Mean ms of `fn` replayed as a CUDA graph, L2 flushed before each replay."""
+def _time_graph(fn, steps: int, flush, warm: int = 3, stat: str = "mean") -> float:
+    """Mean (or median) ms of `fn` replayed as a CUDA graph, L2 flushed before
+    each replay."""
     import torch
     fn()
     torch.cuda.synchronize()
@@ -765,7 +825,10 @@ def _time_graph(fn, steps: int, flush, warm: int = 3) -> float:
         g.replay()
         evs[i][1].record()
     torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in evs) / steps
+    t = [a.elapsed_time(b) for a, b in evs]
+    if stat == "median":
+        return sorted(t)[len(t) // 2]
+    return sum(t) / steps
 
 
 def suite_prefill(steps: int, only_w=None, B_=None, L_=None):

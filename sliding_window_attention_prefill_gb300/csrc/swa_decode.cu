@@ -51,7 +51,15 @@ __device__ int g_decode_error;
 #ifndef SWA_DEC_CTAS_PER_SM_SINGLE
 #define SWA_DEC_CTAS_PER_SM_SINGLE 4
 #endif
-// persistent CTAs per SM with a 1-stage and a 2-stage chunk ring
+#ifndef SWA_DEC_CTAS_PER_SM_WIDE
+#define SWA_DEC_CTAS_PER_SM_WIDE 3
+#endif
+
+// Persistent CTAs per SM: the 1-stage chunk ring (items of one chunk, when
+// they all fit in one wave of these), and the 2-stage ring -- normally
+// SWA_DEC_CTAS_PER_SM, SWA_DEC_CTAS_PER_SM_WIDE when a call has at least two
+// items per CTA at that count (more chunks in flight per SM) and its shared
+// memory fits.
 constexpr int kDecCtasPerSm[2] = {SWA_DEC_CTAS_PER_SM_SINGLE, SWA_DEC_CTAS_PER_SM};
 constexpr int kDecCH = 64;              // slots per chunk
 constexpr int kDecWarps = 4;            // consumer warps, 16 slots each
@@ -218,8 +226,18 @@ __device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p) 
 // first loads is paid once per CTA rather than once per item.
 // The minimum CTAs per SM of the launch bounds keeps the registers within
 // what that many CTAs can hold (the grid assumes they are all resident).
+// Most CTAs per SM a kernel of this shape may run at (its launch bounds).
+template <int D, int G, int ST>
+constexpr int dec_max_ctas() {
+    if (ST == 1) return kDecCtasPerSm[0];
+    return (SWA_DEC_CTAS_PER_SM_WIDE > SWA_DEC_CTAS_PER_SM &&
+            SWA_DEC_CTAS_PER_SM_WIDE * (DecSmem<D, G, 2>::kAlloc + 1024) <= 233472)
+               ? SWA_DEC_CTAS_PER_SM_WIDE
+               : SWA_DEC_CTAS_PER_SM;
+}
+
 template <int D, int G, int ST, int DT>
-__global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm[ST - 1])
+__global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
     swa_decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeParams p) {
     using SL = DecSmem<D, G, ST>;
     constexpr int kDecStages = ST;
@@ -714,7 +732,8 @@ template <int D, int G, int ST, int DT>
 swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, int df,
                          cudaStream_t stream) {
     using SL = DecSmem<D, G, ST>;
-    static_assert(kDecCtasPerSm[ST - 1] * (SL::kAlloc + 1024) <= 233472, "CTAs per SM must fit");
+    constexpr int kMaxCtas = dec_max_ctas<D, G, ST>();
+    static_assert(kMaxCtas * (SL::kAlloc + 1024) <= 233472, "CTAs per SM must fit");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -728,7 +747,9 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, int df,
     const int sms = device_sm_count();
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
-    const long long cap_ctas = static_cast<long long>(kDecCtasPerSm[ST - 1]) * sms;
+    // 2-stage ring: the wide count when every CTA gets at least two items
+    const int cps = (ST == 2 && items >= 2ll * kMaxCtas * sms) ? kMaxCtas : kDecCtasPerSm[ST - 1];
+    const long long cap_ctas = static_cast<long long>(cps) * sms;
     const int grid = static_cast<int>(items < cap_ctas ? items : cap_ctas);
     e = launch_pdl(swa_decode_kernel<D, G, ST, DT>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
                    maps, p);
