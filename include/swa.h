@@ -244,6 +244,36 @@ swa_status swa_decode_noalloc(const void *q, const swa_cache *cache, const int32
                               int w, int s, void *o, swa_stream_t stream);
 
 /*
+ * Bounds-checked debug build.  The library compiled with SWA_CHECK_BOUNDS=1
+ * (the package's build step with that flag) tests, in every kernel, each
+ * global access whose index the kernel computes against the extent of its
+ * buffer.  An index outside the buffer is not accessed: the kernel records
+ * SWA_ERR_BOUNDS (read with swa_get_device_error) and the first such index,
+ * and carries on; nothing traps.  Accesses made by the tensor-copy engine
+ * are clipped to their tensor maps by the hardware and need no test.  In
+ * the normal build the tests are compiled out.  The pages define no such
+ * thing; these calls are a debugging aid of the library.
+ *
+ * swa_debug_bounds_checked -- 1 in the bounds-checked build, else 0.
+ *
+ * swa_debug_bounds_index -- the first index (in elements, or in 16-byte
+ * vectors for vector accesses) a kernel refused since the last call, or -1
+ * if none (always -1 in the normal build); -2 if reading it failed.  Reads
+ * and clears the record; synchronises `stream`.
+ *
+ * swa_debug_set_extent_margin -- bounds-checked build only: from now on the
+ * kernels are told that every buffer they write (outputs, caches, linear
+ * states, workspaces) is `elements` elements shorter than it is, so that
+ * they refuse their last writes -- a way to see the checks work without
+ * any access outside a real buffer.  0 restores the true extents.  Returns
+ * SWA_ERR_UNSUPPORTED in the normal build, SWA_ERR_INVALID_ARG if negative.
+ * Process-wide; not for use while other threads launch work.
+ */
+int swa_debug_bounds_checked(void);
+int64_t swa_debug_bounds_index(swa_stream_t stream);
+swa_status swa_debug_set_extent_margin(int64_t elements);
+
+/*
  * swa_last_cuda_error -- name and description of the CUDA error behind the
  * most recent SWA_ERR_CUDA returned to the calling thread ("" if none).
  * Diagnostic only; static or thread-local storage owned by the library.

@@ -37,23 +37,32 @@ def _inputs() -> list[str]:
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+# The bounds-checked debug build (SWA_CHECK_BOUNDS=1, include/swa.h), beside
+# the normal one.
+CHECKED_BUILD = os.path.join(BUILD, "checked")
+CHECKED_LIB = os.path.join(CHECKED_BUILD, "libswa_checked.so")
+
+
+def stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link the library if it is missing or older than its sources."""
-    if not force and not stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          lib: str = LIB) -> str:
+    """Compile and link the library (to `lib`, objects beside it) if it is
+    missing or older than its sources."""
+    if not force and not stale(lib):
+        return lib
+    out_dir = os.path.dirname(lib)
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
     procs, objs = [], []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
@@ -69,14 +78,23 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
             print(text, file=sys.stderr)
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n\n".join(" ".join(c) + "\n" + t for c, t in failed))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout.decode(errors="replace"))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    """The bounds-checked debug library (every computed global index tested
+    against its buffer's extent; refused accesses recorded, not made)."""
+    return build(force, verbose, ["-DSWA_CHECK_BOUNDS=1"], lib=CHECKED_LIB)
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--checked" in sys.argv:
+        print(build_checked(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

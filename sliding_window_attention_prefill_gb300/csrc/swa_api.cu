@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "swa_internal.h"
@@ -37,6 +38,20 @@ swa_status cuda_fail(cudaError_t e, const char *where) {
 }
 
 const char *last_cuda_error() { return g_last_cuda; }
+
+#ifndef SWA_CHECK_BOUNDS
+#define SWA_CHECK_BOUNDS 0
+#endif
+
+namespace {
+// Test margin of the bounds-checked build (swa_debug_set_extent_margin).
+std::atomic<long long> g_extent_margin{0};
+}  // namespace
+
+long long output_extent(long long n) {
+    const long long m = n - g_extent_margin.load(std::memory_order_relaxed);
+    return m > 0 ? m : 0;
+}
 
 int device_sm_count() {
     static int cached[64] = {};
@@ -479,11 +494,34 @@ swa_status swa_selftest_wait_timeout(swa_stream_t stream) {
 
 swa_status swa_get_device_error(swa_stream_t stream) {
     SWA_NVTX_RANGE("swa_get_device_error");
-    const int a = swa::prefill_read_clear_error(as_cuda(stream));
-    const int b = swa::decode_read_clear_error(as_cuda(stream));
-    if (a == SWA_ERR_CUDA || b == SWA_ERR_CUDA) return SWA_ERR_CUDA;
-    if (a != 0) return static_cast<swa_status>(a);
-    return static_cast<swa_status>(b);
+    const cudaStream_t cs = as_cuda(stream);
+    const int e[4] = {swa::prefill_read_clear_error(cs), swa::decode_read_clear_error(cs),
+                      swa::append_read_clear_error(cs), swa::hybrid_read_clear_error(cs)};
+    for (int v : e)
+        if (v == SWA_ERR_CUDA) return SWA_ERR_CUDA;
+    for (int v : e)
+        if (v != 0) return static_cast<swa_status>(v);
+    return SWA_OK;
+}
+
+int swa_debug_bounds_checked(void) { return SWA_CHECK_BOUNDS ? 1 : 0; }
+
+int64_t swa_debug_bounds_index(swa_stream_t stream) {
+    const cudaStream_t cs = as_cuda(stream);
+    const long long w[4] = {swa::prefill_read_clear_where(cs), swa::decode_read_clear_where(cs),
+                            swa::append_read_clear_where(cs), swa::hybrid_read_clear_where(cs)};
+    for (long long v : w)
+        if (v == -2) return -2;
+    for (long long v : w)
+        if (v != -1) return v;
+    return -1;
+}
+
+swa_status swa_debug_set_extent_margin(int64_t elements) {
+    if (!SWA_CHECK_BOUNDS) return SWA_ERR_UNSUPPORTED;
+    if (elements < 0) return SWA_ERR_INVALID_ARG;
+    swa::g_extent_margin.store(elements, std::memory_order_relaxed);
+    return SWA_OK;
 }
 
 }  // extern "C"

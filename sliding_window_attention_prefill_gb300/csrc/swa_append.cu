@@ -22,6 +22,9 @@
 
 namespace swa {
 
+__device__ int g_append_error;
+__device__ unsigned long long g_append_where;
+
 struct AppendParams {
     const uint4 *k_new;  // [B, n, Hkv, d] as 16-byte vectors
     const uint4 *v_new;
@@ -30,6 +33,7 @@ struct AppendParams {
     int64_t pos0;
     int B, n, Hkv, vpr, vpr_log2, cap, w, s;  // vpr: 16-byte vectors per row (d / 8)
     int a, b0;  // surviving new positions: j in [0, a) and j in [b0, n)
+    long long n_new, n_cache;  // extents in 16-byte vectors (bounds-checked build)
 };
 
 // Grid (vector blocks, surviving positions, sequences): the threads of the x
@@ -56,6 +60,9 @@ __global__ void __launch_bounds__(kAppendThreads) swa_append_kernel(const Append
                 (p.w < 0 || pos < p.s) ? pos : p.s + (pos - p.s) % static_cast<int64_t>(p.w - p.s);
             const int64_t src = (static_cast<int64_t>(b) * p.n + j) * per_pos + t;
             const int64_t dst = ((static_cast<int64_t>(b) * p.Hkv + h) * p.cap + slot) * p.vpr + vec;
+            if (!in_bounds(src, p.n_new, &g_append_error, &g_append_where) ||
+                !in_bounds(dst, p.n_cache, &g_append_error, &g_append_where))
+                continue;
             const uint4 kv = p.k_new[src];
             const uint4 vv = p.v_new[src];
             p.ck[dst] = kv;
@@ -81,6 +88,8 @@ swa_status append_launch(const swa_cache &c, const void *k_new, const void *v_ne
     p.cap = c.cap;
     p.w = c.w < 0 ? -1 : c.w;
     p.s = c.w < 0 ? 0 : c.s;
+    p.n_new = static_cast<long long>(c.B) * n * c.Hkv * c.d / 8;
+    p.n_cache = output_extent(static_cast<long long>(c.B) * c.Hkv * c.cap * c.d) / 8;
     if (p.w < 0) {
         p.a = n;  // every position keeps its own slot
         p.b0 = n;
@@ -118,6 +127,7 @@ struct GatherParams {
     uint4 *wk, *wv;              // gathered [B, q_off + n, Hkv, d]
     int64_t pos0;
     int B, n, Hkv, vpr, vpr_log2, cap, w, s, q_off;
+    long long n_cache, n_new, n_ws;  // extents in 16-byte vectors (bounds-checked build)
 };
 
 __global__ void __launch_bounds__(kAppendThreads) swa_chunk_gather_kernel(const GatherParams p) {
@@ -137,14 +147,17 @@ __global__ void __launch_bounds__(kAppendThreads) swa_chunk_gather_kernel(const 
                 if (p.pos0 > p.w && j >= p.s) pos = p.pos0 - (p.w - p.s) + (j - p.s);
                 const int64_t slot = pos < p.s ? pos : p.s + (pos - p.s) % (p.w - p.s);
                 const int64_t src = ((static_cast<int64_t>(b) * p.Hkv + h) * p.cap + slot) * p.vpr + vec;
+                if (!in_bounds(src, p.n_cache, &g_append_error, &g_append_where)) continue;
                 kv = p.ck[src];
                 vv = p.cv[src];
             } else {
                 const int64_t src = (static_cast<int64_t>(b) * p.n + (j - p.q_off)) * per_pos + t;
+                if (!in_bounds(src, p.n_new, &g_append_error, &g_append_where)) continue;
                 kv = p.k_new[src];
                 vv = p.v_new[src];
             }
             const int64_t dst = (static_cast<int64_t>(b) * Lk + j) * per_pos + t;
+            if (!in_bounds(dst, p.n_ws, &g_append_error, &g_append_where)) continue;
             p.wk[dst] = kv;
             p.wv[dst] = vv;
         }
@@ -171,6 +184,9 @@ swa_status chunk_gather_launch(const swa_cache &c, const void *k_new, const void
     p.s = c.s;
     p.q_off = q_off;
     const int Lk = q_off + n;
+    p.n_cache = static_cast<long long>(c.B) * c.Hkv * c.cap * c.d / 8;
+    p.n_new = static_cast<long long>(c.B) * n * c.Hkv * c.d / 8;
+    p.n_ws = output_extent(static_cast<long long>(c.B) * Lk * c.Hkv * c.d) / 8;
     if (Lk == 0 || c.B == 0) return SWA_OK;
     const int per_pos = p.Hkv * p.vpr;
     const dim3 grid((per_pos + kAppendThreads - 1) / kAppendThreads,
@@ -179,6 +195,16 @@ swa_status chunk_gather_launch(const swa_cache &c, const void *k_new, const void
     const cudaError_t e =
         launch_pdl(swa_chunk_gather_kernel, grid, dim3(kAppendThreads), 0, stream, p);
     return e == cudaSuccess ? SWA_OK : cuda_fail(e, "launch swa_chunk_gather_kernel");
+}
+
+int append_read_clear_error(cudaStream_t stream) {
+    int v = 0;
+    return read_clear_symbol(g_append_error, &v, stream) ? v : SWA_ERR_CUDA;
+}
+
+long long append_read_clear_where(cudaStream_t stream) {
+    unsigned long long w = 0;
+    return read_clear_symbol(g_append_where, &w, stream) ? where_index(w) : -2;
 }
 
 }  // namespace swa

@@ -41,6 +41,7 @@
 namespace swa {
 
 __device__ int g_decode_error;
+__device__ unsigned long long g_decode_where;
 
 #ifndef SWA_DEC_ITEMS_PER_SM
 #define SWA_DEC_ITEMS_PER_SM 4
@@ -87,6 +88,9 @@ struct DecodeParams {
     const uint16_t *k_new, *v_new;
     uint16_t *kc, *vc;
     int s;
+    // extents in elements (bounds-checked build): o, the cache tensors, the
+    // new tokens, the workspace's partials and (max, sum) pairs
+    long long n_o, n_cache, n_new, n_ws_acc, n_ws_ml;
 };
 
 // ST: depth of the chunk ring (2 when items span several chunks; 1 when every
@@ -339,8 +343,10 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
         if (x.snew >= 0 && onew >= 0 && onew < x.end - x.begin && ((onew % kDecCH) >> 4) == warp &&
             lane < D / 8) {
             const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
-            prefetch_l1(p.k_new + src);
-            prefetch_l1(p.v_new + src);
+            if (in_bounds(src / 8, p.n_new / 8, &g_decode_error, &g_decode_where)) {
+                prefetch_l1(p.k_new + src);
+                prefetch_l1(p.v_new + src);
+            }
         }
         float acc[MW][4];  // O^T: d = DW*warp + 16*mt + gq (+8), heads 2tq, 2tq+1
 #pragma unroll
@@ -376,14 +382,17 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                     const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
                     const int64_t dst =
                         ((static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * p.cap + x.snew) * D + lane * 8;
-                    const uint4 kk = *reinterpret_cast<const uint4 *>(p.k_new + src);
-                    const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src);
-                    const int off = (lane >> 3) * SL::kRegion + rnew * 128 +
-                                    (((lane & 7) ^ (rnew & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + off) = kk;
-                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + SL::kChunkBytes + off) = vv;
-                    *reinterpret_cast<uint4 *>(p.kc + dst) = kk;
-                    *reinterpret_cast<uint4 *>(p.vc + dst) = vv;
+                    if (in_bounds(src / 8, p.n_new / 8, &g_decode_error, &g_decode_where) &&
+                        in_bounds(dst / 8, p.n_cache / 8, &g_decode_error, &g_decode_where)) {
+                        const uint4 kk = *reinterpret_cast<const uint4 *>(p.k_new + src);
+                        const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src);
+                        const int off = (lane >> 3) * SL::kRegion + rnew * 128 +
+                                        (((lane & 7) ^ (rnew & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(sm + st * SL::kStage + off) = kk;
+                        *reinterpret_cast<uint4 *>(sm + st * SL::kStage + SL::kChunkBytes + off) = vv;
+                        *reinterpret_cast<uint4 *>(p.kc + dst) = kk;
+                        *reinterpret_cast<uint4 *>(p.vc + dst) = vv;
+                    }
                 }
                 __syncwarp();
             }
@@ -524,8 +533,9 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
             constexpr int kVec = G * DW / 8;
             if (lane < kVec) {
                 const int h = lane / (DW / 8), j = lane % (DW / 8);
-                *reinterpret_cast<uint4 *>(p.o + (orow0 + h) * D + DW * warp + 8 * j) =
-                    *reinterpret_cast<const uint4 *>(ost + h * DW + 8 * j);
+                const int64_t oi = (orow0 + h) * D + DW * warp + 8 * j;
+                if (in_bounds(oi / 8, p.n_o / 8, &g_decode_error, &g_decode_where))
+                    *reinterpret_cast<uint4 *>(p.o + oi) = *reinterpret_cast<const uint4 *>(ost + h * DW + 8 * j);
             }
             __syncwarp();
         } else {
@@ -534,20 +544,26 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
             for (int mt = 0; mt < MW; ++mt) {
                 const int d0 = DW * warp + 16 * mt + gq;
                 if (h0 < G) {
-                    float *a0 = p.ws_acc + ((orow0 + h0) * p.splits + x.split) * D;
-                    a0[d0] = acc[mt][0];
-                    a0[d0 + 8] = acc[mt][2];
+                    const int64_t i0 = ((orow0 + h0) * p.splits + x.split) * D + d0;
+                    if (in_bounds(i0 + 8, p.n_ws_acc, &g_decode_error, &g_decode_where)) {
+                        p.ws_acc[i0] = acc[mt][0];
+                        p.ws_acc[i0 + 8] = acc[mt][2];
+                    }
                 }
                 if (h1 < G) {
-                    float *a1 = p.ws_acc + ((orow0 + h1) * p.splits + x.split) * D;
-                    a1[d0] = acc[mt][1];
-                    a1[d0 + 8] = acc[mt][3];
+                    const int64_t i1 = ((orow0 + h1) * p.splits + x.split) * D + d0;
+                    if (in_bounds(i1 + 8, p.n_ws_acc, &g_decode_error, &g_decode_where)) {
+                        p.ws_acc[i1] = acc[mt][1];
+                        p.ws_acc[i1 + 8] = acc[mt][3];
+                    }
                 }
             }
             if (warp == 0 && tq == 0 && gq < G) {
-                float *ml = p.ws_ml + ((orow0 + gq) * p.splits + x.split) * 2;
-                ml[0] = m_run;
-                ml[1] = l_run;
+                const int64_t im = ((orow0 + gq) * p.splits + x.split) * 2;
+                if (in_bounds(im + 1, p.n_ws_ml, &g_decode_error, &g_decode_where)) {
+                    p.ws_ml[im] = m_run;
+                    p.ws_ml[im + 1] = l_run;
+                }
             }
         }
     }
@@ -587,8 +603,10 @@ __global__ void __launch_bounds__(128) swa_decode_merge_kernel(const DecodeParam
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e)
-        p.o[static_cast<int64_t>(row) * D + lane * E + e] = round16<DT>(a[e] * inv);
+    for (int e = 0; e < E; ++e) {
+        const int64_t oi = static_cast<int64_t>(row) * D + lane * E + e;
+        if (in_bounds(oi, p.n_o, &g_decode_error, &g_decode_where)) p.o[oi] = round16<DT>(a[e] * inv);
+    }
 }
 
 // Hybrid window + linear decode, one CTA per (sequence, query head): the
@@ -686,7 +704,9 @@ __global__ void __launch_bounds__(kHybThreads) swa_hybrid_merge_kernel(const Dec
         l = fmaf(p.ws_ml[base * 2 + 1], f, l);
         acc = fmaf(p.ws_acc[base * D + c], f, acc);
     }
-    p.o[static_cast<int64_t>(row) * D + c] = round16<DT>(l > 0.f ? acc / l : 0.f);
+    const int64_t oi = static_cast<int64_t>(row) * D + c;
+    if (in_bounds(oi, p.n_o, &g_decode_error, &g_decode_where))
+        p.o[oi] = round16<DT>(l > 0.f ? acc / l : 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -819,6 +839,11 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
         p.ws_ml = p.ws_acc + static_cast<size_t>(c.B) * Hq * plan.splits * c.d;
     }
     p.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(c.d));
+    p.n_o = output_extent(static_cast<long long>(c.B) * Hq * c.d);
+    p.n_cache = output_extent(static_cast<long long>(c.B) * c.Hkv * c.cap * c.d);
+    p.n_new = static_cast<long long>(c.B) * c.Hkv * c.d;
+    p.n_ws_acc = output_extent(static_cast<long long>(c.B) * Hq * plan.splits * c.d);
+    p.n_ws_ml = output_extent(static_cast<long long>(c.B) * Hq * plan.splits * 2);
     if (k_new != nullptr) {
         p.k_new = static_cast<const uint16_t *>(k_new);
         p.v_new = static_cast<const uint16_t *>(v_new);
@@ -840,6 +865,11 @@ swa_status decode_launch(const void *q, const swa_cache &c, const int32_t *pos, 
     const int df = lin != nullptr ? lin->df : 0;
     return c.dtype == SWA_F16 ? launch_decode_dt<kF16>(maps, p, c.d, G, single, df, stream)
                               : launch_decode_dt<kBf16>(maps, p, c.d, G, single, df, stream);
+}
+
+long long decode_read_clear_where(cudaStream_t stream) {
+    unsigned long long w = 0;
+    return read_clear_symbol(g_decode_where, &w, stream) ? where_index(w) : -2;
 }
 
 int decode_read_clear_error(cudaStream_t stream) {

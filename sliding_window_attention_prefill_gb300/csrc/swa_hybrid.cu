@@ -19,6 +19,10 @@
 #include "swa_ptx.cuh"
 
 namespace swa {
+
+__device__ int g_hybrid_error;
+__device__ unsigned long long g_hybrid_where;
+
 namespace {
 
 constexpr int kFoldTB = 8;  // evicted tokens per shared-memory batch
@@ -33,6 +37,7 @@ struct FoldParams {
     // >= 0: a one-token append evicting one token; once it is read, the new
     // token is written to this slot (the evicted one's) by the same CTA
     int write_slot;
+    long long n_cache, n_new, n_S, n_z;  // extents in elements (bounds-checked build)
 };
 
 template <int D, int DF, int DT>
@@ -51,11 +56,15 @@ __global__ void __launch_bounds__(4 * DF) swa_hybrid_fold_kernel(const FoldParam
     const int f = tid >> 1, half = tid & 1;
     // The state rows this thread updates, read first (their latency overlaps
     // the staging below), then W of this kv head into shared memory.
-    float *Srow = p.S + (static_cast<int64_t>(bh) * F + f) * D + half * HALF;
+    const int64_t s0 = (static_cast<int64_t>(bh) * F + f) * D + half * HALF;
+    const int64_t zi = static_cast<int64_t>(bh) * F + f;
+    const bool s_ok = in_bounds(s0 + HALF - 1, p.n_S, &g_hybrid_error, &g_hybrid_where);
+    const bool z_ok = half == 0 && in_bounds(zi, p.n_z, &g_hybrid_error, &g_hybrid_where);
+    float *Srow = p.S + s0;
     float acc[HALF];
 #pragma unroll
-    for (int i = 0; i < HALF; ++i) acc[i] = Srow[i];
-    float zacc = half == 0 ? p.z[static_cast<int64_t>(bh) * F + f] : 0.f;
+    for (int i = 0; i < HALF; ++i) acc[i] = s_ok ? Srow[i] : 0.f;
+    float zacc = z_ok ? p.z[zi] : 0.f;
     const float4 *Wh4 = reinterpret_cast<const float4 *>(p.W + static_cast<int64_t>(kvh) * D * DF);
 #pragma unroll
     for (int i = 0; i < D * DF / 4 / NT; ++i)
@@ -73,12 +82,16 @@ __global__ void __launch_bounds__(4 * DF) swa_hybrid_fold_kernel(const FoldParam
                 if (e < p.pos0) {  // still in the ring: its slot
                     const int64_t slot = e < p.s ? e : p.s + (e - p.s) % (p.w - p.s);
                     off = (static_cast<int64_t>(bh) * p.cap + slot) * D + c;
-                    kx = widen16<DT>(p.kc[off]);
-                    vx = widen16<DT>(p.vc[off]);
+                    if (in_bounds(off, p.n_cache, &g_hybrid_error, &g_hybrid_where)) {
+                        kx = widen16<DT>(p.kc[off]);
+                        vx = widen16<DT>(p.vc[off]);
+                    }
                 } else {  // appended by this call and evicted by it too
                     off = ((static_cast<int64_t>(b) * p.n + (e - p.pos0)) * p.Hkv + kvh) * D + c;
-                    kx = widen16<DT>(p.kn[off]);
-                    vx = widen16<DT>(p.vn[off]);
+                    if (in_bounds(off, p.n_new, &g_hybrid_error, &g_hybrid_where)) {
+                        kx = widen16<DT>(p.kn[off]);
+                        vx = widen16<DT>(p.vn[off]);
+                    }
                 }
             }
             sk[t][c] = kx;
@@ -89,8 +102,11 @@ __global__ void __launch_bounds__(4 * DF) swa_hybrid_fold_kernel(const FoldParam
             const int64_t dst = (static_cast<int64_t>(bh) * p.cap + p.write_slot) * D;
             const int64_t src = (static_cast<int64_t>(b) * p.Hkv + kvh) * D;
             for (int c = tid; c < D; c += NT) {
-                p.kc[dst + c] = p.kn[src + c];
-                p.vc[dst + c] = p.vn[src + c];
+                if (in_bounds(dst + c, p.n_cache, &g_hybrid_error, &g_hybrid_where) &&
+                    in_bounds(src + c, p.n_new, &g_hybrid_error, &g_hybrid_where)) {
+                    p.kc[dst + c] = p.kn[src + c];
+                    p.vc[dst + c] = p.vn[src + c];
+                }
             }
         }
         for (int idx = tid; idx < kFoldTB * DF; idx += NT) {
@@ -111,9 +127,11 @@ __global__ void __launch_bounds__(4 * DF) swa_hybrid_fold_kernel(const FoldParam
             zacc += ph;
         }
     }
+    if (s_ok) {
 #pragma unroll
-    for (int i = 0; i < HALF; ++i) Srow[i] = acc[i];
-    if (half == 0) p.z[static_cast<int64_t>(bh) * F + f] = zacc;
+        for (int i = 0; i < HALF; ++i) Srow[i] = acc[i];
+    }
+    if (z_ok) p.z[zi] = zacc;
 }
 
 template <int D, int DF, int DT>
@@ -159,6 +177,10 @@ swa_status hybrid_fold_launch(const swa_cache &c, const swa_linear_state &lin, c
     fp.s = c.s;
     fp.n = n;
     fp.pos0 = pos0;
+    fp.n_cache = output_extent(static_cast<long long>(c.B) * c.Hkv * c.cap * c.d);
+    fp.n_new = static_cast<long long>(c.B) * n * c.Hkv * c.d;
+    fp.n_S = output_extent(static_cast<long long>(c.B) * c.Hkv * 2 * lin.df * c.d);
+    fp.n_z = output_extent(static_cast<long long>(c.B) * c.Hkv * 2 * lin.df);
     // a decode step (one token, evicting one): the fold writes the new token
     fp.write_slot = -1;
     if (n == 1 && fp.e_lo == fp.e_hi) {
@@ -168,6 +190,16 @@ swa_status hybrid_fold_launch(const swa_cache &c, const swa_linear_state &lin, c
     const int grid = c.B * c.Hkv;
     return c.dtype == SWA_F16 ? launch_fold_dt<kF16>(fp, grid, c.d, lin.df, stream)
                               : launch_fold_dt<kBf16>(fp, grid, c.d, lin.df, stream);
+}
+
+int hybrid_read_clear_error(cudaStream_t stream) {
+    int v = 0;
+    return read_clear_symbol(g_hybrid_error, &v, stream) ? v : SWA_ERR_CUDA;
+}
+
+long long hybrid_read_clear_where(cudaStream_t stream) {
+    unsigned long long w = 0;
+    return read_clear_symbol(g_hybrid_where, &w, stream) ? where_index(w) : -2;
 }
 
 }  // namespace swa

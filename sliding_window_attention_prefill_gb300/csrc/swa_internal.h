@@ -121,5 +121,40 @@ swa_status selftest_wait_launch(cudaStream_t stream);
 // Returns 0 or a negative swa_status value.
 int prefill_read_clear_error(cudaStream_t stream);
 int decode_read_clear_error(cudaStream_t stream);
+int append_read_clear_error(cudaStream_t stream);
+int hybrid_read_clear_error(cudaStream_t stream);
+
+// Bounds-checked build: read and clear each module's record of the first
+// refused index (-1 if none; -2 if a CUDA call failed).  Synchronises.
+long long prefill_read_clear_where(cudaStream_t stream);
+long long decode_read_clear_where(cudaStream_t stream);
+long long append_read_clear_where(cudaStream_t stream);
+long long hybrid_read_clear_where(cudaStream_t stream);
+
+// The extent (in elements) the kernels are told an output buffer of n
+// elements has: n, less the test margin of the bounds-checked build
+// (swa_debug_set_extent_margin), never below 0.
+long long output_extent(long long n);
+
+#ifdef __CUDACC__
+// Copy a module's __device__ word to the host and reset it to zero (in the
+// module that defines it: the symbol is that translation unit's own).
+template <typename T>
+inline bool read_clear_symbol(T &symbol, T *out, cudaStream_t stream) {
+    const T zero{};
+    if (cudaMemcpyFromSymbolAsync(out, symbol, sizeof(T), 0, cudaMemcpyDeviceToHost, stream) !=
+        cudaSuccess)
+        return false;
+    if (cudaMemcpyToSymbolAsync(symbol, &zero, sizeof(T), 0, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+        return false;
+    return cudaStreamSynchronize(stream) == cudaSuccess;
+}
+
+// A module's `where` word as the refused index (or -1).
+inline long long where_index(unsigned long long w) {
+    return w == 0 ? -1 : static_cast<long long>(w) - (1ll << 50);
+}
+#endif
 
 }  // namespace swa

@@ -67,6 +67,7 @@
 namespace swa {
 
 __device__ int g_prefill_error;
+__device__ unsigned long long g_prefill_where;
 
 // Key tile width KT: 256 columns (one K or V tile of 64 KB at d = 128, so one
 // stage of each), or 128 columns for narrow bands (two stages of each in the
@@ -415,8 +416,9 @@ __global__ void __launch_bounds__(prefill_threads(EW), 1)
                                      : "=r"(v4.x), "=r"(v4.y), "=r"(v4.z), "=r"(v4.w)
                                      : "r"(src));
                         const int64_t grow = x.r0 + x.t0 + (r >> p.g_log2) - p.q_off;
-                        *reinterpret_cast<uint4 *>(
-                            p.o + (grow * p.Hq + x.kvh * p.G + (r & (p.G - 1))) * D + col) = v4;
+                        const int64_t oi = (grow * p.Hq + x.kvh * p.G + (r & (p.G - 1))) * D + col;
+                        if (in_bounds(oi / 8, p.n_o / 8, &g_prefill_error, &g_prefill_where))
+                            *reinterpret_cast<uint4 *>(p.o + oi) = v4;
                     }
                 }
                 __syncwarp();
@@ -488,8 +490,9 @@ __global__ void __launch_bounds__(prefill_threads(EW), 1)
                 ++ep;
                 if (p.lse != nullptr && ok && pend_valid && half == 0) {
                     const int h = pend_kvh * p.G + hrow;
-                    p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_r0 + pend_t - p.q_off)] =
-                        pend_m * p.scale + logf(l_tot);
+                    const int64_t li = (static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_r0 + pend_t - p.q_off);
+                    if (in_bounds(li, p.n_lse, &g_prefill_error, &g_prefill_where))
+                        p.lse[li] = pend_m * p.scale + logf(l_tot);
                 }
                 return;
             }
@@ -540,16 +543,17 @@ __global__ void __launch_bounds__(prefill_threads(EW), 1)
             for (int v = 0; v < CH; ++v) {
                 const int rr = quarter * 32 + kgrp * CH + v;  // MMA row of ch[v]
                 const int tv = pend_t0 + (rr >> p.g_log2);
-                if (ok && tv <= pend_t1)
-                    *reinterpret_cast<uint4 *>(
-                        p.o + ((static_cast<int64_t>(pend_b) * p.L + (pend_r0 + tv - p.q_off)) * p.Hq + pend_kvh * p.G +
-                               (rr & (p.G - 1))) * D +
-                        half * (D / 2) + cpos * 8) = ch[v];
+                const int64_t oi =
+                    ((static_cast<int64_t>(pend_b) * p.L + (pend_r0 + tv - p.q_off)) * p.Hq + pend_kvh * p.G +
+                     (rr & (p.G - 1))) * D + half * (D / 2) + cpos * 8;
+                if (ok && tv <= pend_t1 && in_bounds(oi / 8, p.n_o / 8, &g_prefill_error, &g_prefill_where))
+                    *reinterpret_cast<uint4 *>(p.o + oi) = ch[v];
             }
             if (p.lse != nullptr && ok && pend_valid && half == 0) {
                 const int h = pend_kvh * p.G + hrow;
-                p.lse[(static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_r0 + pend_t - p.q_off)] =
-                    pend_m * p.scale + logf(l_tot);
+                const int64_t li = (static_cast<int64_t>(pend_b) * p.Hq + h) * p.L + (pend_r0 + pend_t - p.q_off);
+                if (in_bounds(li, p.n_lse, &g_prefill_error, &g_prefill_where))
+                    p.lse[li] = pend_m * p.scale + logf(l_tot);
             }
         };
 
@@ -840,8 +844,9 @@ __global__ void __launch_bounds__(prefill_threads(EW), 1)
                 const int t = x.t0 + (row >> p.g_log2);
                 if (t <= x.t1) {
                     const int h = x.kvh * p.G + (row & (p.G - 1));
-                    p.lse[(static_cast<int64_t>(x.b) * p.Hq + h) * p.L + (x.r0 + t - p.q_off)] =
-                        m * p.scale + logf(l);
+                    const int64_t li = (static_cast<int64_t>(x.b) * p.Hq + h) * p.L + (x.r0 + t - p.q_off);
+                    if (in_bounds(li, p.n_lse, &g_prefill_error, &g_prefill_where))
+                        p.lse[li] = m * p.scale + logf(l);
                 }
             }
         }
@@ -1075,6 +1080,11 @@ swa_status prefill_launch(const void *q, const void *k, const void *v, void *o, 
                           int L, int Hq, int Hkv, int d, int w, int s, int dtype,
                           cudaStream_t stream) {
     return prefill_launch_offset(q, k, v, o, lse, B, L, Hq, Hkv, d, w, s, 0, L, 0, dtype, stream);
+}
+
+long long prefill_read_clear_where(cudaStream_t stream) {
+    unsigned long long w = 0;
+    return read_clear_symbol(g_prefill_where, &w, stream) ? where_index(w) : -2;
 }
 
 int prefill_read_clear_error(cudaStream_t stream) {

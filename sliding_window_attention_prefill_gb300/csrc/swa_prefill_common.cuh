@@ -73,6 +73,7 @@ struct PrefillParams {
     int varlen;
     const int *tile_count;    // number of query tiles (0 if cu_seqlens is invalid)
     const int4 *tile_rec;     // per query tile: {b, tile index, first row, length}
+    long long n_o, n_lse;     // extents of o and lse in elements (bounds-checked build)
 };
 
 // A work unit.  b is the batch coordinate of the tensor maps and r0 the row
@@ -159,6 +160,8 @@ inline PrefillParams make_prefill_params(void *o, float *lse, int B, int L, int 
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
+    p.n_o = output_extent(static_cast<long long>(B) * L * Hq * d);
+    p.n_lse = lse ? output_extent(static_cast<long long>(B) * Hq * L) : 0;
     return p;
 }
 

@@ -22,6 +22,36 @@ constexpr int kErrTimeout = -6;
 constexpr int kErrBounds = -7;
 
 // ---------------------------------------------------------------------------
+// bounds-checked debug build
+// ---------------------------------------------------------------------------
+// With SWA_CHECK_BOUNDS=1 every global access whose index a kernel computes
+// is first tested against the extent of its buffer (in elements of the
+// access).  An index outside [0, n) is not accessed: the first one is kept
+// in *where (as index + kWhereBias, so that 0 means "none") and
+// SWA_ERR_BOUNDS in *err.  Nothing traps.  In the normal build the test is
+// compiled out and always passes.
+#ifndef SWA_CHECK_BOUNDS
+#define SWA_CHECK_BOUNDS 0
+#endif
+constexpr long long kWhereBias = 1ll << 50;
+
+__device__ __forceinline__ bool in_bounds(long long i, long long n, int *err,
+                                          unsigned long long *where) {
+#if SWA_CHECK_BOUNDS
+    if (i >= 0 && i < n) return true;
+    atomicCAS(where, 0ull, static_cast<unsigned long long>(i + kWhereBias));
+    atomicCAS(err, 0, kErrBounds);
+    return false;
+#else
+    (void)i;
+    (void)n;
+    (void)err;
+    (void)where;
+    return true;
+#endif
+}
+
+// ---------------------------------------------------------------------------
 // generic helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -94,6 +94,12 @@ def _declare(L) -> None:
     L.swa_version.restype = ctypes.c_char_p
     L.swa_last_cuda_error.argtypes = []
     L.swa_last_cuda_error.restype = ctypes.c_char_p
+    L.swa_debug_bounds_checked.argtypes = []
+    L.swa_debug_bounds_checked.restype = _c_int
+    L.swa_debug_bounds_index.argtypes = [_c_p]
+    L.swa_debug_bounds_index.restype = _c_i64
+    L.swa_debug_set_extent_margin.argtypes = [_c_i64]
+    L.swa_debug_set_extent_margin.restype = _c_int
     L.swa_selftest_wait_timeout.argtypes = [_c_p]
     L.swa_selftest_wait_timeout.restype = _c_int
     L.swa_prefill_chunk_workspace_bytes.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64]
@@ -133,6 +139,16 @@ def lib():
         _declare(L)
         _lib = L
     return _lib
+
+
+def load_checked():
+    """The bounds-checked debug build of the library (built on first use),
+    loaded beside the normal one and declared the same way.  To run the
+    package's calls on it, assign it to ``swa._lib``."""
+    path = _build.build_checked()
+    L = ctypes.CDLL(path)
+    _declare(L)
+    return L
 
 
 def declared_functions() -> list[str]:

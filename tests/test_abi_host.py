@@ -172,3 +172,23 @@ def test_check_prefill_varlen(L):
     assert c(q, k, v, o, None, cu, 3, 1000, 600, 32, 8, 128, 4, 4, 0, ws, need) == INVALID  # w <= s
     assert c(q, k, v, q, None, cu, *args, ws, need) == INVALID                # o aliases q
     assert c(q, k, v, o, None, cu, *args, _p(1000), need) == INVALID          # workspace aliases q
+
+
+def test_normal_build_has_no_bounds_checks(L):
+    """The normal library reports no checks, refuses the test margin and has
+    no refused index to report (the record is only read on a GPU)."""
+    assert L.swa_debug_bounds_checked() == 0
+    assert L.swa_debug_set_extent_margin(16) == UNSUPPORTED
+
+
+def test_checked_build_compiles_and_reports_itself():
+    """The bounds-checked debug library (SWA_CHECK_BOUNDS=1) cross-compiles
+    for sm_103a, exports the same functions, reports itself as checked and
+    takes a test margin (no GPU is touched)."""
+    C = swa.load_checked()
+    for n in swa.declared_functions():
+        assert hasattr(C, n), n
+    assert C.swa_debug_bounds_checked() == 1
+    assert C.swa_debug_set_extent_margin(-1) == INVALID
+    assert C.swa_debug_set_extent_margin(64) == OK
+    assert C.swa_debug_set_extent_margin(0) == OK
