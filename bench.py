@@ -635,7 +635,9 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         e2e_graph(w)
     if sampler:
         sampler.start("e2e")
-    e2e_ms = sum(e2e_graph(w) for w in D["windows"])
+    # each window's stream replayed three times; the median replay counts
+    # (one replay is a single sample of the host link's state)
+    e2e_ms = sum(sorted(e2e_graph(w) for _ in range(3))[1] for w in D["windows"])
     if sampler:
         sampler.stop("e2e")
     e2e_eager_ms = sum(e2e_eager(w) for w in D["windows"])
@@ -731,7 +733,8 @@ def run_swa(args, rank: int, world: int, local_rank: int):
                           "(append_decode), captured once as a CUDA graph and replayed: every "
                           "step's q, k, v copied up from pinned host memory and its output "
                           "copied back, steps overlapped (double-buffered device buffers, "
-                          "copies on two streams of their own), events around the replay",
+                          "copies on two streams of their own), events around the replay; "
+                          "the median of three replays per window",
                 "eager": {"value": tokens / (e2e_eager_ms * 1e-3), "ms_per_step": e2e_eager_ms,
                           "timing": "the same stream issued call by call from Python"},
                 "clocks": sampler.result("e2e") if sampler else None},
