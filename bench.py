@@ -8,14 +8,20 @@ bf16, N(0,1) inputs, s = 4 sinks):
           append of a 4096-token prompt, then 1024 steps that each append one
           token per sequence and decode it (one append_decode call);
   prefill B=2, L=32768, SWA(w,4) for w in {128, 256, 512}.
+The decode stream runs through a stack of 16 attention layers, each with a
+cache of its own, so that the caches a step reads (268 MB at w = 64, 2.1 GB
+at w = 512) exceed the 129 MB L2 and every launch reads its cache from HBM.
 One step is one pass over all of it: the three prefills, and for each decode
-window the prompt's bulk append and the 1024 decode steps.  Every launch is
-timed alone with CUDA events on its stream, with L2 flushed before it
-(256 MiB written, then another 256 MiB read).  `value` is decoded tokens/s:
-the pass's 2 x 64 x 1024 decoded tokens over the device time of its decode
-steps; `prefill` holds the TFLOP/s, `decode` the KV-read GB/s, `rooflines`
-every kernel against the measured peaks, `flatness` the 4-layer decode sweep
-over 1K..256K positions, `small_prefill` the 4096-token SWA(64,4) prefill.
+window the prompt's bulk append into every layer's cache and the 1024 decode
+steps through the 16 layers.  Prefill and append launches are timed alone
+with CUDA events on their stream, L2 flushed before each (256 MiB written,
+then another 256 MiB read); each window's 1024 x 16 decode launches are one
+CUDA graph, timed with one event pair around its replay (L2 also flushed
+before it).  `value` is decoded tokens/s of one attention layer: the pass's
+2 x 64 x 1024 x 16 layer-tokens over the device time of its decode graphs;
+`prefill` holds the TFLOP/s, `decode` the KV-read GB/s, `rooflines` every
+kernel against the measured peaks, `flatness` the 4-layer decode sweep over
+1K..256K positions, `small_prefill` the 4096-token SWA(64,4) prefill.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl swa|reference]
 Under torchrun each rank runs its own batch on its own GPU (no data exchange;
@@ -44,7 +50,8 @@ sys.path.insert(0, ROOT)
 METRIC = "SWA(w,4) decode tok/s + KV-read GB/s vs HBM peak; prefill TFLOP/s vs tensor peak"
 # The configurations the metric is quoted on.
 PREFILL_CFG = dict(B=2, L=32768, Hq=32, Hkv=8, d=128, s=4, windows=(128, 256, 512))
-DECODE_CFG = dict(B=64, Hq=32, Hkv=8, d=128, s=4, windows=(64, 512), prompt=4096, steps=1024)
+DECODE_CFG = dict(B=64, Hq=32, Hkv=8, d=128, s=4, windows=(64, 512), prompt=4096, steps=1024,
+                  layers=16)
 # The 4096-token prompt of one sequence, SWA(64,4), first 4 key rows x8.
 SMALL_PREFILL = dict(B=1, L=4096, Hq=32, Hkv=8, d=128, w=64, s=4, sink_rows=4)
 WORKLOAD_NAME = ("decode SWA(w,4) w in {64,512}: B=64 Hq=32 Hkv=8 d=128 bf16, cache filled from a "
@@ -52,9 +59,15 @@ WORKLOAD_NAME = ("decode SWA(w,4) w in {64,512}: B=64 Hq=32 Hkv=8 d=128 bf16, ca
                  "decoding it; prefill SWA(w,4) w in {128,256,512}: B=2 L=32768 Hq=32 Hkv=8 d=128 "
                  "bf16 N(0,1)")
 L2_FLUSH_BYTES = 256 << 20
-L2_NOTE = (f"flushed before every timed launch: {L2_FLUSH_BYTES >> 20} MiB written, then another "
-           f"{L2_FLUSH_BYTES >> 20} MiB read, so each launch starts on a cold L2 that holds no "
-           f"dirty lines of the flush")
+L2_NOTE = {
+    "prefill_and_append": (f"flushed before every timed launch: {L2_FLUSH_BYTES >> 20} MiB written, "
+                           f"then another {L2_FLUSH_BYTES >> 20} MiB read, so each launch starts on a "
+                           f"cold L2 that holds no dirty lines of the flush"),
+    "decode": ("inputs larger than L2: each launch reads the cache of one of 16 layers, and the "
+               "15 launches since that cache was last read moved 15 other caches (252 MB at "
+               "w = 64, 2 GB at w = 512) through the 129 MB L2; L2 also flushed before each "
+               "replay of the graph"),
+}
 # Decode context sweep of the flatness key: 4 attention layers, positions
 # 1K .. 256K, every finite window at batch 1 and 256; full causal at batch 1
 # for contrast.
@@ -106,9 +119,11 @@ def kv_read_bytes(B, Hkv, d, n_valid) -> float:
 
 
 def decoded_tokens_per_step(world: int) -> int:
-    """Tokens all ranks decode in one step: each decode window's batch, every step."""
+    """Layer-tokens all ranks decode in one step: each decode window's batch,
+    every step, in every layer of the stack (one layer's tokens/s is then
+    this over the decode time)."""
     C = DECODE_CFG
-    return len(C["windows"]) * C["B"] * C["steps"] * world
+    return len(C["windows"]) * C["B"] * C["steps"] * C["layers"] * world
 
 
 def peaks() -> dict:
@@ -450,22 +465,56 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     qs = inputs.normal16_on((nsteps, B, Hq, d), gen)
     pos = (prompt + torch.arange(nsteps, dtype=torch.int32, device=dev))[:, None]
     pos = pos.expand(nsteps, B).contiguous()
-    caches = {w: swa.Cache(B, Hkv, d, w, s, device=dev) for w in D["windows"]}
-    wsp = {w: swa.workspace_for(caches[w], Hq) for w in D["windows"]}
+    nlay = D["layers"]
+    caches = {w: [swa.Cache(B, Hkv, d, w, s, device=dev) for _ in range(nlay)] for w in D["windows"]}
+    wsp = {w: swa.workspace_for(caches[w][0], Hq) for w in D["windows"]}
     od = {w: torch.empty(B, Hq, d, dtype=torch.bfloat16, device=dev) for w in D["windows"]}
     flush = L2Flush(dev)
+    # Layer l of step i takes the inputs drawn for step (i + l * stride) mod
+    # 1024: different in every layer of a step.
+    stride = nsteps // nlay
 
-    # the launches of one step, in order: (kind, window, call, kernels it launches)
+    def layer_inputs(i, l):
+        j = (i + l * stride) % nsteps
+        return qs[j], ks[j], vs[j]
+
+    def reset_caches(w):
+        for c in caches[w]:
+            c.append(kp, vp, 0)
+
+    def decode_stream(w):
+        for i in range(nsteps):
+            for l in range(nlay):
+                q_, k_, v_ = layer_inputs(i, l)
+                swa.append_decode(q_, k_, v_, caches[w][l], pos[i], out=od[w], workspace=wsp[w])
+
+    # Each window's 1024 x 16 decode launches as one CUDA graph (one call
+    # warmed up outside the capture; the step's appends reset the caches).
+    cap = torch.cuda.Stream(dev)
+    dgraphs = {}
+    for w in D["windows"]:
+        reset_caches(w)
+        q_, k_, v_ = layer_inputs(0, 0)
+        swa.append_decode(q_, k_, v_, caches[w][0], pos[0], out=od[w], workspace=wsp[w])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                decode_stream(w)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        torch.cuda.synchronize()
+        dgraphs[w] = g
+
+    # the timed units of one step, in order: (kind, window, call, kernels it launches)
     units = []
     for w in P["windows"]:
         units.append(("prefill", w, functools.partial(swa.prefill, q3, k3, v3, w, P["s"], out=o3), 1))
     for w in D["windows"]:
-        c = caches[w]
-        units.append(("append", w, functools.partial(c.append, kp, vp, 0), 1))
+        for c in caches[w]:
+            units.append(("append", w, functools.partial(c.append, kp, vp, 0), 1))
         nl = 1 + (1 if wsp[w] is not None else 0)
-        for i in range(nsteps):
-            units.append(("decode", w, functools.partial(
-                swa.append_decode, qs[i], ks[i], vs[i], c, pos[i], out=od[w], workspace=wsp[w]), nl))
+        units.append(("decode", w, dgraphs[w].replay, nsteps * nlay * nl))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in units]
 
@@ -502,7 +551,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
 
     # The cost of the measurement itself: an event pair with nothing between
     # it, after a flush, timed the same way (reported beside the results;
-    # every figure above still includes it).
+    # every launch timed alone still includes it, a decode graph once).
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(200)]
     for i, (a, b_) in enumerate(eev):
@@ -510,14 +559,15 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         a.record()
         b_.record()
     torch.cuda.synchronize()
-    event_pair_ms = sorted(a.elapsed_time(b_) for a, b_ in eev)[len(eev) // 2]
+    event_pair_ms = sum(a.elapsed_time(b_) for a, b_ in eev) / len(eev)
 
     step_ms = sum(sum(t) for t in per_step) / len(per_step)
     dec_ms = sum(sum(t[j] for j, u in enumerate(units) if u[0] == "decode")
                  for t in per_step) / len(per_step)
     pre_ms = {w: mean_of("prefill", w) for w in P["windows"]}
-    app_ms = {w: mean_of("append", w) for w in D["windows"]}
-    tok_ms = {w: mean_of("decode", w) for w in D["windows"]}
+    app_ms = {w: mean_of("append", w) for w in D["windows"]}  # one layer's prompt append
+    graph_ms = {w: mean_of("decode", w) for w in D["windows"]}  # the window's decode graph
+    tok_ms = {w: graph_ms[w] / (nsteps * nlay) for w in D["windows"]}  # per launch
 
     # ---- the 4096-token SWA(64,4) prefill (one sequence), launches timed alone
     sq, sk, sv = inputs.prefill_inputs(S["B"], S["L"], S["Hq"], S["Hkv"], S["d"], seed=rank_seed(rank),
@@ -544,7 +594,8 @@ def run_swa(args, rank: int, world: int, local_rank: int):
 
     # ---- end to end: the decode stream through the public API with host
     # buffers.  Each step's inputs (q, k, v packed in one pinned host row)
-    # go up, append_decode runs, its output comes back; consecutive steps
+    # go up, append_decode runs in each of the 16 layers (every layer takes
+    # the step's q, k, v), the last layer's output comes back; consecutive steps
     # overlap (step i+1's copy up while step i computes and step i-1's output
     # comes down: double-buffered device buffers).  Every copy is inside the
     # timed region.
@@ -561,9 +612,9 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     up, down, comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.current_stream(dev)
 
     def enqueue_stream(w, comp):
-        """Enqueue the window's 1024 steps (copy up, append_decode, copy down)
-        on comp and the two copy streams, forked from and joined back to comp."""
-        c = caches[w]
+        """Enqueue the window's 1024 steps (copy up, append_decode in every
+        layer, copy down) on comp and the two copy streams, forked from and
+        joined back to comp."""
         up.wait_stream(comp)
         down.wait_stream(comp)
         done = []
@@ -579,7 +630,8 @@ def run_swa(args, rank: int, world: int, local_rank: int):
             if i >= 2:  # dev_out[j] was read back by step i-2's copy
                 comp.wait_event(done[i - 2][1])
             qv, kv, vv = views[j]
-            swa.append_decode(qv, kv, vv, c, pos[i], out=dev_out[j], workspace=wsp[w])
+            for c in caches[w]:
+                swa.append_decode(qv, kv, vv, c, pos[i], out=dev_out[j], workspace=wsp[w])
             e_comp = torch.cuda.Event()
             e_comp.record(comp)
             down.wait_event(e_comp)
@@ -592,7 +644,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         comp.wait_stream(down)
 
     def e2e_eager(w):
-        caches[w].append(kp, vp, 0)  # back to the post-prompt state (device inputs; untimed)
+        reset_caches(w)  # back to the post-prompt state (device inputs; untimed)
         torch.cuda.synchronize()
         comp = torch.cuda.current_stream(dev)
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -621,7 +673,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         graphs[w] = g
 
     def e2e_graph(w):
-        caches[w].append(kp, vp, 0)  # back to the post-prompt state (device inputs; untimed)
+        reset_caches(w)  # back to the post-prompt state (device inputs; untimed)
         torch.cuda.synchronize()
         comp = torch.cuda.current_stream(dev)
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -684,17 +736,17 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         by = decode_bytes(B, Hq, Hkv, d, nv)
         kv = kv_read_bytes(B, Hkv, d, nv)
         e = roofline_entry("swa_decode_kernel (append_decode)", tok_ms[w], 4.0 * d * Hq * B * nv, by, pk)
-        e["frac_without_event_pair"] = by / ((tok_ms[w] - event_pair_ms) * 1e-3) / 1e9 / pk["hbm_gbs"]
         e["traffic"] = kernel_traffic("swa_decode.cu", decode_workload(w))
         e["workload"] = decode_workload(w)
         rl[f"decode_w{w}"] = e
-        shares[f"decode_w{w}"] = tok_ms[w] * nsteps / step_ms
-        shares[f"append_w{w}"] = app_ms[w] / step_ms
+        shares[f"decode_w{w}"] = tok_ms[w] * nsteps * nlay / step_ms
+        shares[f"append_w{w}"] = app_ms[w] * nlay / step_ms
         decode_key[f"w{w}"] = {"ms_step": tok_ms[w], "tok_s": B * world / (tok_ms[w] * 1e-3),
                                "kv_read_gbs": kv / (tok_ms[w] * 1e-3) / 1e9,
                                "frac_hbm": e["frac"], "bytes_per_step": by,
                                "kv_bytes_per_step": kv, "cache_bytes": 2 * B * Hkv * w * d * 2,
-                               "prompt_append_ms": app_ms[w]}
+                               "prompt_append_ms": app_ms[w], "layers": nlay,
+                               "graph_ms": tok_ms[w] * nsteps * nlay}
     dom = max((k for k in rl), key=lambda k: shares[k])
     roof = {k: rl[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac")}
     roof.update({"traffic": rl[dom]["traffic"], "kernel": rl[dom]["kernel"], "which": dom,
@@ -712,9 +764,11 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": line_config(world),
-        "timing": ("every launch of the step timed alone: CUDA events on its stream around it, "
-                   "L2 flushed before it; ms_per_step = the step's summed launch times; value = "
-                   "decoded_tokens_per_step / ms_decode_per_step"),
+        "timing": ("prefill and append launches timed alone: CUDA events on their stream "
+                   "around each, L2 flushed before it; each decode window's 1024 steps x 16 "
+                   "layers as one CUDA graph, events around its replay (L2 flushed before "
+                   "it); ms_per_step = the sum of those times; value = decoded_tokens_per_step "
+                   "(layer-tokens) / ms_decode_per_step"),
         "decoded_tokens_per_step": tokens, "ms_decode_per_step": dec_ms,
         "event_pair_us": event_pair_ms * 1e3,
         "gpu_launches": launches,
@@ -730,8 +784,9 @@ def run_swa(args, rank: int, world: int, local_rank: int):
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "timing": "the 1024-step decode stream of each window through the Python API "
-                          "(append_decode), captured once as a CUDA graph and replayed: every "
-                          "step's q, k, v copied up from pinned host memory and its output "
+                          "(append_decode in each of the 16 layers), captured once as a CUDA "
+                          "graph and replayed: every step's q, k, v copied up from pinned host "
+                          "memory once (all layers take them) and the last layer's output "
                           "copied back, steps overlapped (double-buffered device buffers, "
                           "copies on two streams of their own), events around the replay; "
                           "the median of three replays per window",

@@ -15,15 +15,17 @@
 // walks it with a stride of gridDim.x.  In each CTA a producer warp streams
 // the K and V rows of its items in 64-slot chunks, back to back across item
 // boundaries, into shared memory with 2-D TMA copies (128-byte swizzle,
-// mbarrier ring); q of the item rides along with its first chunk.  Four
-// consumer warps take 16 slots each and use the warp-level tensor-core MMA
-// (mma.sync m16n8k16, bf16 or fp16 in, fp32 accumulate) for both products with the
-// G <= 8 heads as the N = 8 dimension:
-//   S^T [16 slots x 8 heads] = K [16 x d] . Q^T [d x 8]   (K via ldmatrix)
-//   O^T [d x 8 heads]       += V^T [d x 16] . P^T [16 x 8] (V via ldmatrix.trans)
-// with an online softmax per head in between (running max raised only when it
-// grows by more than 2^8, which keeps the rescale rare and is exact).  At the
-// end of an item the warps are merged through shared memory.  With several
+// mbarrier ring of 1, 2 or 3 stages); q of the item rides along with its
+// first chunk.  Four consumer warps use the warp-level tensor-core MMA
+// (mma.sync m16n8k16, bf16 or fp16 in, fp32 accumulate) for both products
+// with the G <= 8 heads as the N = 8 dimension:
+//   S^T [16 slots x 8 heads] = K [16 x d] . Q^T [d x 8]      (K via ldmatrix)
+//   O^T [d/4 x 8 heads]     += V^T [d/4 x 64] . P^T [64 x 8] (V via ldmatrix.trans)
+// Warp w computes the scores of slots 16w .. 16w+15 and puts them in shared
+// memory; after one barrier per chunk every warp runs the online softmax over
+// all 64 slots (running max raised only when it grows by more than 2^8, which
+// keeps the rescale rare and is exact) and accumulates its quarter of d, so
+// no merge across warps is needed at the end of an item.  With several
 // splits per (sequence, kv head) the items write fp32 partials (max, sum,
 // weighted values) and a second kernel merges them: m = max m_j,
 // l = sum l_j 2^(m_j - m), o = sum acc_j 2^(m_j - m) / l.
@@ -56,11 +58,11 @@ __device__ unsigned long long g_decode_where;
 #define SWA_DEC_CTAS_PER_SM_WIDE 3
 #endif
 
-// Persistent CTAs per SM: the 1-stage chunk ring (items of one chunk, when
-// they all fit in one wave of these), and the 2-stage ring -- normally
-// SWA_DEC_CTAS_PER_SM, SWA_DEC_CTAS_PER_SM_WIDE when a call has at least two
-// items per CTA at that count (more chunks in flight per SM) and its shared
-// memory fits.
+// Persistent CTAs per SM: the 1-stage chunk ring (items of one chunk), and
+// the rings of several stages -- SWA_DEC_CTAS_PER_SM, or
+// SWA_DEC_CTAS_PER_SM_WIDE with two stages when a call has at least two items
+// per CTA at that count (more chunks in flight per SM) and its shared memory
+// fits.
 constexpr int kDecCtasPerSm[2] = {SWA_DEC_CTAS_PER_SM_SINGLE, SWA_DEC_CTAS_PER_SM};
 constexpr int kDecCH = 64;              // slots per chunk
 constexpr int kDecWarps = 4;            // consumer warps, 16 slots each
@@ -93,8 +95,8 @@ struct DecodeParams {
     long long n_o, n_cache, n_new, n_ws_acc, n_ws_ml;
 };
 
-// ST: depth of the chunk ring (2 when items span several chunks; 1 when every
-// item is a single chunk, which halves shared memory so more CTAs fit).
+// ST: depth of the chunk ring (1 when every item is a single chunk, which
+// leaves room for more CTAs per SM; 2 or 3 when items span several chunks).
 template <int D, int G, int ST>
 struct DecSmem {
     static constexpr int kRegion = kDecCH * 128;            // 64 rows x 64 columns (bf16)
@@ -235,7 +237,7 @@ template <int D, int G, int ST>
 constexpr int dec_max_ctas() {
     if (ST == 1) return kDecCtasPerSm[0];
     return (SWA_DEC_CTAS_PER_SM_WIDE > SWA_DEC_CTAS_PER_SM &&
-            SWA_DEC_CTAS_PER_SM_WIDE * (DecSmem<D, G, 2>::kAlloc + 1024) <= 233472)
+            SWA_DEC_CTAS_PER_SM_WIDE * (DecSmem<D, G, ST>::kAlloc + 1024) <= 233472)
                ? SWA_DEC_CTAS_PER_SM_WIDE
                : SWA_DEC_CTAS_PER_SM;
 }
@@ -768,7 +770,7 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, int df,
     if (sms <= 0) return cuda_fail(cudaErrorInvalidDevice, "device_sm_count");
     const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
     // 2-stage ring: the wide count when every CTA gets at least two items
-    const int cps = (ST == 2 && items >= 2ll * kMaxCtas * sms) ? kMaxCtas : kDecCtasPerSm[ST - 1];
+    const int cps = (ST >= 2 && items >= 2ll * kMaxCtas * sms) ? kMaxCtas : kDecCtasPerSm[ST >= 2 ? 1 : 0];
     const long long cap_ctas = static_cast<long long>(cps) * sms;
     const int grid = static_cast<int>(items < cap_ctas ? items : cap_ctas);
     e = launch_pdl(swa_decode_kernel<D, G, ST, DT>, dim3(grid), dim3(kDecThreads), SL::kAlloc, stream,
@@ -793,14 +795,29 @@ swa_status launch_decode(const DecodeMaps &maps, const DecodeParams &p, int df,
 
 namespace {
 
+// Chunk ring of a launch.  Items of one chunk: one stage (more CTAs per SM).
+// Items of several chunks: two stages on the wide grid when that grid still
+// gives every CTA at least two items (more CTAs in flight per SM), else three
+// stages at SWA_DEC_CTAS_PER_SM per SM -- more of each CTA's chunks in
+// flight, which keeps HBM busy when the grid's last round has CTAs idle.
+template <int D, int G, int DT>
+swa_status launch_decode_gs(const DecodeMaps &maps, const DecodeParams &p, bool single, int df,
+                            cudaStream_t stream) {
+    if (single) return launch_decode<D, G, 1, DT>(maps, p, df, stream);
+    const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
+    if (items >= 2ll * dec_max_ctas<D, G, 2>() * device_sm_count())
+        return launch_decode<D, G, 2, DT>(maps, p, df, stream);
+    return launch_decode<D, G, 3, DT>(maps, p, df, stream);
+}
+
 template <int D, int DT>
 swa_status launch_decode_g(const DecodeMaps &maps, const DecodeParams &p, int G, bool single,
                            int df, cudaStream_t stream) {
     switch (G) {
-        case 1: return single ? launch_decode<D, 1, 1, DT>(maps, p, df, stream) : launch_decode<D, 1, 2, DT>(maps, p, df, stream);
-        case 2: return single ? launch_decode<D, 2, 1, DT>(maps, p, df, stream) : launch_decode<D, 2, 2, DT>(maps, p, df, stream);
-        case 4: return single ? launch_decode<D, 4, 1, DT>(maps, p, df, stream) : launch_decode<D, 4, 2, DT>(maps, p, df, stream);
-        case 8: return single ? launch_decode<D, 8, 1, DT>(maps, p, df, stream) : launch_decode<D, 8, 2, DT>(maps, p, df, stream);
+        case 1: return launch_decode_gs<D, 1, DT>(maps, p, single, df, stream);
+        case 2: return launch_decode_gs<D, 2, DT>(maps, p, single, df, stream);
+        case 4: return launch_decode_gs<D, 4, DT>(maps, p, single, df, stream);
+        case 8: return launch_decode_gs<D, 8, DT>(maps, p, single, df, stream);
         default: return SWA_ERR_UNSUPPORTED;
     }
 }

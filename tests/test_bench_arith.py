@@ -62,7 +62,7 @@ def test_the_bench_workload_figures():
     assert bench.window_sum(P["L"], 512) == 512 * 513 // 2 + (32768 - 512) * 512
     assert bench.kv_read_bytes(D["B"], D["Hkv"], D["d"], 512) == 128 << 20
     assert bench.decode_bytes(D["B"], D["Hq"], D["Hkv"], D["d"], 512) == 135790592
-    assert bench.decoded_tokens_per_step(1) == 131072
+    assert bench.decoded_tokens_per_step(1) == 131072 * 16
     assert bench.prefill_bytes(S["B"], S["L"], S["Hq"], S["Hkv"], S["d"]) == 83886080
     assert bench.prefill_flops(S["B"], S["L"], S["Hq"], S["d"], S["w"]) == 4261937152
 
