@@ -49,4 +49,4 @@ def test_max_over_ranks_and_seeds():
 def test_tokens_scale_with_ranks():
     assert bench.decoded_tokens_per_step(4) == 4 * bench.decoded_tokens_per_step(1)
     D = bench.DECODE_CFG
-    assert bench.decoded_tokens_per_step(1) == len(D["windows"]) * D["B"] * D["steps"]
+    assert bench.decoded_tokens_per_step(1) == len(D["windows"]) * D["B"] * D["steps"] * D["layers"]
