@@ -102,7 +102,9 @@ struct DecSmem {
     static constexpr int kRegion = kDecCH * 128;            // 64 rows x 64 columns (bf16)
     static constexpr int kChunkBytes = (D / 64) * kRegion;  // one of K or V
     static constexpr int kQBytes = G * D * 2;               // q of the G heads of the item
-    static constexpr int kStage = 2 * kChunkBytes + ((kQBytes + 1023) & ~1023);  // K | V | q
+    static constexpr int kNewBytes = 2 * D * 2;             // the appended token's k and v rows
+    // K | V | q | k_new v_new (q and the new rows with an item's first chunk)
+    static constexpr int kStage = 2 * kChunkBytes + ((kQBytes + kNewBytes + 1023) & ~1023);
     static constexpr int kSxRow = kDecCH + 8;       // one head's scores of a chunk (padded)
     static constexpr int kSx = ST * kStage;         // [2 chunk parity][8 heads][kSxRow] f32
     static constexpr int kOst = kSx + 2 * 8 * kSxRow * 4;  // [warp][G][D / 4] 16-bit output
@@ -281,21 +283,34 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                 DecItem x = dec_item_head(it, p);
                 const int row_base = (x.b * p.Hkv + x.kvh) * p.cap;  // row of slot 0
                 const uint16_t *qsrc = p.q + (static_cast<int64_t>(x.b) * p.Hq + x.kvh * G) * D;
-                // chunk c of the item into the next stage; q rides along with chunk 0
+                // append + decode: the new token's k and v rows of this (b, kv head)
+                const int64_t nsrc = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D;
+                const bool stage_new = p.k_new != nullptr &&
+                                       in_bounds(nsrc / 8 + D / 8 - 1, p.n_new / 8, &g_decode_error, &g_decode_where);
+                // chunk c of the item into the next stage; q (and the new
+                // token's rows) ride along with chunk 0
                 auto issue = [&](int c) -> bool {
                     const int st = cg % kDecStages;
                     if (!mbar_wait(empty(st), ((cg / kDecStages) & 1) ^ 1, &g_decode_error, abort_flag))
                         return false;
                     const uint32_t stage = sbase + st * SL::kStage;
                     const int row = row_base + x.begin + c * kDecCH;
-                    mbar_arrive_expect_tx(full(st), 2 * SL::kChunkBytes + (c == 0 ? SL::kQBytes : 0));
+                    mbar_arrive_expect_tx(full(st), 2 * SL::kChunkBytes +
+                                                        (c == 0 ? SL::kQBytes + (stage_new ? SL::kNewBytes : 0) : 0));
 #pragma unroll
                     for (int r = 0; r < D / 64; ++r) {
                         tma_load_2d(stage + r * SL::kRegion, &maps.k, full(st), r * 64, row);
                         tma_load_2d(stage + SL::kChunkBytes + r * SL::kRegion, &maps.v, full(st),
                                     r * 64, row);
                     }
-                    if (c == 0) bulk_load_1d(stage + 2 * SL::kChunkBytes, qsrc, SL::kQBytes, full(st));
+                    if (c == 0) {
+                        bulk_load_1d(stage + 2 * SL::kChunkBytes, qsrc, SL::kQBytes, full(st));
+                        if (stage_new) {
+                            const uint32_t nd = stage + 2 * SL::kChunkBytes + SL::kQBytes;
+                            bulk_load_1d(nd, p.k_new + nsrc, D * 2, full(st));
+                            bulk_load_1d(nd + D * 2, p.v_new + nsrc, D * 2, full(st));
+                        }
+                    }
                     ++cg;
                     return true;
                 };
@@ -338,11 +353,12 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
         DecItem x = dec_item_head(it, p);
         dec_item_pos(x, p);
         if (x.n_chunks == 0) continue;
-        // append + decode: the warp whose 16 slots will hold the new token
-        // prefetches its k and v now, so that their load overlaps the chunk
-        // copy instead of following it
+        // append + decode: the new token's k and v rows arrive with the item's
+        // first chunk; when its slot is in a later chunk, the warp whose 16
+        // slots will hold it also prefetches them now, so that their load
+        // overlaps the chunk copies instead of following them
         const int onew = x.snew - x.begin;  // the new slot's offset in the item
-        if (x.snew >= 0 && onew >= 0 && onew < x.end - x.begin && ((onew % kDecCH) >> 4) == warp &&
+        if (x.snew >= 0 && onew >= kDecCH && onew < x.end - x.begin && ((onew % kDecCH) >> 4) == warp &&
             lane < D / 8) {
             const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
             if (in_bounds(src / 8, p.n_new / 8, &g_decode_error, &g_decode_where)) {
@@ -376,25 +392,35 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
             }
             // append + decode: the warp whose 16 slots hold the new token puts
             // its k and v into the staged chunk (over what the copy read) and
-            // into the cache (warp-uniform test)
+            // into the cache (warp-uniform test).  The proxy fence orders the
+            // stage writes before the stage's next TMA fill; the cache stores
+            // follow it, so it does not wait for them.
             const int rnew = x.snew - (x.begin + c * kDecCH);
             const bool patch = x.snew >= 0 && rnew >= slot0 && rnew < slot0 + 16 && rnew < rows;
             if (patch) {
-                if (lane < D / 8) {
-                    const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
-                    const int64_t dst =
-                        ((static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * p.cap + x.snew) * D + lane * 8;
-                    if (in_bounds(src / 8, p.n_new / 8, &g_decode_error, &g_decode_where) &&
-                        in_bounds(dst / 8, p.n_cache / 8, &g_decode_error, &g_decode_where)) {
-                        const uint4 kk = *reinterpret_cast<const uint4 *>(p.k_new + src);
-                        const uint4 vv = *reinterpret_cast<const uint4 *>(p.v_new + src);
-                        const int off = (lane >> 3) * SL::kRegion + rnew * 128 +
-                                        (((lane & 7) ^ (rnew & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(sm + st * SL::kStage + off) = kk;
-                        *reinterpret_cast<uint4 *>(sm + st * SL::kStage + SL::kChunkBytes + off) = vv;
-                        *reinterpret_cast<uint4 *>(p.kc + dst) = kk;
-                        *reinterpret_cast<uint4 *>(p.vc + dst) = vv;
+                const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
+                const int64_t dst =
+                    ((static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * p.cap + x.snew) * D + lane * 8;
+                const bool ok = lane < D / 8 && in_bounds(src / 8, p.n_new / 8, &g_decode_error, &g_decode_where) &&
+                                in_bounds(dst / 8, p.n_cache / 8, &g_decode_error, &g_decode_where);
+                uint4 kk = make_uint4(0u, 0u, 0u, 0u), vv = kk;
+                if (ok) {
+                    if (c == 0) {  // staged with this chunk
+                        const uint8_t *nb = sm + st * SL::kStage + 2 * SL::kChunkBytes + SL::kQBytes;
+                        kk = *reinterpret_cast<const uint4 *>(nb + lane * 16);
+                        vv = *reinterpret_cast<const uint4 *>(nb + D * 2 + lane * 16);
+                    } else {
+                        kk = *reinterpret_cast<const uint4 *>(p.k_new + src);
+                        vv = *reinterpret_cast<const uint4 *>(p.v_new + src);
                     }
+                    const int off = (lane >> 3) * SL::kRegion + rnew * 128 + (((lane & 7) ^ (rnew & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + off) = kk;
+                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + SL::kChunkBytes + off) = vv;
+                }
+                fence_proxy_async_smem();
+                if (ok) {
+                    *reinterpret_cast<uint4 *>(p.kc + dst) = kk;
+                    *reinterpret_cast<uint4 *>(p.vc + dst) = vv;
                 }
                 __syncwarp();
             }
@@ -501,8 +527,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                     mma_16816<DT>(acc[mt], a, pb[kk][0], pb[kk][1]);
                 }
             }
-            // zeroed or patched rows before the next TMA fill of this stage
-            if (mine < 16 || patch) fence_proxy_async_smem();
+            // zeroed rows before the next TMA fill of this stage
+            if (mine < 16) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty(st));
         }
