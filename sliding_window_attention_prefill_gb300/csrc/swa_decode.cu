@@ -108,8 +108,9 @@ struct DecSmem {
     static constexpr int kSxRow = kDecCH + 8;       // one head's scores of a chunk (padded)
     static constexpr int kSx = ST * kStage;         // [2 chunk parity][8 heads][kSxRow] f32
     static constexpr int kOst = kSx + 2 * 8 * kSxRow * 4;  // [warp][G][D / 4] 16-bit output
-    static constexpr int kBar = kOst + kDecWarps * G * (D / kDecWarps) * 2;  // full[st], empty[st]
-    static constexpr int kAbort = kBar + 2 * ST * 8;
+    // full_k[st], full_v[st], empty_k[st], empty_v[st]
+    static constexpr int kBar = kOst + kDecWarps * G * (D / kDecWarps) * 2;
+    static constexpr int kAbort = kBar + 4 * ST * 8;
     static constexpr int kBytes = kAbort + 16;
     static constexpr int kAlloc = kBytes + 1024;              // align the base to 1024
 };
@@ -206,8 +207,15 @@ __device__ __forceinline__ DecItem dec_item_head(int it, const DecodeParams &p) 
     return x;
 }
 
-__device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p) {
-    const int pos = p.pos[x.b];
+// The position of item it's sequence.  With items of one chunk (a short
+// chain per item) each side loads it one item ahead -- for it + gridDim.x
+// while it works on it -- so the load's latency overlaps an item's work
+// instead of preceding the next one.
+__device__ __forceinline__ int dec_item_load_pos(int it, const DecodeParams &p) {
+    return p.pos[(it / p.splits) / p.Hkv];
+}
+
+__device__ __forceinline__ void dec_item_pos(DecItem &x, const DecodeParams &p, int pos) {
     x.bad = pos < 0 || (p.w < 0 && pos >= p.cap);
     const int cap_eff = p.w < 0 ? p.cap : p.w;
     x.n_valid = x.bad ? 0 : min(pos + 1, cap_eff);
@@ -256,15 +264,24 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
     uint8_t *sm = smem_raw + (sbase - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SL::kAbort);
-    auto full = [&](int st) { return sbase + SL::kBar + 8u * st; };
-    auto empty = [&](int st) { return sbase + SL::kBar + 8u * (kDecStages + st); };
+    // K and V of a stage fill and drain on barriers of their own: a stage's K
+    // is released once the scores are computed, so the next chunk's K (and
+    // its scores and softmax) can go ahead while this chunk's P V runs and
+    // the next V loads.
+    auto full_k = [&](int st) { return sbase + SL::kBar + 8u * st; };
+    auto full_v = [&](int st) { return sbase + SL::kBar + 8u * (kDecStages + st); };
+    auto empty_k = [&](int st) { return sbase + SL::kBar + 8u * (2 * kDecStages + st); };
+    auto empty_v = [&](int st) { return sbase + SL::kBar + 8u * (3 * kDecStages + st); };
     const int n_items = p.B * p.Hkv * p.splits;
+    constexpr bool kPosAhead = (ST == 1);
     pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kDecStages; ++st) {
-            mbar_init(full(st), 1);
-            mbar_init(empty(st), kDecWarps);
+            mbar_init(full_k(st), 1);
+            mbar_init(full_v(st), 1);
+            mbar_init(empty_k(st), kDecWarps);
+            mbar_init(empty_v(st), kDecWarps);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -279,8 +296,15 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
             tma_prefetch_desc(&maps.v);
             int cg = 0;  // chunks issued by this CTA
             bool ok = true;
+            int pos_next = (kPosAhead && blockIdx.x < n_items) ? dec_item_load_pos(blockIdx.x, p) : 0;
             for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
                 DecItem x = dec_item_head(it, p);
+                int pos_it = pos_next;
+                if (kPosAhead) {
+                    if (it + static_cast<int>(gridDim.x) < n_items) pos_next = dec_item_load_pos(it + gridDim.x, p);
+                } else {
+                    pos_it = p.pos[x.b];
+                }
                 const int row_base = (x.b * p.Hkv + x.kvh) * p.cap;  // row of slot 0
                 const uint16_t *qsrc = p.q + (static_cast<int64_t>(x.b) * p.Hq + x.kvh * G) * D;
                 // append + decode: the new token's k and v rows of this (b, kv head)
@@ -291,26 +315,28 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                 // token's rows) ride along with chunk 0
                 auto issue = [&](int c) -> bool {
                     const int st = cg % kDecStages;
-                    if (!mbar_wait(empty(st), ((cg / kDecStages) & 1) ^ 1, &g_decode_error, abort_flag))
-                        return false;
+                    const uint32_t ph = ((cg / kDecStages) & 1) ^ 1;
                     const uint32_t stage = sbase + st * SL::kStage;
                     const int row = row_base + x.begin + c * kDecCH;
-                    mbar_arrive_expect_tx(full(st), 2 * SL::kChunkBytes +
-                                                        (c == 0 ? SL::kQBytes + (stage_new ? SL::kNewBytes : 0) : 0));
+                    if (!mbar_wait(empty_k(st), ph, &g_decode_error, abort_flag)) return false;
+                    mbar_arrive_expect_tx(full_k(st), SL::kChunkBytes +
+                                                          (c == 0 ? SL::kQBytes + (stage_new ? SL::kNewBytes : 0) : 0));
 #pragma unroll
-                    for (int r = 0; r < D / 64; ++r) {
-                        tma_load_2d(stage + r * SL::kRegion, &maps.k, full(st), r * 64, row);
-                        tma_load_2d(stage + SL::kChunkBytes + r * SL::kRegion, &maps.v, full(st),
-                                    r * 64, row);
-                    }
+                    for (int r = 0; r < D / 64; ++r)
+                        tma_load_2d(stage + r * SL::kRegion, &maps.k, full_k(st), r * 64, row);
                     if (c == 0) {
-                        bulk_load_1d(stage + 2 * SL::kChunkBytes, qsrc, SL::kQBytes, full(st));
+                        bulk_load_1d(stage + 2 * SL::kChunkBytes, qsrc, SL::kQBytes, full_k(st));
                         if (stage_new) {
                             const uint32_t nd = stage + 2 * SL::kChunkBytes + SL::kQBytes;
-                            bulk_load_1d(nd, p.k_new + nsrc, D * 2, full(st));
-                            bulk_load_1d(nd + D * 2, p.v_new + nsrc, D * 2, full(st));
+                            bulk_load_1d(nd, p.k_new + nsrc, D * 2, full_k(st));
+                            bulk_load_1d(nd + D * 2, p.v_new + nsrc, D * 2, full_k(st));
                         }
                     }
+                    if (!mbar_wait(empty_v(st), ph, &g_decode_error, abort_flag)) return false;
+                    mbar_arrive_expect_tx(full_v(st), SL::kChunkBytes);
+#pragma unroll
+                    for (int r = 0; r < D / 64; ++r)
+                        tma_load_2d(stage + SL::kChunkBytes + r * SL::kRegion, &maps.v, full_v(st), r * 64, row);
                     ++cg;
                     return true;
                 };
@@ -319,14 +345,15 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                     ok = issue(0);
                     c = 1;
                 }
-                dec_item_pos(x, p);
+                dec_item_pos(x, p, pos_it);
                 if (x.bad && x.kvh == 0 && x.split == 0) atomicCAS(&g_decode_error, 0, kErrBounds);
                 for (; c < x.n_chunks && ok; ++c) ok = issue(c);
             }
             int no_abort = 0;  // drain the copies this thread started
             for (int i = 0; i < kDecStages && i < cg; ++i) {
                 const int c = cg - 1 - i;
-                mbar_wait(full(c % kDecStages), (c / kDecStages) & 1, &g_decode_error, &no_abort);
+                mbar_wait(full_k(c % kDecStages), (c / kDecStages) & 1, &g_decode_error, &no_abort);
+                mbar_wait(full_v(c % kDecStages), (c / kDecStages) & 1, &g_decode_error, &no_abort);
             }
         }
         return;
@@ -349,9 +376,16 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
     const int slot0 = warp * 16;  // this warp's slots within a chunk (scores)
     int cg = 0;                   // chunks consumed by this CTA
 
+    int pos_next = (kPosAhead && blockIdx.x < n_items) ? dec_item_load_pos(blockIdx.x, p) : 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         DecItem x = dec_item_head(it, p);
-        dec_item_pos(x, p);
+        int pos_it = pos_next;
+        if (kPosAhead) {
+            if (it + static_cast<int>(gridDim.x) < n_items) pos_next = dec_item_load_pos(it + gridDim.x, p);
+        } else {
+            pos_it = p.pos[x.b];
+        }
+        dec_item_pos(x, p, pos_it);
         if (x.n_chunks == 0) continue;
         // append + decode: the new token's k and v rows arrive with the item's
         // first chunk; when its slot is in a later chunk, the warp whose 16
@@ -376,7 +410,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
 
         for (int c = 0; c < x.n_chunks; ++c, ++cg) {
             const int st = cg % kDecStages;
-            mbar_wait(full(st), (cg / kDecStages) & 1, &g_decode_error, abort_flag);
+            const uint32_t ph = (cg / kDecStages) & 1;
+            mbar_wait(full_k(st), ph, &g_decode_error, abort_flag);
             // filled slots of this chunk (none past n_valid, e.g. a speculative chunk)
             const int rows = min(kDecCH, min(x.end, x.n_valid) - (x.begin + c * kDecCH));
             const int mine = rows - slot0;  // valid slots among this warp's 16
@@ -391,19 +426,24 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                 }
             }
             // append + decode: the warp whose 16 slots hold the new token puts
-            // its k and v into the staged chunk (over what the copy read) and
-            // into the cache (warp-uniform test).  The proxy fence orders the
-            // stage writes before the stage's next TMA fill; the cache stores
-            // follow it, so it does not wait for them.
+            // its k into the staged chunk now and its v once V has landed
+            // (over what the copies read), and both into the cache
+            // (warp-uniform test).  The proxy fence orders the stage writes
+            // before the stage's next TMA fill; the cache stores follow it,
+            // so it does not wait for them.
             const int rnew = x.snew - (x.begin + c * kDecCH);
             const bool patch = x.snew >= 0 && rnew >= slot0 && rnew < slot0 + 16 && rnew < rows;
+            uint4 vv = make_uint4(0u, 0u, 0u, 0u);  // the new v row's part of this lane
+            bool vok = false;
+            const int off_new = (lane >> 3) * SL::kRegion + rnew * 128 + (((lane & 7) ^ (rnew & 7)) << 4);
             if (patch) {
                 const int64_t src = (static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * D + lane * 8;
                 const int64_t dst =
                     ((static_cast<int64_t>(x.b) * p.Hkv + x.kvh) * p.cap + x.snew) * D + lane * 8;
                 const bool ok = lane < D / 8 && in_bounds(src / 8, p.n_new / 8, &g_decode_error, &g_decode_where) &&
                                 in_bounds(dst / 8, p.n_cache / 8, &g_decode_error, &g_decode_where);
-                uint4 kk = make_uint4(0u, 0u, 0u, 0u), vv = kk;
+                uint4 kk = make_uint4(0u, 0u, 0u, 0u);
+                vok = ok;
                 if (ok) {
                     if (c == 0) {  // staged with this chunk
                         const uint8_t *nb = sm + st * SL::kStage + 2 * SL::kChunkBytes + SL::kQBytes;
@@ -413,9 +453,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                         kk = *reinterpret_cast<const uint4 *>(p.k_new + src);
                         vv = *reinterpret_cast<const uint4 *>(p.v_new + src);
                     }
-                    const int off = (lane >> 3) * SL::kRegion + rnew * 128 + (((lane & 7) ^ (rnew & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + off) = kk;
-                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + SL::kChunkBytes + off) = vv;
+                    *reinterpret_cast<uint4 *>(sm + st * SL::kStage + off_new) = kk;
                 }
                 fence_proxy_async_smem();
                 if (ok) {
@@ -426,18 +464,6 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
             }
             const uint32_t kst = sbase + st * SL::kStage;
             const uint32_t vst = kst + SL::kChunkBytes;
-            if (mine < 16) {
-                // Every warp reads the V rows of all 64 slots: the rows of this
-                // warp's slots past the filled ones hold whatever the cache has
-                // there, so zero them (0-weights never meet a non-finite value).
-                uint8_t *vb = sm + st * SL::kStage + SL::kChunkBytes;
-                const int first = mine > 0 ? mine : 0;
-                for (int i = lane; i < (16 - first) * (D / 8); i += 32) {
-                    const int r = slot0 + first + i / (D / 8), cc = i % (D / 8);
-                    *reinterpret_cast<uint4 *>(vb + (cc >> 3) * SL::kRegion + r * 128 +
-                                               ((cc & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
             // ---- S^T = K Q^T for this warp's 16 slots, into the exchange buffer
             float s[4] = {0.f, 0.f, 0.f, 0.f};
             if (mine > 0) {
@@ -461,7 +487,10 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                     sxb[h1 * SXR + slot0 + gq + 8] = vb_ ? s[3] * p.scale_log2 : -INFINITY;
                 }
             }
-            // scores, patched and zeroed rows of all four warps are in place
+            // this warp is done with the stage's K (and q and the staged rows)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_k(st));
+            // the scores of all four warps are in place
             asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
             // ---- online softmax of head gq over the chunk's 64 slots: this
             // lane takes slots 16kk + {2t, 2t+1, 2t+8, 2t+9}, kk = 0..3 (the
@@ -516,6 +545,27 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                     acc[mt][3] *= a1;
                 }
             }
+            // ---- V: wait for it, then put in the new token's row and zero the
+            // rows past the filled slots (a CTA-uniform test), all before any
+            // warp reads them
+            mbar_wait(full_v(st), ph, &g_decode_error, abort_flag);
+            if ((x.snew >= 0 && rnew >= 0 && rnew < rows) || rows < kDecCH) {
+                if (vok) *reinterpret_cast<uint4 *>(sm + st * SL::kStage + SL::kChunkBytes + off_new) = vv;
+                if (mine < 16) {
+                    // Every warp reads the V rows of all 64 slots: the rows of this
+                    // warp's slots past the filled ones hold whatever the cache has
+                    // there, so zero them (0-weights never meet a non-finite value).
+                    uint8_t *vb = sm + st * SL::kStage + SL::kChunkBytes;
+                    const int first = mine > 0 ? mine : 0;
+                    for (int i = lane; i < (16 - first) * (D / 8); i += 32) {
+                        const int r = slot0 + first + i / (D / 8), cc = i % (D / 8);
+                        *reinterpret_cast<uint4 *>(vb + (cc >> 3) * SL::kRegion + r * 128 +
+                                                   ((cc & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                if (patch || mine < 16) fence_proxy_async_smem();
+                asm volatile("bar.sync 2, %0;" ::"n"(kDecWarps * 32) : "memory");
+            }
             // ---- O^T rows of this warp += V^T P^T over the 64 slots
             const int vrow = ((lane >> 4) << 3) + (lane & 7);
 #pragma unroll
@@ -527,10 +577,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_max_ctas<D, G, ST>())
                     mma_16816<DT>(acc[mt], a, pb[kk][0], pb[kk][1]);
                 }
             }
-            // zeroed rows before the next TMA fill of this stage
-            if (mine < 16) fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty(st));
+            if (lane == 0) mbar_arrive(empty_v(st));
         }
 
         // ---------------------------------------------------------------- output
@@ -829,8 +877,8 @@ namespace {
 template <int D, int G, int DT>
 swa_status launch_decode_gs(const DecodeMaps &maps, const DecodeParams &p, bool single, int df,
                             cudaStream_t stream) {
-    if (single) return launch_decode<D, G, 1, DT>(maps, p, df, stream);
     const long long items = static_cast<long long>(p.B) * p.Hkv * p.splits;
+    if (single) return launch_decode<D, G, 1, DT>(maps, p, df, stream);
     if (items >= 2ll * dec_max_ctas<D, G, 2>() * device_sm_count())
         return launch_decode<D, G, 2, DT>(maps, p, df, stream);
     return launch_decode<D, G, 3, DT>(maps, p, df, stream);
