@@ -81,12 +81,14 @@ CPU_DECODE_STEPS = 16
 class L2Flush:
     """Evicts the timed kernels' data from L2 (129 MB on GB300): write one
     buffer larger than L2, then read a second one, which also writes the
-    first buffer's dirty lines back before the timed launch starts."""
+    first buffer's dirty lines back before the timed launch starts.  The read
+    is a float32 sum, reduced as it is read (an integer sum would first copy
+    the buffer to int64, leaving that copy's dirty lines in L2)."""
 
     def __init__(self, device="cuda"):
         import torch
         self.wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-        self.rbuf = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+        self.rbuf = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
     def __call__(self, i: int = 1) -> None:
         self.wbuf.fill_(i & 0xFF)
@@ -535,8 +537,10 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     if sampler:
         sampler.start("step")
     per_step = []  # [step][unit] ms
-    for _ in range(args.steps):  # the timed steps
+    for _ in range(args.steps):  # the timed steps (an NVTX range each, for a profiler's filter)
+        rid = torch.cuda.nvtx.range_start("bench timed step")
         run_step()
+        torch.cuda.nvtx.range_end(rid)
         torch.cuda.synchronize()
         per_step.append([a.elapsed_time(b) for a, b in ev])
     torch.cuda.synchronize()
