@@ -75,6 +75,8 @@ FLAT_POSITIONS = [1 << e for e in range(10, 19, 2)]
 FLAT_WINDOWS = (64, 128, 256, 512)
 FLAT_BATCHES = (1, 256)
 FLAT_LAYERS = 4
+FLAT_STEPS = 16
+L2_BYTES = 129 * 10**6
 CPU_DECODE_STEPS = 16
 
 
@@ -521,6 +523,11 @@ def run_swa(args, rank: int, world: int, local_rank: int):
           for _ in units]
 
     def run_step():
+        # The GPU idles while the host reads the previous step's events; the
+        # first launch after that idle ran up to 30 % slower, so the step's
+        # first unit runs once untimed before the timed pass.
+        flush(len(units))
+        units[0][2]()
         for j, u in enumerate(units):
             flush(j)
             ev[j][0].record()
@@ -762,7 +769,7 @@ def run_swa(args, rank: int, world: int, local_rank: int):
     sf = prefill_flops(S["B"], S["L"], S["Hq"], S["d"], S["w"])
     small_rl = roofline_entry("swa_prefill_kernel", small_ms, sf, sb, pk)
     small_rl["traffic"] = kernel_traffic("swa_prefill.cu", SMALL_WORKLOAD)
-    launches = sum(u[3] for u in units) * args.steps
+    launches = (sum(u[3] for u in units) + units[0][3]) * args.steps  # with the untimed first unit
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -811,49 +818,62 @@ def run_swa(args, rank: int, world: int, local_rank: int):
 def flatness_sweep(dev, flush, sampler) -> dict:
     """Decode tok/s of a 4-layer attention-only stack at positions 1K .. 256K
     (every layer's cache in the state a prompt of that length leaves, N(0,1)
-    values; one step appends the token and decodes it in each layer, replayed
-    as one CUDA graph, L2 flushed before each replay; the median of 50
-    replays per point, since a batch-1 step of ~70 µs is launch-bound and a
-    mean would carry the launch jitter).  Reports tok/s per
-    point and max/min over the positions for each finite window at batch 1
-    and 256; full causal at batch 1 for contrast."""
+    values; one step appends the token and decodes it in each layer).  Each
+    point is one CUDA graph of FLAT_STEPS steps, L2 flushed before each
+    replay: a single step is too short for the GPU's event timer, which moves
+    in 2.048 µs steps.  Every step of a replay reads caches that are cold in
+    L2: when a stack's caches are smaller than four times L2, the steps go
+    through FLAT_STEPS copies of the stack, one each; larger stacks do not
+    fit in L2 from one step to the next.  The trimmed mean of the replays, per step.
+    Reports tok/s per point and max/min over the positions for each finite
+    window at batch 1 and 256; full causal at batch 1 for contrast."""
     import torch
 
     import sliding_window_attention_prefill_gb300 as swa
     D = DECODE_CFG
     Hq, Hkv, d, s = D["Hq"], D["Hkv"], D["d"], D["s"]
     gen = torch.Generator(device=dev)
-    out = {"positions": FLAT_POSITIONS, "layers": FLAT_LAYERS, "reps_per_point": 50,
-           "statistic": "median of the replays"}
+    reps = 12
+    out = {"positions": FLAT_POSITIONS, "layers": FLAT_LAYERS, "steps_per_replay": FLAT_STEPS,
+           "replays_per_point": reps,
+           "statistic": "mean of the replays without the fastest and slowest, per step"}
     if sampler:
         sampler.start("flatness")
     pts = [(B, w) for B in FLAT_BATCHES for w in FLAT_WINDOWS] + [(1, -1)]
     for B, w in pts:
-        toks = []
+        toks, copies = [], []
         for P in FLAT_POSITIONS:
             gen.manual_seed(B * 1000003 + P * 7 + (w + 1))
-            layers = []
-            for _ in range(FLAT_LAYERS):
-                c = swa.Cache(B, Hkv, d, w, s if w > 0 else 0, max_len=(P + 1 if w < 0 else None),
-                              device=dev)
-                c.k.normal_(generator=gen)
-                c.v.normal_(generator=gen)
-                kn = torch.randn(B, 1, Hkv, d, generator=gen, device=dev).to(torch.bfloat16)
-                vn = torch.randn(B, 1, Hkv, d, generator=gen, device=dev).to(torch.bfloat16)
-                q = torch.randn(B, Hq, d, generator=gen, device=dev).to(torch.bfloat16)
-                layers.append((c, kn, vn, q, torch.empty_like(q), swa.workspace_for(c, Hq)))
+            cap = P + 1 if w < 0 else w
+            stack_bytes = FLAT_LAYERS * 2 * B * Hkv * cap * d * 2
+            n_copies = FLAT_STEPS if stack_bytes < 4 * L2_BYTES else 1
+            stacks = []
+            for _ in range(n_copies):
+                layers = []
+                for _ in range(FLAT_LAYERS):
+                    c = swa.Cache(B, Hkv, d, w, s if w > 0 else 0, max_len=(P + 1 if w < 0 else None),
+                                  device=dev)
+                    c.k.normal_(generator=gen)
+                    c.v.normal_(generator=gen)
+                    kn = torch.randn(B, 1, Hkv, d, generator=gen, device=dev).to(torch.bfloat16)
+                    vn = torch.randn(B, 1, Hkv, d, generator=gen, device=dev).to(torch.bfloat16)
+                    q = torch.randn(B, Hq, d, generator=gen, device=dev).to(torch.bfloat16)
+                    layers.append((c, kn, vn, q, torch.empty_like(q), swa.workspace_for(c, Hq)))
+                stacks.append(layers)
             pos = torch.full((B,), P, dtype=torch.int32, device=dev)
 
-            def step():
-                for c, kn, vn, q, o, ws in layers:
-                    swa.append_decode(q, kn, vn, c, pos, out=o, workspace=ws)
+            def steps():
+                for i in range(FLAT_STEPS):
+                    for c, kn, vn, q, o, ws in stacks[i % n_copies]:
+                        swa.append_decode(q, kn, vn, c, pos, out=o, workspace=ws)
 
-            ms = _time_graph(step, out["reps_per_point"], flush, stat="median")
+            ms = _time_graph(steps, reps, flush, stat="trimmed") / FLAT_STEPS
             toks.append(B / (ms * 1e-3))
-            del layers, step
+            copies.append(n_copies)
+            del stacks, steps
             torch.cuda.empty_cache()
         key = f"B{B}_w{w}" if w > 0 else f"B{B}_full_causal"
-        out[key] = {"tok_s": toks, "max_over_min": max(toks) / min(toks)}
+        out[key] = {"tok_s": toks, "max_over_min": max(toks) / min(toks), "stack_copies": copies}
     finite = [out[f"B{B}_w{w}"]["max_over_min"] for B in FLAT_BATCHES for w in FLAT_WINDOWS]
     out["worst_max_over_min_finite_w"] = max(finite)
     if sampler:
@@ -863,8 +883,8 @@ def flatness_sweep(dev, flush, sampler) -> dict:
 
 
 def _time_graph(fn, steps: int, flush, warm: int = 3, stat: str = "mean") -> float:
-    """Mean (or median) ms of `fn` replayed as a CUDA graph, L2 flushed before
-    each replay."""
+    """Mean (or median, or trimmed mean) ms of `fn` replayed as a CUDA graph,
+    L2 flushed before each replay."""
     import torch
     fn()
     torch.cuda.synchronize()
@@ -890,6 +910,8 @@ def _time_graph(fn, steps: int, flush, warm: int = 3, stat: str = "mean") -> flo
     t = [a.elapsed_time(b) for a, b in evs]
     if stat == "median":
         return sorted(t)[len(t) // 2]
+    if stat == "trimmed" and steps > 2:  # without the fastest and the slowest replay
+        return sum(sorted(t)[1:-1]) / (steps - 2)
     return sum(t) / steps
 
 
