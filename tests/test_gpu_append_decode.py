@@ -30,6 +30,7 @@ CASES = [
     (64, 32, 8, 128, 512, 4, 4096, 2, None, torch.bfloat16),   # one split per sequence and head
     (1, 32, 8, 128, 512, 4, 1000, 2, None, torch.bfloat16),    # several splits (merge kernel)
     (1, 16, 16, 64, 64, 4, 4096, 2, None, torch.float16),      # the pages' shape, fp16
+    (2, 32, 8, 128, 128, 4, 129, 3, None, torch.bfloat16),     # two-chunk items, new slot in the first
 ]
 
 
