@@ -901,11 +901,22 @@ swa_status launch_prefill(const PrefillMaps &maps, const PrefillParams &p, cudaS
 // 990 / 825, SWA(768,4) 1018 / 968, SWA(1024,4) 1097 / 1055, SWA(2048,4)
 // 1196 / 1239, full causal 1219 / 1412; d = 64, 16 heads: SWA(1024,4)
 // 529 / 581, full causal 703 / 781.
+// At d = 64 the 256-column tiles also pay when they cover a unit in half as
+// many tiles as 128-column ones, at least four of those (the same columns
+// computed, half the per-tile work of the softmax chain).  Kernel alone, 16
+// heads of 64, fp16, L = 32768, µs (128 / 256-column tiles): SWA(128,4)
+// 78.0 / 91.6 (3 / 2 tiles), SWA(256,4) 101.3 / 95.1 (4 / 2), SWA(384,4)
+// 124.4 / 132.5 (5 / 3), SWA(512,4) 147.7 / 135.3 (6 / 3); SWA(64,4)
+// 57.5 / 62.0 (2 / 1).
 int prefill_key_tile(const PrefillParams &p, int d) {
     if (SWA_PREFILL_FORCE_KT != 0) return SWA_PREFILL_FORCE_KT;
     const long long cols =
         p.w < 0 ? static_cast<long long>(p.Lk) : static_cast<long long>(p.s_pad) + (p.w - p.s) + p.P - 1;
     if (cols > (d == 128 ? 1280 : 768)) return 256;
+    if (d == 64) {
+        const long long n128 = (cols + 127) / 128, n256 = (cols + 255) / 256;
+        if (n128 >= 4 && 2 * n256 == n128) return 256;
+    }
     return d == 128 ? 112 : 128;
 }
 

@@ -58,6 +58,7 @@ CASES = [
     (1, 2600, 8, 2, 128, 1501, 4),
     (1, 5000, 4, 1, 128, 2048, 4),
     (2, 700, 8, 2, 64, 300, 4),      # d=64 on the two-tile kernel, two sequences
+    (1, 900, 4, 4, 64, 300, 4),      # d=64, G=1: 256-column tiles (2 instead of 4 of 128)
     # Large groups over several key tiles (the epilogue warpgroup's row ->
     # position / head mapping): G=16 (8 positions per unit) and G=8 at d=64.
     (1, 600, 32, 2, 128, 300, 4),
